@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of the VQ KV-cache decode step on GB300.
+
+One step = the whole hot path over one batch: the new token's K and V rows
+are quantised into the cache (vqkv_encode, keys smoothed + rotated), then
+decode attention runs over the packed cache (vqkv_decode_attn).  The
+workload is the Llama-3.1-8B-shaped 2-bit decode at 196,608 cached tokens
+(batch 1, 32 query heads over 8 KV heads, head_dim 128); its cache is
+produced by the library's own GPU encoder from seeded synthetic K/V.
+
+Prints one JSON line (see README of the result keys in the design doc).
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from vector_quantized_bit_gb300 import calib, synth  # noqa: E402
+
+METRIC = "decode-attn KV tokens/s and HBM GB/s vs GB300 peak (2-bit, Llama-8B shape, 196k)"
+WORKLOAD_ID = 1
+GRAPH_STEPS = 100           # steps captured per CUDA graph
+SOAK_S = 0.5                # untimed load on each side of the timed region for clock sampling
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_vq2_llama8b_196k.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- workload
+
+def _gen_head(args):
+    w, b, kvh = args
+    return synth.keys(w, b, kvh, 0, w.seq_len), synth.values(w, b, kvh, 0, w.seq_len)
+
+
+def _cal_head(args):
+    w, kvh = args
+    return calib.calibrate_head(w, kvh)
+
+
+def host_workload(w):
+    """Calibration and synthetic K/V on host worker processes (spawned before
+    any CUDA call)."""
+    import concurrent.futures
+    import multiprocessing
+    n = min(w.Hkv, os.cpu_count() or 1)
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(n, mp_context=ctx) as ex:
+        cal = list(ex.map(_cal_head, [(w, h) for h in range(w.Hkv)]))
+        kv = list(ex.map(_gen_head, [(w, 0, h) for h in range(w.Hkv)]))
+    s = np.stack([c[0] for c in cal])
+    kcb = np.stack([c[1] for c in cal])
+    vcb = np.stack([c[2] for c in cal])
+    return s, kcb, vcb, kv
+
+
+def algorithmic_bytes(w, lens):
+    """Packed indices + codebooks + q + O per decode call."""
+    E, dsub = synth.MODE_GEOMETRY[w.mode]
+    code_bits = int(math.log2(E))
+    th = int(np.sum(lens)) * w.Hkv
+    idx = 2 * th * (128 // dsub) * code_bits // 8
+    cbs = 2 * w.Hkv * E * dsub * 2
+    qo = 2 * w.B * w.Hq * 128 * 2
+    return idx + cbs + qo
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="vqkv_clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- cpu baseline (the oracle)
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_setup(max_tokens):
+    """Inputs of the oracle sample (built once per worker, not timed)."""
+    w = synth.WORKLOADS[WORKLOAD_ID]
+    s, kcb, vcb = calib.calibrate_head(w, 0, sample_tokens=512, iters=2)
+    _ORACLE_INPUTS.update(
+        s=s[None], kcb=kcb[None], vcb=vcb[None], q=synth.queries(w)[:, :w.g],
+        kc=synth.uniform_codes(w, 0, 0, 0, max_tokens), vc=synth.uniform_codes(w, 0, 0, 1, max_tokens))
+    return True
+
+
+def _oracle_decode_sample(n_tokens):
+    """Seconds the oracle takes for the g query heads of KV head 0 over n tokens."""
+    import oracle
+    d = _ORACLE_INPUTS
+    t0 = time.perf_counter()
+    oracle.decode_attention(d["q"], [[d["kc"][:n_tokens]]], [[d["vc"][:n_tokens]]], d["kcb"], d["vcb"], d["s"],
+                            np.array([n_tokens]))
+    return time.perf_counter() - t0
+
+
+def _oracle_worker(max_tokens):
+    import concurrent.futures
+    import multiprocessing
+    cores = os.cpu_count() or 1
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = str(cores)
+    ex = concurrent.futures.ProcessPoolExecutor(1, mp_context=multiprocessing.get_context("spawn"),
+                                                initializer=_oracle_setup, initargs=(max_tokens,))
+    return ex, cores
+
+
+def _size_sample(ex, seconds, lo=256, hi=196608):
+    t = ex.submit(_oracle_decode_sample, 2048).result()
+    n = int(min(hi, max(lo, 2048 * seconds / max(t, 1e-4))))
+    return max(16, n // 16 * 16)
+
+
+def cpu_baseline(budget_s=12.0):
+    """The oracle as it stands (fp64 numpy, the plain original-domain path) on
+    a bounded sample of the same workload: KV head 0's 4 query heads over the
+    first n tokens, n sized to about budget_s of host work."""
+    ex, cores = _oracle_worker(196608)
+    with ex:
+        n = _size_sample(ex, budget_s)
+        t = ex.submit(_oracle_decode_sample, n).result()
+    tok_s = n / (t * 8)    # the sample covers 1 of the 8 KV heads of each token
+    return {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"KV head 0 of 8 (its 4 query heads), first {n} of 196608 tokens, {t:.2f} s; "
+                      f"tokens/s scaled to all 8 KV heads"}
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores, each step a
+    bounded sample of the workload, the whole run kept to about 90 s."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[WORKLOAD_ID]
+    lens = synth.seq_lens(w)
+    total = args.steps + args.warmup
+    per_step = 90.0 / max(total, 1)
+    ex, cores = _oracle_worker(196608)
+    with ex:
+        n = _size_sample(ex, per_step, lo=16)
+        times = []
+        for i in range(total):
+            dt = ex.submit(_oracle_decode_sample, n).result()
+            if i >= args.warmup:
+                times.append(dt)
+    step_s = sum(times) / len(times)
+    value = n / (step_s * 8)
+    full_step_ms = 1e3 * int(lens.sum()) / value
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": f"first {n} tokens of KV head 0 (4 query heads) per step; "
+                                                 f"tokens/s scaled to the full 8-KV-head step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"KV head 0 (4 query heads), {n} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------- our arm
+
+def profile_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    try:
+        prof = json.load(open(PROFILE_JSON))
+    except (OSError, ValueError):
+        return None, None
+    src = open(os.path.join(ROOT, "vector_quantized_bit_gb300", "csrc", "decode.cu"), "rb").read()
+    if prof.get("decode_cu_sha256") != hashlib.sha256(src).hexdigest():
+        return None, prof.get("kernel")
+    return prof.get("dram_bytes_per_launch"), prof.get("kernel")
+
+
+def run_ours(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[WORKLOAD_ID]
+    lens = synth.seq_lens(w)
+    s_h, kcb_h, vcb_h, kv = host_workload(w)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    import torch
+    from vector_quantized_bit_gb300 import _build, _lib
+    _build.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    mode, cap = w.mode, w.cap_len
+    sb = _lib.vqkv_code_bytes(mode, cap)
+    s = torch.from_numpy(s_h).to(dev)
+    kcb = torch.from_numpy(kcb_h).to(dev)
+    vcb = torch.from_numpy(vcb_h).to(dev)
+    kcodes = torch.zeros((w.B, w.Hkv, sb), dtype=torch.uint8, device=dev)
+    vcodes = torch.zeros_like(kcodes)
+    zeros = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    # encode the whole cache (all KV heads, all 196,608 positions) in one call per K / V
+    for role, cb, codes in ((0, kcb, kcodes), (1, vcb, vcodes)):
+        x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
+        _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, cb, codes, cap)
+        del x
+    del kv
+    torch.cuda.synchronize()
+
+    # rotating copies of the cache so each step reads from HBM, not L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cache_bytes = 2 * kcodes.numel()
+    n_copies = max(2, math.ceil(3 * l2 / cache_bytes) + 1)
+    copies = [(kcodes, vcodes)] + [(kcodes.clone(), vcodes.clone()) for _ in range(n_copies - 1)]
+
+    q = torch.from_numpy(synth.queries(w)).to(dev)
+    new_k = torch.from_numpy(np.stack([synth.appended_keys(w, 0, h, 1) for h in range(w.Hkv)])[None]).to(dev)
+    new_v = torch.from_numpy(np.stack([synth.values(w, 0, h, w.seq_len, 1) for h in range(w.Hkv)])[None]).to(dev)
+    pos = torch.from_numpy((lens - 1).astype(np.int32)).to(dev)
+    seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
+    max_len = int(lens.max())
+    ws = _lib.decode_workspace(mode, w.B, w.Hq, w.Hkv, cap, max_len, device=dev)
+    dargs = _lib.decode_args(mode, q, kcodes, vcodes, seq, kcb, vcb, s, out, ws, cap, max_len)
+    n_splits = _lib.vqkv_decode_num_splits(dargs)
+
+    def step(i, ev=None):
+        kc, vc = copies[i % n_copies]
+        _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
+        _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
+        if ev is not None:
+            ev[0].record()
+        _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+        if ev is not None:
+            ev[1].record()
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        g_steps = GRAPH_STEPS - GRAPH_STEPS % n_copies if GRAPH_STEPS >= n_copies else n_copies
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(g_steps):
+                step(i)
+        one = []
+        for i in range(g_steps):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream):
+                step(i)
+            one.append(g1)
+        # instrumented graph: events around every decode launch
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(g_steps)]
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            for i in range(g_steps):
+                step(i, evs[i])
+        graph.replay()
+        torch.cuda.synchronize()
+
+        def run_steps(k):
+            full, rest = divmod(k, g_steps)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rest):
+                one[i].replay()
+
+        # time one replay to size the soak
+        t0 = time.perf_counter()
+        graph.replay()
+        torch.cuda.synchronize()
+        per_step = (time.perf_counter() - t0) / g_steps
+        soak = max(1, int(SOAK_S / per_step))
+
+        clocks = ClockSampler(local)
+        clocks.start()
+        run_steps(soak)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_steps(args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms_total = e0.elapsed_time(e1)
+        run_steps(soak)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        # dominant kernel: decode launch durations from the instrumented graph
+        graph_ev.replay()
+        torch.cuda.synchronize()
+        dec_ms = [a.elapsed_time(b) for a, b in evs]
+        dec_avg_ms = sum(dec_ms) / len(dec_ms)
+
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    # end to end through the public API: pinned host buffers, copies inside the timed region
+    q_host = torch.from_numpy(synth.queries(w)).pin_memory()
+    nk_host = new_k.cpu().pin_memory()
+    nv_host = new_v.cpu().pin_memory()
+    o_host = torch.empty((w.B, w.Hq, 128), dtype=torch.float16).pin_memory()
+    e2e_steps = max(20, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        def e2e_step(i):
+            kc, vc = copies[i % n_copies]
+            q.copy_(q_host, non_blocking=True)
+            new_k.copy_(nk_host, non_blocking=True)
+            new_v.copy_(nv_host, non_blocking=True)
+            _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
+            _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
+            _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+            o_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+        for i in range(10):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    tokens = int(lens.sum())
+    ms_step = ms_total / args.steps
+    value = world * tokens / (ms_step * 1e-3)
+    alg = algorithmic_bytes(w, lens)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    achieved = alg / (dec_avg_ms * 1e-3) / 1e9
+    traffic, _ = profile_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
+                   "bits": 2, "splits_per_kv_head": n_splits,
+                   "step": "encode 1 new K row + 1 new V row per sequence, then decode attention",
+                   "cache": "encoded on the GPU by vqkv_encode from seeded synthetic K/V",
+                   "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB > "
+                         f"{l2 / 1e6:.0f} MB L2)",
+                   "timing": f"CUDA graphs of {g_steps} steps, CUDA events on the launch stream",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "decode_vq2_kernel", "launch_ms": dec_avg_ms, "algorithmic_bytes": alg},
+        "clocks": clk,
+        "e2e": {"value": world * tokens / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
+                "d2h_bytes_per_step": out.numel() * 2,
+                "how": "public binding per step: H2D q and new K/V rows, 2 encodes, decode, D2H O, sync"},
+        "gpu_launches": 3 * args.steps,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

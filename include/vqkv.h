@@ -1,0 +1,188 @@
+/*
+ * vqkv.h — C ABI of the GB300 (sm_103a) VQ KV-cache library.
+ *
+ * The library implements the hot path of VecInfer ("VecInfer: Efficient LLM
+ * Inference with Low-Bit KV Cache via Outlier-Suppressed Vector
+ * Quantization"): keys are smoothed channel-wise and rotated by a Hadamard
+ * transform, every subvector of a key or value row is replaced by the index
+ * of its nearest codebook centroid, and decode attention runs directly on
+ * the packed indices with dequantisation fused into the score, softmax and
+ * P.V loop (paper summary page, "Summary"; codebook shapes 2^8 x 4 for
+ * 2 bit and 2^12 x 8 for 1.5 bit, "Key points"; the three stages
+ * preprocessing -> quantisation -> fused kernel, arXiv summary page,
+ * "方法详解").
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" point to memory on the current CUDA device and
+ *     are owned by the caller.  The library allocates nothing, keeps no
+ *     pointer after a call returns and holds no mutable global state beyond a
+ *     per-device cache of device attributes.
+ *   - fp16 data are passed as uint16_t bit patterns (IEEE binary16).
+ *   - head_dim must be 128.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns a status and launches nothing.  Work is enqueued
+ *     asynchronously on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream); no call synchronises the host.
+ *   - A launch failure returns VQKV_ERR_CUDA.  Conditions that can only be
+ *     seen on the device (a sequence length above max_seq_len, a cache
+ *     position outside the capacity) never fault: the kernel clamps or skips
+ *     and sets a bit in a caller-visible device error word.
+ *   - Calls on different streams may run concurrently as long as they do not
+ *     write the same buffers (workspaces included).
+ *
+ * Packed cache layout (the contract between vqkv_encode, vqkv_decode_attn and
+ * any reader).  Each (sequence b, KV head h) owns one K stream and one V
+ * stream of vqkv_code_bytes(mode, cap_len) bytes, at byte offset
+ * (b * Hkv + h) * vqkv_code_bytes(mode, cap_len) of the codes buffer.  A
+ * stream is a sequence of tiles; token t lives in tile t / TILE.
+ *
+ *   VQKV_MODE_VQ2 (256 entries x 4 dims, 8-bit codes, 32 codes per token):
+ *     TILE = 16 tokens, 512 bytes.  With r = t % 16 and subvector j (0..31):
+ *       K: byte 512*(t/16) + 16*(4*(r%8) + j%4) + 8*(r/8) + j/4
+ *       V: byte 512*(t/16) + 16*(4*(j%8) + (r%8)/2) + 4*(j/8) + 2*(r/8) + r%2
+ *     holds the code (0..255) of subvector j (channels 4j..4j+3) of token t.
+ *   VQKV_MODE_VQ15 (4096 entries x 8 dims, 12-bit codes, 16 codes per token):
+ *     the codes of subvectors p and p+8 (p = 0..7) of one token form a pair
+ *     stored in 3 bytes: b0 = c_p & 0xFF, b1 = (c_p >> 8) | ((c_{p+8} & 0xF) << 4),
+ *     b2 = c_{p+8} >> 4.  TILE = 64 tokens, 1536 bytes.  With
+ *     u = (t % 64) / 16 and r = t % 16, the first byte of pair p of token t is
+ *       K: 1536*(t/64) + 48*(4*(r%8) + p%4) + 12*u + 6*(r/8) + 3*(p/4)
+ *       V: 1536*(t/64) + 48*(4*p + (r%8)/2) + 12*u + 3*((r%2) + 2*(r/8))
+ *   Both layouts are token-local: writing token t changes no byte of any other
+ *   token.  Bits per element: 512*8/(16*128) = 2 and 1536*8/(64*128) = 1.5.
+ *   (The layouts place, for each of the 32 lanes of a warp, the codes that
+ *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2)
+ *   or 48-byte (VQ15) run, so a warp reads a tile with coalesced 128-bit
+ *   loads.)
+ */
+#ifndef VQKV_H
+#define VQKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VQKV_OK = 0,
+  VQKV_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size, a misaligned pointer */
+  VQKV_ERR_UNSUPPORTED = 2,   /* head_dim != 128, GQA group above 8, unknown mode */
+  VQKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+  VQKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  VQKV_ERR_NO_DEVICE = 5      /* no usable CUDA device / device query failed */
+} vqkv_status;
+
+typedef enum {
+  VQKV_MODE_VQ2 = 0,   /* 2 bit:   2^8 entries x 4 dims, 8-bit codes  */
+  VQKV_MODE_VQ15 = 1   /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
+} vqkv_mode;
+
+typedef enum {
+  VQKV_ROLE_K = 0,     /* keys: x' = (x / s) . Hn before the search       */
+  VQKV_ROLE_V = 1      /* values: quantised as they are                   */
+} vqkv_role;
+
+/* Bits of the device error word (see error_flags / workspace word 0). */
+#define VQKV_DEVERR_SEQ_LEN   0x1u  /* a seq_lens[b] outside [0, max_seq_len]: clamped */
+#define VQKV_DEVERR_POSITION  0x2u  /* an encode row outside [0, cap_len): not written */
+
+/*
+ * vqkv_encode — smoothing, Hadamard rotation, nearest-centroid assignment and
+ * packing of new K or V rows (paper summary page, "Summary": channel-wise
+ * smoothing followed by a Hadamard rotation of the keys, K-Means codebook;
+ * arXiv summary page, "方法详解", stages 1-2).
+ *
+ * For row n (0 <= n < n_rows) of sequence b and KV head h:
+ *   role K: y = x / s[h] (per channel), x' = y . Hn with Hn = H/sqrt(128),
+ *           H[i][k] = (-1)^popcount(i & k), x' rounded to fp32;
+ *   role V: x' = x.
+ *   For each subvector j of x' (d_sub = 4 or 8 channels) the code is
+ *   argmin_c sum_i (x'_{j,i} - C[h][c][i])^2 over the KV head's codebook C,
+ *   decided on fp32 distances with ties to the lowest index, and is written
+ *   at cache position pos[b] + n of stream (b, h) in the layout above.
+ */
+typedef struct {
+  int32_t mode;        /* vqkv_mode */
+  int32_t role;        /* vqkv_role */
+  int32_t B;           /* sequences, >= 0 (0: nothing to do) */
+  int32_t Hkv;         /* KV heads, >= 1 */
+  int32_t head_dim;    /* must be 128 */
+  int32_t n_rows;      /* rows per (sequence, KV head) to encode, >= 0 */
+  int32_t cap_len;     /* cache capacity in tokens, >= 1 */
+  const uint16_t* x;          /* device fp16 [B][Hkv][n_rows][128], 8-byte aligned */
+  const int32_t* pos;         /* device [B]: position of row 0 of each sequence */
+  const float* s;             /* device fp32 [Hkv][128], > 0; role K only (NULL for V) */
+  const uint16_t* codebook;   /* device fp16 [Hkv][E][d_sub], 16-byte aligned, finite */
+  uint8_t* codes;             /* device [B][Hkv][vqkv_code_bytes(mode, cap_len)] */
+  unsigned long long* near_tie_count; /* device, optional: += subvectors whose best and
+                                         second-best fp32 distances differ by less than
+                                         1e-6 relative */
+  uint32_t* error_flags;      /* device, optional: VQKV_DEVERR_POSITION is or-ed in when a
+                                 row's position is outside [0, cap_len) (row not written) */
+} vqkv_encode_args;
+
+/*
+ * vqkv_decode_attn — single-query decode attention straight from the packed
+ * cache (paper summary page, "Summary": dequantisation inside the attention
+ * computation; arXiv summary page, "方法详解", stage 3; the query gets the
+ * matching inverse transform so scores are unchanged).
+ *
+ * For sequence b and query head hq (KV head h = hq / (Hq / Hkv)):
+ *   q' = (q ⊙ s[h]) . Hn,  score_t = softmax_scale * q' . K'_t,
+ *   O = sum_t softmax(score)_t V_t over t < seq_lens[b],
+ * where K'_t and V_t are the concatenated centroids of token t's codes.
+ * fp32 accumulation, fp16 output; seq_lens[b] == 0 gives a zero row.
+ * The sequence is split across CTAs (split-KV); the last CTA of each
+ * (b, KV head) merges the partial softmax states and writes O.
+ */
+typedef struct {
+  int32_t mode;          /* vqkv_mode */
+  int32_t B;             /* sequences, >= 0 (0: nothing to do) */
+  int32_t Hq;            /* query heads, multiple of Hkv, Hq/Hkv <= 8 */
+  int32_t Hkv;           /* KV heads, >= 1 */
+  int32_t head_dim;      /* must be 128 */
+  int32_t cap_len;       /* cache capacity in tokens (stream size), >= 1 */
+  int32_t max_seq_len;   /* upper bound of seq_lens, 0 <= max_seq_len <= cap_len */
+  const uint16_t* q;          /* device fp16 [B][Hq][128], 8-byte aligned */
+  const uint8_t* k_codes;     /* device [B][Hkv][vqkv_code_bytes], 16-byte aligned */
+  const uint8_t* v_codes;     /* device [B][Hkv][vqkv_code_bytes], 16-byte aligned */
+  const int32_t* seq_lens;    /* device [B] */
+  const uint16_t* k_codebook; /* device fp16 [Hkv][E][d_sub], 16-byte aligned, finite */
+  const uint16_t* v_codebook; /* device fp16 [Hkv][E][d_sub], 16-byte aligned, finite */
+  const float* s;             /* device fp32 [Hkv][128] key smoothing factors, > 0 */
+  float softmax_scale;   /* <= 0 selects 1/sqrt(head_dim) */
+  int32_t num_splits;    /* CTAs per (sequence, KV head); 0 = planned automatically */
+  void* workspace;       /* device, >= vqkv_decode_workspace_bytes(args), 256-byte aligned,
+                            zero-filled before its first use; every completed call leaves
+                            it ready for the next.  Word 0 (uint32) is the device error
+                            word (VQKV_DEVERR_SEQ_LEN; sticky, the caller may clear it) */
+  size_t workspace_bytes;
+  uint16_t* out;         /* device fp16 [B][Hq][128] */
+} vqkv_decode_args;
+
+/* Bytes of one cache stream (one of K or V of one (sequence, KV head)):
+ * ceil(cap_len / TILE) * tile bytes; 0 for an unknown mode or cap_len < 0. */
+size_t vqkv_code_bytes(int32_t mode, int32_t cap_len);
+
+/* Workspace bytes vqkv_decode_attn needs for these arguments (the same split
+ * plan the call will use on the current device); 0 when the arguments are
+ * invalid. */
+size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* args);
+
+/* CTAs per (sequence, KV head) vqkv_decode_attn will use on the current
+ * device (for the caller's bookkeeping); -1 when the arguments are invalid. */
+int32_t vqkv_decode_num_splits(const vqkv_decode_args* args);
+
+vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);
+vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
+
+/* Static, never NULL. */
+const char* vqkv_status_string(vqkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQKV_H */

@@ -1,0 +1,138 @@
+"""The C-ABI library builds, loads and exports what include/vqkv.h declares;
+argument validation that happens before any CUDA call.  No GPU needed."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+from vector_quantized_bit_gb300 import _build, _lib
+
+HEADER = os.path.join(ROOT, "include", "vqkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vqkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTED), names
+    nm = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (vqkv_\w+)", nm))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_struct_layout_matches_header(tmp_path):
+    """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
+    fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
+    for cname, cls in fields.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0;}")
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)], check=True)
+    out = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                              check=True).stdout.split("\n") if line)
+    for cname, cls in fields.items():
+        assert int(out[cname]) == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert int(out[f"{cname}.{f}"]) == getattr(cls, f).offset, (cname, f)
+
+
+def test_code_bytes(lib):
+    assert lib.vqkv_code_bytes(0, 196608) == 196608 * 32
+    assert lib.vqkv_code_bytes(1, 65536) == 65536 * 24
+    assert lib.vqkv_code_bytes(0, 1) == 512
+    assert lib.vqkv_code_bytes(1, 65) == 3072
+    assert lib.vqkv_code_bytes(7, 16) == 0
+    assert lib.vqkv_code_bytes(0, -1) == 0
+
+
+def _dec(**kw):
+    a = _lib.DecodeArgs(mode=0, B=1, Hq=4, Hkv=1, head_dim=128, cap_len=64, max_seq_len=64,
+                        q=0x1000, k_codes=0x2000, v_codes=0x3000, seq_lens=0x4000, k_codebook=0x5000,
+                        v_codebook=0x6000, s=0x7000, softmax_scale=0.0, num_splits=0, workspace=0x8000,
+                        workspace_bytes=1 << 20, out=0x9000)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _enc(**kw):
+    a = _lib.EncodeArgs(mode=0, role=0, B=1, Hkv=1, head_dim=128, n_rows=4, cap_len=64, x=0x1000,
+                        pos=0x2000, s=0x3000, codebook=0x4000, codes=0x5000)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2), (dict(mode=3), 2), (dict(Hq=36, Hkv=4), 2), (dict(Hq=6, Hkv=4), 1),
+    (dict(Hkv=0), 1), (dict(B=-1), 1), (dict(max_seq_len=65), 1), (dict(max_seq_len=-1), 1),
+    (dict(cap_len=0, max_seq_len=0), 1), (dict(q=None), 1), (dict(k_codes=None), 1), (dict(s=None), 1),
+    (dict(out=None), 1), (dict(k_codes=0x2008), 1), (dict(k_codebook=0x5004), 1), (dict(q=0x1002), 1),
+    (dict(num_splits=-2), 1), (dict(softmax_scale=float("nan")), 1),
+])
+def test_decode_validation(lib, kw, status):
+    assert lib.vqkv_decode_attn(ctypes.byref(_dec(**kw)), None) == status
+    assert lib.vqkv_decode_workspace_bytes(ctypes.byref(_dec(**kw))) == 0
+    assert lib.vqkv_decode_num_splits(ctypes.byref(_dec(**kw))) == -1
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    # B == 0: nothing to validate beyond the sizes, nothing launched
+    assert lib.vqkv_decode_attn(ctypes.byref(_dec(B=0, q=None, out=None)), None) == 0
+
+
+def test_null_args(lib):
+    assert lib.vqkv_decode_attn(None, None) == 1
+    assert lib.vqkv_encode(None, None) == 1
+    assert lib.vqkv_decode_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=256), 2), (dict(mode=2), 2), (dict(role=2), 1), (dict(Hkv=0), 1), (dict(n_rows=-1), 1),
+    (dict(cap_len=0), 1), (dict(x=None), 1), (dict(pos=None), 1), (dict(codebook=None), 1),
+    (dict(codes=None), 1), (dict(s=None), 1), (dict(x=0x1004), 1), (dict(codebook=0x4008), 1),
+])
+def test_encode_validation(lib, kw, status):
+    assert lib.vqkv_encode(ctypes.byref(_enc(**kw)), None) == status
+
+
+def test_encode_empty_is_a_no_op(lib):
+    assert lib.vqkv_encode(ctypes.byref(_enc(n_rows=0, x=None)), None) == 0
+    assert lib.vqkv_encode(ctypes.byref(_enc(B=0, x=None)), None) == 0
+    # values need no smoothing vector
+    assert lib.vqkv_encode(ctypes.byref(_enc(role=1, s=None, n_rows=0)), None) == 0
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert lib.vqkv_status_string(st)
+    assert lib.vqkv_status_string(99) == b"unknown status"
+
+
+def test_product_path_has_no_cpu_fallback(monkeypatch, tmp_path):
+    """Without the built library the binding raises instead of computing."""
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib(str(tmp_path / "missing.so"))
+    src = open(_lib.__file__).read() + open(os.path.join(ROOT, "vector_quantized_bit_gb300", "__init__.py")).read()
+    assert "oracle" not in src.replace("no fallback", "")

@@ -1,0 +1,163 @@
+"""Encode parity: codes from the CUDA path (through the C ABI) against the
+oracle's nearest-centroid codes — bit-exact, except near-ties (oracle fp32
+distances within 1e-6 relative), which are counted."""
+import numpy as np
+import pytest
+
+from oracle import vqkv_oracle as vo
+from tests import helpers as H
+from vector_quantized_bit_gb300 import _build, _lib, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def unpack_all(mode, role, buf, L):
+    B, Hkv = buf.shape[:2]
+    return [[vo.unpack_stream_fast(buf[b, h], mode, role, L) for h in range(Hkv)] for b in range(B)]
+
+
+def compare(mode, role, x, s, cb, gpu_buf, pos, n_rows):
+    """Oracle-encode every row and compare with the GPU stream bytes."""
+    B, Hkv = x.shape[:2]
+    ties = fails = 0
+    for b in range(B):
+        for h in range(Hkv):
+            ref, d32 = vo.encode_rows(x[b, h], role, s[h] if s is not None else None, cb[h])
+            got = vo.unpack_stream_fast(gpu_buf[b, h], mode, role, pos[b] + n_rows)[pos[b]:pos[b] + n_rows]
+            t, f = H.check_codes(got, ref, d32)
+            ties += t
+            fails += f
+    return ties, fails
+
+
+def test_tiny_config_keys_and_values():
+    w = synth.WORKLOADS[0]
+    s, kcb, vcb = H.calibrate(w)
+    k = synth.keys(w, 0, 0, 0, w.seq_len)[None, None]
+    v = synth.values(w, 0, 0, 0, w.seq_len)[None, None]
+    for role, x, cb in ((vo.ROLE_K, k, kcb), (vo.ROLE_V, v, vcb)):
+        buf, nties, err = H.gpu_encode(0, role, x, [0], s if role == 0 else None, cb, w.cap_len, with_ties=True)
+        assert err == 0
+        ties, fails = compare(0, role, x, s if role == 0 else None, cb, buf, [0], w.seq_len)
+        assert fails == 0, (role, ties, fails)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("role", [0, 1])
+def test_ragged_positions_multi_head(mode, role):
+    w = synth.WORKLOADS[3 if mode else 1].scaled(seq_len=2048, cap_len=2048)
+    kw = dict(sample_tokens=512, iters=3) if mode else dict(sample_tokens=512, iters=5)
+    s, kcb, vcb = H.calibrate(w.scaled(Hkv=2), **kw)
+    cb = kcb if role == 0 else vcb
+    n = 37
+    x = np.stack([np.stack([(synth.keys if role == 0 else synth.values)(w, b, h, 100, n) for h in range(2)])
+                  for b in range(3)])
+    pos = [0, 5, 130]
+    cap = 200
+    prefill = np.random.default_rng(0).integers(0, 256, size=(3, 2, vo.code_bytes(mode, cap)), dtype=np.uint8)
+    buf = H.gpu_encode(mode, role, x, pos, s if role == 0 else None, cb, cap, codes=prefill)
+    ties, fails = compare(mode, role, x, s if role == 0 else None, cb, buf, pos, n)
+    assert fails == 0, (ties, fails)
+    # bytes of tokens outside [pos, pos+n) are untouched
+    for b in range(3):
+        for h in range(2):
+            L = vo.TILE_TOKENS[mode] * (-(-cap // vo.TILE_TOKENS[mode]))
+            off = vo.offset_table(mode, role, L)
+            if mode == 0:
+                touched = off[pos[b]:pos[b] + n].reshape(-1)
+            else:
+                touched = (off[pos[b]:pos[b] + n, :, None] + np.arange(3)).reshape(-1)
+            mask = np.ones(buf.shape[2], dtype=bool)
+            mask[touched] = False
+            assert np.array_equal(buf[b, h][mask], prefill[b, h][mask])
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_positions_out_of_range_are_skipped_and_reported(mode):
+    s, kcb, vcb = H.random_codebooks(mode, 1, 3)
+    x = np.random.default_rng(1).standard_normal((2, 1, 4, 128)).astype(np.float16)
+    cap = 64
+    prefill = np.full((2, 1, vo.code_bytes(mode, cap)), 0xA5, dtype=np.uint8)
+    buf, _, err = H.gpu_encode(mode, 0, x, [62, -3], s, kcb, cap, codes=prefill, with_ties=True)
+    assert err & _lib.VQKV_DEVERR_POSITION
+    # sequence 0: rows at 62, 63 written; 64, 65 skipped.  sequence 1: rows at -3..-1 skipped, 0 written
+    got0 = vo.unpack_stream_fast(buf[0, 0], mode, 0, 64)
+    ref0, d0 = vo.encode_rows(x[0, 0], 0, s[0], kcb[0])
+    assert H.check_codes(got0[62:64], ref0[:2], d0[:2])[1] == 0
+    changed = np.flatnonzero(buf[1, 0] != 0xA5)
+    off = vo.offset_table(mode, 0, 1)
+    allowed = off.reshape(-1) if mode == 0 else (off[..., None] + np.arange(3)).reshape(-1)
+    assert set(changed.tolist()) <= set(allowed.tolist())
+
+
+def test_encode_then_decode_matches_oracle_pipeline():
+    """GPU encode + GPU decode against oracle encode + oracle decode."""
+    w = synth.WORKLOADS[1].scaled(seq_len=3000, cap_len=3008)
+    wh = w.scaled(Hkv=2, Hq=8)
+    s, kcb, vcb = H.calibrate(wh, sample_tokens=1024, iters=5)
+    k = np.stack([synth.keys(w, 0, h, 0, w.seq_len) for h in range(2)])[None]
+    v = np.stack([synth.values(w, 0, h, 0, w.seq_len) for h in range(2)])[None]
+    kbuf = H.gpu_encode(0, 0, k, [0], s, kcb, w.cap_len)
+    vbuf = H.gpu_encode(0, 1, v, [0], None, vcb, w.cap_len)
+    q = synth.queries(wh)
+    o = H.gpu_decode(0, q, kbuf, vbuf, [w.seq_len], kcb, vcb, s, w.cap_len, w.seq_len)
+    kc = [[vo.encode_rows(k[0, h], 0, s[h], kcb[h])[0] for h in range(2)]]
+    vc = [[vo.encode_rows(v[0, h], 1, None, vcb[h])[0] for h in range(2)]]
+    ref = vo.decode_attention(q, kc, vc, kcb, vcb, s, [w.seq_len])
+    assert vo.o_error(o, ref).max() <= H.O_TOL
+
+
+def test_near_tie_counter_counts_exact_ties():
+    """Two identical centroids make every subvector nearest to them a tie."""
+    s, kcb, vcb = H.random_codebooks(0, 1, 5)
+    vcb[0, 7] = vcb[0, 3]
+    x = np.tile(vcb[0, 3].astype(np.float16), 32)[None, None, None]   # one V row of centroid 3
+    buf, nties, err = H.gpu_encode(0, 1, x, [0], None, vcb, 16, with_ties=True)
+    assert nties == 32 and err == 0
+    assert np.all(vo.unpack_stream_fast(buf[0, 0], 0, 1, 1) == 3)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [0, 1])
+def test_full_size_prefill_and_append_sampled(mode):
+    """Mistral-7B-shaped encode at full size (16 sequences x 8 KV heads x
+    16,384 prefill rows, then 256 appended rows at positions 16,384..16,639),
+    launched as one call each; the oracle re-encodes sampled rows."""
+    w = synth.WORKLOADS[4].with_mode(mode)
+    kw = dict(sample_tokens=2048, iters=2) if mode else dict(sample_tokens=2048, iters=10)
+    s, kcb, vcb = H.calibrate(w, **kw)
+    import torch
+    sb = vo.code_bytes(mode, w.cap_len)
+    kcodes = torch.zeros((w.B, w.Hkv, sb), dtype=torch.uint8, device="cuda")
+    r = np.random.default_rng(mode)
+    samples = [(int(r.integers(w.B)), int(r.integers(w.Hkv)), int(r.integers(w.prefill))) for _ in range(48)]
+    samples += [(w.B - 1, w.Hkv - 1, w.prefill - 1)]
+    # generate the prefill one sequence at a time (host memory), encode in one call per sequence batch
+    x = np.empty((w.B, w.Hkv, w.prefill, 128), dtype=np.float16)
+    with H.pool() as ex:
+        futs = {(b, h): ex.submit(synth.keys, w, b, h, 0, w.prefill) for b in range(w.B) for h in range(w.Hkv)}
+        for (b, h), f in futs.items():
+            x[b, h] = f.result()
+    ties = H.torch().zeros(1, dtype=torch.int64, device="cuda")
+    _lib.vqkv_encode(mode, 0, H.dev(x), H.dev(np.zeros(w.B, np.int32)), H.dev(s), H.dev(kcb), kcodes, w.cap_len,
+                     near_tie_count=ties)
+    app = np.stack([np.stack([synth.appended_keys(w, b, h, w.append) for h in range(w.Hkv)]) for b in range(w.B)])
+    _lib.vqkv_encode(mode, 0, H.dev(app), H.dev(np.full(w.B, w.prefill, np.int32)), H.dev(s), H.dev(kcb), kcodes,
+                     w.cap_len, near_tie_count=ties)
+    torch.cuda.synchronize()
+    buf = kcodes.cpu().numpy()
+    fails = 0
+    for b, h, t in samples:
+        for row, tt in ((x[b, h, t:t + 1], t), (app[b, h, t % w.append:t % w.append + 1], w.prefill + t % w.append)):
+            ref, d32 = vo.encode_rows(row, 0, s[h], kcb[h])
+            got = vo.unpack_stream_fast(buf[b, h], mode, 0, tt + 1)[tt:tt + 1]
+            _, f = H.check_codes(got, ref, d32)
+            fails += f
+    assert fails == 0

@@ -1,0 +1,172 @@
+"""ctypes binding of libvqkv (include/vqkv.h): argument marshalling only.
+
+Every function here forwards to the C ABI; all arithmetic of the hot path
+runs in the CUDA kernels of the library.  The library must have been built
+(``vector_quantized_bit_gb300._build.build()``): there is no fallback, and a
+missing library raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+VQKV_MODE_VQ2 = 0
+VQKV_MODE_VQ15 = 1
+VQKV_ROLE_K = 0
+VQKV_ROLE_V = 1
+VQKV_DEVERR_SEQ_LEN = 0x1
+VQKV_DEVERR_POSITION = 0x2
+
+STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3: "VQKV_ERR_WORKSPACE",
+          4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
+
+EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_encode",
+            "vqkv_decode_attn", "vqkv_status_string"]
+
+
+class VqkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({string(status)})")
+
+
+class EncodeArgs(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("role", ctypes.c_int32), ("B", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("n_rows", ctypes.c_int32),
+                ("cap_len", ctypes.c_int32), ("x", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("s", ctypes.c_void_p), ("codebook", ctypes.c_void_p), ("codes", ctypes.c_void_p),
+                ("near_tie_count", ctypes.c_void_p), ("error_flags", ctypes.c_void_p)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("B", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("cap_len", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("q", ctypes.c_void_p), ("k_codes", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("k_codebook", ctypes.c_void_p),
+                ("v_codebook", ctypes.c_void_p), ("s", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
+                ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded library (built in-tree); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libvqkv is not built ({path} missing); run __graft_entry__.build()")
+        # make sure the CUDA runtime PyTorch ships is loaded first, so the
+        # library binds to the same libcudart (one runtime per process)
+        try:
+            import torch  # noqa: F401
+        except ImportError:
+            pass
+        L = ctypes.CDLL(path)
+        L.vqkv_code_bytes.restype = ctypes.c_size_t
+        L.vqkv_code_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        L.vqkv_decode_workspace_bytes.restype = ctypes.c_size_t
+        L.vqkv_decode_workspace_bytes.argtypes = [ctypes.POINTER(DecodeArgs)]
+        L.vqkv_decode_num_splits.restype = ctypes.c_int32
+        L.vqkv_decode_num_splits.argtypes = [ctypes.POINTER(DecodeArgs)]
+        L.vqkv_encode.restype = ctypes.c_int
+        L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
+        L.vqkv_decode_attn.restype = ctypes.c_int
+        L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_status_string.restype = ctypes.c_char_p
+        L.vqkv_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def string(status: int) -> str:
+    return lib().vqkv_status_string(status).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def vqkv_code_bytes(mode: int, cap_len: int) -> int:
+    return int(lib().vqkv_code_bytes(mode, cap_len))
+
+
+def encode_args(mode, role, x, pos, s, codebook, codes, cap_len, near_tie_count=None, error_flags=None):
+    B, Hkv, n_rows, D = (x.shape if x is not None else (0, codebook.shape[0], 0, 128))
+    return EncodeArgs(mode=mode, role=role, B=B, Hkv=Hkv, head_dim=D, n_rows=n_rows, cap_len=cap_len,
+                      x=_ptr(x), pos=_ptr(pos), s=_ptr(s), codebook=_ptr(codebook), codes=_ptr(codes),
+                      near_tie_count=_ptr(near_tie_count), error_flags=_ptr(error_flags))
+
+
+def vqkv_encode(mode, role, x, pos, s, codebook, codes, cap_len, near_tie_count=None, error_flags=None,
+                stream=None) -> None:
+    """Quantise rows x [B][Hkv][n_rows][128] (fp16, device) into ``codes``.
+
+    pos int32 [B]; s fp32 [Hkv][128] (keys) or None; codebook fp16 [Hkv][E][d_sub];
+    codes uint8 [B][Hkv][vqkv_code_bytes(mode, cap_len)].
+    """
+    a = encode_args(mode, role, x, pos, s, codebook, codes, cap_len, near_tie_count, error_flags)
+    st = lib().vqkv_encode(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_encode")
+
+
+def decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,
+                max_seq_len, softmax_scale=0.0, num_splits=0, workspace_bytes=None):
+    B, Hq, D = q.shape
+    Hkv = k_codebook.shape[0]
+    wb = workspace_bytes if workspace_bytes is not None else (
+        workspace.numel() * workspace.element_size() if workspace is not None else 0)
+    return DecodeArgs(mode=mode, B=B, Hq=Hq, Hkv=Hkv, head_dim=D, cap_len=cap_len, max_seq_len=max_seq_len,
+                      q=_ptr(q), k_codes=_ptr(k_codes), v_codes=_ptr(v_codes), seq_lens=_ptr(seq_lens),
+                      k_codebook=_ptr(k_codebook), v_codebook=_ptr(v_codebook), s=_ptr(s),
+                      softmax_scale=softmax_scale, num_splits=num_splits, workspace=_ptr(workspace),
+                      workspace_bytes=wb, out=_ptr(out))
+
+
+def vqkv_decode_workspace_bytes(args: DecodeArgs) -> int:
+    return int(lib().vqkv_decode_workspace_bytes(ctypes.byref(args)))
+
+
+def vqkv_decode_num_splits(args: DecodeArgs) -> int:
+    return int(lib().vqkv_decode_num_splits(ctypes.byref(args)))
+
+
+def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace,
+                     cap_len, max_seq_len, softmax_scale=0.0, num_splits=0, stream=None) -> None:
+    """O = decode attention of q [B][Hq][128] (fp16) over the packed cache.
+
+    Writes ``out`` (fp16 [B][Hq][128]).  ``workspace``: a zero-initialised
+    device buffer of at least vqkv_decode_workspace_bytes bytes.
+    """
+    a = decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,
+                    max_seq_len, softmax_scale, num_splits)
+    st = lib().vqkv_decode_attn(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_attn")
+
+
+def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda"):
+    """A zero-filled workspace tensor of the size the decode call needs."""
+    import torch
+    a = DecodeArgs(mode=mode, B=B, Hq=Hq, Hkv=Hkv, head_dim=128, cap_len=cap_len, max_seq_len=max_seq_len,
+                   num_splits=num_splits)
+    n = vqkv_decode_workspace_bytes(a)
+    if n == 0:
+        raise VqkvError(1, "vqkv_decode_workspace_bytes")
+    return torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=device)

@@ -1,0 +1,247 @@
+// Host side of the C ABI declared in include/vqkv.h: argument validation,
+// the split-KV plan, workspace layout and kernel launches.  Nothing here
+// allocates device memory or synchronises the host.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "vqkv.h"
+
+namespace vqkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kWsHeader = 256;   // word 0: device error flags
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int decode_bpsm[2] = {0, 0};   // resident decode CTAs per SM, per mode
+  int encode_bpsm[2] = {0, 0};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device attributes, queried once (kernel attributes set here too).
+vqkv_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VQKV_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return VQKV_ERR_NO_DEVICE;
+    for (int m = 0; m < 2; ++m) {
+      if (decode_prepare(m) != cudaSuccess || encode_prepare(m) != cudaSuccess) return VQKV_ERR_CUDA;
+      if (decode_occupancy(m, &d.decode_bpsm[m]) != cudaSuccess) return VQKV_ERR_CUDA;
+      if (encode_occupancy(m, &d.encode_bpsm[m]) != cudaSuccess) return VQKV_ERR_CUDA;
+      if (d.decode_bpsm[m] < 1) d.decode_bpsm[m] = 1;
+      if (d.encode_bpsm[m] < 1) d.encode_bpsm[m] = 1;
+    }
+    d.ready = true;
+  }
+  *out = d;
+  return VQKV_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+vqkv_status validate_decode(const vqkv_decode_args* a) {
+  if (a == nullptr) return VQKV_ERR_INVALID_ARG;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
+  if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq / a->Hkv > 8) return VQKV_ERR_UNSUPPORTED;
+  if (a->max_seq_len < 0 || a->max_seq_len > a->cap_len) return VQKV_ERR_INVALID_ARG;
+  if (a->num_splits < 0) return VQKV_ERR_INVALID_ARG;
+  if (!(std::isfinite(a->softmax_scale))) return VQKV_ERR_INVALID_ARG;
+  if (a->B == 0) return VQKV_OK;
+  if (!a->q || !a->k_codes || !a->v_codes || !a->seq_lens || !a->k_codebook || !a->v_codebook || !a->s ||
+      !a->out)
+    return VQKV_ERR_INVALID_ARG;
+  if (!aligned(a->q, 8) || !aligned(a->k_codes, 16) || !aligned(a->v_codes, 16) || !aligned(a->k_codebook, 16) ||
+      !aligned(a->v_codebook, 16) || !aligned(a->s, 16) || !aligned(a->seq_lens, 4) || !aligned(a->out, 2))
+    return VQKV_ERR_INVALID_ARG;
+  return VQKV_OK;
+}
+
+struct DecodePlan {
+  int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1;
+  size_t tickets_off = 0, partials_off = 0, ws_bytes = 0;
+};
+
+// Split-KV plan.  Work is (sequence group, KV head, split); every CTA of a
+// split processes `tps` tiles of each sequence in its group.  The plan picks
+// the split count that minimises (waves of CTAs) x (tiles per CTA + a fixed
+// per-CTA setup cost), assuming full-length sequences; short sequences make
+// some CTAs finish early, which the hardware scheduler backfills.
+vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
+  DeviceInfo di;
+  vqkv_status st = device_info(&di);
+  if (st != VQKV_OK) return st;
+  const int T = decode_tile_tokens(a->mode);
+  const int g = a->Hq / a->Hkv;
+  const long long tiles_max = std::max(1, (a->max_seq_len + T - 1) / T);
+  const long long slots = (long long)di.sms * di.decode_bpsm[a->mode];
+  const int B = std::max(a->B, 1);
+  // 1.5-bit CTAs load 128 KB of codebooks: keep one CTA per KV head and split
+  // across sequences only when the batch alone cannot fill the GPU.
+  int bpg = 1;
+  if (a->mode == VQKV_MODE_VQ15 && (long long)B * a->Hkv < slots) bpg = B;
+  const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg);
+  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 6.0 : 24.0;   // per-CTA prologue in tile units
+  long long best_n = 1;
+  double best_cost = 1e300;
+  if (a->num_splits > 0) {
+    best_n = std::min<long long>(a->num_splits, tiles_max);
+  } else {
+    const long long n_hi = std::min<long long>(tiles_max, 4 * ((slots + pairs - 1) / pairs) + 64);
+    for (long long n = 1; n <= n_hi; ++n) {
+      const long long tps = (tiles_max + n - 1) / n;
+      const long long waves = (pairs * n + slots - 1) / slots;
+      const double cost = (double)waves * ((double)tps * bpg + setup_tiles);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_n = n;
+      }
+    }
+  }
+  const long long tps = (tiles_max + best_n - 1) / best_n;
+  pl->tps = (int)tps;
+  pl->n_splits = (int)((tiles_max + tps - 1) / tps);
+  pl->bpg = bpg;
+  pl->n_bgroups = (B + bpg - 1) / bpg;
+  pl->tickets_off = kWsHeader;
+  pl->partials_off = round_up(kWsHeader + sizeof(unsigned) * (size_t)B * a->Hkv, 256);
+  pl->ws_bytes = pl->partials_off +
+                 sizeof(float) * (size_t)B * a->Hkv * pl->n_splits * g * kPartialStride;
+  return VQKV_OK;
+}
+
+vqkv_status validate_encode(const vqkv_encode_args* a) {
+  if (a == nullptr) return VQKV_ERR_INVALID_ARG;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->role != VQKV_ROLE_K && a->role != VQKV_ROLE_V) return VQKV_ERR_INVALID_ARG;
+  if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
+  if (a->B < 0 || a->Hkv < 1 || a->n_rows < 0 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
+  if (a->B == 0 || a->n_rows == 0) return VQKV_OK;
+  if (!a->x || !a->pos || !a->codebook || !a->codes) return VQKV_ERR_INVALID_ARG;
+  if (a->role == VQKV_ROLE_K && !a->s) return VQKV_ERR_INVALID_ARG;
+  if (!aligned(a->x, 8) || !aligned(a->codebook, 16) || !aligned(a->pos, 4) ||
+      (a->role == VQKV_ROLE_K && !aligned(a->s, 16)) || (a->near_tie_count && !aligned(a->near_tie_count, 8)) ||
+      (a->error_flags && !aligned(a->error_flags, 4)))
+    return VQKV_ERR_INVALID_ARG;
+  if ((long long)a->B * a->n_rows > 0x7fffffffLL) return VQKV_ERR_INVALID_ARG;
+  return VQKV_OK;
+}
+
+}  // namespace
+}  // namespace vqkv
+
+using namespace vqkv;
+
+extern "C" {
+
+size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
+  if (cap_len < 0) return 0;
+  if (mode == VQKV_MODE_VQ2) return (size_t)((cap_len + 15) / 16) * 512;
+  if (mode == VQKV_MODE_VQ15) return (size_t)((cap_len + 63) / 64) * 1536;
+  return 0;
+}
+
+size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* a) {
+  if (validate_decode(a) != VQKV_OK) return 0;
+  DecodePlan pl;
+  if (plan_decode(a, &pl) != VQKV_OK) return 0;
+  return pl.ws_bytes;
+}
+
+int32_t vqkv_decode_num_splits(const vqkv_decode_args* a) {
+  if (validate_decode(a) != VQKV_OK) return -1;
+  DecodePlan pl;
+  if (plan_decode(a, &pl) != VQKV_OK) return -1;
+  return pl.n_splits;
+}
+
+vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
+  vqkv_status st = validate_decode(a);
+  if (st != VQKV_OK || a->B == 0) return st;
+  DecodePlan pl;
+  st = plan_decode(a, &pl);
+  if (st != VQKV_OK) return st;
+  if (a->workspace == nullptr || a->workspace_bytes < pl.ws_bytes) return VQKV_ERR_WORKSPACE;
+  if (!aligned(a->workspace, 256)) return VQKV_ERR_INVALID_ARG;
+  DecodeParams p;
+  unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+  p.q = reinterpret_cast<const __half*>(a->q);
+  p.kc = a->k_codes;
+  p.vc = a->v_codes;
+  p.seq_lens = a->seq_lens;
+  p.kcb = reinterpret_cast<const __half*>(a->k_codebook);
+  p.vcb = reinterpret_cast<const __half*>(a->v_codebook);
+  p.s = a->s;
+  p.out = reinterpret_cast<__half*>(a->out);
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.tickets = reinterpret_cast<unsigned*>(ws + pl.tickets_off);
+  p.partials = reinterpret_cast<float*>(ws + pl.partials_off);
+  p.stream_bytes = (long long)vqkv_code_bytes(a->mode, a->cap_len);
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.g = a->Hq / a->Hkv;
+  p.max_seq_len = a->max_seq_len;
+  p.n_splits = pl.n_splits;
+  p.tps = pl.tps;
+  p.bpg = pl.bpg;
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
+  p.qscale = scale * 1.4426950408889634f / std::sqrt(128.0f);
+  const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
+  if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
+  return VQKV_OK;
+}
+
+vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
+  vqkv_status st = validate_encode(a);
+  if (st != VQKV_OK || a->B == 0 || a->n_rows == 0) return st;
+  DeviceInfo di;
+  st = device_info(&di);
+  if (st != VQKV_OK) return st;
+  EncodeParams p;
+  p.x = reinterpret_cast<const __half*>(a->x);
+  p.pos = a->pos;
+  p.s = a->s;
+  p.cb = reinterpret_cast<const __half*>(a->codebook);
+  p.codes = a->codes;
+  p.near_tie = a->near_tie_count;
+  p.err = a->error_flags;
+  p.stream_bytes = (long long)vqkv_code_bytes(a->mode, a->cap_len);
+  p.B = a->B;
+  p.Hkv = a->Hkv;
+  p.n_rows = a->n_rows;
+  p.cap_len = a->cap_len;
+  p.role = a->role;
+  const long long rows = (long long)a->B * a->n_rows;
+  const long long want = (rows + encode_warps_per_cta() - 1) / encode_warps_per_cta();
+  long long cap = ((long long)di.sms * di.encode_bpsm[a->mode] * 4 + a->Hkv - 1) / a->Hkv;
+  if (cap < 1) cap = 1;
+  const int blocks_x = (int)std::min(want, cap);
+  if (launch_encode(a->mode, p, blocks_x, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
+  return VQKV_OK;
+}
+
+const char* vqkv_status_string(vqkv_status s) {
+  switch (s) {
+    case VQKV_OK: return "ok";
+    case VQKV_ERR_INVALID_ARG: return "invalid argument";
+    case VQKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VQKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case VQKV_ERR_CUDA: return "CUDA error";
+    case VQKV_ERR_NO_DEVICE: return "no usable CUDA device";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,534 @@
+// Fused VQ decode attention for sm_103a.
+//
+// One CTA handles one KV head, one token range ("split") of each sequence
+// in its group, and all g query heads of that KV head, so every code byte
+// is read from HBM once per KV head (GQA grouping).  Per 16-token tile a
+// warp computes
+//   scores  S[t][h] = sum_d K'[t][d] q'[h][d]      (tensor cores, K' gathered
+//                                                  from the smem codebook)
+//   online softmax over t                         (exp2; q' carries
+//                                                  scale*log2(e))
+//   O[d][h] += sum_t V[t][d] P[t][h]              (tensor cores, V gathered
+//                                                  from the smem codebook)
+// Dequantisation happens only in registers: codes stream from HBM with
+// 128-bit loads straight into the fragment layout (the cache layout puts each
+// lane's codes in one contiguous run), centroids come from shared memory.
+//
+// The per-query transform is q' = (q * s) . Hn, so q'.K'^T = q.K^T
+// (VecInfer paper summary page, "Summary": matching inverse operations on
+// the queries keep attention scores unchanged).  Split partials (m, l, O)
+// are merged by the last CTA of each (sequence, KV head), chosen with an
+// atomic ticket (no waiting).
+//
+// Fragment maps (mma.m16n8k16, lane = 4*gid + tig):
+//   score MMA  A = K' tile: rows = tokens {gid, gid+8}, k = the 4 channels of
+//              one subvector (VQ2: j = 4s+tig at k-step s; VQ15: half of
+//              subvector j = 4s'+tig at k-steps 2s', 2s'+1), so one 8/16-byte
+//              centroid load fills a0a1|a4a5 (token gid) or a2a3|a6a7;
+//              B = q' (k = channels, n = heads, rows >= g are zero);
+//              D: tokens {gid, gid+8} x heads {2tig, 2tig+1}.
+//   P          D -> fp16 -> movmatrix.trans -> B operand of the P.V MMA
+//              (k = tokens {2tig, 2tig+1, 2tig+8, 2tig+9}, n = head gid).
+//   P.V MMA    A = V^T: rows = channels of subvector J (VQ2: J = 8p+gid over
+//              M-tiles 2p, 2p+1; VQ15: J = 8p+gid over M-tiles 4p..4p+3),
+//              k = the four tokens above; centroid halves are paired across
+//              tokens with byte permutes.
+#include "common.cuh"
+#include "internal.h"
+
+namespace vqkv {
+namespace {
+
+constexpr float kSoftmaxSlack = 8.0f;   // rescale only when a score exceeds m by 2^8
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// ------------------------------------------------------------------ VQ2
+constexpr int V2_WARPS = 8;
+constexpr int V2_THREADS = V2_WARPS * 32;
+constexpr int V2_TILE = 16;
+constexpr int V2_TILE_BYTES = 512;
+constexpr int V2_REPL = 16;                      // codebook replicas (bank spreading)
+constexpr int V2_CB_BYTES = 256 * V2_REPL * 8;   // 32 KB per codebook
+constexpr int V2_PF_TILES = 4 * V2_WARPS;        // L2 prefetch distance (tiles)
+
+// ------------------------------------------------------------------ VQ15
+constexpr int V15_WARPS = 16;
+constexpr int V15_THREADS = V15_WARPS * 32;
+constexpr int V15_TILE = 64;
+constexpr int V15_TILE_BYTES = 1536;
+constexpr int V15_CB_BYTES = 4096 * 16;          // 64 KB per codebook
+constexpr int V15_PF_TILES = 2 * V15_WARPS;
+
+template <int WARPS>
+struct CombineSmem {
+  static constexpr int kO = WARPS * 8 * 128;     // floats
+  static constexpr int kBytes = (kO + 2 * WARPS * 8) * 4;
+};
+
+constexpr size_t kV2Smem = 2 * V2_CB_BYTES + CombineSmem<V2_WARPS>::kBytes;
+constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
+
+// q' for the g heads of (b, kvh) into s_qp[h][128] (fp32, scaled), by warps 0..g-1.
+__device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
+                                                  int lane, float* s_qp) {
+  if (warp < p.g) {
+    const int hq = kvh * p.g + warp;
+    const uint2 qq = *reinterpret_cast<const uint2*>(p.q + ((size_t)b * p.Hq + hq) * kHeadDim + 4 * lane);
+    const float4 ss = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+    const __half2 q01 = *reinterpret_cast<const __half2*>(&qq.x);
+    const __half2 q23 = *reinterpret_cast<const __half2*>(&qq.y);
+    float v[4] = {__low2float(q01) * ss.x, __high2float(q01) * ss.y, __low2float(q23) * ss.z,
+                  __high2float(q23) * ss.w};
+    fwht128_f32(v, lane);
+    float4 o = make_float4(v[0] * p.qscale, v[1] * p.qscale, v[2] * p.qscale, v[3] * p.qscale);
+    *reinterpret_cast<float4*>(s_qp + warp * kHeadDim + 4 * lane) = o;
+  }
+}
+
+// Clamp the sequence length to [0, max_seq_len]; report out-of-range once.
+__device__ __forceinline__ int load_len(const DecodeParams& p, int b) {
+  int L = p.seq_lens[b];
+  if (L < 0 || L > p.max_seq_len) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.err, VQKV_DEVERR_SEQ_LEN);
+    L = L < 0 ? 0 : p.max_seq_len;
+  }
+  return L;
+}
+
+// Online-softmax update for one tile.  sc = scores for tokens {gid, gid+8}
+// x heads {2tig, 2tig+1} (log2 domain).  Returns P packed for the P.V MMA.
+template <int NACC>
+__device__ __forceinline__ void softmax_tile(float (&sc)[4], float& m0, float& m1, float& l0,
+                                             float& l1, float (&acc)[NACC][4], uint32_t& bP0,
+                                             uint32_t& bP1) {
+  const bool need = (sc[0] > m0 + kSoftmaxSlack) | (sc[2] > m0 + kSoftmaxSlack) |
+                    (sc[1] > m1 + kSoftmaxSlack) | (sc[3] > m1 + kSoftmaxSlack);
+  if (__any_sync(0xffffffffu, need)) {
+    float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float a0 = (n0 == neg_inf()) ? 1.f : fast_exp2(m0 - n0);
+    const float a1 = (n1 == neg_inf()) ? 1.f : fast_exp2(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    l0 *= a0;
+    l1 *= a1;
+#pragma unroll
+    for (int i = 0; i < NACC; ++i) {
+      acc[i][0] *= a0;
+      acc[i][1] *= a1;
+      acc[i][2] *= a0;
+      acc[i][3] *= a1;
+    }
+  }
+  const float ms0 = (m0 == neg_inf()) ? 0.f : m0;
+  const float ms1 = (m1 == neg_inf()) ? 0.f : m1;
+  const float p0 = fast_exp2(sc[0] - ms0), p1 = fast_exp2(sc[1] - ms1);
+  const float p2 = fast_exp2(sc[2] - ms0), p3 = fast_exp2(sc[3] - ms1);
+  l0 += p0 + p2;
+  l1 += p1 + p3;
+  bP0 = movmatrix_t(pack_half2(p0, p1));   // P[tokens 2tig, 2tig+1][head gid]
+  bP1 = movmatrix_t(pack_half2(p2, p3));   // P[tokens 2tig+8, 2tig+9][head gid]
+}
+
+// Merge the per-warp states of the CTA into one partial (m, l, O) per head
+// and write it to the workspace; then take the (b, kvh) ticket and, if this
+// CTA is the last one, merge all split partials into O (fp16).
+template <int WARPS>
+__device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
+                                                float* s_comb, int* s_last) {
+  const float* wO = s_comb;
+  const float* wm = s_comb + CombineSmem<WARPS>::kO;
+  const float* wl = wm + WARPS * 8;
+  const int G = p.g;
+  float* part = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * G * kPartialStride;
+  for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
+    const int h = e >> 7, d = e & 127;
+    float M = neg_inf();
+#pragma unroll 4
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, wm[w * 8 + h]);
+    float o = 0.f, l = 0.f;
+    if (M != neg_inf()) {
+#pragma unroll 4
+      for (int w = 0; w < WARPS; ++w) {
+        const float f = fast_exp2(wm[w * 8 + h] - M);
+        o += wO[(w * 8 + h) * kHeadDim + d] * f;
+        l += wl[w * 8 + h] * f;
+      }
+    }
+    part[h * kPartialStride + d] = o;
+    if (d == 0) {
+      part[h * kPartialStride + 128] = M;
+      part[h * kPartialStride + 129] = l;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(p.tickets + b * p.Hkv + kvh, 1u);
+    *s_last = (prev == (unsigned)(p.n_splits - 1));
+  }
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * G * kPartialStride;
+    const int split_stride = G * kPartialStride;
+    for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
+      const int h = e >> 7, d = e & 127;
+      const float* ph = base + h * kPartialStride;
+      float M = neg_inf();
+      for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(ph + s * split_stride + 128));
+      float o = 0.f, l = 0.f;
+      if (M != neg_inf()) {
+        for (int s = 0; s < p.n_splits; ++s) {
+          const float f = fast_exp2(__ldcg(ph + s * split_stride + 128) - M);
+          o += __ldcg(ph + s * split_stride + d) * f;
+          l += __ldcg(ph + s * split_stride + 129) * f;
+        }
+      }
+      p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+    }
+    if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
+  }
+}
+
+// Store one warp's (m, l, O) into the combine area.  acc holds O^T fragments:
+// acc[mt] = rows {gid, gid+8} (channels dim0(mt), dim0(mt)+1) x heads {2tig, 2tig+1}.
+template <int WARPS, int NMT, typename DimOf>
+__device__ __forceinline__ void stash_warp(float* s_comb, int warp, int lane, const float (&acc)[NMT][4],
+                                           float m0, float m1, float l0, float l1, DimOf dim_of) {
+  const int gid = lane >> 2, tig = lane & 3;
+  float* wO = s_comb;
+  float* wm = s_comb + CombineSmem<WARPS>::kO;
+  float* wl = wm + WARPS * 8;
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  const int h0 = warp * 8 + 2 * tig;
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt) {
+    const int d0 = dim_of(mt, gid);
+    wO[h0 * kHeadDim + d0] = acc[mt][0];
+    wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
+    wO[h0 * kHeadDim + d0 + 1] = acc[mt][2];
+    wO[(h0 + 1) * kHeadDim + d0 + 1] = acc[mt][3];
+  }
+  if (gid == 0) {
+    wm[h0] = m0;
+    wm[h0 + 1] = m1;
+    wl[h0] = l0;
+    wl[h0 + 1] = l1;
+  }
+}
+
+struct Vq2Dim {
+  __device__ int operator()(int mt, int gid) const { return 4 * (8 * (mt >> 1) + gid) + 2 * (mt & 1); }
+};
+struct Vq15Dim {
+  __device__ int operator()(int mt, int gid) const { return 8 * (8 * (mt >> 2) + gid) + 2 * (mt & 3); }
+};
+
+__global__ void __launch_bounds__(V2_THREADS, 2) decode_vq2_kernel(const DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint2* s_kcb = reinterpret_cast<uint2*>(smem);
+  uint2* s_vcb = reinterpret_cast<uint2*>(smem + V2_CB_BYTES);
+  float* s_comb = reinterpret_cast<float*>(smem + 2 * V2_CB_BYTES);
+  float* s_qp = s_comb;   // q' lives in the combine area until the tile loop starts
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int b_begin = blockIdx.z * p.bpg;
+  const int b_end = min(b_begin + p.bpg, p.B);
+  const uint32_t kcb_s = smem_u32(s_kcb) + (lane & 15) * 8;   // this lane's replica
+  const uint32_t vcb_s = smem_u32(s_vcb) + (lane & 15) * 8;
+  bool have_cb = false;
+
+  for (int b = b_begin; b < b_end; ++b) {
+    const int L = load_len(p, b);
+    const int ntiles = (L + V2_TILE - 1) / V2_TILE;
+    const int t_begin = split * p.tps;
+    const int t_end = min(t_begin + p.tps, ntiles);
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+
+    if (t_begin < t_end) {
+      if (!have_cb) {
+        // replica r of entry c at [c*16 + r]; consecutive threads write consecutive slots
+        const uint2* gk = reinterpret_cast<const uint2*>(p.kcb) + (size_t)kvh * 256;
+        const uint2* gv = reinterpret_cast<const uint2*>(p.vcb) + (size_t)kvh * 256;
+#pragma unroll 4
+        for (int k = threadIdx.x; k < 256 * V2_REPL; k += V2_THREADS) {
+          s_kcb[k] = __ldg(gk + (k >> 4));
+          s_vcb[k] = __ldg(gv + (k >> 4));
+        }
+        have_cb = true;
+      }
+      transform_queries(p, b, kvh, warp, lane, s_qp);
+      __syncthreads();
+      uint32_t qf[8][2];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int j = 4 * s + tig;
+        if (gid < p.g) {
+          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + 4 * j);
+          qf[s][0] = pack_half2(v.x, v.y);
+          qf[s][1] = pack_half2(v.z, v.w);
+        } else {
+          qf[s][0] = qf[s][1] = 0u;
+        }
+      }
+      __syncthreads();   // s_qp is reused by the combine below
+
+      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      int tile = t_begin + warp;
+      uint4 kq = make_uint4(0, 0, 0, 0), vq = make_uint4(0, 0, 0, 0);
+      if (tile < t_end) {
+        kq = ldg_stream(kbase + (size_t)tile * V2_TILE_BYTES + lane * 16);
+        vq = ldg_stream(vbase + (size_t)tile * V2_TILE_BYTES + lane * 16);
+      }
+      for (; tile < t_end; tile += V2_WARPS) {
+        const int nxt = tile + V2_WARPS;
+        uint4 kn = kq, vn = vq;
+        if (nxt < t_end) {
+          kn = ldg_stream(kbase + (size_t)nxt * V2_TILE_BYTES + lane * 16);
+          vn = ldg_stream(vbase + (size_t)nxt * V2_TILE_BYTES + lane * 16);
+        }
+        if (lane == 0) {
+          const int pf = tile + V2_PF_TILES;
+          if (pf < t_end) {
+            prefetch_l2_bulk(kbase + (size_t)pf * V2_TILE_BYTES, V2_TILE_BYTES);
+            prefetch_l2_bulk(vbase + (size_t)pf * V2_TILE_BYTES, V2_TILE_BYTES);
+          }
+        }
+
+        // ---- scores: 8 k-steps of 16 channels (4 subvectors)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t w0 = (s < 4) ? kq.x : kq.y;   // token gid
+          const uint32_t w1 = (s < 4) ? kq.z : kq.w;   // token gid + 8
+          const uint32_t c0 = (w0 >> (8 * (s & 3))) & 0xffu;
+          const uint32_t c1 = (w1 >> (8 * (s & 3))) & 0xffu;
+          const uint2 A = lds64(kcb_s + c0 * (V2_REPL * 8));
+          const uint2 B = lds64(kcb_s + c1 * (V2_REPL * 8));
+          mma_16816(sc, A.x, B.x, A.y, B.y, qf[s][0], qf[s][1]);
+        }
+        // ---- mask the tail of the sequence
+        if ((tile + 1) * V2_TILE > L) {
+          const int t0 = tile * V2_TILE + gid;
+          if (t0 >= L) sc[0] = sc[1] = neg_inf();
+          if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
+        }
+        uint32_t bP0, bP1;
+        softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
+
+        // ---- O^T += V^T P: subvector J = 8*pp + gid, tokens (2tig, 2tig+1, 2tig+8, 2tig+9)
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const uint32_t w = (pp == 0) ? vq.x : (pp == 1) ? vq.y : (pp == 2) ? vq.z : vq.w;
+          const uint2 R0 = lds64(vcb_s + ((w)&0xffu) * (V2_REPL * 8));
+          const uint2 R1 = lds64(vcb_s + ((w >> 8) & 0xffu) * (V2_REPL * 8));
+          const uint2 R2 = lds64(vcb_s + ((w >> 16) & 0xffu) * (V2_REPL * 8));
+          const uint2 R3 = lds64(vcb_s + (w >> 24) * (V2_REPL * 8));
+          mma_16816(acc[2 * pp], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632),
+                    __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP0, bP1);
+          mma_16816(acc[2 * pp + 1], __byte_perm(R0.y, R1.y, 0x5410), __byte_perm(R0.y, R1.y, 0x7632),
+                    __byte_perm(R2.y, R3.y, 0x5410), __byte_perm(R2.y, R3.y, 0x7632), bP0, bP1);
+        }
+        kq = kn;
+        vq = vn;
+      }
+    }
+    stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
+    __syncthreads();
+    finish_sequence<V2_WARPS>(p, b, kvh, split, s_comb, &s_last);
+    __syncthreads();
+  }
+}
+
+// 24-bit code pair k (bytes 3k..3k+2) of a lane's 12-byte run (3 words).
+__device__ __forceinline__ uint32_t pair24(uint32_t w0, uint32_t w1, uint32_t w2, int k) {
+  if (k == 0) return w0 & 0xffffffu;
+  if (k == 1) return __funnelshift_r(w0, w1, 24) & 0xffffffu;
+  if (k == 2) return __funnelshift_r(w1, w2, 16) & 0xffffffu;
+  return w2 >> 8;
+}
+
+__global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint4* s_kcb = reinterpret_cast<uint4*>(smem);
+  uint4* s_vcb = reinterpret_cast<uint4*>(smem + V15_CB_BYTES);
+  float* s_comb = reinterpret_cast<float*>(smem + 2 * V15_CB_BYTES);
+  float* s_qp = s_comb;
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int b_begin = blockIdx.z * p.bpg;
+  const int b_end = min(b_begin + p.bpg, p.B);
+  const uint32_t kcb_s = smem_u32(s_kcb);
+  const uint32_t vcb_s = smem_u32(s_vcb);
+  bool have_cb = false;
+
+  for (int b = b_begin; b < b_end; ++b) {
+    const int L = load_len(p, b);
+    const int ntiles = (L + V15_TILE - 1) / V15_TILE;
+    const int t_begin = split * p.tps;
+    const int t_end = min(t_begin + p.tps, ntiles);
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+
+    if (t_begin < t_end) {
+      if (!have_cb) {
+        const uint4* gk = reinterpret_cast<const uint4*>(p.kcb) + (size_t)kvh * 4096;
+        const uint4* gv = reinterpret_cast<const uint4*>(p.vcb) + (size_t)kvh * 4096;
+#pragma unroll 4
+        for (int k = threadIdx.x; k < 4096; k += V15_THREADS) {
+          s_kcb[k] = __ldg(gk + k);
+          s_vcb[k] = __ldg(gv + k);
+        }
+        have_cb = true;
+      }
+      transform_queries(p, b, kvh, warp, lane, s_qp);
+      __syncthreads();
+      uint32_t qf[8][2];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int j = 4 * (s >> 1) + tig;     // subvector
+        const int c = 8 * j + 4 * (s & 1);    // first channel of this half
+        if (gid < p.g) {
+          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + c);
+          qf[s][0] = pack_half2(v.x, v.y);
+          qf[s][1] = pack_half2(v.z, v.w);
+        } else {
+          qf[s][0] = qf[s][1] = 0u;
+        }
+      }
+      __syncthreads();
+
+      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      for (int tile = t_begin + warp; tile < t_end; tile += V15_WARPS) {
+        if (lane == 0) {
+          const int pf = tile + V15_PF_TILES;
+          if (pf < t_end) {
+            prefetch_l2_bulk(kbase + (size_t)pf * V15_TILE_BYTES, V15_TILE_BYTES);
+            prefetch_l2_bulk(vbase + (size_t)pf * V15_TILE_BYTES, V15_TILE_BYTES);
+          }
+        }
+        uint32_t kw[12], vw[12];
+        {
+          const uint8_t* kp = kbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+          const uint8_t* vp = vbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const uint4 a = ldg_stream(kp + 16 * i);
+            kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
+            const uint4 c = ldg_stream(vp + 16 * i);
+            vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int tq = tile * V15_TILE + 16 * u;   // first token of this quarter
+          if (tq >= L) break;
+          const uint32_t k0 = kw[3 * u], k1 = kw[3 * u + 1], k2 = kw[3 * u + 2];
+          // pairs: token gid -> bytes 0..5 (pair index tig, tig+4), token gid+8 -> bytes 6..11
+          const uint32_t pa0 = pair24(k0, k1, k2, 0), pa1 = pair24(k0, k1, k2, 1);
+          const uint32_t pb0 = pair24(k0, k1, k2, 2), pb1 = pair24(k0, k1, k2, 3);
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s2 = 0; s2 < 4; ++s2) {
+            // subvector j = 4*s2 + tig: s2 0 -> lo(pair0), 1 -> lo(pair1), 2 -> hi(pair0), 3 -> hi(pair1)
+            const uint32_t va = (s2 & 1) ? pa1 : pa0;
+            const uint32_t vb = (s2 & 1) ? pb1 : pb0;
+            const uint32_t ca = (s2 < 2) ? (va & 0xfffu) : (va >> 12);
+            const uint32_t cb = (s2 < 2) ? (vb & 0xfffu) : (vb >> 12);
+            const uint4 X = lds128(kcb_s + ca * 16);
+            const uint4 Y = lds128(kcb_s + cb * 16);
+            mma_16816(sc, X.x, Y.x, X.y, Y.y, qf[2 * s2][0], qf[2 * s2][1]);
+            mma_16816(sc, X.z, Y.z, X.w, Y.w, qf[2 * s2 + 1][0], qf[2 * s2 + 1][1]);
+          }
+          if (tq + 16 > L) {
+            const int t0 = tq + gid;
+            if (t0 >= L) sc[0] = sc[1] = neg_inf();
+            if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
+          }
+          uint32_t bP0, bP1;
+          softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
+
+          const uint32_t v0 = vw[3 * u], v1 = vw[3 * u + 1], v2 = vw[3 * u + 2];
+          const uint32_t q0 = pair24(v0, v1, v2, 0), q1 = pair24(v0, v1, v2, 1);
+          const uint32_t q2 = pair24(v0, v1, v2, 2), q3 = pair24(v0, v1, v2, 3);
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            // subvector J = gid + 8*pp: low code of each pair for pp = 0, high for pp = 1
+            const uint32_t c0 = pp ? (q0 >> 12) : (q0 & 0xfffu);
+            const uint32_t c1 = pp ? (q1 >> 12) : (q1 & 0xfffu);
+            const uint32_t c2 = pp ? (q2 >> 12) : (q2 & 0xfffu);
+            const uint32_t c3 = pp ? (q3 >> 12) : (q3 & 0xfffu);
+            const uint4 R0 = lds128(vcb_s + c0 * 16);
+            const uint4 R1 = lds128(vcb_s + c1 * 16);
+            const uint4 R2 = lds128(vcb_s + c2 * 16);
+            const uint4 R3 = lds128(vcb_s + c3 * 16);
+            mma_16816(acc[4 * pp + 0], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632),
+                      __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP0, bP1);
+            mma_16816(acc[4 * pp + 1], __byte_perm(R0.y, R1.y, 0x5410), __byte_perm(R0.y, R1.y, 0x7632),
+                      __byte_perm(R2.y, R3.y, 0x5410), __byte_perm(R2.y, R3.y, 0x7632), bP0, bP1);
+            mma_16816(acc[4 * pp + 2], __byte_perm(R0.z, R1.z, 0x5410), __byte_perm(R0.z, R1.z, 0x7632),
+                      __byte_perm(R2.z, R3.z, 0x5410), __byte_perm(R2.z, R3.z, 0x7632), bP0, bP1);
+            mma_16816(acc[4 * pp + 3], __byte_perm(R0.w, R1.w, 0x5410), __byte_perm(R0.w, R1.w, 0x7632),
+                      __byte_perm(R2.w, R3.w, 0x5410), __byte_perm(R2.w, R3.w, 0x7632), bP0, bP1);
+          }
+        }
+      }
+    }
+    stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
+    __syncthreads();
+    finish_sequence<V15_WARPS>(p, b, kvh, split, s_comb, &s_last);
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TILE : V15_TILE; }
+size_t decode_smem_bytes(int mode) { return mode == VQKV_MODE_VQ2 ? kV2Smem : kV15Smem; }
+int decode_threads(int mode) { return mode == VQKV_MODE_VQ2 ? V2_THREADS : V15_THREADS; }
+
+cudaError_t decode_prepare(int mode) {
+  if (mode == VQKV_MODE_VQ2)
+    return cudaFuncSetAttribute(decode_vq2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV2Smem);
+  return cudaFuncSetAttribute(decode_vq15_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV15Smem);
+}
+
+cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
+  if (mode == VQKV_MODE_VQ2)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel, V2_THREADS, kV2Smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel, V15_THREADS, kV15Smem);
+}
+
+cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  if (mode == VQKV_MODE_VQ2)
+    decode_vq2_kernel<<<grid, V2_THREADS, kV2Smem, stream>>>(p);
+  else
+    decode_vq15_kernel<<<grid, V15_THREADS, kV15Smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vqkv

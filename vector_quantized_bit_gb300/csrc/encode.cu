@@ -1,0 +1,292 @@
+// VQ encode for sm_103a: smoothing, Hadamard rotation, nearest centroid, pack
+// (VecInfer paper summary page, "Summary": channel-wise smoothing followed by
+// a Hadamard rotation of the keys, K-Means codebook; arXiv summary page,
+// "方法详解", stages 1-2).
+//
+// One warp per row; lane l holds channels 4l..4l+3.  For keys the transform
+// x' = (x / s) . H / sqrt(128) is carried in double-float arithmetic (pairs
+// of fp32 with error-free sums and products) and rounded to fp32 once, so the
+// vector handed to the nearest-centroid search is the correctly rounded fp32
+// value of the exact transform.  Distances are fp32 direct differences; the
+// argmin keeps the lowest index on equal distances.
+#include "common.cuh"
+#include "internal.h"
+
+namespace vqkv {
+namespace {
+
+constexpr int ENC_WARPS = 8;
+constexpr int ENC_THREADS = ENC_WARPS * 32;
+
+// ------------------------------------------------------- double-float
+struct df {
+  float h, l;
+};
+
+__device__ __forceinline__ df fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  const float e = __fsub_rn(b, __fsub_rn(s, a));
+  return {s, e};
+}
+
+__device__ __forceinline__ df two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+__device__ __forceinline__ df df_add(df a, df b) {
+  df s = two_sum(a.h, b.h);
+  const float e = __fadd_rn(s.l, __fadd_rn(a.l, b.l));
+  return fast_two_sum(s.h, e);
+}
+
+__device__ __forceinline__ df df_neg(df a) { return {-a.h, -a.l}; }
+
+__device__ __forceinline__ df df_mul(df a, float ch, float cl) {
+  const float p = __fmul_rn(a.h, ch);
+  float e = __fmaf_rn(a.h, ch, -p);
+  e = __fmaf_rn(a.h, cl, e);
+  e = __fmaf_rn(a.l, ch, e);
+  return fast_two_sum(p, e);
+}
+
+// x / s as a double-float: quotient, plus the exact remainder divided by s.
+__device__ __forceinline__ df df_div(float x, float s) {
+  const float q = __fdiv_rn(x, s);
+  const float r = __fmaf_rn(-q, s, x);
+  return fast_two_sum(q, __fdiv_rn(r, s));
+}
+
+// Unnormalised FWHT (H[i][k] = (-1)^popcount(i & k)) of a 128-vector in
+// double-float, 4 entries per lane.
+__device__ __forceinline__ void fwht128_df(df (&v)[4], int lane) {
+  {
+    const df a = df_add(v[0], v[1]), b = df_add(v[0], df_neg(v[1]));
+    const df c = df_add(v[2], v[3]), d = df_add(v[2], df_neg(v[3]));
+    v[0] = df_add(a, c);
+    v[2] = df_add(a, df_neg(c));
+    v[1] = df_add(b, d);
+    v[3] = df_add(b, df_neg(d));
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      df o;
+      o.h = __shfl_xor_sync(0xffffffffu, v[i].h, m);
+      o.l = __shfl_xor_sync(0xffffffffu, v[i].l, m);
+      v[i] = upper ? df_add(o, df_neg(v[i])) : df_add(v[i], o);
+    }
+  }
+}
+
+// sqrt(2) as fp32 hi + lo; 1/sqrt(128) = sqrt(2) / 16.
+__device__ __forceinline__ float sqrt2_hi() { return __int_as_float(0x3fb504f3); }
+__device__ __forceinline__ float sqrt2_lo() { return __int_as_float(0x32cfe77a); }
+
+// Transform of one row: lane's four channels, fp32 result.
+__device__ __forceinline__ void transform_row(const EncodeParams& p, int kvh, const __half* xrow, int lane,
+                                              float (&x)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(xrow + 4 * lane);
+  const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x);
+  const __half2 x23 = *reinterpret_cast<const __half2*>(&raw.y);
+  x[0] = __low2float(x01);
+  x[1] = __high2float(x01);
+  x[2] = __low2float(x23);
+  x[3] = __high2float(x23);
+  if (p.role == VQKV_ROLE_K) {
+    const float4 s = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+    df v[4] = {df_div(x[0], s.x), df_div(x[1], s.y), df_div(x[2], s.z), df_div(x[3], s.w)};
+    fwht128_df(v, lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const df r = df_mul(v[i], sqrt2_hi(), sqrt2_lo());
+      x[i] = __fmul_rn(r.h, 0.0625f);   // exact scaling; r.h is RN(r.h + r.l)
+    }
+  }
+}
+
+__device__ __forceinline__ void count_near_ties(const EncodeParams& p, bool tie, int lane, unsigned mask) {
+  if (p.near_tie == nullptr) return;
+  const unsigned n = __popc(__ballot_sync(0xffffffffu, tie) & mask);
+  if (lane == 0 && n) atomicAdd(p.near_tie, (unsigned long long)n);
+}
+
+__device__ __forceinline__ bool is_near_tie(float best, float second) {
+  return __fsub_rn(second, best) < 1e-6f * fmaxf(best, 1e-30f);
+}
+
+// ------------------------------------------------------------------ VQ2
+__global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodeParams p) {
+  __shared__ float4 s_cb[256];
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = threadIdx.x; c < 256; c += ENC_THREADS) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * 256 + c);
+    const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
+    const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
+    s_cb[c] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+  }
+  __syncthreads();
+  const int rows = p.B * p.n_rows;
+  for (int r = blockIdx.x * ENC_WARPS + warp; r < rows; r += gridDim.x * ENC_WARPS) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    const int t = p.pos[b] + n;
+    if (t < 0 || t >= p.cap_len) {
+      if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      continue;
+    }
+    float x[4];
+    transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
+    // lane = subvector j (channels 4j..4j+3)
+    float best = __int_as_float(0x7f800000), second = best;
+    int bi = 0;
+#pragma unroll 4
+    for (int c = 0; c < 256; ++c) {
+      const float4 cc = s_cb[c];
+      const float e0 = __fsub_rn(x[0], cc.x), e1 = __fsub_rn(x[1], cc.y);
+      const float e2 = __fsub_rn(x[2], cc.z), e3 = __fsub_rn(x[3], cc.w);
+      float d = __fmul_rn(e0, e0);
+      d = __fmaf_rn(e1, e1, d);
+      d = __fmaf_rn(e2, e2, d);
+      d = __fmaf_rn(e3, e3, d);
+      if (d < best) {
+        second = best;
+        best = d;
+        bi = c;
+      } else if (d < second) {
+        second = d;
+      }
+    }
+    count_near_ties(p, is_near_tie(best, second), lane, 0xffffffffu);
+    // pack: byte offset of (t, j = lane) in the stream
+    const int tile = t >> 4, rr = t & 15, j = lane;
+    const long long off = (p.role == VQKV_ROLE_K)
+                              ? 512LL * tile + 16 * (4 * (rr & 7) + (j & 3)) + 8 * (rr >> 3) + (j >> 2)
+                              : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
+    p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + off] = (uint8_t)bi;
+  }
+}
+
+// ------------------------------------------------------------------ VQ15
+// Codebook as fp32 in shared memory (128 KB).  The two lanes of a subvector
+// (channels 8J..8J+7 live on lanes 2J, 2J+1) both hold all 8 channels and
+// search half of the 4096 centroids each; the halves are merged at the end.
+__global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodeParams p) {
+  extern __shared__ __align__(16) float4 s_cb15[];   // [4096][2]
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = threadIdx.x; c < 4096; c += ENC_THREADS) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
+    const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
+    const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
+    const __half2 cc = *reinterpret_cast<const __half2*>(&raw.z);
+    const __half2 d = *reinterpret_cast<const __half2*>(&raw.w);
+    s_cb15[2 * c] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+    s_cb15[2 * c + 1] = make_float4(__low2float(cc), __high2float(cc), __low2float(d), __high2float(d));
+  }
+  __syncthreads();
+  const int rows = p.B * p.n_rows;
+  const int half = lane & 1;
+  for (int r = blockIdx.x * ENC_WARPS + warp; r < rows; r += gridDim.x * ENC_WARPS) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    const int t = p.pos[b] + n;
+    if (t < 0 || t >= p.cap_len) {
+      if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      continue;
+    }
+    float x[4];
+    transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
+      y[i] = half ? o : x[i];
+      y[4 + i] = half ? x[i] : o;
+    }
+    float best = __int_as_float(0x7f800000), second = best;
+    int bi = 0;
+    const int c0 = half * 2048;
+#pragma unroll 2
+    for (int c = c0; c < c0 + 2048; ++c) {
+      const float4 lo = s_cb15[2 * c], hi = s_cb15[2 * c + 1];
+      float e = __fsub_rn(y[0], lo.x);
+      float d = __fmul_rn(e, e);
+      e = __fsub_rn(y[1], lo.y); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[2], lo.z); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[3], lo.w); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[4], hi.x); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[5], hi.y); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[6], hi.z); d = __fmaf_rn(e, e, d);
+      e = __fsub_rn(y[7], hi.w); d = __fmaf_rn(e, e, d);
+      if (d < best) {
+        second = best;
+        best = d;
+        bi = c;
+      } else if (d < second) {
+        second = d;
+      }
+    }
+    // merge the two halves: lower distance, then lower index
+    const float ob = __shfl_xor_sync(0xffffffffu, best, 1);
+    const float os = __shfl_xor_sync(0xffffffffu, second, 1);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, 1);
+    float mb, ms;
+    int mi;
+    if (ob < best || (ob == best && oi < bi)) {
+      mb = ob;
+      mi = oi;
+      ms = fminf(os, best);
+    } else {
+      mb = best;
+      mi = bi;
+      ms = fminf(second, ob);
+    }
+    count_near_ties(p, is_near_tie(mb, ms), lane, 0x55555555u);
+    // lanes 2p (p < 8) hold subvector p; subvector p+8 sits on lane 2p+16
+    const int hi_code = __shfl_down_sync(0xffffffffu, mi, 16);
+    if (lane < 16 && half == 0) {
+      const int pair = lane >> 1;
+      const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
+      const long long off = (p.role == VQKV_ROLE_K)
+                                ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
+                                : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
+      uint8_t* dst = p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + off;
+      dst[0] = (uint8_t)(mi & 0xff);
+      dst[1] = (uint8_t)(((mi >> 8) & 0xf) | ((hi_code & 0xf) << 4));
+      dst[2] = (uint8_t)(hi_code >> 4);
+    }
+  }
+}
+
+constexpr size_t kV15EncSmem = 4096 * 2 * sizeof(float4);
+
+}  // namespace
+
+int encode_warps_per_cta() { return ENC_WARPS; }
+
+cudaError_t encode_prepare(int mode) {
+  if (mode == VQKV_MODE_VQ15)
+    return cudaFuncSetAttribute(encode_vq15_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV15EncSmem);
+  return cudaSuccess;
+}
+
+cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
+  if (mode == VQKV_MODE_VQ2)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel, ENC_THREADS, 0);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_kernel, ENC_THREADS, kV15EncSmem);
+}
+
+cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, cudaStream_t stream) {
+  const dim3 grid(blocks_x, p.Hkv);
+  if (mode == VQKV_MODE_VQ2)
+    encode_vq2_kernel<<<grid, ENC_THREADS, 0, stream>>>(p);
+  else
+    encode_vq15_kernel<<<grid, ENC_THREADS, kV15EncSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vqkv

@@ -1,0 +1,61 @@
+// Internal interface between the host shim (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace vqkv {
+
+// Everything a decode kernel needs; built and validated by api.cu.
+struct DecodeParams {
+  const __half* q;          // [B][Hq][128]
+  const uint8_t* kc;        // [B][Hkv][stream_bytes]
+  const uint8_t* vc;
+  const int32_t* seq_lens;  // [B]
+  const __half* kcb;        // [Hkv][E][d_sub]
+  const __half* vcb;
+  const float* s;           // [Hkv][128]
+  __half* out;              // [B][Hq][128]
+  float* partials;          // [B][Hkv][n_splits][g][kPartialStride]
+  unsigned* tickets;        // [B][Hkv], zero between calls
+  unsigned* err;            // device error word
+  long long stream_bytes;
+  int B, Hq, Hkv, g;
+  int max_seq_len;
+  int n_splits;             // CTAs per (sequence, KV head)
+  int tps;                  // tiles per split
+  int bpg;                  // sequences per CTA (grid.z = ceil(B / bpg))
+  float qscale;             // softmax_scale * log2(e) / sqrt(128)
+};
+
+constexpr int kPartialStride = 130;  // O[128], m, l
+
+struct EncodeParams {
+  const __half* x;          // [B][Hkv][n_rows][128]
+  const int32_t* pos;       // [B]
+  const float* s;           // [Hkv][128] (keys) or nullptr
+  const __half* cb;         // [Hkv][E][d_sub]
+  uint8_t* codes;           // [B][Hkv][stream_bytes]
+  unsigned long long* near_tie;
+  unsigned* err;
+  long long stream_bytes;
+  int B, Hkv, n_rows, cap_len, role;
+};
+
+// Decode kernels (decode.cu).  tile_tokens: 16 (VQ2) / 64 (VQ15).
+int decode_tile_tokens(int mode);
+size_t decode_smem_bytes(int mode);
+int decode_threads(int mode);
+cudaError_t decode_prepare(int mode);                // set smem attributes (once per device)
+cudaError_t decode_occupancy(int mode, int* blocks_per_sm);
+cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
+// Encode kernels (encode.cu).
+cudaError_t encode_prepare(int mode);
+cudaError_t encode_occupancy(int mode, int* blocks_per_sm);
+cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, cudaStream_t stream);
+int encode_warps_per_cta();
+
+}  // namespace vqkv
