@@ -167,12 +167,15 @@ typedef struct {
 size_t vqkv_code_bytes(int32_t mode, int32_t cap_len);
 
 /* Workspace bytes vqkv_decode_attn needs for these arguments (the same split
- * plan the call will use on the current device); 0 when the arguments are
- * invalid. */
+ * plan the call will use on the current device).  Only the sizes are read
+ * (mode, B, Hq, Hkv, head_dim, cap_len, max_seq_len, num_splits); pointers
+ * are ignored.  0 when a size is invalid or no device is usable. */
 size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* args);
 
 /* CTAs per (sequence, KV head) vqkv_decode_attn will use on the current
- * device (for the caller's bookkeeping); -1 when the arguments are invalid. */
+ * device (for the caller's bookkeeping).  Reads the sizes only, like
+ * vqkv_decode_workspace_bytes; -1 when a size is invalid or no device is
+ * usable. */
 int32_t vqkv_decode_num_splits(const vqkv_decode_args* args);
 
 vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);

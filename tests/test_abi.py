@@ -92,8 +92,10 @@ def _enc(**kw):
 ])
 def test_decode_validation(lib, kw, status):
     assert lib.vqkv_decode_attn(ctypes.byref(_dec(**kw)), None) == status
-    assert lib.vqkv_decode_workspace_bytes(ctypes.byref(_dec(**kw))) == 0
-    assert lib.vqkv_decode_num_splits(ctypes.byref(_dec(**kw))) == -1
+    pointer_only = all(k in ("q", "k_codes", "v_codes", "s", "out", "k_codebook", "softmax_scale") for k in kw)
+    if not pointer_only:   # the size queries read sizes only
+        assert lib.vqkv_decode_workspace_bytes(ctypes.byref(_dec(**kw))) == 0
+        assert lib.vqkv_decode_num_splits(ctypes.byref(_dec(**kw))) == -1
 
 
 def test_decode_empty_batch_is_a_no_op(lib):

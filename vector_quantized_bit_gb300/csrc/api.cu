@@ -48,6 +48,19 @@ vqkv_status device_info(DeviceInfo* out) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Sizes only (what the split plan and the workspace size depend on).
+vqkv_status validate_decode_sizes(const vqkv_decode_args* a) {
+  if (a == nullptr) return VQKV_ERR_INVALID_ARG;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
+  if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq / a->Hkv > 8) return VQKV_ERR_UNSUPPORTED;
+  if (a->max_seq_len < 0 || a->max_seq_len > a->cap_len) return VQKV_ERR_INVALID_ARG;
+  if (a->num_splits < 0) return VQKV_ERR_INVALID_ARG;
+  return VQKV_OK;
+}
+
 vqkv_status validate_decode(const vqkv_decode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
   if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
@@ -153,14 +166,14 @@ size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
 }
 
 size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* a) {
-  if (validate_decode(a) != VQKV_OK) return 0;
+  if (validate_decode_sizes(a) != VQKV_OK) return 0;
   DecodePlan pl;
   if (plan_decode(a, &pl) != VQKV_OK) return 0;
   return pl.ws_bytes;
 }
 
 int32_t vqkv_decode_num_splits(const vqkv_decode_args* a) {
-  if (validate_decode(a) != VQKV_OK) return -1;
+  if (validate_decode_sizes(a) != VQKV_OK) return -1;
   DecodePlan pl;
   if (plan_decode(a, &pl) != VQKV_OK) return -1;
   return pl.n_splits;
