@@ -181,6 +181,43 @@ int32_t vqkv_decode_num_splits(const vqkv_decode_args* args);
 vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);
 vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
 
+/* Size of the scratch array compiled into the library for
+ * vqkv_decode_attn_static (8 MiB, held on every GPU that loads the library
+ * until the process exits). */
+#define VQKV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * vqkv_decode_attn_static — vqkv_decode_attn for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is a
+ * deployment variant of this library, not a step of the method.
+ *
+ * Some callers cannot obtain a workspace: a serving engine whose memory pool
+ * has reserved all device memory up front and forbids allocation after
+ * start-up, a plugin whose host framework owns every allocation and offers
+ * no scratch buffer in its interface, or code that must not call cudaMalloc
+ * on its hot path.  This entry point computes exactly what vqkv_decode_attn
+ * computes (same kernels, same split plan) but keeps the split-KV scratch in
+ * a fixed array of VQKV_STATIC_SCRATCH_BYTES inside the library, so it
+ * allocates nothing and calls no allocating routine; the caller still
+ * passes every input and the output.  args->workspace and
+ * args->workspace_bytes are ignored.
+ *
+ *   - Arguments are checked exactly as in vqkv_decode_attn.  When the split
+ *     plan needs more scratch than VQKV_STATIC_SCRATCH_BYTES
+ *     (vqkv_decode_workspace_bytes(args) tells how much), the call returns
+ *     VQKV_ERR_WORKSPACE and enqueues nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current, once per device); make that first call before any
+ *     stream capture.
+ *   - Each call clears the scratch's error word and tickets with
+ *     cudaMemsetAsync on `stream`, then launches.  The array is shared by
+ *     every call on a device and keeps the last call's contents: calls whose
+ *     execution overlaps on the GPU (different streams, not ordered) race on
+ *     it and must be serialised by the caller.  Device-side error bits are
+ *     not reported back by this entry point (lengths are still clamped).
+ */
+vqkv_status vqkv_decode_attn_static(const vqkv_decode_args* args, void* stream);
+
 /* Static, never NULL. */
 const char* vqkv_status_string(vqkv_status status);
 

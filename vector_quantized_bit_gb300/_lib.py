@@ -23,7 +23,8 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_encode",
-            "vqkv_decode_attn", "vqkv_status_string"]
+            "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_status_string"]
+STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class VqkvError(RuntimeError):
@@ -77,6 +78,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_decode_attn_static.restype = ctypes.c_int
+        L.vqkv_decode_attn_static.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
         L.vqkv_status_string.restype = ctypes.c_char_p
         L.vqkv_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -159,6 +162,18 @@ def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook
     st = lib().vqkv_decode_attn(ctypes.byref(a), _stream(stream))
     if st != 0:
         raise VqkvError(st, "vqkv_decode_attn")
+
+
+def vqkv_decode_attn_static(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, cap_len,
+                            max_seq_len, softmax_scale=0.0, num_splits=0, stream=None) -> None:
+    """vqkv_decode_attn without a workspace: for callers that cannot allocate
+    device memory.  The split-KV scratch is an 8 MiB array inside the library,
+    shared by all calls on a device (calls must not overlap on the GPU)."""
+    a = decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, None, cap_len,
+                    max_seq_len, softmax_scale, num_splits)
+    st = lib().vqkv_decode_attn_static(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_attn_static")
 
 
 def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda"):

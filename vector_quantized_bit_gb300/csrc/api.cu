@@ -81,6 +81,10 @@ vqkv_status validate_decode(const vqkv_decode_args* a) {
   return VQKV_OK;
 }
 
+}  // namespace
+size_t decode_ticket_region_bytes(int B, int Hkv);
+namespace {
+
 struct DecodePlan {
   int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1;
   size_t tickets_off = 0, partials_off = 0, ws_bytes = 0;
@@ -128,7 +132,7 @@ vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
   pl->bpg = bpg;
   pl->n_bgroups = (B + bpg - 1) / bpg;
   pl->tickets_off = kWsHeader;
-  pl->partials_off = round_up(kWsHeader + sizeof(unsigned) * (size_t)B * a->Hkv, 256);
+  pl->partials_off = decode_ticket_region_bytes(B, a->Hkv);
   pl->ws_bytes = pl->partials_off +
                  sizeof(float) * (size_t)B * a->Hkv * pl->n_splits * g * kPartialStride;
   return VQKV_OK;
@@ -152,6 +156,13 @@ vqkv_status validate_encode(const vqkv_encode_args* a) {
 }
 
 }  // namespace
+
+vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(a); }
+
+size_t decode_ticket_region_bytes(int B, int Hkv) {
+  return round_up(kWsHeader + sizeof(unsigned) * (size_t)std::max(B, 1) * Hkv, 256);
+}
+
 }  // namespace vqkv
 
 using namespace vqkv;

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "vqkv.h"
+
 namespace vqkv {
 
 // Everything a decode kernel needs; built and validated by api.cu.
@@ -51,6 +53,10 @@ int decode_threads(int mode);
 cudaError_t decode_prepare(int mode);                // set smem attributes (once per device)
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm);
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
+// Host-side helpers of api.cu shared with decode_static.cu.
+vqkv_status decode_validate(const vqkv_decode_args* a);   // every check of vqkv_decode_attn
+size_t decode_ticket_region_bytes(int B, int Hkv);       // error word + tickets, bytes
 
 // Encode kernels (encode.cu).
 cudaError_t encode_prepare(int mode);
