@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="set up the workload, run this many plain (eager) steps and exit: "
+                         "the command the ncu summaries under profiles/ are taken with")
     return ap.parse_args()
 
 
@@ -245,7 +248,7 @@ def run_ours(args):
     lens = synth.seq_lens(w)
     s_h, kcb_h, vcb_h, kv = host_workload(w)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_steps:
         cpu = cpu_baseline()
 
     import torch
@@ -298,6 +301,13 @@ def run_ours(args):
         _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
         if ev is not None:
             ev[1].record()
+
+    if args.profile_steps:
+        for i in range(args.profile_steps):
+            step(i)
+        torch.cuda.synchronize()
+        print(f"profile run: {args.profile_steps} steps of {w.name}, {n_splits} splits per KV head", flush=True)
+        return
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()

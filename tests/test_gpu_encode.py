@@ -51,12 +51,12 @@ def test_tiny_config_keys_and_values():
 
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("role", [0, 1])
-def test_ragged_positions_multi_head(mode, role):
+@pytest.mark.parametrize("n", [37, 3])   # 3 rows: the few-rows launch (candidates split over warps)
+def test_ragged_positions_multi_head(mode, role, n):
     w = synth.WORKLOADS[3 if mode else 1].scaled(seq_len=2048, cap_len=2048)
     kw = dict(sample_tokens=512, iters=3) if mode else dict(sample_tokens=512, iters=5)
     s, kcb, vcb = H.calibrate(w.scaled(Hkv=2), **kw)
     cb = kcb if role == 0 else vcb
-    n = 37
     x = np.stack([np.stack([(synth.keys if role == 0 else synth.values)(w, b, h, 100, n) for h in range(2)])
                   for b in range(3)])
     pos = [0, 5, 130]

@@ -109,7 +109,7 @@ vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
   int bpg = 1;
   if (a->mode == VQKV_MODE_VQ15 && (long long)B * a->Hkv < slots) bpg = B;
   const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg);
-  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 6.0 : 24.0;   // per-CTA prologue in tile units
+  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 12.0 : 24.0;   // per-CTA prologue in tile units
   long long best_n = 1;
   double best_cost = 1e300;
   if (a->num_splits > 0) {
@@ -247,12 +247,21 @@ vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
   p.n_rows = a->n_rows;
   p.cap_len = a->cap_len;
   p.role = a->role;
-  const long long rows = (long long)a->B * a->n_rows;
-  const long long want = (rows + encode_warps_per_cta() - 1) / encode_warps_per_cta();
-  long long cap = ((long long)di.sms * di.encode_bpsm[a->mode] * 4 + a->Hkv - 1) / a->Hkv;
-  if (cap < 1) cap = 1;
-  const int blocks_x = (int)std::min(want, cap);
-  if (launch_encode(a->mode, p, blocks_x, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
+  const long long rows = (long long)a->B * a->n_rows;   // per KV head
+  // Few rows (a decode-step append): one row per CTA, its candidates split
+  // over the CTA's warps, for latency.  Many rows: one row per warp.
+  const bool split_rows = rows * a->Hkv * encode_warps_per_cta() <= (long long)di.sms * 8;
+  int blocks_x;
+  if (split_rows) {
+    blocks_x = (int)rows;
+  } else {
+    const long long want = (rows + encode_warps_per_cta() - 1) / encode_warps_per_cta();
+    long long cap = ((long long)di.sms * di.encode_bpsm[a->mode] * 4 + a->Hkv - 1) / a->Hkv;
+    if (cap < 1) cap = 1;
+    blocks_x = (int)std::min(want, cap);
+  }
+  if (launch_encode(a->mode, p, blocks_x, split_rows, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
 

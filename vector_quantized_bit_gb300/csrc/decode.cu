@@ -42,15 +42,21 @@ namespace {
 constexpr float kSoftmaxSlack = 8.0f;   // rescale only when a score exceeds m by 2^8
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+// Initial running max: finite, so exp2(m_old - m_new) and exp2(score - m)
+// never see inf - inf; masked scores are -inf and give p = 0.
+constexpr float kMInit = -1e30f;
 
 // ------------------------------------------------------------------ VQ2
-constexpr int V2_WARPS = 8;
+constexpr int V2_WARPS = 16;                       // one CTA per SM
 constexpr int V2_THREADS = V2_WARPS * 32;
 constexpr int V2_TILE = 16;
 constexpr int V2_TILE_BYTES = 512;
-constexpr int V2_REPL = 16;                      // codebook replicas (bank spreading)
-constexpr int V2_CB_BYTES = 256 * V2_REPL * 8;   // 32 KB per codebook
-constexpr int V2_PF_TILES = 4 * V2_WARPS;        // L2 prefetch distance (tiles)
+constexpr int V2_REPL = 32;                         // codebook replicas: one per lane
+constexpr int V2_K_BYTES = 256 * 256;               // K: [code][row d01|d23][32 replicas] fp16x2 words
+constexpr int V2_V_BYTES = 256 * 256;               // V: [code][32 replicas] 8-byte centroids
+constexpr int V2_Q_OFF = V2_K_BYTES + V2_V_BYTES;   // q' (fp32 [8][128]) after the codebooks
+constexpr int V2_PF_CHUNK = 16;                     // tiles per L2 prefetch request
+constexpr int V2_PF_AHEAD = 96;                     // tiles kept in flight ahead of warp 0
 
 // ------------------------------------------------------------------ VQ15
 constexpr int V15_WARPS = 16;
@@ -66,7 +72,9 @@ struct CombineSmem {
   static constexpr int kBytes = (kO + 2 * WARPS * 8) * 4;
 };
 
-constexpr size_t kV2Smem = 2 * V2_CB_BYTES + CombineSmem<V2_WARPS>::kBytes;
+// Codebooks + q'; the combine area reuses the codebook region after the tile loop.
+constexpr size_t kV2Smem = V2_Q_OFF + 8 * 128 * 4;
+static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_Q_OFF, "combine area must fit in the codebook region");
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
 
 // q' for the g heads of (b, kvh) into s_qp[h][128] (fp32, scaled), by warps 0..g-1.
@@ -112,8 +120,8 @@ __device__ __forceinline__ void softmax_tile(float (&sc)[4], float& m0, float& m
       x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
     }
     const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float a0 = (n0 == neg_inf()) ? 1.f : fast_exp2(m0 - n0);
-    const float a1 = (n1 == neg_inf()) ? 1.f : fast_exp2(m1 - n1);
+    const float a0 = fast_exp2(m0 - n0);
+    const float a1 = fast_exp2(m1 - n1);
     m0 = n0;
     m1 = n1;
     l0 *= a0;
@@ -126,10 +134,8 @@ __device__ __forceinline__ void softmax_tile(float (&sc)[4], float& m0, float& m
       acc[i][3] *= a1;
     }
   }
-  const float ms0 = (m0 == neg_inf()) ? 0.f : m0;
-  const float ms1 = (m1 == neg_inf()) ? 0.f : m1;
-  const float p0 = fast_exp2(sc[0] - ms0), p1 = fast_exp2(sc[1] - ms1);
-  const float p2 = fast_exp2(sc[2] - ms0), p3 = fast_exp2(sc[3] - ms1);
+  const float p0 = fast_exp2(sc[0] - m0), p1 = fast_exp2(sc[1] - m1);
+  const float p2 = fast_exp2(sc[2] - m0), p3 = fast_exp2(sc[3] - m1);
   l0 += p0 + p2;
   l1 += p1 + p3;
   bP0 = movmatrix_t(pack_half2(p0, p1));   // P[tokens 2tig, 2tig+1][head gid]
@@ -149,17 +155,15 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
   float* part = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * G * kPartialStride;
   for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
     const int h = e >> 7, d = e & 127;
-    float M = neg_inf();
+    float M = kMInit;
 #pragma unroll 4
     for (int w = 0; w < WARPS; ++w) M = fmaxf(M, wm[w * 8 + h]);
     float o = 0.f, l = 0.f;
-    if (M != neg_inf()) {
 #pragma unroll 4
-      for (int w = 0; w < WARPS; ++w) {
-        const float f = fast_exp2(wm[w * 8 + h] - M);
-        o += wO[(w * 8 + h) * kHeadDim + d] * f;
-        l += wl[w * 8 + h] * f;
-      }
+    for (int w = 0; w < WARPS; ++w) {
+      const float f = fast_exp2(wm[w * 8 + h] - M);
+      o += wO[(w * 8 + h) * kHeadDim + d] * f;
+      l += wl[w * 8 + h] * f;
     }
     part[h * kPartialStride + d] = o;
     if (d == 0) {
@@ -181,15 +185,13 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
       const int h = e >> 7, d = e & 127;
       const float* ph = base + h * kPartialStride;
-      float M = neg_inf();
+      float M = kMInit;
       for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(ph + s * split_stride + 128));
       float o = 0.f, l = 0.f;
-      if (M != neg_inf()) {
-        for (int s = 0; s < p.n_splits; ++s) {
-          const float f = fast_exp2(__ldcg(ph + s * split_stride + 128) - M);
-          o += __ldcg(ph + s * split_stride + d) * f;
-          l += __ldcg(ph + s * split_stride + 129) * f;
-        }
+      for (int s = 0; s < p.n_splits; ++s) {
+        const float f = fast_exp2(__ldcg(ph + s * split_stride + 128) - M);
+        o += __ldcg(ph + s * split_stride + d) * f;
+        l += __ldcg(ph + s * split_stride + 129) * f;
       }
       p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
     }
@@ -235,12 +237,77 @@ struct Vq15Dim {
   __device__ int operator()(int mt, int gid) const { return 8 * (8 * (mt >> 2) + gid) + 2 * (mt & 3); }
 };
 
-__global__ void __launch_bounds__(V2_THREADS, 2) decode_vq2_kernel(const DecodeParams p) {
+// Shared-memory offset of a gathered centroid: one byte permute puts code
+// byte K of `codes` into bits 8..15 and the lane's replica offset (byte 0 of
+// `lane_byte`) into bits 0..7: (code << 8) | replica offset.
+template <int K>
+__device__ __forceinline__ uint32_t cb_offset(uint32_t codes, uint32_t lane_byte) {
+  return __byte_perm(codes, lane_byte, 0x5504 | (K << 4));
+}
+
+template <typename T>
+__device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const T*>(base + off);
+}
+
+// One 16-token tile of the 2-bit path: scores, online softmax, P.V.
+//   kq: this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig)
+//   vq: this lane's 16 value-code bytes (word p: tokens 2tig, 2tig+1,
+//       2tig+8, 2tig+9 of subvector 8p+gid)
+__device__ __forceinline__ void vq2_tile(const unsigned char* s_k, const unsigned char* s_v, uint32_t klane,
+                                         uint32_t vlane, const uint32_t (&qf)[8][2], uint4 kq, uint4 vq,
+                                         int tile, int L, int gid, float& m0, float& m1, float& l0, float& l1,
+                                         float (&acc)[8][4]) {
+  // ---- scores: 8 k-steps of 16 channels; two independent MMA chains.
+  // a0a1/a4a5 = channels (0,1)/(2,3) of token gid, a2a3/a6a7 of token gid+8:
+  // four 32-bit gathers straight into the operand registers.
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#define VQKV_SCORE_STEP(S, ACC)                                                   \
+  {                                                                               \
+    const uint32_t oa = cb_offset<(S)&3>(((S) < 4) ? kq.x : kq.y, klane);         \
+    const uint32_t ob = cb_offset<(S)&3>(((S) < 4) ? kq.z : kq.w, klane);         \
+    mma_16816(ACC, lds_at<uint32_t>(s_k, oa), lds_at<uint32_t>(s_k, ob),          \
+              lds_at<uint32_t>(s_k + 128, oa), lds_at<uint32_t>(s_k + 128, ob),   \
+              qf[S][0], qf[S][1]);                                                \
+  }
+  VQKV_SCORE_STEP(0, sa) VQKV_SCORE_STEP(1, sb) VQKV_SCORE_STEP(2, sa) VQKV_SCORE_STEP(3, sb)
+  VQKV_SCORE_STEP(4, sa) VQKV_SCORE_STEP(5, sb) VQKV_SCORE_STEP(6, sa) VQKV_SCORE_STEP(7, sb)
+#undef VQKV_SCORE_STEP
+  float sc[4] = {sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]};
+  if ((tile + 1) * V2_TILE > L) {   // tail of the sequence
+    const int t0 = tile * V2_TILE + gid;
+    if (t0 >= L) sc[0] = sc[1] = neg_inf();
+    if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
+  }
+  uint32_t bP0, bP1;
+  softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
+  // ---- O^T += V^T P: subvector J = 8*pp + gid, tokens (2tig, 2tig+1, 2tig+8, 2tig+9)
+#define VQKV_PV_STEP(PP, W)                                                                    \
+  {                                                                                            \
+    const uint2 R0 = lds_at<uint2>(s_v, cb_offset<0>(W, vlane));                               \
+    const uint2 R1 = lds_at<uint2>(s_v, cb_offset<1>(W, vlane));                               \
+    const uint2 R2 = lds_at<uint2>(s_v, cb_offset<2>(W, vlane));                               \
+    const uint2 R3 = lds_at<uint2>(s_v, cb_offset<3>(W, vlane));                               \
+    mma_16816(acc[2 * (PP)], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632), \
+              __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP0, bP1);     \
+    mma_16816(acc[2 * (PP) + 1], __byte_perm(R0.y, R1.y, 0x5410),                              \
+              __byte_perm(R0.y, R1.y, 0x7632), __byte_perm(R2.y, R3.y, 0x5410),                \
+              __byte_perm(R2.y, R3.y, 0x7632), bP0, bP1);                                      \
+  }
+  VQKV_PV_STEP(0, vq.x) VQKV_PV_STEP(1, vq.y) VQKV_PV_STEP(2, vq.z) VQKV_PV_STEP(3, vq.w)
+#undef VQKV_PV_STEP
+}
+
+__global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint2* s_kcb = reinterpret_cast<uint2*>(smem);
-  uint2* s_vcb = reinterpret_cast<uint2*>(smem + V2_CB_BYTES);
-  float* s_comb = reinterpret_cast<float*>(smem + 2 * V2_CB_BYTES);
-  float* s_qp = s_comb;   // q' lives in the combine area until the tile loop starts
+  // K: word (code c, row, replica r) at c*256 + row*128 + r*4, row 0 = channels
+  // (0,1), row 1 = (2,3); V: 8-byte centroid c, replica r at c*256 + r*8.
+  // Lane l reads replica l: the 32 lanes of a 32-bit gather hit 32 banks, the
+  // 16 lanes of each half-warp phase of a 64-bit gather hit 16 bank pairs.
+  unsigned char* s_k = smem;
+  unsigned char* s_v = smem + V2_K_BYTES;
+  float* s_qp = reinterpret_cast<float*>(smem + V2_Q_OFF);
+  float* s_comb = reinterpret_cast<float*>(smem);   // after the tile loop only
   __shared__ int s_last;
 
   const int split = blockIdx.x, kvh = blockIdx.y;
@@ -248,9 +315,8 @@ __global__ void __launch_bounds__(V2_THREADS, 2) decode_vq2_kernel(const DecodeP
   const int gid = lane >> 2, tig = lane & 3;
   const int b_begin = blockIdx.z * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
-  const uint32_t kcb_s = smem_u32(s_kcb) + (lane & 15) * 8;   // this lane's replica
-  const uint32_t vcb_s = smem_u32(s_vcb) + (lane & 15) * 8;
-  bool have_cb = false;
+  const uint32_t klane = (uint32_t)lane << 2;
+  const uint32_t vlane = (uint32_t)lane << 3;
 
   for (int b = b_begin; b < b_end; ++b) {
     const int L = load_len(p, b);
@@ -260,19 +326,32 @@ __global__ void __launch_bounds__(V2_THREADS, 2) decode_vq2_kernel(const DecodeP
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
-      if (!have_cb) {
-        // replica r of entry c at [c*16 + r]; consecutive threads write consecutive slots
+      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      if (threadIdx.x == 0) {   // first window of the L2 prefetch
+        const int pf_end = min(t_end, t_begin + V2_PF_AHEAD);
+        for (int t = t_begin; t < pf_end; t += V2_PF_CHUNK) {
+          const uint32_t n = (uint32_t)(min(V2_PF_CHUNK, pf_end - t) * V2_TILE_BYTES);
+          prefetch_l2_bulk(kbase + (size_t)t * V2_TILE_BYTES, n);
+          prefetch_l2_bulk(vbase + (size_t)t * V2_TILE_BYTES, n);
+        }
+      }
+      {
         const uint2* gk = reinterpret_cast<const uint2*>(p.kcb) + (size_t)kvh * 256;
         const uint2* gv = reinterpret_cast<const uint2*>(p.vcb) + (size_t)kvh * 256;
+        uint32_t* sk = reinterpret_cast<uint32_t*>(s_k);
+        uint2* sv = reinterpret_cast<uint2*>(s_v);
+        // consecutive threads write consecutive words
 #pragma unroll 4
-        for (int k = threadIdx.x; k < 256 * V2_REPL; k += V2_THREADS) {
-          s_kcb[k] = __ldg(gk + (k >> 4));
-          s_vcb[k] = __ldg(gv + (k >> 4));
+        for (int k = threadIdx.x; k < 256 * 64; k += V2_THREADS) {
+          const uint2 e = __ldg(gk + (k >> 6));
+          sk[k] = ((k >> 5) & 1) ? e.y : e.x;
         }
-        have_cb = true;
+#pragma unroll 4
+        for (int k = threadIdx.x; k < 256 * 32; k += V2_THREADS) sv[k] = __ldg(gv + (k >> 5));
       }
       transform_queries(p, b, kvh, warp, lane, s_qp);
       __syncthreads();
@@ -288,69 +367,37 @@ __global__ void __launch_bounds__(V2_THREADS, 2) decode_vq2_kernel(const DecodeP
           qf[s][0] = qf[s][1] = 0u;
         }
       }
-      __syncthreads();   // s_qp is reused by the combine below
 
-      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      // Two code buffers (A, B) alternate; the next tile's load is clamped to
+      // the last tile of the range instead of branching.
+      const uint8_t* kl = kbase + lane * 16;
+      const uint8_t* vl = vbase + lane * 16;
+      const int last = t_end - 1;
       int tile = t_begin + warp;
-      uint4 kq = make_uint4(0, 0, 0, 0), vq = make_uint4(0, 0, 0, 0);
-      if (tile < t_end) {
-        kq = ldg_stream(kbase + (size_t)tile * V2_TILE_BYTES + lane * 16);
-        vq = ldg_stream(vbase + (size_t)tile * V2_TILE_BYTES + lane * 16);
-      }
-      for (; tile < t_end; tile += V2_WARPS) {
-        const int nxt = tile + V2_WARPS;
-        uint4 kn = kq, vn = vq;
-        if (nxt < t_end) {
-          kn = ldg_stream(kbase + (size_t)nxt * V2_TILE_BYTES + lane * 16);
-          vn = ldg_stream(vbase + (size_t)nxt * V2_TILE_BYTES + lane * 16);
+      int pf_next = t_begin + V2_PF_AHEAD;   // warp 0: next prefetch position
+      uint4 kA = ldg_stream(kl + (size_t)min(tile, last) * V2_TILE_BYTES);
+      uint4 vA = ldg_stream(vl + (size_t)min(tile, last) * V2_TILE_BYTES);
+      while (tile < t_end) {
+        if (warp == 0 && lane == 0 && pf_next < t_end && pf_next <= tile + V2_PF_AHEAD) {
+          const uint32_t n = (uint32_t)(min(V2_PF_CHUNK, t_end - pf_next) * V2_TILE_BYTES);
+          prefetch_l2_bulk(kbase + (size_t)pf_next * V2_TILE_BYTES, n);
+          prefetch_l2_bulk(vbase + (size_t)pf_next * V2_TILE_BYTES, n);
+          pf_next += V2_PF_CHUNK;
         }
-        if (lane == 0) {
-          const int pf = tile + V2_PF_TILES;
-          if (pf < t_end) {
-            prefetch_l2_bulk(kbase + (size_t)pf * V2_TILE_BYTES, V2_TILE_BYTES);
-            prefetch_l2_bulk(vbase + (size_t)pf * V2_TILE_BYTES, V2_TILE_BYTES);
-          }
-        }
-
-        // ---- scores: 8 k-steps of 16 channels (4 subvectors)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint32_t w0 = (s < 4) ? kq.x : kq.y;   // token gid
-          const uint32_t w1 = (s < 4) ? kq.z : kq.w;   // token gid + 8
-          const uint32_t c0 = (w0 >> (8 * (s & 3))) & 0xffu;
-          const uint32_t c1 = (w1 >> (8 * (s & 3))) & 0xffu;
-          const uint2 A = lds64(kcb_s + c0 * (V2_REPL * 8));
-          const uint2 B = lds64(kcb_s + c1 * (V2_REPL * 8));
-          mma_16816(sc, A.x, B.x, A.y, B.y, qf[s][0], qf[s][1]);
-        }
-        // ---- mask the tail of the sequence
-        if ((tile + 1) * V2_TILE > L) {
-          const int t0 = tile * V2_TILE + gid;
-          if (t0 >= L) sc[0] = sc[1] = neg_inf();
-          if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
-        }
-        uint32_t bP0, bP1;
-        softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
-
-        // ---- O^T += V^T P: subvector J = 8*pp + gid, tokens (2tig, 2tig+1, 2tig+8, 2tig+9)
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const uint32_t w = (pp == 0) ? vq.x : (pp == 1) ? vq.y : (pp == 2) ? vq.z : vq.w;
-          const uint2 R0 = lds64(vcb_s + ((w)&0xffu) * (V2_REPL * 8));
-          const uint2 R1 = lds64(vcb_s + ((w >> 8) & 0xffu) * (V2_REPL * 8));
-          const uint2 R2 = lds64(vcb_s + ((w >> 16) & 0xffu) * (V2_REPL * 8));
-          const uint2 R3 = lds64(vcb_s + (w >> 24) * (V2_REPL * 8));
-          mma_16816(acc[2 * pp], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632),
-                    __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP0, bP1);
-          mma_16816(acc[2 * pp + 1], __byte_perm(R0.y, R1.y, 0x5410), __byte_perm(R0.y, R1.y, 0x7632),
-                    __byte_perm(R2.y, R3.y, 0x5410), __byte_perm(R2.y, R3.y, 0x7632), bP0, bP1);
-        }
-        kq = kn;
-        vq = vn;
+        const int t1 = min(tile + V2_WARPS, last);
+        const uint4 kB = ldg_stream(kl + (size_t)t1 * V2_TILE_BYTES);
+        const uint4 vB = ldg_stream(vl + (size_t)t1 * V2_TILE_BYTES);
+        vq2_tile(s_k, s_v, klane, vlane, qf, kA, vA, tile, L, gid, m0, m1, l0, l1, acc);
+        tile += V2_WARPS;
+        if (tile >= t_end) break;
+        const int t2 = min(tile + V2_WARPS, last);
+        kA = ldg_stream(kl + (size_t)t2 * V2_TILE_BYTES);
+        vA = ldg_stream(vl + (size_t)t2 * V2_TILE_BYTES);
+        vq2_tile(s_k, s_v, klane, vlane, qf, kB, vB, tile, L, gid, m0, m1, l0, l1, acc);
+        tile += V2_WARPS;
       }
     }
+    __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
     stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
     __syncthreads();
     finish_sequence<V2_WARPS>(p, b, kvh, split, s_comb, &s_last);
@@ -391,7 +438,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
       if (!have_cb) {

@@ -119,9 +119,60 @@ __device__ __forceinline__ bool is_near_tie(float best, float second) {
   return __fsub_rn(second, best) < 1e-6f * fmaxf(best, 1e-30f);
 }
 
+// Running nearest-centroid state of one search chain: best distance, its
+// index, second-best distance.  Chains scan disjoint candidate sets in
+// increasing index order, so a strict "<" keeps the lowest index on ties.
+struct Best {
+  float d, s;
+  int i;
+};
+
+__device__ __forceinline__ Best best_init() {
+  const float inf = __int_as_float(0x7f800000);
+  return {inf, inf, 0};
+}
+
+__device__ __forceinline__ void best_push(Best& b, float d, int c) {
+  const bool lt = d < b.d;
+  b.s = lt ? b.d : fminf(b.s, d);
+  b.i = lt ? c : b.i;
+  b.d = lt ? d : b.d;
+}
+
+// Merge two chains over disjoint candidates: lower distance, then lower index.
+__device__ __forceinline__ Best best_merge(Best a, Best b) {
+  if (b.d < a.d || (b.d == a.d && b.i < a.i)) return {b.d, fminf(a.d, b.s), b.i};
+  return {a.d, fminf(a.s, b.d), a.i};
+}
+
+__device__ __forceinline__ Best best_shfl_xor(Best b, int m) {
+  return {__shfl_xor_sync(0xffffffffu, b.d, m), __shfl_xor_sync(0xffffffffu, b.s, m),
+          __shfl_xor_sync(0xffffffffu, b.i, m)};
+}
+
+// Cross-warp merge for SPLIT > 1: every warp searched a slice of the
+// candidates for the same row; warp 0 ends up with the merged state.
+template <int SPLIT>
+__device__ __forceinline__ Best merge_warps(Best b, int warp, int lane, Best* s_part) {
+  if (SPLIT == 1) return b;
+  __syncthreads();   // the previous row's readers are done with s_part
+  s_part[warp * 32 + lane] = b;
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int w = 1; w < SPLIT; ++w) b = best_merge(b, s_part[w * 32 + lane]);
+  }
+  return b;
+}
+
 // ------------------------------------------------------------------ VQ2
+// SPLIT = 1: one warp per row, lane = subvector, 256 candidates per lane.
+// SPLIT = 8: the CTA's 8 warps share one row, 32 candidates each (few rows,
+// e.g. a decode-step append: latency instead of throughput).
+template <int SPLIT>
 __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodeParams p) {
   __shared__ float4 s_cb[256];
+  __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int c = threadIdx.x; c < 256; c += ENC_THREADS) {
@@ -132,51 +183,56 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
   }
   __syncthreads();
   const int rows = p.B * p.n_rows;
-  for (int r = blockIdx.x * ENC_WARPS + warp; r < rows; r += gridDim.x * ENC_WARPS) {
+  const int r0 = (SPLIT == 1) ? blockIdx.x * ENC_WARPS + warp : blockIdx.x;
+  const int rstep = (SPLIT == 1) ? gridDim.x * ENC_WARPS : gridDim.x;
+  const int c_lo = (SPLIT == 1) ? 0 : warp * (256 / SPLIT);
+  const int c_hi = c_lo + 256 / SPLIT;
+  for (int r = r0; r < rows; r += rstep) {
     const int b = r / p.n_rows, n = r - b * p.n_rows;
     const int t = p.pos[b] + n;
     if (t < 0 || t >= p.cap_len) {
-      if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      if (lane == 0 && (SPLIT == 1 || warp == 0) && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
       continue;
     }
     float x[4];
     transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
-    // lane = subvector j (channels 4j..4j+3)
-    float best = __int_as_float(0x7f800000), second = best;
-    int bi = 0;
+    // lane = subvector j (channels 4j..4j+3); two chains (even / odd candidates)
+    Best e = best_init(), o = best_init();
 #pragma unroll 4
-    for (int c = 0; c < 256; ++c) {
-      const float4 cc = s_cb[c];
-      const float e0 = __fsub_rn(x[0], cc.x), e1 = __fsub_rn(x[1], cc.y);
-      const float e2 = __fsub_rn(x[2], cc.z), e3 = __fsub_rn(x[3], cc.w);
-      float d = __fmul_rn(e0, e0);
-      d = __fmaf_rn(e1, e1, d);
-      d = __fmaf_rn(e2, e2, d);
-      d = __fmaf_rn(e3, e3, d);
-      if (d < best) {
-        second = best;
-        best = d;
-        bi = c;
-      } else if (d < second) {
-        second = d;
-      }
+    for (int c = c_lo; c < c_hi; c += 2) {
+      const float4 ca = s_cb[c], cb = s_cb[c + 1];
+      float u = __fsub_rn(x[0], ca.x), d0 = __fmul_rn(u, u);
+      u = __fsub_rn(x[1], ca.y); d0 = __fmaf_rn(u, u, d0);
+      u = __fsub_rn(x[2], ca.z); d0 = __fmaf_rn(u, u, d0);
+      u = __fsub_rn(x[3], ca.w); d0 = __fmaf_rn(u, u, d0);
+      float v = __fsub_rn(x[0], cb.x), d1 = __fmul_rn(v, v);
+      v = __fsub_rn(x[1], cb.y); d1 = __fmaf_rn(v, v, d1);
+      v = __fsub_rn(x[2], cb.z); d1 = __fmaf_rn(v, v, d1);
+      v = __fsub_rn(x[3], cb.w); d1 = __fmaf_rn(v, v, d1);
+      best_push(e, d0, c);
+      best_push(o, d1, c + 1);
     }
-    count_near_ties(p, is_near_tie(best, second), lane, 0xffffffffu);
-    // pack: byte offset of (t, j = lane) in the stream
-    const int tile = t >> 4, rr = t & 15, j = lane;
-    const long long off = (p.role == VQKV_ROLE_K)
-                              ? 512LL * tile + 16 * (4 * (rr & 7) + (j & 3)) + 8 * (rr >> 3) + (j >> 2)
-                              : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
-    p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + off] = (uint8_t)bi;
+    Best bst = merge_warps<SPLIT>(best_merge(e, o), warp, lane, s_part);
+    if (SPLIT == 1 || warp == 0) {
+      count_near_ties(p, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+      // pack: byte offset of (t, j = lane) in the stream
+      const int tile = t >> 4, rr = t & 15, j = lane;
+      const long long off = (p.role == VQKV_ROLE_K)
+                                ? 512LL * tile + 16 * (4 * (rr & 7) + (j & 3)) + 8 * (rr >> 3) + (j >> 2)
+                                : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
+      p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + off] = (uint8_t)bst.i;
+    }
   }
 }
 
 // ------------------------------------------------------------------ VQ15
 // Codebook as fp32 in shared memory (128 KB).  The two lanes of a subvector
 // (channels 8J..8J+7 live on lanes 2J, 2J+1) both hold all 8 channels and
-// search half of the 4096 centroids each; the halves are merged at the end.
+// search half of the candidates each (of the CTA's slice when SPLIT > 1).
+template <int SPLIT>
 __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodeParams p) {
   extern __shared__ __align__(16) float4 s_cb15[];   // [4096][2]
+  __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int c = threadIdx.x; c < 4096; c += ENC_THREADS) {
@@ -191,11 +247,16 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodePa
   __syncthreads();
   const int rows = p.B * p.n_rows;
   const int half = lane & 1;
-  for (int r = blockIdx.x * ENC_WARPS + warp; r < rows; r += gridDim.x * ENC_WARPS) {
+  const int r0 = (SPLIT == 1) ? blockIdx.x * ENC_WARPS + warp : blockIdx.x;
+  const int rstep = (SPLIT == 1) ? gridDim.x * ENC_WARPS : gridDim.x;
+  constexpr int kSlice = 4096 / SPLIT;   // candidates of this warp
+  const int c_lo = ((SPLIT == 1) ? 0 : warp * kSlice) + half * (kSlice / 2);
+  const int c_hi = c_lo + kSlice / 2;
+  for (int r = r0; r < rows; r += rstep) {
     const int b = r / p.n_rows, n = r - b * p.n_rows;
     const int t = p.pos[b] + n;
     if (t < 0 || t >= p.cap_len) {
-      if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      if (lane == 0 && (SPLIT == 1 || warp == 0) && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
       continue;
     }
     float x[4];
@@ -207,57 +268,46 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodePa
       y[i] = half ? o : x[i];
       y[4 + i] = half ? x[i] : o;
     }
-    float best = __int_as_float(0x7f800000), second = best;
-    int bi = 0;
-    const int c0 = half * 2048;
+    Best e = best_init(), od = best_init();
 #pragma unroll 2
-    for (int c = c0; c < c0 + 2048; ++c) {
-      const float4 lo = s_cb15[2 * c], hi = s_cb15[2 * c + 1];
-      float e = __fsub_rn(y[0], lo.x);
-      float d = __fmul_rn(e, e);
-      e = __fsub_rn(y[1], lo.y); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[2], lo.z); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[3], lo.w); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[4], hi.x); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[5], hi.y); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[6], hi.z); d = __fmaf_rn(e, e, d);
-      e = __fsub_rn(y[7], hi.w); d = __fmaf_rn(e, e, d);
-      if (d < best) {
-        second = best;
-        best = d;
-        bi = c;
-      } else if (d < second) {
-        second = d;
+    for (int c = c_lo; c < c_hi; c += 2) {
+      float dd[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float4 lo = s_cb15[2 * (c + k)], hi = s_cb15[2 * (c + k) + 1];
+        float u = __fsub_rn(y[0], lo.x);
+        float d = __fmul_rn(u, u);
+        u = __fsub_rn(y[1], lo.y); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[2], lo.z); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[3], lo.w); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[4], hi.x); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[5], hi.y); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[6], hi.z); d = __fmaf_rn(u, u, d);
+        u = __fsub_rn(y[7], hi.w); d = __fmaf_rn(u, u, d);
+        dd[k] = d;
       }
+      best_push(e, dd[0], c);
+      best_push(od, dd[1], c + 1);
     }
-    // merge the two halves: lower distance, then lower index
-    const float ob = __shfl_xor_sync(0xffffffffu, best, 1);
-    const float os = __shfl_xor_sync(0xffffffffu, second, 1);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, 1);
-    float mb, ms;
-    int mi;
-    if (ob < best || (ob == best && oi < bi)) {
-      mb = ob;
-      mi = oi;
-      ms = fminf(os, best);
-    } else {
-      mb = best;
-      mi = bi;
-      ms = fminf(second, ob);
-    }
-    count_near_ties(p, is_near_tie(mb, ms), lane, 0x55555555u);
-    // lanes 2p (p < 8) hold subvector p; subvector p+8 sits on lane 2p+16
-    const int hi_code = __shfl_down_sync(0xffffffffu, mi, 16);
-    if (lane < 16 && half == 0) {
-      const int pair = lane >> 1;
-      const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
-      const long long off = (p.role == VQKV_ROLE_K)
-                                ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
-                                : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
-      uint8_t* dst = p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + off;
-      dst[0] = (uint8_t)(mi & 0xff);
-      dst[1] = (uint8_t)(((mi >> 8) & 0xf) | ((hi_code & 0xf) << 4));
-      dst[2] = (uint8_t)(hi_code >> 4);
+    // the two halves of the pair hold disjoint candidate sets: merge them
+    Best mine = best_merge(e, od);
+    Best bst = best_merge(mine, best_shfl_xor(mine, 1));
+    bst = merge_warps<SPLIT>(bst, warp, lane, s_part);
+    if (SPLIT == 1 || warp == 0) {
+      count_near_ties(p, is_near_tie(bst.d, bst.s), lane, 0x55555555u);
+      // lanes 2p (p < 8) hold subvector p; subvector p+8 sits on lane 2p+16
+      const int hi_code = __shfl_down_sync(0xffffffffu, bst.i, 16);
+      if (lane < 16 && half == 0) {
+        const int pair = lane >> 1;
+        const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
+        const long long off = (p.role == VQKV_ROLE_K)
+                                  ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
+                                  : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
+        uint8_t* dst = p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + off;
+        dst[0] = (uint8_t)(bst.i & 0xff);
+        dst[1] = (uint8_t)(((bst.i >> 8) & 0xf) | ((hi_code & 0xf) << 4));
+        dst[2] = (uint8_t)(hi_code >> 4);
+      }
     }
   }
 }
@@ -269,23 +319,35 @@ constexpr size_t kV15EncSmem = 4096 * 2 * sizeof(float4);
 int encode_warps_per_cta() { return ENC_WARPS; }
 
 cudaError_t encode_prepare(int mode) {
-  if (mode == VQKV_MODE_VQ15)
-    return cudaFuncSetAttribute(encode_vq15_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV15EncSmem);
-  return cudaSuccess;
+  if (mode != VQKV_MODE_VQ15) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(encode_vq15_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kV15EncSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(encode_vq15_kernel<ENC_WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kV15EncSmem);
 }
 
 cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel, ENC_THREADS, 0);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_kernel, ENC_THREADS, kV15EncSmem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1>, ENC_THREADS, 0);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_kernel<1>, ENC_THREADS,
+                                                       kV15EncSmem);
 }
 
-cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, cudaStream_t stream) {
+// split_rows: one row per CTA, candidates split over the CTA's warps.
+cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool split_rows, cudaStream_t stream) {
   const dim3 grid(blocks_x, p.Hkv);
-  if (mode == VQKV_MODE_VQ2)
-    encode_vq2_kernel<<<grid, ENC_THREADS, 0, stream>>>(p);
-  else
-    encode_vq15_kernel<<<grid, ENC_THREADS, kV15EncSmem, stream>>>(p);
+  if (mode == VQKV_MODE_VQ2) {
+    if (split_rows)
+      encode_vq2_kernel<ENC_WARPS><<<grid, ENC_THREADS, 0, stream>>>(p);
+    else
+      encode_vq2_kernel<1><<<grid, ENC_THREADS, 0, stream>>>(p);
+  } else {
+    if (split_rows)
+      encode_vq15_kernel<ENC_WARPS><<<grid, ENC_THREADS, kV15EncSmem, stream>>>(p);
+    else
+      encode_vq15_kernel<1><<<grid, ENC_THREADS, kV15EncSmem, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -61,7 +61,7 @@ size_t decode_ticket_region_bytes(int B, int Hkv);       // error word + tickets
 // Encode kernels (encode.cu).
 cudaError_t encode_prepare(int mode);
 cudaError_t encode_occupancy(int mode, int* blocks_per_sm);
-cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, cudaStream_t stream);
+cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool split_rows, cudaStream_t stream);
 int encode_warps_per_cta();
 
 }  // namespace vqkv
