@@ -87,6 +87,7 @@ typedef enum {
 /* Bits of the device error word (see error_flags / workspace word 0). */
 #define VQKV_DEVERR_SEQ_LEN   0x1u  /* a seq_lens[b] outside [0, max_seq_len]: clamped */
 #define VQKV_DEVERR_POSITION  0x2u  /* an encode row outside [0, cap_len): not written */
+#define VQKV_DEVERR_TIMEOUT   0x4u  /* a bounded on-chip wait gave up; that CTA's output is invalid */
 
 /*
  * vqkv_encode — smoothing, Hadamard rotation, nearest-centroid assignment and
@@ -157,7 +158,8 @@ typedef struct {
   void* workspace;       /* device, >= vqkv_decode_workspace_bytes(args), 256-byte aligned,
                             zero-filled before its first use; every completed call leaves
                             it ready for the next.  Word 0 (uint32) is the device error
-                            word (VQKV_DEVERR_SEQ_LEN; sticky, the caller may clear it) */
+                            word (VQKV_DEVERR_SEQ_LEN, VQKV_DEVERR_TIMEOUT; sticky, the
+                            caller may clear it) */
   size_t workspace_bytes;
   uint16_t* out;         /* device fp16 [B][Hq][128] */
 } vqkv_decode_args;

@@ -126,7 +126,8 @@ vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
       }
     }
   }
-  const long long tps = (tiles_max + best_n - 1) / best_n;
+  const long long unit = decode_tiles_per_step(a->mode);
+  const long long tps = ((tiles_max + best_n - 1) / best_n + unit - 1) / unit * unit;
   pl->tps = (int)tps;
   pl->n_splits = (int)((tiles_max + tps - 1) / tps);
   pl->bpg = bpg;

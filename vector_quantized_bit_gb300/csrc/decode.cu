@@ -47,16 +47,30 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 constexpr float kMInit = -1e30f;
 
 // ------------------------------------------------------------------ VQ2
-constexpr int V2_WARPS = 16;                       // one CTA per SM
+#ifndef VQKV_V2_WARPS
+#define VQKV_V2_WARPS 16
+#endif
+#ifndef VQKV_V2_TPI
+#define VQKV_V2_TPI 2
+#endif
+#ifndef VQKV_V2_STAGES
+#define VQKV_V2_STAGES 4
+#endif
+constexpr int V2_WARPS = VQKV_V2_WARPS;             // one CTA per SM
+constexpr int V2_TPI = VQKV_V2_TPI;                 // 16-token tiles per step (a "super-tile")
 constexpr int V2_THREADS = V2_WARPS * 32;
 constexpr int V2_TILE = 16;
 constexpr int V2_TILE_BYTES = 512;
-constexpr int V2_REPL = 32;                         // codebook replicas: one per lane
-constexpr int V2_K_BYTES = 256 * 256;               // K: [code][row d01|d23][32 replicas] fp16x2 words
-constexpr int V2_V_BYTES = 256 * 256;               // V: [code][32 replicas] 8-byte centroids
-constexpr int V2_Q_OFF = V2_K_BYTES + V2_V_BYTES;   // q' (fp32 [8][128]) after the codebooks
-constexpr int V2_PF_CHUNK = 16;                     // tiles per L2 prefetch request
-constexpr int V2_PF_AHEAD = 96;                     // tiles kept in flight ahead of warp 0
+constexpr int V2_REPL = 16;                         // replicas of each centroid (bank spreading)
+static_assert(V2_REPL * 8 == 128, "one 128-byte half row per codebook");
+constexpr int V2_CB_BYTES = 256 * 256;              // [code][K replicas (128 B) | V replicas (128 B)]
+constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][128]) after the codebooks
+constexpr int V2_STAGES = VQKV_V2_STAGES;           // per-warp ring of super-tiles (K then V)
+constexpr int V2_STAGE_BYTES = 2 * V2_TPI * V2_TILE_BYTES;
+constexpr int V2_RING_OFF = V2_Q_OFF + 8 * 128 * 4;
+constexpr int V2_RING_BYTES = V2_WARPS * V2_STAGES * V2_STAGE_BYTES;
+constexpr int V2_MBAR_OFF = V2_RING_OFF + V2_RING_BYTES;
+constexpr uint32_t kMaxPolls = 1u << 22;            // bounded mbarrier waits
 
 // ------------------------------------------------------------------ VQ15
 constexpr int V15_WARPS = 16;
@@ -72,9 +86,10 @@ struct CombineSmem {
   static constexpr int kBytes = (kO + 2 * WARPS * 8) * 4;
 };
 
-// Codebooks + q'; the combine area reuses the codebook region after the tile loop.
-constexpr size_t kV2Smem = V2_Q_OFF + 8 * 128 * 4;
-static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_Q_OFF, "combine area must fit in the codebook region");
+// Codebooks, q', code ring, ring barriers; the combine area reuses the
+// codebook and q' region after the tile loop.
+constexpr size_t kV2Smem = V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8;
+static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must fit below the ring");
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
 
 // q' for the g heads of (b, kvh) into s_qp[h][128] (fp32, scaled), by warps 0..g-1.
@@ -140,6 +155,53 @@ __device__ __forceinline__ void softmax_tile(float (&sc)[4], float& m0, float& m
   l1 += p1 + p3;
   bP0 = movmatrix_t(pack_half2(p0, p1));   // P[tokens 2tig, 2tig+1][head gid]
   bP1 = movmatrix_t(pack_half2(p2, p3));   // P[tokens 2tig+8, 2tig+9][head gid]
+}
+
+// Online-softmax update for T tiles at once (one running max for all of
+// them), then P packed for the P.V MMA of each tile.
+template <int T, int NACC>
+__device__ __forceinline__ void softmax_tiles(float (&sc)[T][4], float& m0, float& m1, float& l0, float& l1,
+                                              float (&acc)[NACC][4], uint32_t (&bP)[T][2]) {
+  bool need = false;
+#pragma unroll
+  for (int i = 0; i < T; ++i)
+    need |= (sc[i][0] > m0 + kSoftmaxSlack) | (sc[i][2] > m0 + kSoftmaxSlack) |
+            (sc[i][1] > m1 + kSoftmaxSlack) | (sc[i][3] > m1 + kSoftmaxSlack);
+  if (__any_sync(0xffffffffu, need)) {
+    float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+    for (int i = 1; i < T; ++i) {
+      x0 = fmaxf(x0, fmaxf(sc[i][0], sc[i][2]));
+      x1 = fmaxf(x1, fmaxf(sc[i][1], sc[i][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    l0 *= a0;
+    l1 *= a1;
+#pragma unroll
+    for (int i = 0; i < NACC; ++i) {
+      acc[i][0] *= a0;
+      acc[i][1] *= a1;
+      acc[i][2] *= a0;
+      acc[i][3] *= a1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    const float p0 = fast_exp2(sc[i][0] - m0), p1 = fast_exp2(sc[i][1] - m1);
+    const float p2 = fast_exp2(sc[i][2] - m0), p3 = fast_exp2(sc[i][3] - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    bP[i][0] = movmatrix_t(pack_half2(p0, p1));
+    bP[i][1] = movmatrix_t(pack_half2(p2, p3));
+  }
 }
 
 // Merge the per-warp states of the CTA into one partial (m, l, O) per head
@@ -250,62 +312,144 @@ __device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
   return *reinterpret_cast<const T*>(base + off);
 }
 
-// One 16-token tile of the 2-bit path: scores, online softmax, P.V.
-//   kq: this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig)
-//   vq: this lane's 16 value-code bytes (word p: tokens 2tig, 2tig+1,
-//       2tig+8, 2tig+9 of subvector 8p+gid)
-__device__ __forceinline__ void vq2_tile(const unsigned char* s_k, const unsigned char* s_v, uint32_t klane,
-                                         uint32_t vlane, const uint32_t (&qf)[8][2], uint4 kq, uint4 vq,
-                                         int tile, int L, int gid, float& m0, float& m1, float& l0, float& l1,
-                                         float (&acc)[8][4]) {
-  // ---- scores: 8 k-steps of 16 channels; two independent MMA chains.
-  // a0a1/a4a5 = channels (0,1)/(2,3) of token gid, a2a3/a6a7 of token gid+8:
-  // four 32-bit gathers straight into the operand registers.
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#define VQKV_SCORE_STEP(S, ACC)                                                   \
-  {                                                                               \
-    const uint32_t oa = cb_offset<(S)&3>(((S) < 4) ? kq.x : kq.y, klane);         \
-    const uint32_t ob = cb_offset<(S)&3>(((S) < 4) ? kq.z : kq.w, klane);         \
-    mma_16816(ACC, lds_at<uint32_t>(s_k, oa), lds_at<uint32_t>(s_k, ob),          \
-              lds_at<uint32_t>(s_k + 128, oa), lds_at<uint32_t>(s_k + 128, ob),   \
-              qf[S][0], qf[S][1]);                                                \
+// One step of the 2-bit path over T consecutive 16-token tiles.
+//
+// Scores run as S[h][t] = q'[h] . K'[t] with heads as MMA rows (rows g..15
+// are zero) and 8 tokens as columns per MMA: the B operand of k-step s for
+// token n = gid is channels 4j..4j+3 of subvector j = 4s+tig, i.e. exactly one
+// 8-byte centroid gather, and the result (head gid x tokens 2tig, 2tig+1) is
+// already the B operand the P.V MMA wants for that head.
+//   kq[i]: this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig)
+//   vq[i]: this lane's 16 value-code bytes (word p: tokens 2tig, 2tig+1,
+//          2tig+8, 2tig+9 of subvector 8p+gid)
+// Softmax state m, l belongs to head gid; O^T fragments hold heads 2tig, 2tig+1.
+template <int T>
+__device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
+                                         const uint32_t (&qa)[8][2], const uint4 (&kq)[T], const uint4 (&vq)[T],
+                                         int tile0, int L, int lane, float& m, float& l, float (&acc)[8][4]) {
+  const int tig = lane & 3;
+  // sc[i][u][e]: score of head gid for token 16(tile0+i) + 8u + 2tig + e
+  float sc[T][2][2];
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t w_lo = u ? kq[i].z : kq[i].x;   // subvectors 4s+tig, s = 0..3
+      const uint32_t w_hi = u ? kq[i].w : kq[i].y;   // s = 4..7
+#define VQKV_SCORE_STEP(S, ACC)                                                          \
+  {                                                                                      \
+    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? w_lo : w_hi, kbyte)); \
+    mma_16816(ACC, qa[S][0], 0u, qa[S][1], 0u, c.x, c.y);                                \
   }
-  VQKV_SCORE_STEP(0, sa) VQKV_SCORE_STEP(1, sb) VQKV_SCORE_STEP(2, sa) VQKV_SCORE_STEP(3, sb)
-  VQKV_SCORE_STEP(4, sa) VQKV_SCORE_STEP(5, sb) VQKV_SCORE_STEP(6, sa) VQKV_SCORE_STEP(7, sb)
+      VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
+      VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
 #undef VQKV_SCORE_STEP
-  float sc[4] = {sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]};
-  if ((tile + 1) * V2_TILE > L) {   // tail of the sequence
-    const int t0 = tile * V2_TILE + gid;
-    if (t0 >= L) sc[0] = sc[1] = neg_inf();
-    if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
+      sc[i][u][0] = da[0] + db[0];
+      sc[i][u][1] = da[1] + db[1];
+    }
   }
-  uint32_t bP0, bP1;
-  softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
+  if ((tile0 + T) * V2_TILE > L) {   // tail of the sequence
+#pragma unroll
+    for (int i = 0; i < T; ++i)
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if ((tile0 + i) * V2_TILE + 8 * u + 2 * tig + e >= L) sc[i][u][e] = neg_inf();
+  }
+  // ---- online softmax for head gid (rescale only when a score exceeds m by 2^8)
+  bool need = false;
+#pragma unroll
+  for (int i = 0; i < T; ++i)
+    need |= (sc[i][0][0] > m + kSoftmaxSlack) | (sc[i][0][1] > m + kSoftmaxSlack) |
+            (sc[i][1][0] > m + kSoftmaxSlack) | (sc[i][1][1] > m + kSoftmaxSlack);
+  if (__any_sync(0xffffffffu, need)) {
+    float x = fmaxf(fmaxf(sc[0][0][0], sc[0][0][1]), fmaxf(sc[0][1][0], sc[0][1][1]));
+#pragma unroll
+    for (int i = 1; i < T; ++i)
+      x = fmaxf(x, fmaxf(fmaxf(sc[i][0][0], sc[i][0][1]), fmaxf(sc[i][1][0], sc[i][1][1])));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+    const float n = fmaxf(m, x);
+    const float alpha = fast_exp2(m - n);
+    m = n;
+    l *= alpha;
+    // O^T columns of this lane are heads 2tig, 2tig+1: their factors live on lanes 8tig, 8tig+4
+    const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+    const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= a0;
+      acc[mt][1] *= a1;
+      acc[mt][2] *= a0;
+      acc[mt][3] *= a1;
+    }
+  }
+  uint32_t bP[T][2];
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    float p[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) p[u][e] = fast_exp2(sc[i][u][e] - m);
+    l += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+    bP[i][0] = pack_half2(p[0][0], p[0][1]);   // tokens 2tig, 2tig+1 of head gid
+    bP[i][1] = pack_half2(p[1][0], p[1][1]);   // tokens 8+2tig, 9+2tig
+  }
   // ---- O^T += V^T P: subvector J = 8*pp + gid, tokens (2tig, 2tig+1, 2tig+8, 2tig+9)
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
 #define VQKV_PV_STEP(PP, W)                                                                    \
   {                                                                                            \
-    const uint2 R0 = lds_at<uint2>(s_v, cb_offset<0>(W, vlane));                               \
-    const uint2 R1 = lds_at<uint2>(s_v, cb_offset<1>(W, vlane));                               \
-    const uint2 R2 = lds_at<uint2>(s_v, cb_offset<2>(W, vlane));                               \
-    const uint2 R3 = lds_at<uint2>(s_v, cb_offset<3>(W, vlane));                               \
+    const uint2 R0 = lds_at<uint2>(s_cb, cb_offset<0>(W, vbyte));                              \
+    const uint2 R1 = lds_at<uint2>(s_cb, cb_offset<1>(W, vbyte));                              \
+    const uint2 R2 = lds_at<uint2>(s_cb, cb_offset<2>(W, vbyte));                              \
+    const uint2 R3 = lds_at<uint2>(s_cb, cb_offset<3>(W, vbyte));                              \
     mma_16816(acc[2 * (PP)], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632), \
-              __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP0, bP1);     \
+              __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP[i][0], bP[i][1]); \
     mma_16816(acc[2 * (PP) + 1], __byte_perm(R0.y, R1.y, 0x5410),                              \
               __byte_perm(R0.y, R1.y, 0x7632), __byte_perm(R2.y, R3.y, 0x5410),                \
-              __byte_perm(R2.y, R3.y, 0x7632), bP0, bP1);                                      \
+              __byte_perm(R2.y, R3.y, 0x7632), bP[i][0], bP[i][1]);                            \
   }
-  VQKV_PV_STEP(0, vq.x) VQKV_PV_STEP(1, vq.y) VQKV_PV_STEP(2, vq.z) VQKV_PV_STEP(3, vq.w)
+    VQKV_PV_STEP(0, vq[i].x) VQKV_PV_STEP(1, vq[i].y) VQKV_PV_STEP(2, vq[i].z) VQKV_PV_STEP(3, vq[i].w)
 #undef VQKV_PV_STEP
+  }
+}
+
+// Store one warp's (m, l, O) of the 2-bit path into the combine area: m and
+// l are per head gid (l summed over the warp's token columns), O^T as in
+// stash_warp.
+__device__ __forceinline__ void stash_warp_vq2(float* s_comb, int warp, int lane, const float (&acc)[8][4],
+                                               float m, float l) {
+  const int gid = lane >> 2, tig = lane & 3;
+  float* wO = s_comb;
+  float* wm = s_comb + CombineSmem<V2_WARPS>::kO;
+  float* wl = wm + V2_WARPS * 8;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  const int h0 = warp * 8 + 2 * tig;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d0 = Vq2Dim()(mt, gid);
+    wO[h0 * kHeadDim + d0] = acc[mt][0];
+    wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
+    wO[h0 * kHeadDim + d0 + 1] = acc[mt][2];
+    wO[(h0 + 1) * kHeadDim + d0 + 1] = acc[mt][3];
+  }
+  if (tig == 0) {
+    wm[warp * 8 + gid] = m;
+    wl[warp * 8 + gid] = l;
+  }
 }
 
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  // K: word (code c, row, replica r) at c*256 + row*128 + r*4, row 0 = channels
-  // (0,1), row 1 = (2,3); V: 8-byte centroid c, replica r at c*256 + r*8.
-  // Lane l reads replica l: the 32 lanes of a 32-bit gather hit 32 banks, the
-  // 16 lanes of each half-warp phase of a 64-bit gather hit 16 bank pairs.
-  unsigned char* s_k = smem;
-  unsigned char* s_v = smem + V2_K_BYTES;
+  extern __shared__ __align__(128) unsigned char smem[];
+  // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
+  // c*256 + r*8, V replicas at c*256 + 128 + r*8.  Lane l reads replica
+  // l % 16, so each half-warp phase of a 64-bit gather hits 16 bank pairs.
+  const unsigned char* s_cb = smem;
   float* s_qp = reinterpret_cast<float*>(smem + V2_Q_OFF);
   float* s_comb = reinterpret_cast<float*>(smem);   // after the tile loop only
   __shared__ int s_last;
@@ -315,8 +459,18 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int gid = lane >> 2, tig = lane & 3;
   const int b_begin = blockIdx.z * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
-  const uint32_t klane = (uint32_t)lane << 2;
-  const uint32_t vlane = (uint32_t)lane << 3;
+  const uint32_t kbyte = (uint32_t)(lane & 15) << 3;
+  const uint32_t vbyte = 128u | ((uint32_t)(lane & 15) << 3);
+  // this warp's ring: stage st holds the K super-tile, then the V super-tile
+  const uint32_t ring = smem_u32(smem + V2_RING_OFF) + warp * (V2_STAGES * V2_STAGE_BYTES);
+  const uint32_t mbar = smem_u32(smem + V2_MBAR_OFF) + warp * (V2_STAGES * 8);
+  if (lane == 0) {
+    for (int st = 0; st < V2_STAGES; ++st) mbar_init(mbar + 8 * st, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  uint32_t uses = 0;        // super-tiles this warp has taken through its ring (all sequences)
+  bool timed_out = false;
 
   for (int b = b_begin; b < b_end; ++b) {
     const int L = load_len(p, b);
@@ -326,82 +480,93 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
+    float m = kMInit, l = 0.f;
 
     if (t_begin < t_end) {
       const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
       const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-      if (threadIdx.x == 0) {   // first window of the L2 prefetch
-        const int pf_end = min(t_end, t_begin + V2_PF_AHEAD);
-        for (int t = t_begin; t < pf_end; t += V2_PF_CHUNK) {
-          const uint32_t n = (uint32_t)(min(V2_PF_CHUNK, pf_end - t) * V2_TILE_BYTES);
-          prefetch_l2_bulk(kbase + (size_t)t * V2_TILE_BYTES, n);
-          prefetch_l2_bulk(vbase + (size_t)t * V2_TILE_BYTES, n);
-        }
-      }
+      // super-tiles of V2_TPI tiles: this warp takes k = warp + j * V2_WARPS,
+      // j < n_mine, starting at tile t_begin + k * V2_TPI.  The split length is
+      // a multiple of V2_TPI, so a super-tile never reaches into the next split;
+      // tiles past the sequence end are masked, tiles past the capacity are not
+      // copied.
+      const int cap_tiles = (int)(p.stream_bytes / V2_TILE_BYTES);
+      const int n_super = (t_end - t_begin + V2_TPI - 1) / V2_TPI;
+      const int n_mine = warp < n_super ? (n_super - warp + V2_WARPS - 1) / V2_WARPS : 0;
+      auto issue = [&](int j) {
+        const uint32_t st = (uses + j) % V2_STAGES;
+        const int tile0 = t_begin + (warp + j * V2_WARPS) * V2_TPI;
+        const uint32_t n = (uint32_t)min(V2_TPI, cap_tiles - tile0) * V2_TILE_BYTES;
+        const size_t off = (size_t)tile0 * V2_TILE_BYTES;
+        mbar_expect_tx(mbar + 8 * st, 2 * n);
+        tma_load_1d(ring + st * V2_STAGE_BYTES, kbase + off, n, mbar + 8 * st);
+        tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, vbase + off, n, mbar + 8 * st);
+      };
+      // start the ring before the prologue so the copies overlap it
+      if (lane == 0)
+        for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
       {
         const uint2* gk = reinterpret_cast<const uint2*>(p.kcb) + (size_t)kvh * 256;
         const uint2* gv = reinterpret_cast<const uint2*>(p.vcb) + (size_t)kvh * 256;
-        uint32_t* sk = reinterpret_cast<uint32_t*>(s_k);
-        uint2* sv = reinterpret_cast<uint2*>(s_v);
-        // consecutive threads write consecutive words
+        uint2* cb = reinterpret_cast<uint2*>(smem);
+        // slot k = 32*c + j: consecutive threads write consecutive 8-byte slots
 #pragma unroll 4
-        for (int k = threadIdx.x; k < 256 * 64; k += V2_THREADS) {
-          const uint2 e = __ldg(gk + (k >> 6));
-          sk[k] = ((k >> 5) & 1) ? e.y : e.x;
+        for (int k = threadIdx.x; k < 256 * 32; k += V2_THREADS) {
+          const int c = k >> 5, j = k & 31;
+          cb[k] = __ldg((j < 16 ? gk : gv) + c);
         }
-#pragma unroll 4
-        for (int k = threadIdx.x; k < 256 * 32; k += V2_THREADS) sv[k] = __ldg(gv + (k >> 5));
       }
       transform_queries(p, b, kvh, warp, lane, s_qp);
       __syncthreads();
-      uint32_t qf[8][2];
+      // A operand of the score MMA: head gid, channels 4j..4j+3 of j = 4s+tig
+      uint32_t qa[8][2];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * s + tig;
         if (gid < p.g) {
           const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + 4 * j);
-          qf[s][0] = pack_half2(v.x, v.y);
-          qf[s][1] = pack_half2(v.z, v.w);
+          qa[s][0] = pack_half2(v.x, v.y);
+          qa[s][1] = pack_half2(v.z, v.w);
         } else {
-          qf[s][0] = qf[s][1] = 0u;
+          qa[s][0] = qa[s][1] = 0u;
         }
       }
 
-      // Two code buffers (A, B) alternate; the next tile's load is clamped to
-      // the last tile of the range instead of branching.
-      const uint8_t* kl = kbase + lane * 16;
-      const uint8_t* vl = vbase + lane * 16;
-      const int last = t_end - 1;
-      int tile = t_begin + warp;
-      int pf_next = t_begin + V2_PF_AHEAD;   // warp 0: next prefetch position
-      uint4 kA = ldg_stream(kl + (size_t)min(tile, last) * V2_TILE_BYTES);
-      uint4 vA = ldg_stream(vl + (size_t)min(tile, last) * V2_TILE_BYTES);
-      while (tile < t_end) {
-        if (warp == 0 && lane == 0 && pf_next < t_end && pf_next <= tile + V2_PF_AHEAD) {
-          const uint32_t n = (uint32_t)(min(V2_PF_CHUNK, t_end - pf_next) * V2_TILE_BYTES);
-          prefetch_l2_bulk(kbase + (size_t)pf_next * V2_TILE_BYTES, n);
-          prefetch_l2_bulk(vbase + (size_t)pf_next * V2_TILE_BYTES, n);
-          pf_next += V2_PF_CHUNK;
+      for (int j = 0; j < n_mine; ++j) {
+        const uint32_t st = (uses + j) % V2_STAGES;
+        const uint32_t par = ((uses + j) / V2_STAGES) & 1u;
+        if (!mbar_wait_bounded(mbar + 8 * st, par, kMaxPolls)) {
+          timed_out = true;
+          break;
         }
-        const int t1 = min(tile + V2_WARPS, last);
-        const uint4 kB = ldg_stream(kl + (size_t)t1 * V2_TILE_BYTES);
-        const uint4 vB = ldg_stream(vl + (size_t)t1 * V2_TILE_BYTES);
-        vq2_tile(s_k, s_v, klane, vlane, qf, kA, vA, tile, L, gid, m0, m1, l0, l1, acc);
-        tile += V2_WARPS;
-        if (tile >= t_end) break;
-        const int t2 = min(tile + V2_WARPS, last);
-        kA = ldg_stream(kl + (size_t)t2 * V2_TILE_BYTES);
-        vA = ldg_stream(vl + (size_t)t2 * V2_TILE_BYTES);
-        vq2_tile(s_k, s_v, klane, vlane, qf, kB, vB, tile, L, gid, m0, m1, l0, l1, acc);
-        tile += V2_WARPS;
+        uint4 kq[V2_TPI], vq[V2_TPI];
+#pragma unroll
+        for (int i = 0; i < V2_TPI; ++i) {
+          kq[i] = lds128(ring + st * V2_STAGE_BYTES + i * V2_TILE_BYTES + lane * 16);
+          vq[i] = lds128(ring + st * V2_STAGE_BYTES + (V2_TPI + i) * V2_TILE_BYTES + lane * 16);
+        }
+        __syncwarp();
+        // refill the stage this warp finished with in the previous step
+        if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
+        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, L, lane, m,
+                         l, acc);
       }
+      if (timed_out) {
+        // give the copies already issued a bounded chance to land before the
+        // ring is reused or the CTA exits, and report the failure
+        for (int j = 0; j < n_mine && j < V2_STAGES; ++j) {
+          const uint32_t st = (uses + n_mine - 1 - j) % V2_STAGES;
+          mbar_wait_bounded(mbar + 8 * st, ((uses + n_mine - 1 - j) / V2_STAGES) & 1u, kMaxPolls);
+        }
+        if (lane == 0) atomicOr(p.err, VQKV_DEVERR_TIMEOUT);
+      }
+      uses += n_mine;
     }
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
-    stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
+    stash_warp_vq2(s_comb, warp, lane, acc, m, l);
     __syncthreads();
     finish_sequence<V2_WARPS>(p, b, kvh, split, s_comb, &s_last);
-    __syncthreads();
+    __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
 
@@ -414,7 +579,7 @@ __device__ __forceinline__ uint32_t pair24(uint32_t w0, uint32_t w1, uint32_t w2
 }
 
 __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const DecodeParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   uint4* s_kcb = reinterpret_cast<uint4*>(smem);
   uint4* s_vcb = reinterpret_cast<uint4*>(smem + V15_CB_BYTES);
   float* s_comb = reinterpret_cast<float*>(smem + 2 * V15_CB_BYTES);
@@ -555,6 +720,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
 }  // namespace
 
 int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TILE : V15_TILE; }
+int decode_tiles_per_step(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TPI : 1; }
 size_t decode_smem_bytes(int mode) { return mode == VQKV_MODE_VQ2 ? kV2Smem : kV15Smem; }
 int decode_threads(int mode) { return mode == VQKV_MODE_VQ2 ? V2_THREADS : V15_THREADS; }
 

@@ -48,6 +48,7 @@ struct EncodeParams {
 
 // Decode kernels (decode.cu).  tile_tokens: 16 (VQ2) / 64 (VQ15).
 int decode_tile_tokens(int mode);
+int decode_tiles_per_step(int mode);   // tiles per split are a multiple of this
 size_t decode_smem_bytes(int mode);
 int decode_threads(int mode);
 cudaError_t decode_prepare(int mode);                // set smem attributes (once per device)
