@@ -210,6 +210,7 @@ __device__ __forceinline__ void softmax_tiles(float (&sc)[T][4], float& m0, floa
 template <int WARPS>
 __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
                                                 float* s_comb, int* s_last) {
+  static_assert(WARPS * 32 * 2 >= 8 * kHeadDim, "two outputs per thread must cover g * 128");
   const float* wO = s_comb;
   const float* wm = s_comb + CombineSmem<WARPS>::kO;
   const float* wl = wm + WARPS * 8;
@@ -242,20 +243,44 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
   __syncthreads();
   if (*s_last) {
     __threadfence();
+    // All split partials of (b, kvh) are staged in shared memory by the whole
+    // CTA (coalesced, every load in flight at once), then each thread merges
+    // one output (head, channel) with a running max.  Chunks of splits when
+    // they do not all fit.
     const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * G * kPartialStride;
-    const int split_stride = G * kPartialStride;
-    for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
-      const int h = e >> 7, d = e & 127;
-      const float* ph = base + h * kPartialStride;
-      float M = kMInit;
-      for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(ph + s * split_stride + 128));
-      float o = 0.f, l = 0.f;
-      for (int s = 0; s < p.n_splits; ++s) {
-        const float f = fast_exp2(__ldcg(ph + s * split_stride + 128) - M);
-        o += __ldcg(ph + s * split_stride + d) * f;
-        l += __ldcg(ph + s * split_stride + 129) * f;
+    const int per_split = G * kPartialStride;
+    const int chunk = max(1, min(p.n_splits, CombineSmem<WARPS>::kBytes / 4 / per_split));
+    float M[2], O[2], Ls[2];
+    for (int k = 0; k < 2; ++k) M[k] = kMInit, O[k] = 0.f, Ls[k] = 0.f;
+    for (int s0 = 0; s0 < p.n_splits; s0 += chunk) {
+      const int ns = min(chunk, p.n_splits - s0);
+      for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) s_comb[i] = __ldcg(base + s0 * per_split + i);
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = threadIdx.x + k * WARPS * 32;
+        if (e < G * kHeadDim) {
+          const int h = e >> 7, d = e & 127;
+          for (int s = 0; s < ns; ++s) {
+            const float* ph = s_comb + s * per_split + h * kPartialStride;
+            const float ms = ph[128];
+            const float n = fmaxf(M[k], ms);
+            const float fa = fast_exp2(M[k] - n), fb = fast_exp2(ms - n);
+            O[k] = O[k] * fa + ph[d] * fb;
+            Ls[k] = Ls[k] * fa + ph[129] * fb;
+            M[k] = n;
+          }
+        }
       }
-      p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = threadIdx.x + k * WARPS * 32;
+      if (e < G * kHeadDim) {
+        const int h = e >> 7, d = e & 127;
+        p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
+      }
     }
     if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
   }
@@ -506,15 +531,15 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       if (lane == 0)
         for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
       {
-        const uint2* gk = reinterpret_cast<const uint2*>(p.kcb) + (size_t)kvh * 256;
-        const uint2* gv = reinterpret_cast<const uint2*>(p.vcb) + (size_t)kvh * 256;
-        uint2* cb = reinterpret_cast<uint2*>(smem);
-        // slot k = 32*c + j: consecutive threads write consecutive 8-byte slots
-#pragma unroll 4
-        for (int k = threadIdx.x; k < 256 * 32; k += V2_THREADS) {
-          const int c = k >> 5, j = k & 31;
-          cb[k] = __ldg((j < 16 ? gk : gv) + c);
-        }
+        // thread t loads centroid t & 255 of K (t < 256) or V (t >= 256) once and
+        // writes its 16 replicas; replica (i + lane) % 16 at step i keeps the 16
+        // lanes of each half-warp on 16 different bank pairs
+        static_assert(V2_THREADS == 512, "one thread per K and V centroid");
+        const int c = threadIdx.x & 255, role = threadIdx.x >> 8;
+        const uint2 e = __ldg(reinterpret_cast<const uint2*>(role ? p.vcb : p.kcb) + (size_t)kvh * 256 + c);
+        uint2* row = reinterpret_cast<uint2*>(smem + c * 256 + role * 128);
+#pragma unroll 1
+        for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
       }
       transform_queries(p, b, kvh, warp, lane, s_qp);
       __syncthreads();
