@@ -272,6 +272,7 @@ def run_ours(args):
         x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
         _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, cb, codes, cap)
         del x
+    kv_fp16 = None if args.profile_steps else kv   # kept for the fp16-KV comparison
     del kv
     torch.cuda.synchronize()
 
@@ -383,6 +384,8 @@ def run_ours(args):
     nk_host = new_k.cpu().pin_memory()
     nv_host = new_v.cpu().pin_memory()
     o_host = torch.empty((w.B, w.Hq, 128), dtype=torch.float16).pin_memory()
+    fp16 = fp16_baseline(w, kv_fp16, lens, dev, stream) if kv_fp16 is not None else None
+    del kv_fp16
     e2e_steps = max(20, min(args.steps, 2000))
     with torch.cuda.stream(stream):
         def e2e_step(i):
@@ -441,10 +444,49 @@ def run_ours(args):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if fp16 is not None:
+        fp16["vq_decode_speedup"] = fp16["launch_us"] / (dec_avg_ms * 1e3)
+        line["fp16_kv_decode"] = fp16
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
+    """The same decode over a plain fp16 K/V cache (vqkv_decode_attn_fp16):
+    average launch time from CUDA events around a graph of launches.  The
+    805 MB cache is larger than L2, so consecutive launches stream from HBM."""
+    import torch
+    from vector_quantized_bit_gb300 import _lib
+    k = torch.from_numpy(np.stack([kv[h][0] for h in range(w.Hkv)])[None]).to(dev)
+    v = torch.from_numpy(np.stack([kv[h][1] for h in range(w.Hkv)])[None]).to(dev)
+    q = torch.from_numpy(synth.queries(w)).to(dev)
+    seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
+    max_len = int(lens.max())
+    ws = _lib.fp16_decode_workspace(w.B, w.Hq, w.Hkv, w.cap_len, max_len, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            _lib.vqkv_decode_attn_fp16(q, k, v, seq, out, ws, max_len)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(launches):
+                _lib.vqkv_decode_attn_fp16(q, k, v, seq, out, ws, max_len)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (launches * reps)
+    nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2
+    tokens = int(lens.sum())
+    return {"launch_us": us, "tokens_per_s": tokens / (us * 1e-6), "GB_per_s": nbytes / us / 1e3,
+            "algorithmic_bytes": nbytes, "kernel": "decode_fp16_kernel",
+            "how": "graph of 60 launches x 5 replays, CUDA events; fp16 K/V of the same synthetic cache"}
 
 
 def main():

@@ -183,6 +183,31 @@ int32_t vqkv_decode_num_splits(const vqkv_decode_args* args);
 vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);
 vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
 
+/*
+ * vqkv_decode_attn_fp16 — the same decode attention over a plain fp16 KV
+ * cache, the comparison point for the quantised path on the same shapes
+ * (the paper measures its speed-up against FP16 attention, summary page,
+ * "Key points"):  O = softmax(softmax_scale * q . K_t^T) . V_t, t < seq_lens[b],
+ * no smoothing, no rotation, no codebooks.  Same split-KV plan, GQA grouping
+ * and workspace rules as vqkv_decode_attn (vqkv_fp16_decode_workspace_bytes
+ * gives the size).
+ */
+typedef struct {
+  int32_t B, Hq, Hkv, head_dim, cap_len, max_seq_len;
+  const uint16_t* q;          /* device fp16 [B][Hq][128], 4-byte aligned */
+  const uint16_t* k;          /* device fp16 [B][Hkv][cap_len][128], 16-byte aligned */
+  const uint16_t* v;          /* device fp16 [B][Hkv][cap_len][128], 16-byte aligned */
+  const int32_t* seq_lens;    /* device [B] */
+  float softmax_scale;        /* <= 0 selects 1/sqrt(head_dim) */
+  int32_t num_splits;         /* 0 = planned automatically */
+  void* workspace;            /* as for vqkv_decode_attn */
+  size_t workspace_bytes;
+  uint16_t* out;              /* device fp16 [B][Hq][128] */
+} vqkv_fp16_decode_args;
+
+size_t vqkv_fp16_decode_workspace_bytes(const vqkv_fp16_decode_args* args);
+vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* args, void* stream);
+
 /* Size of the scratch array compiled into the library for
  * vqkv_decode_attn_static (8 MiB, held on every GPU that loads the library
  * until the process exits). */

@@ -37,7 +37,8 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_matches_header(tmp_path):
     """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
-    fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs}
+    fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs,
+              "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')

@@ -23,7 +23,8 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_encode",
-            "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_status_string"]
+            "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_fp16_decode_workspace_bytes",
+            "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -47,6 +48,15 @@ class DecodeArgs(ctypes.Structure):
                 ("max_seq_len", ctypes.c_int32), ("q", ctypes.c_void_p), ("k_codes", ctypes.c_void_p),
                 ("v_codes", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("k_codebook", ctypes.c_void_p),
                 ("v_codebook", ctypes.c_void_p), ("s", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
+                ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
+
+
+class Fp16DecodeArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("cap_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
                 ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
 
@@ -80,6 +90,10 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn_static.restype = ctypes.c_int
         L.vqkv_decode_attn_static.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_fp16_decode_workspace_bytes.restype = ctypes.c_size_t
+        L.vqkv_fp16_decode_workspace_bytes.argtypes = [ctypes.POINTER(Fp16DecodeArgs)]
+        L.vqkv_decode_attn_fp16.restype = ctypes.c_int
+        L.vqkv_decode_attn_fp16.argtypes = [ctypes.POINTER(Fp16DecodeArgs), ctypes.c_void_p]
         L.vqkv_status_string.restype = ctypes.c_char_p
         L.vqkv_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -184,4 +198,33 @@ def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, devic
     n = vqkv_decode_workspace_bytes(a)
     if n == 0:
         raise VqkvError(1, "vqkv_decode_workspace_bytes")
+    return torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=device)
+
+
+def fp16_decode_args(q, k, v, seq_lens, out, workspace, max_seq_len, softmax_scale=0.0, num_splits=0):
+    B, Hq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return Fp16DecodeArgs(B=B, Hq=Hq, Hkv=Hkv, head_dim=D, cap_len=cap, max_seq_len=max_seq_len, q=_ptr(q),
+                          k=_ptr(k), v=_ptr(v), seq_lens=_ptr(seq_lens), softmax_scale=softmax_scale,
+                          num_splits=num_splits, workspace=_ptr(workspace), workspace_bytes=wb, out=_ptr(out))
+
+
+def vqkv_decode_attn_fp16(q, k, v, seq_lens, out, workspace, max_seq_len, softmax_scale=0.0, num_splits=0,
+                          stream=None) -> None:
+    """Decode attention over a plain fp16 cache k, v [B][Hkv][cap][128] (the
+    comparison kernel for the quantised path)."""
+    a = fp16_decode_args(q, k, v, seq_lens, out, workspace, max_seq_len, softmax_scale, num_splits)
+    st = lib().vqkv_decode_attn_fp16(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_attn_fp16")
+
+
+def fp16_decode_workspace(B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda"):
+    import torch
+    a = Fp16DecodeArgs(B=B, Hq=Hq, Hkv=Hkv, head_dim=128, cap_len=cap_len, max_seq_len=max_seq_len,
+                       num_splits=num_splits)
+    n = int(lib().vqkv_fp16_decode_workspace_bytes(ctypes.byref(a)))
+    if n == 0:
+        raise VqkvError(1, "vqkv_fp16_decode_workspace_bytes")
     return torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=device)

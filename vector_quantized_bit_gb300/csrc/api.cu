@@ -17,7 +17,7 @@ constexpr size_t kWsHeader = 256;   // word 0: device error flags
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int decode_bpsm[2] = {0, 0};   // resident decode CTAs per SM, per mode
+  int decode_bpsm[3] = {0, 0, 0};   // resident decode CTAs per SM: VQ2, VQ15, fp16
   int encode_bpsm[2] = {0, 0};
 };
 
@@ -39,6 +39,9 @@ vqkv_status device_info(DeviceInfo* out) {
       if (d.decode_bpsm[m] < 1) d.decode_bpsm[m] = 1;
       if (d.encode_bpsm[m] < 1) d.encode_bpsm[m] = 1;
     }
+    if (decode_fp16_prepare() != cudaSuccess || decode_fp16_occupancy(&d.decode_bpsm[kModeFp16]) != cudaSuccess)
+      return VQKV_ERR_CUDA;
+    if (d.decode_bpsm[kModeFp16] < 1) d.decode_bpsm[kModeFp16] = 1;
     d.ready = true;
   }
   *out = d;
@@ -95,11 +98,17 @@ struct DecodePlan {
 // the split count that minimises (waves of CTAs) x (tiles per CTA + a fixed
 // per-CTA setup cost), assuming full-length sequences; short sequences make
 // some CTAs finish early, which the hardware scheduler backfills.
-vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
+struct PlanInput {
+  int mode;   // VQKV_MODE_VQ2, VQKV_MODE_VQ15 or kModeFp16
+  int B, Hq, Hkv, max_seq_len, num_splits;
+};
+
+vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   DeviceInfo di;
   vqkv_status st = device_info(&di);
   if (st != VQKV_OK) return st;
-  const int T = decode_tile_tokens(a->mode);
+  const int T = a->mode == kModeFp16 ? 16 : decode_tile_tokens(a->mode);
+  const int unit_tiles = a->mode == kModeFp16 ? 1 : decode_tiles_per_step(a->mode);
   const int g = a->Hq / a->Hkv;
   const long long tiles_max = std::max(1, (a->max_seq_len + T - 1) / T);
   const long long slots = (long long)di.sms * di.decode_bpsm[a->mode];
@@ -109,7 +118,8 @@ vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
   int bpg = 1;
   if (a->mode == VQKV_MODE_VQ15 && (long long)B * a->Hkv < slots) bpg = B;
   const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg);
-  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 12.0 : 24.0;   // per-CTA prologue in tile units
+  // per-CTA prologue + merge in tile units
+  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 12.0 : (a->mode == VQKV_MODE_VQ15) ? 24.0 : 4.0;
   long long best_n = 1;
   double best_cost = 1e300;
   if (a->num_splits > 0) {
@@ -126,7 +136,7 @@ vqkv_status plan_decode(const vqkv_decode_args* a, DecodePlan* pl) {
       }
     }
   }
-  const long long unit = decode_tiles_per_step(a->mode);
+  const long long unit = unit_tiles;
   const long long tps = ((tiles_max + best_n - 1) / best_n + unit - 1) / unit * unit;
   pl->tps = (int)tps;
   pl->n_splits = (int)((tiles_max + tps - 1) / tps);
@@ -156,6 +166,30 @@ vqkv_status validate_encode(const vqkv_encode_args* a) {
   return VQKV_OK;
 }
 
+PlanInput plan_input(const vqkv_decode_args* a) {
+  return PlanInput{a->mode, a->B, a->Hq, a->Hkv, a->max_seq_len, a->num_splits};
+}
+
+vqkv_status validate_fp16(const vqkv_fp16_decode_args* a, bool sizes_only) {
+  if (a == nullptr) return VQKV_ERR_INVALID_ARG;
+  if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
+  if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
+  if (a->Hq / a->Hkv > 8) return VQKV_ERR_UNSUPPORTED;
+  if (a->max_seq_len < 0 || a->max_seq_len > a->cap_len) return VQKV_ERR_INVALID_ARG;
+  if (a->num_splits < 0 || !std::isfinite(a->softmax_scale)) return VQKV_ERR_INVALID_ARG;
+  if (sizes_only || a->B == 0) return VQKV_OK;
+  if (!a->q || !a->k || !a->v || !a->seq_lens || !a->out) return VQKV_ERR_INVALID_ARG;
+  if (!aligned(a->q, 4) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->seq_lens, 4) ||
+      !aligned(a->out, 2))
+    return VQKV_ERR_INVALID_ARG;
+  return VQKV_OK;
+}
+
+PlanInput plan_input(const vqkv_fp16_decode_args* a) {
+  return PlanInput{kModeFp16, a->B, a->Hq, a->Hkv, a->max_seq_len, a->num_splits};
+}
+
 }  // namespace
 
 vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(a); }
@@ -180,14 +214,16 @@ size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
 size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* a) {
   if (validate_decode_sizes(a) != VQKV_OK) return 0;
   DecodePlan pl;
-  if (plan_decode(a, &pl) != VQKV_OK) return 0;
+  const PlanInput in = plan_input(a);
+  if (plan_decode(&in, &pl) != VQKV_OK) return 0;
   return pl.ws_bytes;
 }
 
 int32_t vqkv_decode_num_splits(const vqkv_decode_args* a) {
   if (validate_decode_sizes(a) != VQKV_OK) return -1;
   DecodePlan pl;
-  if (plan_decode(a, &pl) != VQKV_OK) return -1;
+  const PlanInput in = plan_input(a);
+  if (plan_decode(&in, &pl) != VQKV_OK) return -1;
   return pl.n_splits;
 }
 
@@ -195,7 +231,8 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK || a->B == 0) return st;
   DecodePlan pl;
-  st = plan_decode(a, &pl);
+  const PlanInput in = plan_input(a);
+  st = plan_decode(&in, &pl);
   if (st != VQKV_OK) return st;
   if (a->workspace == nullptr || a->workspace_bytes < pl.ws_bytes) return VQKV_ERR_WORKSPACE;
   if (!aligned(a->workspace, 256)) return VQKV_ERR_INVALID_ARG;
@@ -263,6 +300,49 @@ vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
   }
   if (launch_encode(a->mode, p, blocks_x, split_rows, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VQKV_ERR_CUDA;
+  return VQKV_OK;
+}
+
+size_t vqkv_fp16_decode_workspace_bytes(const vqkv_fp16_decode_args* a) {
+  if (validate_fp16(a, true) != VQKV_OK) return 0;
+  DecodePlan pl;
+  const PlanInput in = plan_input(a);
+  if (plan_decode(&in, &pl) != VQKV_OK) return 0;
+  return pl.ws_bytes;
+}
+
+vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* a, void* stream) {
+  vqkv_status st = validate_fp16(a, false);
+  if (st != VQKV_OK || a->B == 0) return st;
+  DecodePlan pl;
+  const PlanInput in = plan_input(a);
+  st = plan_decode(&in, &pl);
+  if (st != VQKV_OK) return st;
+  if (a->workspace == nullptr || a->workspace_bytes < pl.ws_bytes) return VQKV_ERR_WORKSPACE;
+  if (!aligned(a->workspace, 256)) return VQKV_ERR_INVALID_ARG;
+  unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+  DecodeParams p{};
+  p.q = reinterpret_cast<const __half*>(a->q);
+  p.kc = reinterpret_cast<const uint8_t*>(a->k);
+  p.vc = reinterpret_cast<const uint8_t*>(a->v);
+  p.seq_lens = a->seq_lens;
+  p.out = reinterpret_cast<__half*>(a->out);
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.tickets = reinterpret_cast<unsigned*>(ws + pl.tickets_off);
+  p.partials = reinterpret_cast<float*>(ws + pl.partials_off);
+  p.stream_bytes = (long long)a->cap_len * 256;
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.g = a->Hq / a->Hkv;
+  p.max_seq_len = a->max_seq_len;
+  p.n_splits = pl.n_splits;
+  p.tps = pl.tps;
+  p.bpg = pl.bpg;
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
+  p.qscale = scale * 1.4426950408889634f;
+  const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
+  if (launch_decode_fp16(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
 

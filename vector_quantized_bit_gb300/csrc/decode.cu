@@ -34,17 +34,11 @@
 //              k = the four tokens above; centroid halves are paired across
 //              tokens with byte permutes.
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "internal.h"
 
 namespace vqkv {
 namespace {
-
-constexpr float kSoftmaxSlack = 8.0f;   // rescale only when a score exceeds m by 2^8
-
-__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-// Initial running max: finite, so exp2(m_old - m_new) and exp2(score - m)
-// never see inf - inf; masked scores are -inf and give p = 0.
-constexpr float kMInit = -1e30f;
 
 // ------------------------------------------------------------------ VQ2
 #ifndef VQKV_V2_WARPS
@@ -80,12 +74,6 @@ constexpr int V15_TILE_BYTES = 1536;
 constexpr int V15_CB_BYTES = 4096 * 16;          // 64 KB per codebook
 constexpr int V15_PF_TILES = 2 * V15_WARPS;
 
-template <int WARPS>
-struct CombineSmem {
-  static constexpr int kO = WARPS * 8 * 128;     // floats
-  static constexpr int kBytes = (kO + 2 * WARPS * 8) * 4;
-};
-
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
 // codebook and q' region after the tile loop.
 constexpr size_t kV2Smem = V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8;
@@ -108,221 +96,6 @@ __device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, 
     *reinterpret_cast<float4*>(s_qp + warp * kHeadDim + 4 * lane) = o;
   }
 }
-
-// Clamp the sequence length to [0, max_seq_len]; report out-of-range once.
-__device__ __forceinline__ int load_len(const DecodeParams& p, int b) {
-  int L = p.seq_lens[b];
-  if (L < 0 || L > p.max_seq_len) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.err, VQKV_DEVERR_SEQ_LEN);
-    L = L < 0 ? 0 : p.max_seq_len;
-  }
-  return L;
-}
-
-// Online-softmax update for one tile.  sc = scores for tokens {gid, gid+8}
-// x heads {2tig, 2tig+1} (log2 domain).  Returns P packed for the P.V MMA.
-template <int NACC>
-__device__ __forceinline__ void softmax_tile(float (&sc)[4], float& m0, float& m1, float& l0,
-                                             float& l1, float (&acc)[NACC][4], uint32_t& bP0,
-                                             uint32_t& bP1) {
-  const bool need = (sc[0] > m0 + kSoftmaxSlack) | (sc[2] > m0 + kSoftmaxSlack) |
-                    (sc[1] > m1 + kSoftmaxSlack) | (sc[3] > m1 + kSoftmaxSlack);
-  if (__any_sync(0xffffffffu, need)) {
-    float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float a0 = fast_exp2(m0 - n0);
-    const float a1 = fast_exp2(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    l0 *= a0;
-    l1 *= a1;
-#pragma unroll
-    for (int i = 0; i < NACC; ++i) {
-      acc[i][0] *= a0;
-      acc[i][1] *= a1;
-      acc[i][2] *= a0;
-      acc[i][3] *= a1;
-    }
-  }
-  const float p0 = fast_exp2(sc[0] - m0), p1 = fast_exp2(sc[1] - m1);
-  const float p2 = fast_exp2(sc[2] - m0), p3 = fast_exp2(sc[3] - m1);
-  l0 += p0 + p2;
-  l1 += p1 + p3;
-  bP0 = movmatrix_t(pack_half2(p0, p1));   // P[tokens 2tig, 2tig+1][head gid]
-  bP1 = movmatrix_t(pack_half2(p2, p3));   // P[tokens 2tig+8, 2tig+9][head gid]
-}
-
-// Online-softmax update for T tiles at once (one running max for all of
-// them), then P packed for the P.V MMA of each tile.
-template <int T, int NACC>
-__device__ __forceinline__ void softmax_tiles(float (&sc)[T][4], float& m0, float& m1, float& l0, float& l1,
-                                              float (&acc)[NACC][4], uint32_t (&bP)[T][2]) {
-  bool need = false;
-#pragma unroll
-  for (int i = 0; i < T; ++i)
-    need |= (sc[i][0] > m0 + kSoftmaxSlack) | (sc[i][2] > m0 + kSoftmaxSlack) |
-            (sc[i][1] > m1 + kSoftmaxSlack) | (sc[i][3] > m1 + kSoftmaxSlack);
-  if (__any_sync(0xffffffffu, need)) {
-    float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
-#pragma unroll
-    for (int i = 1; i < T; ++i) {
-      x0 = fmaxf(x0, fmaxf(sc[i][0], sc[i][2]));
-      x1 = fmaxf(x1, fmaxf(sc[i][1], sc[i][3]));
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    l0 *= a0;
-    l1 *= a1;
-#pragma unroll
-    for (int i = 0; i < NACC; ++i) {
-      acc[i][0] *= a0;
-      acc[i][1] *= a1;
-      acc[i][2] *= a0;
-      acc[i][3] *= a1;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < T; ++i) {
-    const float p0 = fast_exp2(sc[i][0] - m0), p1 = fast_exp2(sc[i][1] - m1);
-    const float p2 = fast_exp2(sc[i][2] - m0), p3 = fast_exp2(sc[i][3] - m1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-    bP[i][0] = movmatrix_t(pack_half2(p0, p1));
-    bP[i][1] = movmatrix_t(pack_half2(p2, p3));
-  }
-}
-
-// Merge the per-warp states of the CTA into one partial (m, l, O) per head
-// and write it to the workspace; then take the (b, kvh) ticket and, if this
-// CTA is the last one, merge all split partials into O (fp16).
-template <int WARPS>
-__device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
-                                                float* s_comb, int* s_last) {
-  static_assert(WARPS * 32 * 2 >= 8 * kHeadDim, "two outputs per thread must cover g * 128");
-  const float* wO = s_comb;
-  const float* wm = s_comb + CombineSmem<WARPS>::kO;
-  const float* wl = wm + WARPS * 8;
-  const int G = p.g;
-  float* part = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * G * kPartialStride;
-  for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
-    const int h = e >> 7, d = e & 127;
-    float M = kMInit;
-#pragma unroll 4
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, wm[w * 8 + h]);
-    float o = 0.f, l = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < WARPS; ++w) {
-      const float f = fast_exp2(wm[w * 8 + h] - M);
-      o += wO[(w * 8 + h) * kHeadDim + d] * f;
-      l += wl[w * 8 + h] * f;
-    }
-    part[h * kPartialStride + d] = o;
-    if (d == 0) {
-      part[h * kPartialStride + 128] = M;
-      part[h * kPartialStride + 129] = l;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(p.tickets + b * p.Hkv + kvh, 1u);
-    *s_last = (prev == (unsigned)(p.n_splits - 1));
-  }
-  __syncthreads();
-  if (*s_last) {
-    __threadfence();
-    // All split partials of (b, kvh) are staged in shared memory by the whole
-    // CTA (coalesced, every load in flight at once), then each thread merges
-    // one output (head, channel) with a running max.  Chunks of splits when
-    // they do not all fit.
-    const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * G * kPartialStride;
-    const int per_split = G * kPartialStride;
-    const int chunk = max(1, min(p.n_splits, CombineSmem<WARPS>::kBytes / 4 / per_split));
-    float M[2], O[2], Ls[2];
-    for (int k = 0; k < 2; ++k) M[k] = kMInit, O[k] = 0.f, Ls[k] = 0.f;
-    for (int s0 = 0; s0 < p.n_splits; s0 += chunk) {
-      const int ns = min(chunk, p.n_splits - s0);
-      for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) s_comb[i] = __ldcg(base + s0 * per_split + i);
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int e = threadIdx.x + k * WARPS * 32;
-        if (e < G * kHeadDim) {
-          const int h = e >> 7, d = e & 127;
-          for (int s = 0; s < ns; ++s) {
-            const float* ph = s_comb + s * per_split + h * kPartialStride;
-            const float ms = ph[128];
-            const float n = fmaxf(M[k], ms);
-            const float fa = fast_exp2(M[k] - n), fb = fast_exp2(ms - n);
-            O[k] = O[k] * fa + ph[d] * fb;
-            Ls[k] = Ls[k] * fa + ph[129] * fb;
-            M[k] = n;
-          }
-        }
-      }
-      __syncthreads();
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int e = threadIdx.x + k * WARPS * 32;
-      if (e < G * kHeadDim) {
-        const int h = e >> 7, d = e & 127;
-        p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
-      }
-    }
-    if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
-  }
-}
-
-// Store one warp's (m, l, O) into the combine area.  acc holds O^T fragments:
-// acc[mt] = rows {gid, gid+8} (channels dim0(mt), dim0(mt)+1) x heads {2tig, 2tig+1}.
-template <int WARPS, int NMT, typename DimOf>
-__device__ __forceinline__ void stash_warp(float* s_comb, int warp, int lane, const float (&acc)[NMT][4],
-                                           float m0, float m1, float l0, float l1, DimOf dim_of) {
-  const int gid = lane >> 2, tig = lane & 3;
-  float* wO = s_comb;
-  float* wm = s_comb + CombineSmem<WARPS>::kO;
-  float* wl = wm + WARPS * 8;
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  const int h0 = warp * 8 + 2 * tig;
-#pragma unroll
-  for (int mt = 0; mt < NMT; ++mt) {
-    const int d0 = dim_of(mt, gid);
-    wO[h0 * kHeadDim + d0] = acc[mt][0];
-    wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
-    wO[h0 * kHeadDim + d0 + 1] = acc[mt][2];
-    wO[(h0 + 1) * kHeadDim + d0 + 1] = acc[mt][3];
-  }
-  if (gid == 0) {
-    wm[h0] = m0;
-    wm[h0 + 1] = m1;
-    wl[h0] = l0;
-    wl[h0 + 1] = l1;
-  }
-}
-
-struct Vq2Dim {
-  __device__ int operator()(int mt, int gid) const { return 4 * (8 * (mt >> 1) + gid) + 2 * (mt & 1); }
-};
-struct Vq15Dim {
-  __device__ int operator()(int mt, int gid) const { return 8 * (8 * (mt >> 2) + gid) + 2 * (mt & 3); }
-};
 
 // Shared-memory offset of a gathered centroid: one byte permute puts code
 // byte K of `codes` into bits 8..15 and the lane's replica offset (byte 0 of
@@ -457,11 +230,11 @@ __device__ __forceinline__ void stash_warp_vq2(float* s_comb, int warp, int lane
   const int h0 = warp * 8 + 2 * tig;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = Vq2Dim()(mt, gid);
+    const int d0 = Vq2Dim()(mt, gid), d1 = Vq2Dim()(mt, gid + 8);
     wO[h0 * kHeadDim + d0] = acc[mt][0];
     wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
-    wO[h0 * kHeadDim + d0 + 1] = acc[mt][2];
-    wO[(h0 + 1) * kHeadDim + d0 + 1] = acc[mt][3];
+    wO[h0 * kHeadDim + d1] = acc[mt][2];
+    wO[(h0 + 1) * kHeadDim + d1] = acc[mt][3];
   }
   if (tig == 0) {
     wm[warp * 8 + gid] = m;

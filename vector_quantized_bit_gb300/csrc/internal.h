@@ -55,6 +55,15 @@ cudaError_t decode_prepare(int mode);                // set smem attributes (onc
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm);
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
+// fp16-KV comparison kernel (decode_fp16.cu); DecodeParams.kc / .vc point to
+// the fp16 K / V caches, stream_bytes = cap_len * 256.
+constexpr int kModeFp16 = 2;   // plan index next to VQKV_MODE_VQ2 / VQKV_MODE_VQ15
+size_t decode_fp16_smem_bytes();
+int decode_fp16_threads();
+cudaError_t decode_fp16_prepare();
+cudaError_t decode_fp16_occupancy(int* blocks_per_sm);
+cudaError_t launch_decode_fp16(const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
 // Host-side helpers of api.cu shared with decode_static.cu.
 vqkv_status decode_validate(const vqkv_decode_args* a);   // every check of vqkv_decode_attn
 size_t decode_ticket_region_bytes(int B, int Hkv);       // error word + tickets, bytes
