@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[1, 2, 3, 4],
+                    help="1: Llama-3.1-8B 196k 2-bit (default); 2: ragged batch of 32; "
+                         "3: Qwen2.5-14B 1.5-bit; 4: Mistral-7B encode + decode")
+    ap.add_argument("--mode", type=int, default=None, choices=[0, 1],
+                    help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit)")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
@@ -62,6 +67,21 @@ def _gen_head(args):
 def _cal_head(args):
     w, kvh = args
     return calib.calibrate_head(w, kvh)
+
+
+def _cal_head_small(args):
+    w, kvh = args
+    return calib.calibrate_head(w, kvh, sample_tokens=2048, iters=2 if w.mode else 10)
+
+
+def host_calibration(w):
+    """Codebooks and s only (no full K/V on the host)."""
+    import concurrent.futures
+    import multiprocessing
+    n = min(w.Hkv, os.cpu_count() or 1)
+    with concurrent.futures.ProcessPoolExecutor(n, mp_context=multiprocessing.get_context("spawn")) as ex:
+        cal = list(ex.map(_cal_head_small, [(w, h) for h in range(w.Hkv)]))
+    return np.stack([c[0] for c in cal]), np.stack([c[1] for c in cal]), np.stack([c[2] for c in cal])
 
 
 def host_workload(w):
@@ -244,11 +264,18 @@ def run_ours(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = synth.WORKLOADS[WORKLOAD_ID]
+    w = synth.WORKLOADS[args.workload]
+    if args.mode is not None:
+        w = w.with_mode(args.mode)
+    headline = args.workload == WORKLOAD_ID and w.mode == synth.MODE_VQ2
     lens = synth.seq_lens(w)
-    s_h, kcb_h, vcb_h, kv = host_workload(w)
+    if headline:
+        s_h, kcb_h, vcb_h, kv = host_workload(w)
+    else:
+        s_h, kcb_h, vcb_h = host_calibration(w)
+        kv = None
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_steps:
+    if headline and rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_steps:
         cpu = cpu_baseline()
 
     import torch
@@ -267,11 +294,18 @@ def run_ours(args):
     kcodes = torch.zeros((w.B, w.Hkv, sb), dtype=torch.uint8, device=dev)
     vcodes = torch.zeros_like(kcodes)
     zeros = torch.zeros(w.B, dtype=torch.int32, device=dev)
-    # encode the whole cache (all KV heads, all 196,608 positions) in one call per K / V
-    for role, cb, codes in ((0, kcb, kcodes), (1, vcb, vcodes)):
-        x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
-        _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, cb, codes, cap)
-        del x
+    if kv is not None:
+        # encode the whole cache (all KV heads, all positions) in one call per K / V
+        for role, cb, codes in ((0, kcb, kcodes), (1, vcb, vcodes)):
+            x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
+            _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, cb, codes, cap)
+            del x
+    else:
+        # other workloads: seeded uniform codes (decode cost does not depend on code values)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed * 1000 + w.config_id)
+        kcodes.random_(0, 256, generator=gen)
+        vcodes.random_(0, 256, generator=gen)
     kv_fp16 = None if args.profile_steps else kv   # kept for the fp16-KV comparison
     del kv
     torch.cuda.synchronize()
@@ -283,8 +317,10 @@ def run_ours(args):
     copies = [(kcodes, vcodes)] + [(kcodes.clone(), vcodes.clone()) for _ in range(n_copies - 1)]
 
     q = torch.from_numpy(synth.queries(w)).to(dev)
-    new_k = torch.from_numpy(np.stack([synth.appended_keys(w, 0, h, 1) for h in range(w.Hkv)])[None]).to(dev)
-    new_v = torch.from_numpy(np.stack([synth.values(w, 0, h, w.seq_len, 1) for h in range(w.Hkv)])[None]).to(dev)
+    new_k = torch.from_numpy(np.stack([np.stack([synth.appended_keys(w, b, h, 1) for h in range(w.Hkv)])
+                                       for b in range(w.B)])).to(dev)
+    new_v = torch.from_numpy(np.stack([np.stack([synth.values(w, b, h, int(lens[b]) - 1, 1) for h in range(w.Hkv)])
+                                       for b in range(w.B)])).to(dev)
     pos = torch.from_numpy((lens - 1).astype(np.int32)).to(dev)
     seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
     out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
@@ -384,7 +420,7 @@ def run_ours(args):
     nk_host = new_k.cpu().pin_memory()
     nv_host = new_v.cpu().pin_memory()
     o_host = torch.empty((w.B, w.Hq, 128), dtype=torch.float16).pin_memory()
-    fp16 = fp16_baseline(w, kv_fp16, lens, dev, stream) if kv_fp16 is not None else None
+    fp16 = None if args.profile_steps else fp16_baseline(w, kv_fp16, lens, dev, stream)
     del kv_fp16
     e2e_steps = max(20, min(args.steps, 2000))
     with torch.cuda.stream(stream):
@@ -419,22 +455,26 @@ def run_ours(args):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     achieved = alg / (dec_avg_ms * 1e-3) / 1e9
-    traffic, _ = profile_traffic()
+    traffic = profile_traffic()[0] if headline else None
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if headline else f"decode-attn KV tokens/s and HBM GB/s ({w.name}, "
+                                                 f"{'2' if w.mode == 0 else '1.5'}-bit)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
-                   "bits": 2, "splits_per_kv_head": n_splits,
+                   "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits,
                    "step": "encode 1 new K row + 1 new V row per sequence, then decode attention",
-                   "cache": "encoded on the GPU by vqkv_encode from seeded synthetic K/V",
+                   "cache": ("encoded on the GPU by vqkv_encode from seeded synthetic K/V" if headline
+                             else "seeded uniform codes (decode cost does not depend on code values)"),
                    "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB > "
                          f"{l2 / 1e6:.0f} MB L2)",
                    "timing": f"CUDA graphs of {g_steps} steps, CUDA events on the launch stream",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "decode_vq2_kernel", "launch_ms": dec_avg_ms, "algorithmic_bytes": alg},
+                     "kernel": "decode_vq2_kernel" if w.mode == 0 else "decode_vq15_kernel",
+                     "launch_ms": dec_avg_ms, "algorithmic_bytes": alg},
         "clocks": clk,
         "e2e": {"value": world * tokens / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
@@ -447,20 +487,70 @@ def run_ours(args):
     if fp16 is not None:
         fp16["vq_decode_speedup"] = fp16["launch_us"] / (dec_avg_ms * 1e3)
         line["fp16_kv_decode"] = fp16
+    if args.workload == 4 and not args.profile_steps:
+        line["encode_prefill"] = encode_prefill_bench(w, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
-    """The same decode over a plain fp16 K/V cache (vqkv_decode_attn_fp16):
-    average launch time from CUDA events around a graph of launches.  The
-    805 MB cache is larger than L2, so consecutive launches stream from HBM."""
+def encode_prefill_bench(w, dev, reps=3):
+    """vqkv_encode of the whole prefill (B x Hkv x prefill rows) for K and V in
+    both bit-widths; keys are Gaussian with the workload's outlier channels,
+    made on the GPU; codebooks calibrated on the host."""
     import torch
     from vector_quantized_bit_gb300 import _lib
-    k = torch.from_numpy(np.stack([kv[h][0] for h in range(w.Hkv)])[None]).to(dev)
-    v = torch.from_numpy(np.stack([kv[h][1] for h in range(w.Hkv)])[None]).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + w.config_id + 31)
+    res = {}
+    for mode in (synth.MODE_VQ2, synth.MODE_VQ15):
+        wm = w.with_mode(mode)
+        s_h, kcb_h, vcb_h = host_calibration(wm)
+        s, kcb, vcb = (torch.from_numpy(a).to(dev) for a in (s_h, kcb_h, vcb_h))
+        codes = torch.zeros((w.B, w.Hkv, _lib.vqkv_code_bytes(mode, w.cap_len)), dtype=torch.uint8, device=dev)
+        pos = torch.zeros(w.B, dtype=torch.int32, device=dev)
+        out = {}
+        for role in (0, 1):
+            x = torch.randn((w.B, w.Hkv, w.prefill, 128), generator=gen, device=dev)
+            if role == 0:
+                for h in range(w.Hkv):
+                    ch, sc = synth.outlier_channels(w, h)
+                    x[:, h, :, torch.from_numpy(ch).to(dev)] *= torch.from_numpy(sc).to(dev)
+            x = x.half()
+            call = lambda: _lib.vqkv_encode(mode, role, x, pos, s if role == 0 else None,  # noqa: E731
+                                            kcb if role == 0 else vcb, codes, w.cap_len)
+            call()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            out["K" if role == 0 else "V"] = {"ms": ms, "rows_per_s": w.B * w.Hkv * w.prefill / (ms * 1e-3)}
+            del x
+        res["2-bit" if mode == 0 else "1.5-bit"] = out
+    return res
+
+
+def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
+    """The same decode over a plain fp16 K/V cache (vqkv_decode_attn_fp16):
+    average launch time from CUDA events around a graph of launches.  The fp16
+    cache is larger than L2, so consecutive launches stream from HBM.  kv:
+    the workload's host K/V rows, or None for seeded Gaussian rows made on the
+    GPU."""
+    import torch
+    from vector_quantized_bit_gb300 import _lib
+    if kv is not None:
+        k = torch.from_numpy(np.stack([kv[h][0] for h in range(w.Hkv)])[None]).to(dev)
+        v = torch.from_numpy(np.stack([kv[h][1] for h in range(w.Hkv)])[None]).to(dev)
+    else:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed * 1000 + w.config_id + 17)
+        k = torch.randn((w.B, w.Hkv, w.cap_len, 128), generator=gen, device=dev, dtype=torch.float16)
+        v = torch.randn((w.B, w.Hkv, w.cap_len, 128), generator=gen, device=dev, dtype=torch.float16)
     q = torch.from_numpy(synth.queries(w)).to(dev)
     seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
     out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
@@ -482,8 +572,8 @@ def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
         e1.record(stream)
         torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (launches * reps)
-    nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2
     tokens = int(lens.sum())
+    nbytes = tokens * w.Hkv * 2 * 128 * 2 + 2 * q.numel() * 2   # K and V rows read, q read, O written
     return {"launch_us": us, "tokens_per_s": tokens / (us * 1e-6), "GB_per_s": nbytes / us / 1e3,
             "algorithmic_bytes": nbytes, "kernel": "decode_fp16_kernel",
             "how": "graph of 60 launches x 5 replays, CUDA events; fp16 K/V of the same synthetic cache"}
