@@ -141,6 +141,35 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization, so it may become resident while
+// the previous kernel on the stream is still running.  Before it reads any
+// input or writes any output it calls grid_dependency_wait(), which returns
+// once the previous grid has completed and its writes are visible; then
+// grid_dependents_launch() lets the next kernel start its own launch (it
+// orders no memory).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------------- FWHT
 
 // In-warp fast Walsh-Hadamard transform of a 128-vector held 4 per lane

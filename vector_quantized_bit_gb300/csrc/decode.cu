@@ -10,9 +10,11 @@
 //                                                  scale*log2(e))
 //   O[d][h] += sum_t V[t][d] P[t][h]              (tensor cores, V gathered
 //                                                  from the smem codebook)
-// Dequantisation happens only in registers: codes stream from HBM with
-// 128-bit loads straight into the fragment layout (the cache layout puts each
-// lane's codes in one contiguous run), centroids come from shared memory.
+// Dequantisation happens only in registers: the cache layout puts each
+// lane's codes for its MMA fragments in one contiguous 16-byte (2-bit) or
+// 48-byte (1.5-bit) run; 2-bit codes reach shared memory through a per-warp
+// ring of TMA bulk copies, 1.5-bit codes come with 128-bit loads straight
+// into registers; centroids are gathered from shared memory.
 //
 // The per-query transform is q' = (q * s) . Hn, so q'.K'^T = q.K^T
 // (VecInfer paper summary page, "Summary": matching inverse operations on
@@ -25,7 +27,7 @@
 //              one subvector (VQ2: j = 4s+tig at k-step s; VQ15: half of
 //              subvector j = 4s'+tig at k-steps 2s', 2s'+1), so one 8/16-byte
 //              centroid load fills a0a1|a4a5 (token gid) or a2a3|a6a7;
-//              B = q' (k = channels, n = heads, rows >= g are zero);
+//              B = q' (k = channels, n = heads, columns >= g are zero);
 //              D: tokens {gid, gid+8} x heads {2tig, 2tig+1}.
 //   P          D -> fp16 -> movmatrix.trans -> B operand of the P.V MMA
 //              (k = tokens {2tig, 2tig+1, 2tig+8, 2tig+9}, n = head gid).
@@ -112,91 +114,47 @@ __device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
 
 // One step of the 2-bit path over T consecutive 16-token tiles.
 //
-// Scores run as S[h][t] = q'[h] . K'[t] with heads as MMA rows (rows g..15
-// are zero) and 8 tokens as columns per MMA: the B operand of k-step s for
-// token n = gid is channels 4j..4j+3 of subvector j = 4s+tig, i.e. exactly one
-// 8-byte centroid gather, and the result (head gid x tokens 2tig, 2tig+1) is
-// already the B operand the P.V MMA wants for that head.
+// Scores: tokens are the MMA rows, heads the 8 columns.  The A operand of
+// k-step s is two 8-byte centroid gathers (tokens gid and gid+8, channels
+// 4j..4j+3 of subvector j = 4s+tig), B is q' (qa), so a 16-token tile takes
+// 8 score MMAs.  movmatrix turns the scores into the P.V B operand.
 //   kq[i]: this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig)
 //   vq[i]: this lane's 16 value-code bytes (word p: tokens 2tig, 2tig+1,
 //          2tig+8, 2tig+9 of subvector 8p+gid)
-// Softmax state m, l belongs to head gid; O^T fragments hold heads 2tig, 2tig+1.
+// Softmax state m0/l0, m1/l1 belongs to heads 2tig, 2tig+1, the columns of
+// this lane's O^T fragments.
 template <int T>
 __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
-                                         const uint32_t (&qa)[8][2], const uint4 (&kq)[T], const uint4 (&vq)[T],
-                                         int tile0, int L, int lane, float& m, float& l, float (&acc)[8][4]) {
-  const int tig = lane & 3;
-  // sc[i][u][e]: score of head gid for token 16(tile0+i) + 8u + 2tig + e
-  float sc[T][2][2];
+                                            const uint32_t (&qa)[8][2], const uint4 (&kq)[T],
+                                            const uint4 (&vq)[T], int tile0, int L, int lane, float& m0,
+                                            float& m1, float& l0, float& l1, float (&acc)[8][4]) {
+  const int gid = lane >> 2;
+  float sc[T][4];
 #pragma unroll
   for (int i = 0; i < T; ++i) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t w_lo = u ? kq[i].z : kq[i].x;   // subvectors 4s+tig, s = 0..3
-      const uint32_t w_hi = u ? kq[i].w : kq[i].y;   // s = 4..7
-#define VQKV_SCORE_STEP(S, ACC)                                                          \
-  {                                                                                      \
-    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? w_lo : w_hi, kbyte)); \
-    mma_16816(ACC, qa[S][0], 0u, qa[S][1], 0u, c.x, c.y);                                \
+    float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#define VQKV_SCORE_STEP(S, ACC)                                                              \
+  {                                                                                          \
+    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i].x : kq[i].y, kbyte)); \
+    const uint2 d = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i].z : kq[i].w, kbyte)); \
+    mma_16816(ACC, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);                                   \
   }
-      VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
-      VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
+    VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
+    VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
 #undef VQKV_SCORE_STEP
-      sc[i][u][0] = da[0] + db[0];
-      sc[i][u][1] = da[1] + db[1];
-    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[i][e] = da[e] + db[e];
   }
   if ((tile0 + T) * V2_TILE > L) {   // tail of the sequence
 #pragma unroll
-    for (int i = 0; i < T; ++i)
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if ((tile0 + i) * V2_TILE + 8 * u + 2 * tig + e >= L) sc[i][u][e] = neg_inf();
-  }
-  // ---- online softmax for head gid (rescale only when a score exceeds m by 2^8)
-  bool need = false;
-#pragma unroll
-  for (int i = 0; i < T; ++i)
-    need |= (sc[i][0][0] > m + kSoftmaxSlack) | (sc[i][0][1] > m + kSoftmaxSlack) |
-            (sc[i][1][0] > m + kSoftmaxSlack) | (sc[i][1][1] > m + kSoftmaxSlack);
-  if (__any_sync(0xffffffffu, need)) {
-    float x = fmaxf(fmaxf(sc[0][0][0], sc[0][0][1]), fmaxf(sc[0][1][0], sc[0][1][1]));
-#pragma unroll
-    for (int i = 1; i < T; ++i)
-      x = fmaxf(x, fmaxf(fmaxf(sc[i][0][0], sc[i][0][1]), fmaxf(sc[i][1][0], sc[i][1][1])));
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-    const float n = fmaxf(m, x);
-    const float alpha = fast_exp2(m - n);
-    m = n;
-    l *= alpha;
-    // O^T columns of this lane are heads 2tig, 2tig+1: their factors live on lanes 8tig, 8tig+4
-    const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-    const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc[mt][0] *= a0;
-      acc[mt][1] *= a1;
-      acc[mt][2] *= a0;
-      acc[mt][3] *= a1;
+    for (int i = 0; i < T; ++i) {
+      const int t0 = (tile0 + i) * V2_TILE + gid;
+      if (t0 >= L) sc[i][0] = sc[i][1] = neg_inf();
+      if (t0 + 8 >= L) sc[i][2] = sc[i][3] = neg_inf();
     }
   }
   uint32_t bP[T][2];
-#pragma unroll
-  for (int i = 0; i < T; ++i) {
-    float p[2][2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) p[u][e] = fast_exp2(sc[i][u][e] - m);
-    l += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-    bP[i][0] = pack_half2(p[0][0], p[0][1]);   // tokens 2tig, 2tig+1 of head gid
-    bP[i][1] = pack_half2(p[1][0], p[1][1]);   // tokens 8+2tig, 9+2tig
-  }
-  // ---- O^T += V^T P: subvector J = 8*pp + gid, tokens (2tig, 2tig+1, 2tig+8, 2tig+9)
+  softmax_tiles<T, 8>(sc, m0, m1, l0, l1, acc, bP);
 #pragma unroll
   for (int i = 0; i < T; ++i) {
 #define VQKV_PV_STEP(PP, W)                                                                    \
@@ -213,32 +171,6 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   }
     VQKV_PV_STEP(0, vq[i].x) VQKV_PV_STEP(1, vq[i].y) VQKV_PV_STEP(2, vq[i].z) VQKV_PV_STEP(3, vq[i].w)
 #undef VQKV_PV_STEP
-  }
-}
-
-// Store one warp's (m, l, O) of the 2-bit path into the combine area: m and
-// l are per head gid (l summed over the warp's token columns), O^T as in
-// stash_warp.
-__device__ __forceinline__ void stash_warp_vq2(float* s_comb, int warp, int lane, const float (&acc)[8][4],
-                                               float m, float l) {
-  const int gid = lane >> 2, tig = lane & 3;
-  float* wO = s_comb;
-  float* wm = s_comb + CombineSmem<V2_WARPS>::kO;
-  float* wl = wm + V2_WARPS * 8;
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
-  const int h0 = warp * 8 + 2 * tig;
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = Vq2Dim()(mt, gid), d1 = Vq2Dim()(mt, gid + 8);
-    wO[h0 * kHeadDim + d0] = acc[mt][0];
-    wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
-    wO[h0 * kHeadDim + d1] = acc[mt][2];
-    wO[(h0 + 1) * kHeadDim + d1] = acc[mt][3];
-  }
-  if (tig == 0) {
-    wm[warp * 8 + gid] = m;
-    wl[warp * 8 + gid] = l;
   }
 }
 
@@ -267,6 +199,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     mbar_init_fence();
   }
   __syncwarp();
+  grid_dependency_wait();
+  grid_dependents_launch();
   uint32_t uses = 0;        // super-tiles this warp has taken through its ring (all sequences)
   bool timed_out = false;
 
@@ -278,7 +212,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m = kMInit, l = 0.f;
+    float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
       const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
@@ -346,8 +280,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         __syncwarp();
         // refill the stage this warp finished with in the previous step
         if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
-        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, L, lane, m,
-                         l, acc);
+        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, L, lane, m0,
+                         m1, l0, l1, acc);
       }
       if (timed_out) {
         // give the copies already issued a bounded chance to land before the
@@ -361,7 +295,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       uses += n_mine;
     }
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
-    stash_warp_vq2(s_comb, warp, lane, acc, m, l);
+    stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
     __syncthreads();
     finish_sequence<V2_WARPS>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
@@ -392,6 +326,8 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
   const uint32_t kcb_s = smem_u32(s_kcb);
   const uint32_t vcb_s = smem_u32(s_vcb);
   bool have_cb = false;
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   for (int b = b_begin; b < b_end; ++b) {
     const int L = load_len(p, b);
@@ -535,11 +471,8 @@ cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  if (mode == VQKV_MODE_VQ2)
-    decode_vq2_kernel<<<grid, V2_THREADS, kV2Smem, stream>>>(p);
-  else
-    decode_vq15_kernel<<<grid, V15_THREADS, kV15Smem, stream>>>(p);
-  return cudaGetLastError();
+  if (mode == VQKV_MODE_VQ2) return launch_pdl(decode_vq2_kernel, grid, dim3(V2_THREADS), kV2Smem, stream, p);
+  return launch_pdl(decode_vq15_kernel, grid, dim3(V15_THREADS), kV15Smem, stream, p);
 }
 
 }  // namespace vqkv

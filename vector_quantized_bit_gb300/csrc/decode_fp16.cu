@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(F_THREADS, 1) decode_fp16_kernel(const DecodeP
   const int b_begin = blockIdx.z * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
   const uint32_t ring = smem_u32(smem) + warp * (F_STAGES * F_STAGE_BYTES);
-  const long long cap = p.stream_bytes / F_ROW_BYTES;   // tokens per (b, kvh) stream
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   for (int b = b_begin; b < b_end; ++b) {
     const int L = load_len(p, b);
@@ -142,7 +143,6 @@ __global__ void __launch_bounds__(F_THREADS, 1) decode_fp16_kernel(const DecodeP
     finish_sequence<F_WARPS>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();
   }
-  (void)cap;
 }
 
 }  // namespace
@@ -159,8 +159,7 @@ cudaError_t decode_fp16_occupancy(int* blocks_per_sm) {
 }
 
 cudaError_t launch_decode_fp16(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  decode_fp16_kernel<<<grid, F_THREADS, kF16Smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_fp16_kernel, grid, dim3(F_THREADS), kF16Smem, stream, p);
 }
 
 }  // namespace vqkv

@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
   __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_dependents_launch();
   for (int c = threadIdx.x; c < 256; c += ENC_THREADS) {
     const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * 256 + c);
     const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
@@ -235,6 +237,8 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodePa
   __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_dependents_launch();
   for (int c = threadIdx.x; c < 4096; c += ENC_THREADS) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
     const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
@@ -369,6 +373,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   // B table and the largest centroid norm of this KV head
   float cmax = 0.f;
@@ -537,17 +543,11 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
 cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool split_rows, cudaStream_t stream) {
   const dim3 grid(blocks_x, p.Hkv);
   if (mode == VQKV_MODE_VQ2) {
-    if (split_rows)
-      encode_vq2_kernel<ENC_WARPS><<<grid, ENC_THREADS, 0, stream>>>(p);
-    else
-      encode_vq2_kernel<1><<<grid, ENC_THREADS, 0, stream>>>(p);
-  } else {
-    if (split_rows)
-      encode_vq15_kernel<ENC_WARPS><<<grid, ENC_THREADS, kV15EncSmem, stream>>>(p);
-    else
-      encode_vq15_tc_kernel<<<grid, TC_THREADS, kTcSmem, stream>>>(p);
+    if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_vq2_kernel<1>, grid, dim3(ENC_THREADS), 0, stream, p);
   }
-  return cudaGetLastError();
+  if (split_rows) return launch_pdl(encode_vq15_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), kV15EncSmem, stream, p);
+  return launch_pdl(encode_vq15_tc_kernel, grid, dim3(TC_THREADS), kTcSmem, stream, p);
 }
 
 }  // namespace vqkv
