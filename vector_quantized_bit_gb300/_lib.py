@@ -18,6 +18,7 @@ VQKV_ROLE_K = 0
 VQKV_ROLE_V = 1
 VQKV_DEVERR_SEQ_LEN = 0x1
 VQKV_DEVERR_POSITION = 0x2
+VQKV_DEVERR_TIMEOUT = 0x4
 
 STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3: "VQKV_ERR_WORKSPACE",
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
@@ -168,8 +169,9 @@ def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook
                      cap_len, max_seq_len, softmax_scale=0.0, num_splits=0, stream=None) -> None:
     """O = decode attention of q [B][Hq][128] (fp16) over the packed cache.
 
-    Writes ``out`` (fp16 [B][Hq][128]).  ``workspace``: a zero-initialised
-    device buffer of at least vqkv_decode_workspace_bytes bytes.
+    Writes ``out`` (fp16 [B][Hq][128]).  ``workspace``: a device buffer of
+    at least vqkv_decode_workspace_bytes bytes; its first word is the sticky
+    device error word (zero it before reading it).
     """
     a = decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,
                     max_seq_len, softmax_scale, num_splits)

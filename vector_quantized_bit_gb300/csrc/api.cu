@@ -258,10 +258,13 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
   p.n_splits = pl.n_splits;
   p.tps = pl.tps;
   p.bpg = pl.bpg;
+  p.defer_merge = pl.bpg > 1 ? 1 : 0;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
   p.qscale = scale * 1.4426950408889634f / std::sqrt(128.0f);
   const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
   if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
+  if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
 
@@ -339,10 +342,13 @@ vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* a, void* stream) 
   p.n_splits = pl.n_splits;
   p.tps = pl.tps;
   p.bpg = pl.bpg;
+  p.defer_merge = pl.bpg > 1 ? 1 : 0;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
   p.qscale = scale * 1.4426950408889634f;
   const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
   if (launch_decode_fp16(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
+  if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
 

@@ -20,7 +20,8 @@
 // (VecInfer paper summary page, "Summary": matching inverse operations on
 // the queries keep attention scores unchanged).  Split partials (m, l, O)
 // are merged by the last CTA of each (sequence, KV head), chosen with an
-// atomic ticket (no waiting).
+// atomic ticket (no waiting), or, when a CTA covers several sequences, by a
+// small combine kernel launched right after the decode kernel.
 //
 // Fragment maps (mma.m16n8k16, lane = 4*gid + tig):
 //   score MMA  A = K' tile: rows = tokens {gid, gid+8}, k = the 4 channels of
@@ -74,13 +75,21 @@ constexpr int V15_THREADS = V15_WARPS * 32;
 constexpr int V15_TILE = 64;
 constexpr int V15_TILE_BYTES = 1536;
 constexpr int V15_CB_BYTES = 4096 * 16;          // 64 KB per codebook
-constexpr int V15_PF_TILES = 2 * V15_WARPS;
+// Per-lane code slot: the lane's 48 key-code bytes and 48 value-code bytes
+// of the next tile, copied with cp.async one tile ahead (each lane copies
+// and reads only its own bytes).
+constexpr int V15_SLOT_OFF = 2 * V15_CB_BYTES;
+constexpr int V15_SLOT_BYTES = V15_THREADS * 96;  // 48 KB
+constexpr int V15_Q_OFF = V15_SLOT_OFF + V15_SLOT_BYTES;
 
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
 // codebook and q' region after the tile loop.
 constexpr size_t kV2Smem = V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8;
 static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must fit below the ring");
+// The combine area (after the tile loop) and q' (before it) overlap the
+// code slots, which are idle at those times.
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
+static_assert(V15_Q_OFF + 8 * 128 * 4 <= (int)kV15Smem, "q' must fit in the combine area");
 
 // q' for the g heads of (b, kvh) into s_qp[h][128] (fp32, scaled), by warps 0..g-1.
 __device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
@@ -315,7 +324,8 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
   uint4* s_kcb = reinterpret_cast<uint4*>(smem);
   uint4* s_vcb = reinterpret_cast<uint4*>(smem + V15_CB_BYTES);
   float* s_comb = reinterpret_cast<float*>(smem + 2 * V15_CB_BYTES);
-  float* s_qp = s_comb;
+  float* s_qp = reinterpret_cast<float*>(smem + V15_Q_OFF);
+  const uint32_t slot = smem_u32(smem + V15_SLOT_OFF) + threadIdx.x * 96;
   __shared__ int s_last;
 
   const int split = blockIdx.x, kvh = blockIdx.y;
@@ -340,6 +350,21 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
+      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+      // this lane's 48 + 48 code bytes of `tile` into its slot
+      auto copy_codes = [&](int tile) {
+        const uint8_t* kp = kbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+        const uint8_t* vp = vbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          cp_async16(slot + 16 * i, kp + 16 * i, 16);
+          cp_async16(slot + 48 + 16 * i, vp + 16 * i, 16);
+        }
+        cp_async_commit();
+      };
+      // the first tile's copy overlaps the prologue
+      if (t_begin + warp < t_end) copy_codes(t_begin + warp);
       if (!have_cb) {
         const uint4* gk = reinterpret_cast<const uint4*>(p.kcb) + (size_t)kvh * 4096;
         const uint4* gv = reinterpret_cast<const uint4*>(p.vcb) + (size_t)kvh * 4096;
@@ -367,27 +392,23 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
       }
       __syncthreads();
 
-      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
       for (int tile = t_begin + warp; tile < t_end; tile += V15_WARPS) {
-        if (lane == 0) {
-          const int pf = tile + V15_PF_TILES;
-          if (pf < t_end) {
-            prefetch_l2_bulk(kbase + (size_t)pf * V15_TILE_BYTES, V15_TILE_BYTES);
-            prefetch_l2_bulk(vbase + (size_t)pf * V15_TILE_BYTES, V15_TILE_BYTES);
-          }
-        }
         uint32_t kw[12], vw[12];
-        {
-          const uint8_t* kp = kbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
-          const uint8_t* vp = vbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+        cp_async_wait<0>();
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
-            const uint4 a = ldg_stream(kp + 16 * i);
-            kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
-            const uint4 c = ldg_stream(vp + 16 * i);
-            vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
-          }
+        for (int i = 0; i < 3; ++i) {
+          const uint4 a = lds128(slot + 16 * i);
+          kw[4 * i] = a.x; kw[4 * i + 1] = a.y; kw[4 * i + 2] = a.z; kw[4 * i + 3] = a.w;
+          const uint4 c = lds128(slot + 48 + 16 * i);
+          vw[4 * i] = c.x; vw[4 * i + 1] = c.y; vw[4 * i + 2] = c.z; vw[4 * i + 3] = c.w;
+        }
+        if (tile + V15_WARPS < t_end) {
+          // the slot is overwritten only after every word above has arrived
+          asm volatile("" ::"r"(kw[0]), "r"(kw[1]), "r"(kw[2]), "r"(kw[3]), "r"(kw[4]), "r"(kw[5]),
+                       "r"(kw[6]), "r"(kw[7]), "r"(kw[8]), "r"(kw[9]), "r"(kw[10]), "r"(kw[11]));
+          asm volatile("" ::"r"(vw[0]), "r"(vw[1]), "r"(vw[2]), "r"(vw[3]), "r"(vw[4]), "r"(vw[5]),
+                       "r"(vw[6]), "r"(vw[7]), "r"(vw[8]), "r"(vw[9]), "r"(vw[10]), "r"(vw[11]));
+          copy_codes(tile + V15_WARPS);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -444,6 +465,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
         }
       }
     }
+    __syncthreads();   // every warp is done with its code slot: the combine area overlaps them
     stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
     __syncthreads();
     finish_sequence<V15_WARPS>(p, b, kvh, split, s_comb, &s_last);
@@ -451,7 +473,18 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
   }
 }
 
+// One CTA per (query head, sequence), one thread per channel.
+__global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodeParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  combine_splits(p);
+}
+
 }  // namespace
+
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+  return launch_pdl(decode_combine_kernel, dim3(p.Hq, p.B), dim3(kHeadDim), 0, stream, p);
+}
 
 int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TILE : V15_TILE; }
 int decode_tiles_per_step(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TPI : 1; }

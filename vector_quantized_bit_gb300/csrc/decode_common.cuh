@@ -117,9 +117,15 @@ __device__ __forceinline__ void softmax_tiles(float (&sc)[T][4], float& m0, floa
   }
 }
 
-// Merge the per-warp states of the CTA into one partial (m, l, O) per head
-// and write it to the workspace; then take the (b, kvh) ticket and, if this
-// CTA is the last one, merge all split partials into O (fp16).
+// Merge the per-warp states of the CTA into one partial (m, l, O) per head.
+// With one split that is O itself.  Otherwise write the partial to the
+// workspace; then, when the plan defers the merge (CTAs that cover several
+// sequences must not stall between them), the combine kernel merges the
+// splits after the decode kernel.  Else take the (b, kvh) ticket; the CTA
+// that arrives last merges all split partials into O (fp16).  Ordering: the CTA's partial stores
+// happen before thread 0's acq_rel ticket increment (CTA barrier, then a
+// cumulative gpu-scope release); the last CTA's acquire and the barrier
+// after it order its partial loads after every other CTA's stores.
 template <int WARPS>
 __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
                                                 float* s_comb, int* s_last) {
@@ -141,21 +147,28 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
       o += wO[(w * 8 + h) * kHeadDim + d] * f;
       l += wl[w * 8 + h] * f;
     }
+    if (p.n_splits == 1) {
+      p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+      continue;
+    }
     part[h * kPartialStride + d] = o;
     if (d == 0) {
       part[h * kPartialStride + 128] = M;
       part[h * kPartialStride + 129] = l;
     }
   }
-  __threadfence();
+  if (p.n_splits == 1 || p.defer_merge) return;
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(p.tickets + b * p.Hkv + kvh, 1u);
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(p.tickets + b * p.Hkv + kvh)
+                 : "memory");
     *s_last = (prev == (unsigned)(p.n_splits - 1));
   }
   __syncthreads();
   if (*s_last) {
-    __threadfence();
     // All split partials of (b, kvh) are staged in shared memory by the whole
     // CTA (coalesced, every load in flight at once), then each thread merges
     // one output (head, channel) with a running max.  Chunks of splits when
@@ -197,6 +210,38 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     }
     if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
   }
+}
+
+// Merge the split partials of query head hq = blockIdx.x of sequence
+// b = blockIdx.y into O (fp16); thread d owns channel d.  The combine kernel
+// of plans that defer the merge.
+__device__ __forceinline__ void combine_splits(const DecodeParams& p) {
+  constexpr int U = 8;   // splits whose loads are in flight together
+  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int kvh = hq / p.g, h = hq - kvh * p.g;
+  const size_t stride = (size_t)p.g * kPartialStride;
+  const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * stride + h * kPartialStride;
+  float M = kMInit, O = 0.f, Ls = 0.f;
+  for (int s0 = 0; s0 < p.n_splits; s0 += U) {
+    float ms[U], ls[U], os[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool in = s0 + u < p.n_splits;
+      const float* ph = base + (in ? s0 + u : 0) * stride;
+      ms[u] = in ? __ldcg(ph + 128) : kMInit;
+      ls[u] = in ? __ldcg(ph + 129) : 0.f;
+      os[u] = in ? __ldcg(ph + d) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float n = fmaxf(M, ms[u]);
+      const float fa = fast_exp2(M - n), fb = fast_exp2(ms[u] - n);
+      O = O * fa + os[u] * fb;
+      Ls = Ls * fa + ls[u] * fb;
+      M = n;
+    }
+  }
+  p.out[((size_t)b * p.Hq + hq) * kHeadDim + d] = __float2half_rn(Ls > 0.f ? O / Ls : 0.f);
 }
 
 // Store one warp's (m, l, O) into the combine area.  acc holds O^T fragments:

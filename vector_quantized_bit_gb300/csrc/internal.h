@@ -29,6 +29,7 @@ struct DecodeParams {
   int n_splits;             // CTAs per (sequence, KV head)
   int tps;                  // tiles per split
   int bpg;                  // sequences per CTA (grid.z = ceil(B / bpg))
+  int defer_merge;          // 1: split partials are merged by the combine kernel
   float qscale;             // softmax_scale * log2(e) / sqrt(128)
 };
 
@@ -54,6 +55,9 @@ int decode_threads(int mode);
 cudaError_t decode_prepare(int mode);                // set smem attributes (once per device)
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm);
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream);
+// Merge of the split partials into O, after a decode kernel whose plan
+// defers the merge (p.defer_merge, n_splits > 1).
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
 
 // fp16-KV comparison kernel (decode_fp16.cu); DecodeParams.kc / .vc point to
 // the fp16 K / V caches, stream_bytes = cap_len * 256.
