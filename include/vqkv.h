@@ -180,6 +180,12 @@ size_t vqkv_decode_workspace_bytes(const vqkv_decode_args* args);
  * usable. */
 int32_t vqkv_decode_num_splits(const vqkv_decode_args* args);
 
+/* Kernels one vqkv_decode_attn call with these arguments enqueues on the
+ * current device: 1, or 2 when the plan merges the split partials in a
+ * second kernel (CTAs that cover several sequences).  Reads the sizes only;
+ * 0 for B == 0, -1 when a size is invalid or no device is usable. */
+int32_t vqkv_decode_kernel_count(const vqkv_decode_args* args);
+
 vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);
 vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
 

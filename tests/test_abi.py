@@ -97,6 +97,7 @@ def test_decode_validation(lib, kw, status):
     if not pointer_only:   # the size queries read sizes only
         assert lib.vqkv_decode_workspace_bytes(ctypes.byref(_dec(**kw))) == 0
         assert lib.vqkv_decode_num_splits(ctypes.byref(_dec(**kw))) == -1
+        assert lib.vqkv_decode_kernel_count(ctypes.byref(_dec(**kw))) == -1
 
 
 def test_decode_empty_batch_is_a_no_op(lib):

@@ -23,8 +23,8 @@ VQKV_DEVERR_TIMEOUT = 0x4
 STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3: "VQKV_ERR_WORKSPACE",
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
-EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_encode",
-            "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_fp16_decode_workspace_bytes",
+EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
+            "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_fp16_decode_workspace_bytes",
             "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -85,6 +85,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_decode_workspace_bytes.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.vqkv_decode_num_splits.restype = ctypes.c_int32
         L.vqkv_decode_num_splits.argtypes = [ctypes.POINTER(DecodeArgs)]
+        L.vqkv_decode_kernel_count.restype = ctypes.c_int32
+        L.vqkv_decode_kernel_count.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.vqkv_encode.restype = ctypes.c_int
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
@@ -163,6 +165,10 @@ def vqkv_decode_workspace_bytes(args: DecodeArgs) -> int:
 
 def vqkv_decode_num_splits(args: DecodeArgs) -> int:
     return int(lib().vqkv_decode_num_splits(ctypes.byref(args)))
+
+
+def vqkv_decode_kernel_count(args: DecodeArgs) -> int:
+    return int(lib().vqkv_decode_kernel_count(ctypes.byref(args)))
 
 
 def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace,

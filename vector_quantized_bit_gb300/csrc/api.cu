@@ -227,6 +227,15 @@ int32_t vqkv_decode_num_splits(const vqkv_decode_args* a) {
   return pl.n_splits;
 }
 
+int32_t vqkv_decode_kernel_count(const vqkv_decode_args* a) {
+  if (validate_decode_sizes(a) != VQKV_OK) return -1;
+  if (a->B == 0) return 0;
+  DecodePlan pl;
+  const PlanInput in = plan_input(a);
+  if (plan_decode(&in, &pl) != VQKV_OK) return -1;
+  return (pl.bpg > 1 && pl.n_splits > 1) ? 2 : 1;
+}
+
 vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK || a->B == 0) return st;

@@ -48,10 +48,10 @@ namespace {
 #define VQKV_V2_WARPS 16
 #endif
 #ifndef VQKV_V2_TPI
-#define VQKV_V2_TPI 2
+#define VQKV_V2_TPI 3
 #endif
 #ifndef VQKV_V2_STAGES
-#define VQKV_V2_STAGES 4
+#define VQKV_V2_STAGES 2
 #endif
 constexpr int V2_WARPS = VQKV_V2_WARPS;             // one CTA per SM
 constexpr int V2_TPI = VQKV_V2_TPI;                 // 16-token tiles per step (a "super-tile")
