@@ -254,6 +254,22 @@ def run_reference(args):
 
 # ------------------------------------------------------------- our arm
 
+def max_over_ranks(x, world, device):
+    """The largest x over all ranks (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_replica, ms_per_step, world):
+    """Whole-job KV tokens/s of `world` independent replicas (weak scaling:
+    every rank decodes its own copy of the workload; no data-path collective)."""
+    return world * tokens_per_replica / (ms_per_step * 1e-3)
+
+
 def profile_traffic():
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source."""
@@ -435,10 +451,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         dec_avg_ms = d0.elapsed_time(d1) / (reps * g_steps)
 
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
     q_host = torch.from_numpy(synth.queries(w)).pin_memory()
@@ -469,7 +482,7 @@ def run_ours(args):
 
     tokens = int(lens.sum())
     ms_step = ms_total / args.steps
-    value = world * tokens / (ms_step * 1e-3)
+    value = replica_throughput(tokens, ms_step, world)
     alg = algorithmic_bytes(w, lens)
     peaks = {}
     try:
