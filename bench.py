@@ -51,6 +51,9 @@ def parse():
                          "3: Qwen2.5-14B 1.5-bit; 4: Mistral-7B encode + decode")
     ap.add_argument("--mode", type=int, default=None, choices=[0, 1],
                     help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="2-bit: run a step as vqkv_encode (K) + vqkv_encode (V) + vqkv_decode_attn instead of "
+                         "the fused vqkv_decode_append")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
@@ -353,13 +356,31 @@ def run_ours(args):
     n_splits = _lib.vqkv_decode_num_splits(dargs)
     dec_kernels = _lib.vqkv_decode_kernel_count(dargs)
 
-    def step(i, ev=None):
+    fused = mode == synth.MODE_VQ2 and not args.unfused
+
+    def step_unfused(i, ev=None):
         kc, vc = copies[i % n_copies]
         _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
         _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
         if ev is not None:
             ev[0].record()
         _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+        if ev is not None:
+            ev[1].record()
+
+    def decode_call(i):
+        kc, vc = copies[i % n_copies]
+        if fused:
+            _lib.vqkv_decode_append(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len, new_k, new_v)
+        else:
+            _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+
+    def step(i, ev=None):
+        if not fused:
+            return step_unfused(i, ev)
+        if ev is not None:
+            ev[0].record()
+        decode_call(i)
         if ev is not None:
             ev[1].record()
 
@@ -438,8 +459,7 @@ def run_ours(args):
         graph_dec = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_dec, stream=stream):
             for i in range(g_steps):
-                kc, vc = copies[i % n_copies]
-                _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+                decode_call(i)
         graph_dec.replay()
         torch.cuda.synchronize()
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -450,6 +470,21 @@ def run_ours(args):
         d1.record(stream)
         torch.cuda.synchronize()
         dec_avg_ms = d0.elapsed_time(d1) / (reps * g_steps)
+        unfused_ms = None
+        if fused:
+            # the same step as three calls (two encodes, then the decode), for comparison
+            graph_unf = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_unf, stream=stream):
+                for i in range(g_steps):
+                    step_unfused(i)
+            graph_unf.replay()
+            torch.cuda.synchronize()
+            d0.record(stream)
+            for _ in range(reps):
+                graph_unf.replay()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            unfused_ms = d0.elapsed_time(d1) / (reps * g_steps)
 
     ms_total = max_over_ranks(ms_total, world, dev)
 
@@ -467,9 +502,12 @@ def run_ours(args):
             q.copy_(q_host, non_blocking=True)
             new_k.copy_(nk_host, non_blocking=True)
             new_v.copy_(nv_host, non_blocking=True)
-            _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
-            _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
-            _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+            if fused:
+                _lib.vqkv_decode_append(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len, new_k, new_v)
+            else:
+                _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
+                _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
+                _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
             o_host.copy_(out, non_blocking=True)
             stream.synchronize()
         for i in range(10):
@@ -484,6 +522,8 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     value = replica_throughput(tokens, ms_step, world)
     alg = algorithmic_bytes(w, lens)
+    if fused:
+        alg += 2 * w.B * w.Hkv * (128 * 2 + 128 // 4)   # the new rows read, their codes written
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -502,7 +542,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
                    "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits,
-                   "step": "encode 1 new K row + 1 new V row per sequence, then decode attention",
+                   "step": ("vqkv_decode_append: 1 new K row + 1 new V row per sequence encoded into the cache "
+                            "and attended in the same kernel" if fused else
+                            "vqkv_encode (1 new K row per sequence), vqkv_encode (V), vqkv_decode_attn"),
                    "cache": ("encoded on the GPU by vqkv_encode from seeded synthetic K/V" if headline
                              else "seeded uniform codes (decode cost does not depend on code values)"),
                    "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB > "
@@ -513,16 +555,20 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": "decode_vq2_kernel" if w.mode == 0 else "decode_vq15_kernel",
                      "launch_ms": dec_avg_ms, "algorithmic_bytes": alg,
-                     "how": f"graph of {g_steps} back-to-back vqkv_decode_attn calls ({dec_kernels} kernel(s) "
-                            "each) over the rotating cache copies, CUDA events on the launch stream",
+                     "how": f"graph of {g_steps} back-to-back {'vqkv_decode_append' if fused else 'vqkv_decode_attn'} "
+                            f"calls ({dec_kernels} kernel(s) each) over the rotating cache copies, CUDA events on "
+                            "the launch stream",
                      "in_step_launch_ms": dec_step_ms},
         "clocks": clk,
         "e2e": {"value": world * tokens / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
                 "d2h_bytes_per_step": out.numel() * 2,
-                "how": "public binding per step: H2D q and new K/V rows, 2 encodes, decode, D2H O, sync"},
-        "gpu_launches": (2 + dec_kernels) * args.steps,
+                "how": "public binding per step: H2D q and new K/V rows, "
+                       + ("vqkv_decode_append" if fused else "2 encodes, decode") + ", D2H O, sync"},
+        "gpu_launches": (dec_kernels if fused else 2 + dec_kernels) * args.steps,
     }
+    if unfused_ms is not None:
+        line["unfused_step_ms"] = unfused_ms
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if fp16 is not None:

@@ -190,6 +190,32 @@ vqkv_status vqkv_encode(const vqkv_encode_args* args, void* stream);
 vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
 
 /*
+ * vqkv_decode_append — one decode step of the path in one call: the encode
+ * of the step's new K and V rows (as vqkv_encode) fused into the decode
+ * attention that reads them (as vqkv_decode_attn).
+ *
+ * For every sequence b with L = seq_lens[b] > 0 (clamped to max_seq_len as
+ * in vqkv_decode_attn), k_new[b][h] and v_new[b][h] are encoded exactly as
+ * vqkv_encode with n_rows = 1 and pos[b] = L - 1 would encode them, and their
+ * codes are written at position L - 1 of the K and V streams of
+ * decode.k_codes / decode.v_codes (which this call therefore writes, despite
+ * their const type).  O is then what vqkv_decode_attn returns for the same
+ * arguments over the L tokens including the new one.  The new token's codes
+ * reach the attention on chip, so the result does not depend on the order
+ * in which the cache bytes land.  Workspace, error word, alignment and
+ * failure rules are those of vqkv_decode_attn.  2-bit mode only
+ * (VQKV_ERR_UNSUPPORTED otherwise).
+ */
+typedef struct {
+  vqkv_decode_args decode;    /* as for vqkv_decode_attn (seq_lens include the new token) */
+  const uint16_t* k_new;      /* device fp16 [B][Hkv][128], 8-byte aligned: new key rows */
+  const uint16_t* v_new;      /* device fp16 [B][Hkv][128], 8-byte aligned: new value rows */
+  unsigned long long* near_tie_count; /* device, optional: as in vqkv_encode_args, for both rows */
+} vqkv_decode_append_args;
+
+vqkv_status vqkv_decode_append(const vqkv_decode_append_args* args, void* stream);
+
+/*
  * vqkv_decode_attn_fp16 — the same decode attention over a plain fp16 KV
  * cache, the comparison point for the quantised path on the same shapes
  * (the paper measures its speed-up against FP16 attention, summary page,

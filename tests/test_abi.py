@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header(tmp_path):
     """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
     fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs,
-              "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs}
+              "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs, "vqkv_decode_append_args": _lib.DecodeAppendArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -140,3 +140,17 @@ def test_product_path_has_no_cpu_fallback(monkeypatch, tmp_path):
         _lib.lib(str(tmp_path / "missing.so"))
     src = open(_lib.__file__).read() + open(os.path.join(ROOT, "vector_quantized_bit_gb300", "__init__.py")).read()
     assert "oracle" not in src.replace("no fallback", "")
+
+
+def test_decode_append_validation(lib):
+    # checked on the host before anything is launched (no device needed)
+    a = _lib.DecodeAppendArgs()
+    a.decode = _dec(mode=1)
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # 2-bit only
+    a.decode = _dec()
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1    # no new rows
+    a.k_new, a.v_new = 0x10000, 0x10004                             # v_new not 8-byte aligned
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1
+    assert lib.vqkv_decode_append(None, None) == 1
+    a.decode = _dec(B=0, q=None, out=None)
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 0    # empty batch: a no-op

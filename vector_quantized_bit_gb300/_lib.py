@@ -24,8 +24,8 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
-            "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_static", "vqkv_fp16_decode_workspace_bytes",
-            "vqkv_decode_attn_fp16", "vqkv_status_string"]
+            "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_append", "vqkv_decode_attn_static",
+            "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -62,6 +62,11 @@ class Fp16DecodeArgs(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
 
 
+class DecodeAppendArgs(ctypes.Structure):
+    _fields_ = [("decode", DecodeArgs), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("near_tie_count", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -91,6 +96,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_decode_append.restype = ctypes.c_int
+        L.vqkv_decode_append.argtypes = [ctypes.POINTER(DecodeAppendArgs), ctypes.c_void_p]
         L.vqkv_decode_attn_static.restype = ctypes.c_int
         L.vqkv_decode_attn_static.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
         L.vqkv_fp16_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -184,6 +191,19 @@ def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook
     st = lib().vqkv_decode_attn(ctypes.byref(a), _stream(stream))
     if st != 0:
         raise VqkvError(st, "vqkv_decode_attn")
+
+
+def vqkv_decode_append(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace,
+                       cap_len, max_seq_len, k_new, v_new, near_tie_count=None, softmax_scale=0.0, num_splits=0,
+                       stream=None) -> None:
+    """One fused decode step: encodes k_new / v_new (fp16 [B][Hkv][128]) at
+    position seq_lens[b] - 1 of the caches, then writes O as vqkv_decode_attn."""
+    a = DecodeAppendArgs(decode=decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out,
+                                            workspace, cap_len, max_seq_len, softmax_scale, num_splits),
+                         k_new=_ptr(k_new), v_new=_ptr(v_new), near_tie_count=_ptr(near_tie_count))
+    st = lib().vqkv_decode_append(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_append")
 
 
 def vqkv_decode_attn_static(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, cap_len,

@@ -194,6 +194,11 @@ PlanInput plan_input(const vqkv_fp16_decode_args* a) {
 
 vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(a); }
 
+namespace {
+// Both decode entry points: ap == nullptr for vqkv_decode_attn.
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, void* stream);
+}  // namespace
+
 size_t decode_ticket_region_bytes(int B, int Hkv) {
   return round_up(kWsHeader + sizeof(unsigned) * (size_t)std::max(B, 1) * Hkv, 256);
 }
@@ -236,9 +241,28 @@ int32_t vqkv_decode_kernel_count(const vqkv_decode_args* a) {
   return (pl.bpg > 1 && pl.n_splits > 1) ? 2 : 1;
 }
 
-vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
+vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) { return decode_launch(a, nullptr, stream); }
+
+vqkv_status vqkv_decode_append(const vqkv_decode_append_args* ap, void* stream) {
+  if (ap == nullptr) return VQKV_ERR_INVALID_ARG;
+  return decode_launch(&ap->decode, ap, stream);
+}
+
+}  // extern "C"
+
+namespace vqkv {
+namespace {
+
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, void* stream) {
+  if (ap != nullptr && a->mode != VQKV_MODE_VQ2) return VQKV_ERR_UNSUPPORTED;
   vqkv_status st = validate_decode(a);
-  if (st != VQKV_OK || a->B == 0) return st;
+  if (st != VQKV_OK) return st;
+  if (ap != nullptr) {
+    if (a->B > 0 && (!ap->k_new || !ap->v_new || !aligned(ap->k_new, 8) || !aligned(ap->v_new, 8) ||
+                     (ap->near_tie_count && !aligned(ap->near_tie_count, 8))))
+      return VQKV_ERR_INVALID_ARG;
+  }
+  if (a->B == 0) return VQKV_OK;
   DecodePlan pl;
   const PlanInput in = plan_input(a);
   st = plan_decode(&in, &pl);
@@ -270,12 +294,24 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) {
   p.defer_merge = pl.bpg > 1 ? 1 : 0;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
   p.qscale = scale * 1.4426950408889634f / std::sqrt(128.0f);
+  if (ap != nullptr) {
+    p.k_new = reinterpret_cast<const __half*>(ap->k_new);
+    p.v_new = reinterpret_cast<const __half*>(ap->v_new);
+    p.kc_w = const_cast<uint8_t*>(a->k_codes);
+    p.vc_w = const_cast<uint8_t*>(a->v_codes);
+    p.near_tie = ap->near_tie_count;
+  }
   const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
   if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
   if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
+
+}  // namespace
+}  // namespace vqkv
+
+extern "C" {
 
 vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
   vqkv_status st = validate_encode(a);

@@ -61,6 +61,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity
   return false;
 }
 
+__device__ __forceinline__ void sts_u8(uint32_t addr, uint8_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy (bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Bulk copy global -> shared (this CTA), completion counted on `mbar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {

@@ -10,6 +10,7 @@
 // value of the exact transform.  Distances are fp32 direct differences; the
 // argmin keeps the lowest index on equal distances.
 #include "common.cuh"
+#include "encode_common.cuh"
 #include "internal.h"
 
 namespace vqkv {
@@ -18,151 +19,9 @@ namespace {
 constexpr int ENC_WARPS = 8;
 constexpr int ENC_THREADS = ENC_WARPS * 32;
 
-// ------------------------------------------------------- double-float
-struct df {
-  float h, l;
-};
-
-__device__ __forceinline__ df fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
-  const float s = __fadd_rn(a, b);
-  const float e = __fsub_rn(b, __fsub_rn(s, a));
-  return {s, e};
-}
-
-__device__ __forceinline__ df two_sum(float a, float b) {
-  const float s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-  return {s, e};
-}
-
-__device__ __forceinline__ df df_add(df a, df b) {
-  df s = two_sum(a.h, b.h);
-  const float e = __fadd_rn(s.l, __fadd_rn(a.l, b.l));
-  return fast_two_sum(s.h, e);
-}
-
-__device__ __forceinline__ df df_neg(df a) { return {-a.h, -a.l}; }
-
-__device__ __forceinline__ df df_mul(df a, float ch, float cl) {
-  const float p = __fmul_rn(a.h, ch);
-  float e = __fmaf_rn(a.h, ch, -p);
-  e = __fmaf_rn(a.h, cl, e);
-  e = __fmaf_rn(a.l, ch, e);
-  return fast_two_sum(p, e);
-}
-
-// x / s as a double-float: quotient, plus the exact remainder divided by s.
-__device__ __forceinline__ df df_div(float x, float s) {
-  const float q = __fdiv_rn(x, s);
-  const float r = __fmaf_rn(-q, s, x);
-  return fast_two_sum(q, __fdiv_rn(r, s));
-}
-
-// Unnormalised FWHT (H[i][k] = (-1)^popcount(i & k)) of a 128-vector in
-// double-float, 4 entries per lane.
-__device__ __forceinline__ void fwht128_df(df (&v)[4], int lane) {
-  {
-    const df a = df_add(v[0], v[1]), b = df_add(v[0], df_neg(v[1]));
-    const df c = df_add(v[2], v[3]), d = df_add(v[2], df_neg(v[3]));
-    v[0] = df_add(a, c);
-    v[2] = df_add(a, df_neg(c));
-    v[1] = df_add(b, d);
-    v[3] = df_add(b, df_neg(d));
-  }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      df o;
-      o.h = __shfl_xor_sync(0xffffffffu, v[i].h, m);
-      o.l = __shfl_xor_sync(0xffffffffu, v[i].l, m);
-      v[i] = upper ? df_add(o, df_neg(v[i])) : df_add(v[i], o);
-    }
-  }
-}
-
-// sqrt(2) as fp32 hi + lo; 1/sqrt(128) = sqrt(2) / 16.
-__device__ __forceinline__ float sqrt2_hi() { return __int_as_float(0x3fb504f3); }
-__device__ __forceinline__ float sqrt2_lo() { return __int_as_float(0x32cfe77a); }
-
-// Transform of one row: lane's four channels, fp32 result.
-__device__ __forceinline__ void transform_row(const EncodeParams& p, int kvh, const __half* xrow, int lane,
-                                              float (&x)[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(xrow + 4 * lane);
-  const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x);
-  const __half2 x23 = *reinterpret_cast<const __half2*>(&raw.y);
-  x[0] = __low2float(x01);
-  x[1] = __high2float(x01);
-  x[2] = __low2float(x23);
-  x[3] = __high2float(x23);
-  if (p.role == VQKV_ROLE_K) {
-    const float4 s = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
-    df v[4] = {df_div(x[0], s.x), df_div(x[1], s.y), df_div(x[2], s.z), df_div(x[3], s.w)};
-    fwht128_df(v, lane);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const df r = df_mul(v[i], sqrt2_hi(), sqrt2_lo());
-      x[i] = __fmul_rn(r.h, 0.0625f);   // exact scaling; r.h is RN(r.h + r.l)
-    }
-  }
-}
-
-__device__ __forceinline__ void count_near_ties(const EncodeParams& p, bool tie, int lane, unsigned mask) {
-  if (p.near_tie == nullptr) return;
-  const unsigned n = __popc(__ballot_sync(0xffffffffu, tie) & mask);
-  if (lane == 0 && n) atomicAdd(p.near_tie, (unsigned long long)n);
-}
-
-__device__ __forceinline__ bool is_near_tie(float best, float second) {
-  return __fsub_rn(second, best) < 1e-6f * fmaxf(best, 1e-30f);
-}
-
-// Running nearest-centroid state of one search chain: best distance, its
-// index, second-best distance.  Chains scan disjoint candidate sets in
-// increasing index order, so a strict "<" keeps the lowest index on ties.
-struct Best {
-  float d, s;
-  int i;
-};
-
-__device__ __forceinline__ Best best_init() {
-  const float inf = __int_as_float(0x7f800000);
-  return {inf, inf, 0};
-}
-
-__device__ __forceinline__ void best_push(Best& b, float d, int c) {
-  const bool lt = d < b.d;
-  b.s = lt ? b.d : fminf(b.s, d);
-  b.i = lt ? c : b.i;
-  b.d = lt ? d : b.d;
-}
-
-// Merge two chains over disjoint candidates: lower distance, then lower index.
-__device__ __forceinline__ Best best_merge(Best a, Best b) {
-  if (b.d < a.d || (b.d == a.d && b.i < a.i)) return {b.d, fminf(a.d, b.s), b.i};
-  return {a.d, fminf(a.s, b.d), a.i};
-}
-
-__device__ __forceinline__ Best best_shfl_xor(Best b, int m) {
-  return {__shfl_xor_sync(0xffffffffu, b.d, m), __shfl_xor_sync(0xffffffffu, b.s, m),
-          __shfl_xor_sync(0xffffffffu, b.i, m)};
-}
-
-// Cross-warp merge for SPLIT > 1: every warp searched a slice of the
-// candidates for the same row; warp 0 ends up with the merged state.
-template <int SPLIT>
-__device__ __forceinline__ Best merge_warps(Best b, int warp, int lane, Best* s_part) {
-  if (SPLIT == 1) return b;
-  __syncthreads();   // the previous row's readers are done with s_part
-  s_part[warp * 32 + lane] = b;
-  __syncthreads();
-  if (warp == 0) {
-#pragma unroll
-    for (int w = 1; w < SPLIT; ++w) b = best_merge(b, s_part[w * 32 + lane]);
-  }
-  return b;
+// Smoothing factors of KV head kvh for keys, nullptr for values.
+__device__ __forceinline__ const float* key_s(const EncodeParams& p, int kvh) {
+  return p.role == VQKV_ROLE_K ? p.s + (size_t)kvh * kHeadDim : nullptr;
 }
 
 // ------------------------------------------------------------------ VQ2
@@ -197,32 +56,13 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
       continue;
     }
     float x[4];
-    transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
-    // lane = subvector j (channels 4j..4j+3); two chains (even / odd candidates)
-    Best e = best_init(), o = best_init();
-#pragma unroll 4
-    for (int c = c_lo; c < c_hi; c += 2) {
-      const float4 ca = s_cb[c], cb = s_cb[c + 1];
-      float u = __fsub_rn(x[0], ca.x), d0 = __fmul_rn(u, u);
-      u = __fsub_rn(x[1], ca.y); d0 = __fmaf_rn(u, u, d0);
-      u = __fsub_rn(x[2], ca.z); d0 = __fmaf_rn(u, u, d0);
-      u = __fsub_rn(x[3], ca.w); d0 = __fmaf_rn(u, u, d0);
-      float v = __fsub_rn(x[0], cb.x), d1 = __fmul_rn(v, v);
-      v = __fsub_rn(x[1], cb.y); d1 = __fmaf_rn(v, v, d1);
-      v = __fsub_rn(x[2], cb.z); d1 = __fmaf_rn(v, v, d1);
-      v = __fsub_rn(x[3], cb.w); d1 = __fmaf_rn(v, v, d1);
-      best_push(e, d0, c);
-      best_push(o, d1, c + 1);
-    }
-    Best bst = merge_warps<SPLIT>(best_merge(e, o), warp, lane, s_part);
+    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
+    // lane = subvector j (channels 4j..4j+3)
+    const Best part = vq2_search(x, c_lo, c_hi, [&](int c) { return s_cb[c]; });
+    Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
     if (SPLIT == 1 || warp == 0) {
-      count_near_ties(p, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
-      // pack: byte offset of (t, j = lane) in the stream
-      const int tile = t >> 4, rr = t & 15, j = lane;
-      const long long off = (p.role == VQKV_ROLE_K)
-                                ? 512LL * tile + 16 * (4 * (rr & 7) + (j & 3)) + 8 * (rr >> 3) + (j >> 2)
-                                : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
-      p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + off] = (uint8_t)bst.i;
+      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+      p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + vq2_code_offset(p.role, t, lane)] = (uint8_t)bst.i;
     }
   }
 }
@@ -264,7 +104,7 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodePa
       continue;
     }
     float x[4];
-    transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
+    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
     float y[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -298,7 +138,7 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodePa
     Best bst = best_merge(mine, best_shfl_xor(mine, 1));
     bst = merge_warps<SPLIT>(bst, warp, lane, s_part);
     if (SPLIT == 1 || warp == 0) {
-      count_near_ties(p, is_near_tie(bst.d, bst.s), lane, 0x55555555u);
+      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0x55555555u);
       // lanes 2p (p < 8) hold subvector p; subvector p+8 sits on lane 2p+16
       const int hi_code = __shfl_down_sync(0xffffffffu, bst.i, 16);
       if (lane < 16 && half == 0) {
@@ -415,7 +255,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
       continue;
     }
     float x[4];
-    transform_row(p, kvh, p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, lane, x);
+    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
     float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
     nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2, j = lane / 2
     __syncwarp();
@@ -497,8 +337,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
       code[h] = cex;
       tie[h] = is_near_tie(dex, dsec);
     }
-    count_near_ties(p, tie[0], lane, 0x11111111u);
-    count_near_ties(p, tie[1], lane, 0x11111111u);
+    count_near_ties(p.near_tie, tie[0], lane, 0x11111111u);
+    count_near_ties(p.near_tie, tie[1], lane, 0x11111111u);
     // lane (gid, tig 0) holds the pair (gid, gid+8) of this token
     if (tig == 0) {
       const int pair = gid;

@@ -1,0 +1,196 @@
+// Device code of the encode step shared by the encode kernels (encode.cu)
+// and the decode kernel's fused append (decode.cu): the key transform in
+// double-float arithmetic, the nearest-centroid search state and the 2-bit
+// search loop (VecInfer paper summary page, "Summary": smoothing, Hadamard
+// rotation, nearest codebook centroid).
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace vqkv {
+namespace {
+
+// ------------------------------------------------------- double-float
+struct df {
+  float h, l;
+};
+
+__device__ __forceinline__ df fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  const float e = __fsub_rn(b, __fsub_rn(s, a));
+  return {s, e};
+}
+
+__device__ __forceinline__ df two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+__device__ __forceinline__ df df_add(df a, df b) {
+  df s = two_sum(a.h, b.h);
+  const float e = __fadd_rn(s.l, __fadd_rn(a.l, b.l));
+  return fast_two_sum(s.h, e);
+}
+
+__device__ __forceinline__ df df_neg(df a) { return {-a.h, -a.l}; }
+
+__device__ __forceinline__ df df_mul(df a, float ch, float cl) {
+  const float p = __fmul_rn(a.h, ch);
+  float e = __fmaf_rn(a.h, ch, -p);
+  e = __fmaf_rn(a.h, cl, e);
+  e = __fmaf_rn(a.l, ch, e);
+  return fast_two_sum(p, e);
+}
+
+// x / s as a double-float: quotient, plus the exact remainder divided by s.
+__device__ __forceinline__ df df_div(float x, float s) {
+  const float q = __fdiv_rn(x, s);
+  const float r = __fmaf_rn(-q, s, x);
+  return fast_two_sum(q, __fdiv_rn(r, s));
+}
+
+// Unnormalised FWHT (H[i][k] = (-1)^popcount(i & k)) of a 128-vector in
+// double-float, 4 entries per lane.
+__device__ __forceinline__ void fwht128_df(df (&v)[4], int lane) {
+  {
+    const df a = df_add(v[0], v[1]), b = df_add(v[0], df_neg(v[1]));
+    const df c = df_add(v[2], v[3]), d = df_add(v[2], df_neg(v[3]));
+    v[0] = df_add(a, c);
+    v[2] = df_add(a, df_neg(c));
+    v[1] = df_add(b, d);
+    v[3] = df_add(b, df_neg(d));
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      df o;
+      o.h = __shfl_xor_sync(0xffffffffu, v[i].h, m);
+      o.l = __shfl_xor_sync(0xffffffffu, v[i].l, m);
+      v[i] = upper ? df_add(o, df_neg(v[i])) : df_add(v[i], o);
+    }
+  }
+}
+
+// sqrt(2) as fp32 hi + lo; 1/sqrt(128) = sqrt(2) / 16.
+__device__ __forceinline__ float sqrt2_hi() { return __int_as_float(0x3fb504f3); }
+__device__ __forceinline__ float sqrt2_lo() { return __int_as_float(0x32cfe77a); }
+
+// Transform of one row: lane's four channels, fp32 result.  s_row (the KV
+// head's 128 smoothing factors) selects the key transform; nullptr leaves the
+// row as it is (values).
+__device__ __forceinline__ void transform_row(const __half* xrow, const float* s_row, int lane, float (&x)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(xrow + 4 * lane);
+  const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x);
+  const __half2 x23 = *reinterpret_cast<const __half2*>(&raw.y);
+  x[0] = __low2float(x01);
+  x[1] = __high2float(x01);
+  x[2] = __low2float(x23);
+  x[3] = __high2float(x23);
+  if (s_row != nullptr) {
+    const float4 s = *reinterpret_cast<const float4*>(s_row + 4 * lane);
+    df v[4] = {df_div(x[0], s.x), df_div(x[1], s.y), df_div(x[2], s.z), df_div(x[3], s.w)};
+    fwht128_df(v, lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const df r = df_mul(v[i], sqrt2_hi(), sqrt2_lo());
+      x[i] = __fmul_rn(r.h, 0.0625f);   // exact scaling; r.h is RN(r.h + r.l)
+    }
+  }
+}
+
+// Adds the lanes of `mask` whose `tie` is set to *counter (if not null).
+__device__ __forceinline__ void count_near_ties(unsigned long long* counter, bool tie, int lane, unsigned mask) {
+  if (counter == nullptr) return;
+  const unsigned n = __popc(__ballot_sync(0xffffffffu, tie) & mask);
+  if (lane == 0 && n) atomicAdd(counter, (unsigned long long)n);
+}
+
+__device__ __forceinline__ bool is_near_tie(float best, float second) {
+  return __fsub_rn(second, best) < 1e-6f * fmaxf(best, 1e-30f);
+}
+
+// Running nearest-centroid state of one search chain: best distance, its
+// index, second-best distance.  Chains scan disjoint candidate sets in
+// increasing index order, so a strict "<" keeps the lowest index on ties.
+struct Best {
+  float d, s;
+  int i;
+};
+
+__device__ __forceinline__ Best best_init() {
+  const float inf = __int_as_float(0x7f800000);
+  return {inf, inf, 0};
+}
+
+__device__ __forceinline__ void best_push(Best& b, float d, int c) {
+  const bool lt = d < b.d;
+  b.s = lt ? b.d : fminf(b.s, d);
+  b.i = lt ? c : b.i;
+  b.d = lt ? d : b.d;
+}
+
+// Merge two chains over disjoint candidates: lower distance, then lower index.
+__device__ __forceinline__ Best best_merge(Best a, Best b) {
+  if (b.d < a.d || (b.d == a.d && b.i < a.i)) return {b.d, fminf(a.d, b.s), b.i};
+  return {a.d, fminf(a.s, b.d), a.i};
+}
+
+__device__ __forceinline__ Best best_shfl_xor(Best b, int m) {
+  return {__shfl_xor_sync(0xffffffffu, b.d, m), __shfl_xor_sync(0xffffffffu, b.s, m),
+          __shfl_xor_sync(0xffffffffu, b.i, m)};
+}
+
+// Cross-warp merge for SPLIT > 1: every warp searched a slice of the
+// candidates for the same row; warp 0 ends up with the merged state.
+template <int SPLIT>
+__device__ __forceinline__ Best merge_warps(Best b, int warp, int lane, Best* s_part) {
+  if (SPLIT == 1) return b;
+  __syncthreads();   // the previous row's readers are done with s_part
+  s_part[warp * 32 + lane] = b;
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int w = 1; w < SPLIT; ++w) b = best_merge(b, s_part[w * 32 + lane]);
+  }
+  return b;
+}
+
+// 2-bit search of one subvector (lane's 4 channels x) over candidates
+// [c_lo, c_hi) (an even count): fp32 direct differences, two chains over
+// even / odd candidates, merged.  load(c) returns centroid c as a float4.
+template <typename Load>
+__device__ __forceinline__ Best vq2_search(const float (&x)[4], int c_lo, int c_hi, Load load) {
+  Best e = best_init(), o = best_init();
+#pragma unroll 4
+  for (int c = c_lo; c < c_hi; c += 2) {
+    const float4 ca = load(c), cb = load(c + 1);
+    float u = __fsub_rn(x[0], ca.x), d0 = __fmul_rn(u, u);
+    u = __fsub_rn(x[1], ca.y); d0 = __fmaf_rn(u, u, d0);
+    u = __fsub_rn(x[2], ca.z); d0 = __fmaf_rn(u, u, d0);
+    u = __fsub_rn(x[3], ca.w); d0 = __fmaf_rn(u, u, d0);
+    float v = __fsub_rn(x[0], cb.x), d1 = __fmul_rn(v, v);
+    v = __fsub_rn(x[1], cb.y); d1 = __fmaf_rn(v, v, d1);
+    v = __fsub_rn(x[2], cb.z); d1 = __fmaf_rn(v, v, d1);
+    v = __fsub_rn(x[3], cb.w); d1 = __fmaf_rn(v, v, d1);
+    best_push(e, d0, c);
+    best_push(o, d1, c + 1);
+  }
+  return best_merge(e, o);
+}
+
+// Byte offset of 2-bit code (token t, subvector j) in a K or V stream
+// (the layout of include/vqkv.h).
+__device__ __forceinline__ long long vq2_code_offset(int role, int t, int j) {
+  const int tile = t >> 4, rr = t & 15;
+  return (role == VQKV_ROLE_K)
+             ? 512LL * tile + 16 * (4 * (rr & 7) + (j & 3)) + 8 * (rr >> 3) + (j >> 2)
+             : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
+}
+
+}  // namespace
+}  // namespace vqkv

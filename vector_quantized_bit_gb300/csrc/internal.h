@@ -31,6 +31,12 @@ struct DecodeParams {
   int bpg;                  // sequences per CTA (grid.z = ceil(B / bpg))
   int defer_merge;          // 1: split partials are merged by the combine kernel
   float qscale;             // softmax_scale * log2(e) / sqrt(128)
+  // Fused append (vqkv_decode_append): new rows [B][Hkv][128], or nullptr.
+  const __half* k_new = nullptr;
+  const __half* v_new = nullptr;
+  uint8_t* kc_w = nullptr;  // the same caches as kc / vc, written by the append
+  uint8_t* vc_w = nullptr;
+  unsigned long long* near_tie = nullptr;
 };
 
 constexpr int kPartialStride = 130;  // O[128], m, l
