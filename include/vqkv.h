@@ -200,11 +200,11 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
  * codes are written at position L - 1 of the K and V streams of
  * decode.k_codes / decode.v_codes (which this call therefore writes, despite
  * their const type).  O is then what vqkv_decode_attn returns for the same
- * arguments over the L tokens including the new one.  The new token's codes
- * reach the attention on chip, so the result does not depend on the order
- * in which the cache bytes land.  Workspace, error word, alignment and
- * failure rules are those of vqkv_decode_attn.  2-bit mode only
- * (VQKV_ERR_UNSUPPORTED otherwise).
+ * arguments over the L tokens including the new one.  Inside the kernel the
+ * CTA that holds position L - 1 writes the new codes before it starts
+ * streaming that tile, so one kernel does the whole step.  Workspace, error
+ * word, alignment and failure rules are those of vqkv_decode_attn.  2-bit
+ * mode only (VQKV_ERR_UNSUPPORTED otherwise).
  */
 typedef struct {
   vqkv_decode_args decode;    /* as for vqkv_decode_attn (seq_lens include the new token) */

@@ -61,14 +61,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity
   return false;
 }
 
-__device__ __forceinline__ void sts_u8(uint32_t addr, uint8_t v) {
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
-}
-
-// Orders this thread's earlier generic-proxy shared-memory writes before
-// later async-proxy (bulk copy) accesses of the same bytes.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Orders this thread's earlier generic-proxy global writes before later
+// async-proxy (bulk copy) reads of the same bytes (with a barrier between
+// this thread and the issuing one).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Bulk copy global -> shared (this CTA), completion counted on `mbar`.

@@ -85,10 +85,9 @@ constexpr int V15_Q_OFF = V15_SLOT_OFF + V15_SLOT_BYTES;
 
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
 // codebook and q' region after the tile loop.
-// Fused append (vqkv_decode_append): per-warp partial searches, then the new
-// token's 32 K and 32 V codes.
+// Fused append (vqkv_decode_append): per-warp partial searches.
 constexpr int V2_APP_OFF = (V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
-constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best) + 64;
+constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
 constexpr size_t kV2Smem = V2_APP_OFF + V2_APP_BYTES;
 static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must fit below the ring");
 // The combine area (after the tile loop) and q' (before it) overlap the
@@ -188,6 +187,43 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   }
 }
 
+// Encode of the new K row (warps 0-7) and V row (warps 8-15) of one
+// (sequence, KV head) for the fused append, from the lane's 4 channels of its
+// row (raw) and smoothing factors (s, keys): each warp searches 32 of the 256
+// candidates (replica 0 of the shared codebook, one broadcast per load), the
+// slices are merged as in the encode kernel, and lane j of warps 0 / 8 writes
+// the code of subvector j to the cache at token t_new.  The writes are made
+// visible to the bulk copies (async proxy) that the CTA issues after the
+// closing barrier.  Called by every thread of the CTA after the codebook is
+// in shared memory.
+__device__ __noinline__ void append_rows(uint2 raw, float4 s, uint8_t* k_stream, uint8_t* v_stream,
+                                         unsigned long long* near_tie, int t_new, const unsigned char* s_cb,
+                                         Best* s_part) {
+  static_assert(V2_WARPS == 16, "two roles x 8 candidate slices");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int role = warp >> 3, slice = warp & 7;
+  float x[4];
+  transform_loaded(raw, role == 0, s, lane, x);
+  const unsigned char* cb_role = s_cb + role * 128;
+  const Best part = vq2_search(x, slice * 32, slice * 32 + 32, [&](int c) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(cb_role + c * 256);
+    const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
+    const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
+    return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+  });
+  s_part[warp * 32 + lane] = part;
+  __syncthreads();
+  if (slice == 0) {
+    Best bst = part;
+#pragma unroll
+    for (int w = 1; w < 8; ++w) bst = best_merge(bst, s_part[(warp + w) * 32 + lane]);
+    count_near_ties(near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+    (role ? v_stream : k_stream)[vq2_code_offset(role, t_new, lane)] = (uint8_t)bst.i;
+    fence_proxy_async_global();
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
@@ -248,9 +284,25 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         tma_load_1d(ring + st * V2_STAGE_BYTES, kbase + off, n, mbar + 8 * st);
         tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, vbase + off, n, mbar + 8 * st);
       };
-      // start the ring before the prologue so the copies overlap it
-      if (lane == 0)
+      // Fused append: the CTA whose split holds position L - 1 encodes the
+      // new rows in its prologue and writes their codes before any copy of
+      // that tile is issued, so the ring reads them like any other code.
+      const int t_new = L - 1;
+      const bool append = p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
+      const int k_new = append ? ((t_new >> 4) - t_begin) / V2_TPI : 0;   // super-tile of the new token
+      const bool late_start = append && k_new % V2_WARPS == warp && k_new / V2_WARPS < V2_STAGES - 1;
+      // start the ring before the prologue so the copies overlap it (after
+      // the append for the one warp whose first copies hold the new token)
+      if (lane == 0 && !late_start)
         for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
+      // the new rows' loads overlap the codebook fill
+      uint2 xraw = make_uint2(0u, 0u);
+      float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (append) {
+        const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
+        xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
+        if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+      }
       {
         // thread t loads centroid t & 255 of K (t < 256) or V (t >= 256) once and
         // writes its 16 replicas; replica (i + lane) % 16 at step i keeps the 16
@@ -263,42 +315,13 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
       }
       transform_queries(p, b, kvh, warp, lane, s_qp);
-      // Fused append: the CTA whose split holds position L - 1 encodes the
-      // new K row (warps 0-7) and V row (warps 8-15), 32 candidates per warp.
-      const int t_new = L - 1;
-      const bool append = p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
-      Best* s_part = reinterpret_cast<Best*>(smem + V2_APP_OFF);
-      uint8_t* s_new = smem + V2_APP_OFF + V2_WARPS * 32 * sizeof(Best);
-      float xa[4];
-      if (append) {
-        static_assert(V2_WARPS == 16, "two roles x 8 candidate slices");
-        const int role = warp >> 3;
-        transform_row((role ? p.v_new : p.k_new) + ((size_t)b * p.Hkv + kvh) * kHeadDim,
-                      role ? nullptr : p.s + (size_t)kvh * kHeadDim, lane, xa);
-      }
       __syncthreads();
       if (append) {
-        const int role = warp >> 3, slice = warp & 7;
-        // every lane reads replica 0 of candidate c (one broadcast per load)
-        const unsigned char* cb_role = smem + role * 128;
-        const Best part = vq2_search(xa, slice * 32, slice * 32 + 32, [&](int c) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(cb_role + c * 256);
-          const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
-          const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
-          return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
-        });
-        s_part[warp * 32 + lane] = part;
-        __syncthreads();
-        if (slice == 0) {
-          Best bst = part;
-#pragma unroll
-          for (int w = 1; w < 8; ++w) bst = best_merge(bst, s_part[(warp + w) * 32 + lane]);
-          count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
-          uint8_t* cw = (role ? p.vc_w : p.kc_w) + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-          cw[vq2_code_offset(role, t_new, lane)] = (uint8_t)bst.i;
-          s_new[role * 32 + lane] = (uint8_t)bst.i;
-        }
-        __syncthreads();
+        const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
+        append_rows(xraw, xs, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
+                    reinterpret_cast<Best*>(smem + V2_APP_OFF));
+        if (lane == 0 && late_start)
+          for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
       }
       // A operand of the score MMA: head gid, channels 4j..4j+3 of j = 4s+tig
       uint32_t qa[8][2];
@@ -320,20 +343,6 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         if (!mbar_wait_bounded(mbar + 8 * st, par, kMaxPolls)) {
           timed_out = true;
           break;
-        }
-        if (append) {
-          // the new token's codes come from the encode above, not from the
-          // copy (whose global bytes this call is writing concurrently)
-          const int i = (t_new >> 4) - (t_begin + (warp + j * V2_WARPS) * V2_TPI);
-          if (i >= 0 && i < V2_TPI) {
-            const uint32_t sb = ring + st * V2_STAGE_BYTES;
-            const int r = t_new & 15;
-            sts_u8(sb + i * V2_TILE_BYTES + (uint32_t)vq2_code_offset(VQKV_ROLE_K, r, lane), s_new[lane]);
-            sts_u8(sb + (V2_TPI + i) * V2_TILE_BYTES + (uint32_t)vq2_code_offset(VQKV_ROLE_V, r, lane),
-                   s_new[32 + lane]);
-            fence_proxy_async_smem();   // before the ring's next bulk copy into this stage
-            __syncwarp();
-          }
         }
         uint4 kq[V2_TPI], vq[V2_TPI];
 #pragma unroll

@@ -80,19 +80,16 @@ __device__ __forceinline__ void fwht128_df(df (&v)[4], int lane) {
 __device__ __forceinline__ float sqrt2_hi() { return __int_as_float(0x3fb504f3); }
 __device__ __forceinline__ float sqrt2_lo() { return __int_as_float(0x32cfe77a); }
 
-// Transform of one row: lane's four channels, fp32 result.  s_row (the KV
-// head's 128 smoothing factors) selects the key transform; nullptr leaves the
-// row as it is (values).
-__device__ __forceinline__ void transform_row(const __half* xrow, const float* s_row, int lane, float (&x)[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(xrow + 4 * lane);
+// Transform of one row from the lane's four fp16 channels (raw) and, for a
+// key, their smoothing factors s: fp32 result.  Values stay as they are.
+__device__ __forceinline__ void transform_loaded(uint2 raw, bool key, float4 s, int lane, float (&x)[4]) {
   const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x);
   const __half2 x23 = *reinterpret_cast<const __half2*>(&raw.y);
   x[0] = __low2float(x01);
   x[1] = __high2float(x01);
   x[2] = __low2float(x23);
   x[3] = __high2float(x23);
-  if (s_row != nullptr) {
-    const float4 s = *reinterpret_cast<const float4*>(s_row + 4 * lane);
+  if (key) {
     df v[4] = {df_div(x[0], s.x), df_div(x[1], s.y), df_div(x[2], s.z), df_div(x[3], s.w)};
     fwht128_df(v, lane);
 #pragma unroll
@@ -101,6 +98,13 @@ __device__ __forceinline__ void transform_row(const __half* xrow, const float* s
       x[i] = __fmul_rn(r.h, 0.0625f);   // exact scaling; r.h is RN(r.h + r.l)
     }
   }
+}
+
+// The same, reading the lane's 4 fp16 channels and smoothing factors.
+__device__ __forceinline__ void transform_row(const __half* xrow, const float* s_row, int lane, float (&x)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(xrow + 4 * lane);
+  const float4 s = s_row != nullptr ? *reinterpret_cast<const float4*>(s_row + 4 * lane) : make_float4(1.f, 1.f, 1.f, 1.f);
+  transform_loaded(raw, s_row != nullptr, s, lane, x);
 }
 
 // Adds the lanes of `mask` whose `tie` is set to *counter (if not null).
