@@ -3,7 +3,9 @@
 // a Hadamard rotation of the keys, K-Means codebook; arXiv summary page,
 // "方法详解", stages 1-2).
 //
-// One warp per row; lane l holds channels 4l..4l+3.  For keys the transform
+// 2-bit: one warp per row (or one CTA per row when rows are few); lane l
+// holds channels 4l..4l+3.  1.5-bit: tensor-core screening with an exact
+// re-rank (below).  For keys the transform
 // x' = (x / s) . H / sqrt(128) is carried in double-float arithmetic (pairs
 // of fp32 with error-free sums and products) and rounded to fp32 once, so the
 // vector handed to the nearest-centroid search is the correctly rounded fp32
@@ -67,96 +69,6 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
   }
 }
 
-// ------------------------------------------------------------------ VQ15
-// Codebook as fp32 in shared memory (128 KB).  The two lanes of a subvector
-// (channels 8J..8J+7 live on lanes 2J, 2J+1) both hold all 8 channels and
-// search half of the candidates each (of the CTA's slice when SPLIT > 1).
-template <int SPLIT>
-__global__ void __launch_bounds__(ENC_THREADS) encode_vq15_kernel(const EncodeParams p) {
-  extern __shared__ __align__(16) float4 s_cb15[];   // [4096][2]
-  __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
-  const int kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  grid_dependency_wait();
-  grid_dependents_launch();
-  for (int c = threadIdx.x; c < 4096; c += ENC_THREADS) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
-    const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
-    const __half2 cc = *reinterpret_cast<const __half2*>(&raw.z);
-    const __half2 d = *reinterpret_cast<const __half2*>(&raw.w);
-    s_cb15[2 * c] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
-    s_cb15[2 * c + 1] = make_float4(__low2float(cc), __high2float(cc), __low2float(d), __high2float(d));
-  }
-  __syncthreads();
-  const int rows = p.B * p.n_rows;
-  const int half = lane & 1;
-  const int r0 = (SPLIT == 1) ? blockIdx.x * ENC_WARPS + warp : blockIdx.x;
-  const int rstep = (SPLIT == 1) ? gridDim.x * ENC_WARPS : gridDim.x;
-  constexpr int kSlice = 4096 / SPLIT;   // candidates of this warp
-  const int c_lo = ((SPLIT == 1) ? 0 : warp * kSlice) + half * (kSlice / 2);
-  const int c_hi = c_lo + kSlice / 2;
-  for (int r = r0; r < rows; r += rstep) {
-    const int b = r / p.n_rows, n = r - b * p.n_rows;
-    const int t = p.pos[b] + n;
-    if (t < 0 || t >= p.cap_len) {
-      if (lane == 0 && (SPLIT == 1 || warp == 0) && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
-      continue;
-    }
-    float x[4];
-    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
-    float y[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
-      y[i] = half ? o : x[i];
-      y[4 + i] = half ? x[i] : o;
-    }
-    Best e = best_init(), od = best_init();
-#pragma unroll 2
-    for (int c = c_lo; c < c_hi; c += 2) {
-      float dd[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float4 lo = s_cb15[2 * (c + k)], hi = s_cb15[2 * (c + k) + 1];
-        float u = __fsub_rn(y[0], lo.x);
-        float d = __fmul_rn(u, u);
-        u = __fsub_rn(y[1], lo.y); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[2], lo.z); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[3], lo.w); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[4], hi.x); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[5], hi.y); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[6], hi.z); d = __fmaf_rn(u, u, d);
-        u = __fsub_rn(y[7], hi.w); d = __fmaf_rn(u, u, d);
-        dd[k] = d;
-      }
-      best_push(e, dd[0], c);
-      best_push(od, dd[1], c + 1);
-    }
-    // the two halves of the pair hold disjoint candidate sets: merge them
-    Best mine = best_merge(e, od);
-    Best bst = best_merge(mine, best_shfl_xor(mine, 1));
-    bst = merge_warps<SPLIT>(bst, warp, lane, s_part);
-    if (SPLIT == 1 || warp == 0) {
-      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0x55555555u);
-      // lanes 2p (p < 8) hold subvector p; subvector p+8 sits on lane 2p+16
-      const int hi_code = __shfl_down_sync(0xffffffffu, bst.i, 16);
-      if (lane < 16 && half == 0) {
-        const int pair = lane >> 1;
-        const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
-        const long long off = (p.role == VQKV_ROLE_K)
-                                  ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
-                                  : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
-        uint8_t* dst = p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + off;
-        dst[0] = (uint8_t)(bst.i & 0xff);
-        dst[1] = (uint8_t)(((bst.i >> 8) & 0xf) | ((hi_code & 0xf) << 4));
-        dst[2] = (uint8_t)(hi_code >> 4);
-      }
-    }
-  }
-}
-
-constexpr size_t kV15EncSmem = 4096 * 2 * sizeof(float4);
 
 // ------------------------------------------------------------------ VQ15, tensor-core screening
 // Many rows of 1.5-bit encode: the distance search against 4096 centroids is
@@ -168,8 +80,9 @@ constexpr size_t kV15EncSmem = 4096 * 2 * sizeof(float4);
 // centroid columns.  A centroid whose screened distance is within 2*eps of
 // the best can be the exact nearest, where eps bounds the screening error
 // (fp16 rounding of x' and |c|^2, fp32 accumulation); those candidates are
-// re-ranked with the exact fp32 direct differences of the CUDA-core search,
-// so every decision equals that search's.  If a lane's second-best is also
+// re-ranked with exact fp32 direct differences (channel order 0..7, one
+// rounding per operation), so every decision equals the exhaustive fp32
+// search's.  If a lane's second-best is also
 // within the margin (a third candidate may hide behind it) the subvector is
 // searched exhaustively.
 constexpr int TC_WARPS = 16;
@@ -184,8 +97,8 @@ __device__ __forceinline__ void top2_push(float v, int n, float& b1, float& b2, 
   i1 = lt ? n : i1;
 }
 
-// Exact fp32 distance of subvector x (8 channels) to centroid c, same
-// operation order as the CUDA-core search.
+// Exact fp32 distance of subvector x (8 channels) to centroid c: direct
+// differences in channel order, one rounding per operation.
 __device__ __forceinline__ float exact_d8(const float* x, const uint2* tbl, int c) {
   float y[8];
 #pragma unroll
@@ -204,23 +117,21 @@ __device__ __forceinline__ float exact_d8(const float* x, const uint2* tbl, int 
   return d;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const EncodeParams p) {
-  extern __shared__ __align__(16) unsigned char tsm[];
-  uint2* s_tbl = reinterpret_cast<uint2*>(tsm);
-  float* s_x = reinterpret_cast<float*>(tsm + TC_TABLE_BYTES);           // [warp][128] x'
-  float* s_xn = s_x + TC_WARPS * 128;                                      // [warp][16] |x'_j|^2
-  float* s_cmax = s_xn + TC_WARPS * 16;
-  const int kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  grid_dependency_wait();
-  grid_dependents_launch();
-
-  // B table and the largest centroid norm of this KV head
+// B table [centroid][tig]{-2c pair, (|c|^2, 1) or 0} of KV head kvh in
+// shared memory, and the largest centroid norm (returned; s_cmax is one
+// float of scratch).  Called by every thread of the CTA.
+__device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, uint2* s_tbl, float* s_cmax) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = 4096 / TC_THREADS;
+  uint4 raws[kPer];   // every load in flight before the first use
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    raws[k] = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + threadIdx.x + k * TC_THREADS);
   float cmax = 0.f;
-  for (int c = threadIdx.x; c < 4096; c += TC_THREADS) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int c = threadIdx.x + k * TC_THREADS;
+    const uint32_t w[4] = {raws[k].x, raws[k].y, raws[k].z, raws[k].w};
     float nn = 0.f;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -241,7 +152,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
   __syncthreads();
   if (lane == 0) atomicMax(reinterpret_cast<int*>(s_cmax), __float_as_int(cmax));   // non-negative floats
   __syncthreads();
-  const float Cmax = *s_cmax;
+  return *s_cmax;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const EncodeParams p) {
+  extern __shared__ __align__(16) unsigned char tsm[];
+  uint2* s_tbl = reinterpret_cast<uint2*>(tsm);
+  float* s_x = reinterpret_cast<float*>(tsm + TC_TABLE_BYTES);           // [warp][128] x'
+  float* s_xn = s_x + TC_WARPS * 128;                                      // [warp][16] |x'_j|^2
+  float* s_cmax = s_xn + TC_WARPS * 16;
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  grid_dependency_wait();
+  grid_dependents_launch();
+
+  const float Cmax = build_tc_table(p, kvh, s_tbl, s_cmax);
   float* wx = s_x + warp * 128;
   float* wxn = s_xn + warp * 16;
   const uint32_t tbl_lane = smem_u32(s_tbl) + (gid * 4 + tig) * 8;   // + 32 per centroid
@@ -340,17 +266,149 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
     count_near_ties(p.near_tie, tie[0], lane, 0x11111111u);
     count_near_ties(p.near_tie, tie[1], lane, 0x11111111u);
     // lane (gid, tig 0) holds the pair (gid, gid+8) of this token
-    if (tig == 0) {
-      const int pair = gid;
-      const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
-      const long long off = (p.role == VQKV_ROLE_K)
-                                ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
-                                : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
-      uint8_t* dst = p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + off;
-      dst[0] = (uint8_t)(code[0] & 0xff);
-      dst[1] = (uint8_t)(((code[0] >> 8) & 0xf) | ((code[1] & 0xf) << 4));
-      dst[2] = (uint8_t)(code[1] >> 4);
+    if (tig == 0)
+      store_pair(p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + vq15_pair_offset(p.role, t, gid), code[0],
+                 code[1]);
+  }
+}
+
+
+// Few rows of 1.5-bit encode (a decode step's append): one row per CTA, its
+// 4096 candidates split over the 16 warps (256 each, 32 screening MMAs per
+// warp).  The margin test uses the best screened distance over all warps; a
+// subvector any of whose 64 lane slices may hide a third candidate within
+// the margin is searched exhaustively by the whole CTA.  Decisions equal the
+// exhaustive fp32 search's, as in the kernel above.
+constexpr size_t kTcSplitSmem = TC_TABLE_BYTES + (128 + 16 + 4 + TC_WARPS * 16 + 16) * 4 +
+                                (TC_WARPS * 16 + TC_WARPS) * sizeof(Best);
+
+__global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(const EncodeParams p) {
+  extern __shared__ __align__(16) unsigned char tsm[];
+  uint2* s_tbl = reinterpret_cast<uint2*>(tsm);
+  float* s_x = reinterpret_cast<float*>(tsm + TC_TABLE_BYTES);   // [128] x'
+  float* s_xn = s_x + 128;                                        // [16] |x'_j|^2
+  float* s_cmax = s_xn + 16;
+  float* s_red = s_cmax + 4;                                      // [warp][16] screened minima
+  int* s_hidden = reinterpret_cast<int*>(s_red + TC_WARPS * 16);  // [16]
+  Best* s_fin = reinterpret_cast<Best*>(s_hidden + 16);           // [warp][16]
+  Best* s_ex = s_fin + TC_WARPS * 16;                             // [warp] exhaustive partials
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int rows = p.B * p.n_rows;
+  // warp 0 starts the loads of its first row before the table build
+  auto row_ptr = [&](int r) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    return p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim + 4 * lane;
+  };
+  const float* ks = key_s(p, kvh);
+  uint2 xraw = make_uint2(0u, 0u);
+  float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (warp == 0 && (int)blockIdx.x < rows) {
+    xraw = *reinterpret_cast<const uint2*>(row_ptr(blockIdx.x));
+    if (ks != nullptr) xs = *reinterpret_cast<const float4*>(ks + 4 * lane);
+  }
+  const float Cmax = build_tc_table(p, kvh, s_tbl, s_cmax);
+  const uint32_t tbl_lane = smem_u32(s_tbl) + (gid * 4 + tig) * 8;
+  const float inf = __int_as_float(0x7f800000);
+
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    const int t = p.pos[b] + n;
+    if (t < 0 || t >= p.cap_len) {
+      if (threadIdx.x == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      continue;
     }
+    if (warp == 0) {
+      float x[4];
+      if (r != (int)blockIdx.x) xraw = *reinterpret_cast<const uint2*>(row_ptr(r));
+      transform_loaded(xraw, ks != nullptr, xs, lane, x);
+      float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+      nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2, j = lane / 2
+      *reinterpret_cast<float4*>(s_x + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+      if ((lane & 1) == 0) s_xn[lane >> 1] = nx;
+      if (lane < 16) s_hidden[lane] = 0;
+    }
+    __syncthreads();
+    const float2 xa = *reinterpret_cast<const float2*>(s_x + 8 * gid + 2 * tig);
+    const float2 xb = *reinterpret_cast<const float2*>(s_x + 8 * (gid + 8) + 2 * tig);
+    const uint32_t a0 = pack_half2(xa.x, xa.y), a1 = pack_half2(xb.x, xb.y);
+    const uint32_t a2 = tig == 0 ? pack_half2(1.f, s_xn[gid]) : 0u;
+    const uint32_t a3 = tig == 0 ? pack_half2(1.f, s_xn[gid + 8]) : 0u;
+    float b1[2] = {inf, inf}, b2[2] = {inf, inf};
+    int i1[2] = {0, 0};
+    const int c_lo = warp * (4096 / TC_WARPS);
+#pragma unroll 4
+    for (int n0 = c_lo; n0 < c_lo + 4096 / TC_WARPS; n0 += 8) {
+      const uint2 bf = lds64(tbl_lane + n0 * 32);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816(d, a0, a1, a2, a3, bf.x, bf.y);
+      const int c0 = n0 + 2 * tig;
+      top2_push(d[0], c0, b1[0], b2[0], i1[0]);
+      top2_push(d[1], c0 + 1, b1[0], b2[0], i1[0]);
+      top2_push(d[2], c0, b1[1], b2[1], i1[1]);
+      top2_push(d[3], c0 + 1, b1[1], b2[1], i1[1]);
+    }
+    // best screened distance of each subvector over the whole CTA
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float m = b1[h];
+      m = fminf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fminf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      if (tig == 0) s_red[warp * 16 + gid + 8 * h] = m;
+    }
+    __syncthreads();
+    Best cand[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = gid + 8 * h;
+      float best = inf;
+#pragma unroll 4
+      for (int w = 0; w < TC_WARPS; ++w) best = fminf(best, s_red[w * 16 + j]);
+      const float xnorm = sqrtf(s_xn[j]);
+      const float sc = xnorm + Cmax;
+      const float eps = 9.765625e-4f * xnorm * Cmax + 4.8828125e-4f * Cmax * Cmax + 1.5e-5f * sc * sc;
+      const float thr = best + 2.f * eps;
+      if (b2[h] <= thr) atomicOr(&s_hidden[j], 1);   // a third candidate may hide in this slice
+      cand[h] = {inf, inf, 0x7fffffff};
+      if (b1[h] <= thr) cand[h] = {exact_d8(s_x + 8 * j, s_tbl, i1[h]), inf, i1[h]};
+      // merge the group's 4 lanes: lower distance, then lower index
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) cand[h] = best_merge(cand[h], best_shfl_xor(cand[h], o));
+      if (tig == 0) s_fin[warp * 16 + j] = cand[h];
+    }
+    __syncthreads();
+    // subvectors with a possibly hidden candidate: exhaustive exact search,
+    // candidate c = threadIdx.x + k * 512 (increasing per thread)
+    for (int j = 0; j < 16; ++j) {
+      if (!s_hidden[j]) continue;   // uniform: read after the barrier
+      Best e = best_init();
+      for (int c = threadIdx.x; c < 4096; c += TC_THREADS) best_push(e, exact_d8(s_x + 8 * j, s_tbl, c), c);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) e = best_merge(e, best_shfl_xor(e, o));
+      if (lane == 0) s_ex[warp] = e;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        Best m = s_ex[0];
+        for (int w = 1; w < TC_WARPS; ++w) m = best_merge(m, s_ex[w]);
+        s_fin[j] = m;   // warp 0's slot; the other warps' slots are dropped below
+      }
+      __syncthreads();
+    }
+    if (warp == 0) {
+      const int j = lane & 15;
+      Best m = s_fin[j];
+      if (!s_hidden[j])
+        for (int w = 1; w < TC_WARPS; ++w) m = best_merge(m, s_fin[w * 16 + j]);
+      count_near_ties(p.near_tie, is_near_tie(m.d, m.s), lane, 0x0000ffffu);
+      const int hi = __shfl_down_sync(0xffffffffu, m.i, 8);
+      if (lane < 8)
+        store_pair(p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + vq15_pair_offset(p.role, t, lane), m.i,
+                   hi);
+    }
+    __syncthreads();   // s_x, s_hidden and s_fin are reused by the next row
   }
 }
 
@@ -364,19 +422,17 @@ cudaError_t encode_prepare(int mode) {
     const cudaError_t e0 = cudaFuncSetAttribute(encode_vq15_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 (int)kTcSmem);
     if (e0 != cudaSuccess) return e0;
+    const cudaError_t e1 = cudaFuncSetAttribute(encode_vq15_tc_split_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSplitSmem);
+    if (e1 != cudaSuccess) return e1;
   }
-  cudaError_t e = cudaFuncSetAttribute(encode_vq15_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kV15EncSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(encode_vq15_kernel<ENC_WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kV15EncSmem);
+  return cudaSuccess;
 }
 
 cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1>, ENC_THREADS, 0);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_kernel<1>, ENC_THREADS,
-                                                       kV15EncSmem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_tc_kernel, TC_THREADS, kTcSmem);
 }
 
 // split_rows: one row per CTA, candidates split over the CTA's warps.
@@ -386,7 +442,7 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
     if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), 0, stream, p);
     return launch_pdl(encode_vq2_kernel<1>, grid, dim3(ENC_THREADS), 0, stream, p);
   }
-  if (split_rows) return launch_pdl(encode_vq15_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), kV15EncSmem, stream, p);
+  if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
   return launch_pdl(encode_vq15_tc_kernel, grid, dim3(TC_THREADS), kTcSmem, stream, p);
 }
 

@@ -196,5 +196,21 @@ __device__ __forceinline__ long long vq2_code_offset(int role, int t, int j) {
              : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
 }
 
+// Byte offset of the first byte of 1.5-bit pair `pair` (subvectors pair and
+// pair + 8) of token t in a K or V stream (the layout of include/vqkv.h).
+__device__ __forceinline__ long long vq15_pair_offset(int role, int t, int pair) {
+  const int tile = t >> 6, u = (t & 63) >> 4, rr = t & 15;
+  return (role == VQKV_ROLE_K)
+             ? 1536LL * tile + 48 * (4 * (rr & 7) + (pair & 3)) + 12 * u + 6 * (rr >> 3) + 3 * (pair >> 2)
+             : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
+}
+
+// Writes codes lo (subvector pair) and hi (pair + 8) as 3 bytes.
+__device__ __forceinline__ void store_pair(uint8_t* dst, int lo, int hi) {
+  dst[0] = (uint8_t)(lo & 0xff);
+  dst[1] = (uint8_t)(((lo >> 8) & 0xf) | ((hi & 0xf) << 4));
+  dst[2] = (uint8_t)(hi >> 4);
+}
+
 }  // namespace
 }  // namespace vqkv
