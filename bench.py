@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--unfused", action="store_true",
                     help="2-bit: run a step as vqkv_encode (K) + vqkv_encode (V) + vqkv_decode_attn instead of "
                          "the fused vqkv_decode_append")
+    ap.add_argument("--profile-fp16", type=int, default=0,
+                    help="run this many fp16-KV comparison decodes of the workload (eager) and exit: the "
+                         "command the fp16 kernel's ncu summary is taken with")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
@@ -384,6 +387,9 @@ def run_ours(args):
         if ev is not None:
             ev[1].record()
 
+    if args.profile_fp16:
+        fp16_profile_run(w, lens, dev, args.profile_fp16)
+        return
     if args.profile_steps:
         for i in range(args.profile_steps):
             step(i)
@@ -620,6 +626,25 @@ def encode_prefill_bench(w, dev, reps=3):
             del x
         res["2-bit" if mode == 0 else "1.5-bit"] = out
     return res
+
+
+def fp16_profile_run(w, lens, dev, n):
+    """n eager vqkv_decode_attn_fp16 calls over seeded Gaussian fp16 K/V."""
+    import torch
+    from vector_quantized_bit_gb300 import _lib
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + w.config_id + 17)
+    k = torch.randn((w.B, w.Hkv, w.cap_len, 128), generator=gen, device=dev, dtype=torch.float16)
+    v = torch.randn((w.B, w.Hkv, w.cap_len, 128), generator=gen, device=dev, dtype=torch.float16)
+    q = torch.from_numpy(synth.queries(w)).to(dev)
+    seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
+    max_len = int(lens.max())
+    ws = _lib.fp16_decode_workspace(w.B, w.Hq, w.Hkv, w.cap_len, max_len, device=dev)
+    for _ in range(n):
+        _lib.vqkv_decode_attn_fp16(q, k, v, seq, out, ws, max_len)
+    torch.cuda.synchronize()
+    print(f"fp16 profile run: {n} decodes of {w.name}", flush=True)
 
 
 def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
