@@ -320,6 +320,25 @@ def decode_attention(q, k_codes, v_codes, k_cb, v_cb, s, seq_lens, scale=None,
     return out
 
 
+def decode_attention_multi(q, k_codes, v_codes, k_cb, v_cb, s, seq_lens, scale=None) -> np.ndarray:
+    """Several queries per sequence over the same cache (chunked prefill or
+    speculative decoding on a VQ cache: attention over the dequantised cache
+    [P1 Summary], with M new tokens at the end of each sequence).
+
+    Reading: the M queries of sequence b are the tokens at positions
+    L_b - M .. L_b - 1 and attend causally, so query m sees the cached
+    tokens t <= L_b - M + m (none when that is negative: a zero row).
+    q fp16 [B][M][Hq][128]; returns fp64 [B][M][Hq][128].  Each query is a
+    single-query decode over its visible prefix.
+    """
+    B, M = q.shape[0], q.shape[1]
+    out = np.empty(q.shape, dtype=np.float64)
+    for m in range(M):
+        lens_m = [max(0, int(L) - M + m + 1) for L in seq_lens]
+        out[:, m] = decode_attention(q[:, m], k_codes, v_codes, k_cb, v_cb, s, lens_m, scale)
+    return out
+
+
 def decode_attention_rotated(q, k_codes, v_codes, k_cb, v_cb, s, seq_lens, scale=None,
                              heads=None) -> np.ndarray:
     """Same result computed in the rotated domain: scale * q' . K'^T with

@@ -442,3 +442,65 @@ def test_planted_pair_order(monkeypatch):
 
 def test_oracle_is_importable_as_package():
     assert oracle.code_bytes(0, 16) == 512
+
+
+# ---------------------------------------------------------------- multi-query decode
+
+def check_multi_query_vs_sdpa_causal():
+    """M queries per sequence against torch SDPA over the dequantised cache
+    with an explicit boolean mask: query m sees tokens t <= L - M + m."""
+    q1, kc, vc, kcb, vcb, s, lens = _setup()
+    L, M = int(lens[0]), 3
+    q = np.random.default_rng(11).standard_normal((1, M, q1.shape[1], 128)).astype(np.float16)
+    o = vo.decode_attention_multi(q, kc, vc, kcb, vcb, s, lens)
+    mask = np.zeros((M, L), dtype=bool)
+    for m in range(M):
+        mask[m, :L - M + m + 1] = True
+    for h in range(q.shape[2]):
+        kvh = h // (q.shape[2] // kcb.shape[0])
+        k = vo.untransform_keys(vo.dequantize(kc[0, kvh], kcb[kvh]), s[kvh])
+        v = vo.dequantize(vc[0, kvh], vcb[kvh])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[0, :, h].astype(np.float64))[None, None], torch.from_numpy(k)[None, None],
+            torch.from_numpy(v)[None, None], attn_mask=torch.from_numpy(mask)[None, None])[0, 0].numpy()
+        assert np.abs(o[0, :, h] - ref).max() < 1e-12
+
+
+def check_multi_query_closed_forms():
+    """L = M: query 0 sees only token 0 (O = its value row); with q = 0 every
+    query averages the value rows it sees."""
+    r = np.random.default_rng(12)
+    Hkv, M = 1, 4
+    kcb = r.standard_normal((Hkv, 256, 4)).astype(np.float16)
+    vcb = r.standard_normal((Hkv, 256, 4)).astype(np.float16)
+    s = r.uniform(0.5, 2.0, size=(Hkv, 128)).astype(np.float32)
+    kc = r.integers(0, 256, size=(1, Hkv, M, 32))
+    vc = r.integers(0, 256, size=(1, Hkv, M, 32))
+    q = r.standard_normal((1, M, 2, 128)).astype(np.float16)
+    o = vo.decode_attention_multi(q, kc, vc, kcb, vcb, s, [M])
+    v_rows = vcb[0][vc[0, 0]].reshape(M, 128).astype(np.float64)
+    assert np.array_equal(o[0, 0, 0], v_rows[0]) and np.array_equal(o[0, 0, 1], v_rows[0])
+    o0 = vo.decode_attention_multi(np.zeros_like(q), kc, vc, kcb, vcb, s, [M])
+    for m in range(M):
+        assert np.allclose(o0[0, m, 0], v_rows[:m + 1].mean(axis=0), rtol=0, atol=1e-12)
+    # a sequence shorter than its query count: the early queries see nothing
+    o1 = vo.decode_attention_multi(q[:, :, :1], kc, vc, kcb, vcb, s, [2])
+    assert np.all(o1[0, :2] == 0) and np.array_equal(o1[0, 2, 0], v_rows[0])
+
+
+def test_multi_query_vs_sdpa_causal():
+    check_multi_query_vs_sdpa_causal()
+
+
+def test_multi_query_closed_forms():
+    check_multi_query_closed_forms()
+
+
+def test_planted_multi_query_off_by_one(monkeypatch):
+    real = vo.decode_attention
+
+    def shifted(q, kc, vc, kcb, vcb, s, lens, scale=None, heads=None):
+        # each query also sees the token after its own position
+        return real(q, kc, vc, kcb, vcb, s, [L + 1 if L < kc[0][0].shape[0] else L for L in lens], scale)
+    monkeypatch.setattr(vo, "decode_attention", shifted)
+    assert _fails(check_multi_query_vs_sdpa_causal) and _fails(check_multi_query_closed_forms)
