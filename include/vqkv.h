@@ -216,6 +216,28 @@ typedef struct {
 vqkv_status vqkv_decode_append(const vqkv_decode_append_args* args, void* stream);
 
 /*
+ * vqkv_decode_attn_multi — several queries per sequence over the packed
+ * cache: the M = n_queries newest tokens of each sequence attend at once
+ * (chunked prefill or speculative decoding on a VQ cache; attention over
+ * the dequantised cache, paper summary page, "Summary").
+ *
+ * decode.q and decode.out are fp16 [B][M][Hq][128].  Query m of sequence b
+ * is the token at position L - M + m (L = seq_lens[b], clamped as in
+ * vqkv_decode_attn) and attends causally: it sees the cached tokens
+ * t <= L - M + m, and is a zero row when it sees none.  Each code is read
+ * once for all M x (Hq / Hkv) queries of its KV head.  M * (Hq / Hkv) <= 8
+ * (VQKV_ERR_UNSUPPORTED otherwise).  The workspace must hold
+ * n_queries * vqkv_decode_workspace_bytes(&args->decode) bytes; everything
+ * else is as in vqkv_decode_attn, which is this call with n_queries = 1.
+ */
+typedef struct {
+  vqkv_decode_args decode;  /* q, out: [B][n_queries][Hq][128] */
+  int32_t n_queries;        /* M >= 1 */
+} vqkv_decode_multi_args;
+
+vqkv_status vqkv_decode_attn_multi(const vqkv_decode_multi_args* args, void* stream);
+
+/*
  * vqkv_decode_attn_fp16 — the same decode attention over a plain fp16 KV
  * cache, the comparison point for the quantised path on the same shapes
  * (the paper measures its speed-up against FP16 attention, summary page,

@@ -38,7 +38,8 @@ def test_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header(tmp_path):
     """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
     fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs,
-              "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs, "vqkv_decode_append_args": _lib.DecodeAppendArgs}
+              "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs, "vqkv_decode_append_args": _lib.DecodeAppendArgs,
+              "vqkv_decode_multi_args": _lib.DecodeMultiArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -154,3 +155,16 @@ def test_decode_append_validation(lib):
     assert lib.vqkv_decode_append(None, None) == 1
     a.decode = _dec(B=0, q=None, out=None)
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 0    # empty batch: a no-op
+
+
+def test_decode_multi_validation(lib):
+    a = _lib.DecodeMultiArgs()
+    a.decode = _dec(Hq=4, Hkv=1)
+    a.n_queries = 0
+    assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 1    # at least one query
+    a.n_queries = 3
+    assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 2    # 3 queries x 4 heads > 8 columns
+    assert lib.vqkv_decode_attn_multi(None, None) == 1
+    a.decode = _dec(B=0, q=None, out=None)
+    a.n_queries = 2
+    assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 0    # empty batch: a no-op

@@ -24,7 +24,8 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
-            "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_append", "vqkv_decode_attn_static",
+            "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_multi", "vqkv_decode_append",
+            "vqkv_decode_attn_static",
             "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -62,6 +63,10 @@ class Fp16DecodeArgs(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
 
 
+class DecodeMultiArgs(ctypes.Structure):
+    _fields_ = [("decode", DecodeArgs), ("n_queries", ctypes.c_int32)]
+
+
 class DecodeAppendArgs(ctypes.Structure):
     _fields_ = [("decode", DecodeArgs), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
                 ("near_tie_count", ctypes.c_void_p)]
@@ -96,6 +101,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_decode_attn_multi.restype = ctypes.c_int
+        L.vqkv_decode_attn_multi.argtypes = [ctypes.POINTER(DecodeMultiArgs), ctypes.c_void_p]
         L.vqkv_decode_append.restype = ctypes.c_int
         L.vqkv_decode_append.argtypes = [ctypes.POINTER(DecodeAppendArgs), ctypes.c_void_p]
         L.vqkv_decode_attn_static.restype = ctypes.c_int
@@ -193,6 +200,20 @@ def vqkv_decode_attn(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook
         raise VqkvError(st, "vqkv_decode_attn")
 
 
+def vqkv_decode_attn_multi(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace,
+                           cap_len, max_seq_len, softmax_scale=0.0, num_splits=0, stream=None) -> None:
+    """M queries per sequence: q and out fp16 [B][M][Hq][128]; query m sees
+    the cached tokens t <= seq_lens[b] - M + m."""
+    B, M, Hq, D = q.shape
+    a = DecodeMultiArgs(decode=decode_args(mode, q.view(B, M * Hq, D), k_codes, v_codes, seq_lens, k_codebook,
+                                           v_codebook, s, out, workspace, cap_len, max_seq_len, softmax_scale,
+                                           num_splits), n_queries=M)
+    a.decode.Hq = Hq
+    st = lib().vqkv_decode_attn_multi(ctypes.byref(a), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_attn_multi")
+
+
 def vqkv_decode_append(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace,
                        cap_len, max_seq_len, k_new, v_new, near_tie_count=None, softmax_scale=0.0, num_splits=0,
                        stream=None) -> None:
@@ -218,12 +239,13 @@ def vqkv_decode_attn_static(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_c
         raise VqkvError(st, "vqkv_decode_attn_static")
 
 
-def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda"):
-    """A zero-filled workspace tensor of the size the decode call needs."""
+def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda", n_queries=1):
+    """A zero-filled workspace tensor of the size the decode call needs
+    (n_queries > 1: for vqkv_decode_attn_multi)."""
     import torch
     a = DecodeArgs(mode=mode, B=B, Hq=Hq, Hkv=Hkv, head_dim=128, cap_len=cap_len, max_seq_len=max_seq_len,
                    num_splits=num_splits)
-    n = vqkv_decode_workspace_bytes(a)
+    n = vqkv_decode_workspace_bytes(a) * n_queries
     if n == 0:
         raise VqkvError(1, "vqkv_decode_workspace_bytes")
     return torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=device)

@@ -101,6 +101,7 @@ struct DecodePlan {
 struct PlanInput {
   int mode;   // VQKV_MODE_VQ2, VQKV_MODE_VQ15 or kModeFp16
   int B, Hq, Hkv, max_seq_len, num_splits;
+  int M = 1;  // queries per sequence
 };
 
 vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
@@ -145,7 +146,7 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   pl->tickets_off = kWsHeader;
   pl->partials_off = decode_ticket_region_bytes(B, a->Hkv);
   pl->ws_bytes = pl->partials_off +
-                 sizeof(float) * (size_t)B * a->Hkv * pl->n_splits * g * kPartialStride;
+                 sizeof(float) * (size_t)B * a->Hkv * pl->n_splits * g * a->M * kPartialStride;
   return VQKV_OK;
 }
 
@@ -196,7 +197,7 @@ vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(
 
 namespace {
 // Both decode entry points: ap == nullptr for vqkv_decode_attn.
-vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, void* stream);
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream);
 }  // namespace
 
 size_t decode_ticket_region_bytes(int B, int Hkv) {
@@ -241,11 +242,16 @@ int32_t vqkv_decode_kernel_count(const vqkv_decode_args* a) {
   return (pl.bpg > 1 && pl.n_splits > 1) ? 2 : 1;
 }
 
-vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) { return decode_launch(a, nullptr, stream); }
+vqkv_status vqkv_decode_attn(const vqkv_decode_args* a, void* stream) { return decode_launch(a, nullptr, 1, stream); }
+
+vqkv_status vqkv_decode_attn_multi(const vqkv_decode_multi_args* am, void* stream) {
+  if (am == nullptr || am->n_queries < 1) return VQKV_ERR_INVALID_ARG;
+  return decode_launch(&am->decode, nullptr, am->n_queries, stream);
+}
 
 vqkv_status vqkv_decode_append(const vqkv_decode_append_args* ap, void* stream) {
   if (ap == nullptr) return VQKV_ERR_INVALID_ARG;
-  return decode_launch(&ap->decode, ap, stream);
+  return decode_launch(&ap->decode, ap, 1, stream);
 }
 
 }  // extern "C"
@@ -253,10 +259,11 @@ vqkv_status vqkv_decode_append(const vqkv_decode_append_args* ap, void* stream) 
 namespace vqkv {
 namespace {
 
-vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, void* stream) {
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream) {
   if (ap != nullptr && a->mode != VQKV_MODE_VQ2) return VQKV_ERR_UNSUPPORTED;
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK) return st;
+  if ((long long)M * (a->Hq / a->Hkv) > 8) return VQKV_ERR_UNSUPPORTED;   // one 8-column MMA tile
   if (ap != nullptr) {
     if (a->B > 0 && (!ap->k_new || !ap->v_new || !aligned(ap->k_new, 8) || !aligned(ap->v_new, 8) ||
                      (ap->near_tie_count && !aligned(ap->near_tie_count, 8))))
@@ -264,7 +271,8 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
   }
   if (a->B == 0) return VQKV_OK;
   DecodePlan pl;
-  const PlanInput in = plan_input(a);
+  PlanInput in = plan_input(a);
+  in.M = M;
   st = plan_decode(&in, &pl);
   if (st != VQKV_OK) return st;
   if (a->workspace == nullptr || a->workspace_bytes < pl.ws_bytes) return VQKV_ERR_WORKSPACE;
@@ -287,6 +295,8 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.g = a->Hq / a->Hkv;
+  p.M = M;
+  p.ncols = M * p.g;
   p.max_seq_len = a->max_seq_len;
   p.n_splits = pl.n_splits;
   p.tps = pl.tps;
@@ -383,6 +393,8 @@ vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* a, void* stream) 
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.g = a->Hq / a->Hkv;
+  p.M = 1;
+  p.ncols = p.g;
   p.max_seq_len = a->max_seq_len;
   p.n_splits = pl.n_splits;
   p.tps = pl.tps;

@@ -95,12 +95,13 @@ static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must f
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
 static_assert(V15_Q_OFF + 8 * 128 * 4 <= (int)kV15Smem, "q' must fit in the combine area");
 
-// q' for the g heads of (b, kvh) into s_qp[h][128] (fp32, scaled), by warps 0..g-1.
+// q' of the ncols softmax columns of (b, kvh) into s_qp[c][128] (fp32,
+// scaled), by warps 0..ncols-1.
 __device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
                                                   int lane, float* s_qp) {
-  if (warp < p.g) {
-    const int hq = kvh * p.g + warp;
-    const uint2 qq = *reinterpret_cast<const uint2*>(p.q + ((size_t)b * p.Hq + hq) * kHeadDim + 4 * lane);
+  if (warp < p.ncols) {   // column warp: query warp / g, head warp % g
+    const int m = warp / p.g, hq = kvh * p.g + warp - m * p.g;
+    const uint2 qq = *reinterpret_cast<const uint2*>(p.q + (((size_t)b * p.M + m) * p.Hq + hq) * kHeadDim + 4 * lane);
     const float4 ss = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
     const __half2 q01 = *reinterpret_cast<const __half2*>(&qq.x);
     const __half2 q23 = *reinterpret_cast<const __half2*>(&qq.y);
@@ -139,7 +140,7 @@ __device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
 template <int T>
 __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
                                             const uint32_t (&qa)[8][2], const uint4 (&kq)[T],
-                                            const uint4 (&vq)[T], int tile0, int L, int lane, float& m0,
+                                            const uint4 (&vq)[T], int tile0, const ColumnLimits& cl, int lane, float& m0,
                                             float& m1, float& l0, float& l1, float (&acc)[8][4]) {
   const int gid = lane >> 2;
   float sc[T][4];
@@ -158,13 +159,9 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
 #pragma unroll
     for (int e = 0; e < 4; ++e) sc[i][e] = da[e] + db[e];
   }
-  if ((tile0 + T) * V2_TILE > L) {   // tail of the sequence
+  if ((tile0 + T) * V2_TILE > cl.lim_min) {   // tail of the sequence
 #pragma unroll
-    for (int i = 0; i < T; ++i) {
-      const int t0 = (tile0 + i) * V2_TILE + gid;
-      if (t0 >= L) sc[i][0] = sc[i][1] = neg_inf();
-      if (t0 + 8 >= L) sc[i][2] = sc[i][3] = neg_inf();
-    }
+    for (int i = 0; i < T; ++i) mask_scores(sc[i], (tile0 + i) * V2_TILE + gid, cl);
   }
   uint32_t bP[T][2];
   softmax_tiles<T, 8>(sc, m0, m1, l0, l1, acc, bP);
@@ -224,6 +221,9 @@ __device__ __noinline__ void append_rows(uint2 raw, float4 s, uint8_t* k_stream,
   __syncthreads();
 }
 
+// MULTI: several queries per sequence (per-column causal limits); the
+// single-query instantiation keeps one limit, L, for every column.
+template <bool MULTI>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     const int ntiles = (L + V2_TILE - 1) / V2_TILE;
     const int t_begin = split * p.tps;
     const int t_end = min(t_begin + p.tps, ntiles);
+    const ColumnLimits cl = MULTI ? column_limits(p, L, tig) : ColumnLimits{L, L, L};
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * s + tig;
-        if (gid < p.g) {
+        if (gid < p.ncols) {
           const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + 4 * j);
           qa[s][0] = pack_half2(v.x, v.y);
           qa[s][1] = pack_half2(v.z, v.w);
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         __syncwarp();
         // refill the stage this warp finished with in the previous step
         if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
-        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, L, lane, m0,
+        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, cl, lane, m0,
                          m1, l0, l1, acc);
       }
       if (timed_out) {
@@ -383,6 +384,7 @@ __device__ __forceinline__ uint32_t pair24(uint32_t w0, uint32_t w1, uint32_t w2
   return w2 >> 8;
 }
 
+template <bool MULTI>
 __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint4* s_kcb = reinterpret_cast<uint4*>(smem);
@@ -408,6 +410,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     const int ntiles = (L + V15_TILE - 1) / V15_TILE;
     const int t_begin = split * p.tps;
     const int t_end = min(t_begin + p.tps, ntiles);
+    const ColumnLimits cl = MULTI ? column_limits(p, L, tig) : ColumnLimits{L, L, L};
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * (s >> 1) + tig;     // subvector
         const int c = 8 * j + 4 * (s & 1);    // first channel of this half
-        if (gid < p.g) {
+        if (gid < p.ncols) {
           const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + c);
           qf[s][0] = pack_half2(v.x, v.y);
           qf[s][1] = pack_half2(v.z, v.w);
@@ -495,11 +498,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
             mma_16816(sc, X.x, Y.x, X.y, Y.y, qf[2 * s2][0], qf[2 * s2][1]);
             mma_16816(sc, X.z, Y.z, X.w, Y.w, qf[2 * s2 + 1][0], qf[2 * s2 + 1][1]);
           }
-          if (tq + 16 > L) {
-            const int t0 = tq + gid;
-            if (t0 >= L) sc[0] = sc[1] = neg_inf();
-            if (t0 + 8 >= L) sc[2] = sc[3] = neg_inf();
-          }
+          if (tq + 16 > cl.lim_min) mask_scores(sc, tq + gid, cl);
           uint32_t bP0, bP1;
           softmax_tile(sc, m0, m1, l0, l1, acc, bP0, bP1);
 
@@ -547,7 +546,7 @@ __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodePa
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
-  return launch_pdl(decode_combine_kernel, dim3(p.Hq, p.B), dim3(kHeadDim), 0, stream, p);
+  return launch_pdl(decode_combine_kernel, dim3(p.Hkv * p.ncols, p.B), dim3(kHeadDim), 0, stream, p);
 }
 
 int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TILE : V15_TILE; }
@@ -556,20 +555,30 @@ size_t decode_smem_bytes(int mode) { return mode == VQKV_MODE_VQ2 ? kV2Smem : kV
 int decode_threads(int mode) { return mode == VQKV_MODE_VQ2 ? V2_THREADS : V15_THREADS; }
 
 cudaError_t decode_prepare(int mode) {
-  if (mode == VQKV_MODE_VQ2)
-    return cudaFuncSetAttribute(decode_vq2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV2Smem);
-  return cudaFuncSetAttribute(decode_vq15_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kV15Smem);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if (mode == VQKV_MODE_VQ2) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_vq2_kernel<false>, a, (int)kV2Smem);
+    return e != cudaSuccess ? e : cudaFuncSetAttribute(decode_vq2_kernel<true>, a, (int)kV2Smem);
+  }
+  const cudaError_t e = cudaFuncSetAttribute(decode_vq15_kernel<false>, a, (int)kV15Smem);
+  return e != cudaSuccess ? e : cudaFuncSetAttribute(decode_vq15_kernel<true>, a, (int)kV15Smem);
 }
 
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel, V2_THREADS, kV2Smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel, V15_THREADS, kV15Smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<false>, V2_THREADS,
+                                                         kV2Smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<false>, V15_THREADS,
+                                                       kV15Smem);
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  if (mode == VQKV_MODE_VQ2) return launch_pdl(decode_vq2_kernel, grid, dim3(V2_THREADS), kV2Smem, stream, p);
-  return launch_pdl(decode_vq15_kernel, grid, dim3(V15_THREADS), kV15Smem, stream, p);
+  const bool multi = p.M > 1;
+  if (mode == VQKV_MODE_VQ2)
+    return launch_pdl(multi ? decode_vq2_kernel<true> : decode_vq2_kernel<false>, grid, dim3(V2_THREADS), kV2Smem,
+                      stream, p);
+  return launch_pdl(multi ? decode_vq15_kernel<true> : decode_vq15_kernel<false>, grid, dim3(V15_THREADS),
+                    kV15Smem, stream, p);
 }
 
 }  // namespace vqkv

@@ -117,6 +117,33 @@ __device__ __forceinline__ void softmax_tiles(float (&sc)[T][4], float& m0, floa
   }
 }
 
+// Offset of O's row for softmax column c (query c / g, head c % g) of KV
+// head kvh of sequence b; O is [B][M][Hq][128].
+__device__ __forceinline__ size_t out_row(const DecodeParams& p, int b, int kvh, int c) {
+  const int m = c / p.g, h = c - m * p.g;
+  return (((size_t)b * p.M + m) * p.Hq + kvh * p.g + h) * kHeadDim;
+}
+
+// Per-lane visible-token limits of the lane's two softmax columns 2tig and
+// 2tig+1: query m of M sees tokens t < L - M + m + 1 (columns past ncols
+// are padding and see all L).  lim_min is the smallest limit of a real column.
+struct ColumnLimits {
+  int lim0, lim1, lim_min;
+};
+__device__ __forceinline__ ColumnLimits column_limits(const DecodeParams& p, int L, int tig) {
+  const int c0 = 2 * tig, c1 = c0 + 1;
+  return {c0 < p.ncols ? L - p.M + c0 / p.g + 1 : L, c1 < p.ncols ? L - p.M + c1 / p.g + 1 : L, L - p.M + 1};
+}
+
+// Masks the scores of tokens t0 (sc[0], sc[1]) and t0 + 8 (sc[2], sc[3]) in
+// columns 2tig, 2tig+1 that their query does not see.
+__device__ __forceinline__ void mask_scores(float (&sc)[4], int t0, const ColumnLimits& cl) {
+  if (t0 >= cl.lim0) sc[0] = neg_inf();
+  if (t0 >= cl.lim1) sc[1] = neg_inf();
+  if (t0 + 8 >= cl.lim0) sc[2] = neg_inf();
+  if (t0 + 8 >= cl.lim1) sc[3] = neg_inf();
+}
+
 // Merge the per-warp states of the CTA into one partial (m, l, O) per head.
 // With one split that is O itself.  Otherwise write the partial to the
 // workspace; then, when the plan defers the merge (CTAs that cover several
@@ -133,7 +160,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
   const float* wO = s_comb;
   const float* wm = s_comb + CombineSmem<WARPS>::kO;
   const float* wl = wm + WARPS * 8;
-  const int G = p.g;
+  const int G = p.ncols;
   float* part = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * G * kPartialStride;
   for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
     const int h = e >> 7, d = e & 127;
@@ -148,7 +175,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
       l += wl[w * 8 + h] * f;
     }
     if (p.n_splits == 1) {
-      p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+      p.out[out_row(p, b, kvh, h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
       continue;
     }
     part[h * kPartialStride + d] = o;
@@ -205,21 +232,22 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
       const int e = threadIdx.x + k * WARPS * 32;
       if (e < G * kHeadDim) {
         const int h = e >> 7, d = e & 127;
-        p.out[((size_t)b * p.Hq + kvh * G + h) * kHeadDim + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
+        p.out[out_row(p, b, kvh, h) + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
       }
     }
     if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
   }
 }
 
-// Merge the split partials of query head hq = blockIdx.x of sequence
-// b = blockIdx.y into O (fp16); thread d owns channel d.  The combine kernel
+// Merge the split partials of softmax column blockIdx.x % ncols of KV head
+// blockIdx.x / ncols of sequence b = blockIdx.y into O (fp16); thread d owns
+// channel d.  The combine kernel
 // of plans that defer the merge.
 __device__ __forceinline__ void combine_splits(const DecodeParams& p) {
   constexpr int U = 8;   // splits whose loads are in flight together
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int kvh = hq / p.g, h = hq - kvh * p.g;
-  const size_t stride = (size_t)p.g * kPartialStride;
+  const int b = blockIdx.y, d = threadIdx.x;
+  const int kvh = blockIdx.x / p.ncols, h = blockIdx.x - kvh * p.ncols;   // h: softmax column
+  const size_t stride = (size_t)p.ncols * kPartialStride;
   const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * stride + h * kPartialStride;
   float M = kMInit, O = 0.f, Ls = 0.f;
   for (int s0 = 0; s0 < p.n_splits; s0 += U) {
@@ -241,7 +269,7 @@ __device__ __forceinline__ void combine_splits(const DecodeParams& p) {
       M = n;
     }
   }
-  p.out[((size_t)b * p.Hq + hq) * kHeadDim + d] = __float2half_rn(Ls > 0.f ? O / Ls : 0.f);
+  p.out[out_row(p, b, kvh, h) + d] = __float2half_rn(Ls > 0.f ? O / Ls : 0.f);
 }
 
 // Store one warp's (m, l, O) into the combine area.  acc holds O^T fragments:

@@ -25,6 +25,8 @@ struct DecodeParams {
   unsigned* err;            // device error word
   long long stream_bytes;
   int B, Hq, Hkv, g;
+  int M = 1;                // queries per sequence (multi-query decode)
+  int ncols = 0;            // softmax columns per KV head: M * g (query m, head h -> column m * g + h)
   int max_seq_len;
   int n_splits;             // CTAs per (sequence, KV head)
   int tps;                  // tiles per split
