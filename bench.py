@@ -51,6 +51,9 @@ def parse():
                          "3: Qwen2.5-14B 1.5-bit; 4: Mistral-7B encode + decode")
     ap.add_argument("--mode", type=int, default=None, choices=[0, 1],
                     help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit)")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="queries per sequence (multi-query decode, e.g. speculative decoding): a step encodes "
+                         "that many new K/V rows per sequence and runs vqkv_decode_attn_multi")
     ap.add_argument("--unfused", action="store_true",
                     help="2-bit: run a step as vqkv_encode (K) + vqkv_encode (V) + vqkv_decode_attn instead of "
                          "the fused vqkv_decode_append")
@@ -296,7 +299,7 @@ def run_ours(args):
     w = synth.WORKLOADS[args.workload]
     if args.mode is not None:
         w = w.with_mode(args.mode)
-    headline = args.workload == WORKLOAD_ID and w.mode == synth.MODE_VQ2
+    headline = args.workload == WORKLOAD_ID and w.mode == synth.MODE_VQ2 and args.queries == 1
     lens = synth.seq_lens(w)
     if headline:
         s_h, kcb_h, vcb_h, kv = host_workload(w)
@@ -345,21 +348,33 @@ def run_ours(args):
     n_copies = max(2, math.ceil(3 * l2 / cache_bytes) + 1)
     copies = [(kcodes, vcodes)] + [(kcodes.clone(), vcodes.clone()) for _ in range(n_copies - 1)]
 
-    q = torch.from_numpy(synth.queries(w)).to(dev)
-    new_k = torch.from_numpy(np.stack([np.stack([synth.appended_keys(w, b, h, 1) for h in range(w.Hkv)])
+    M = args.queries
+    if M == 1:
+        q = torch.from_numpy(synth.queries(w)).to(dev)
+    else:   # M seeded query sets of the same distribution
+        q = torch.from_numpy(np.stack([synth.queries(w.scaled(seed=w.seed + 101 * m)) for m in range(M)], 1)).to(dev)
+    new_k = torch.from_numpy(np.stack([np.stack([synth.appended_keys(w, b, h, M) for h in range(w.Hkv)])
                                        for b in range(w.B)])).to(dev)
-    new_v = torch.from_numpy(np.stack([np.stack([synth.values(w, b, h, int(lens[b]) - 1, 1) for h in range(w.Hkv)])
+    new_v = torch.from_numpy(np.stack([np.stack([synth.values(w, b, h, int(lens[b]) - M, M) for h in range(w.Hkv)])
                                        for b in range(w.B)])).to(dev)
-    pos = torch.from_numpy((lens - 1).astype(np.int32)).to(dev)
+    pos = torch.from_numpy((lens - M).astype(np.int32)).to(dev)
     seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
-    out = torch.empty((w.B, w.Hq, 128), dtype=torch.float16, device=dev)
+    out = torch.empty(q.shape, dtype=torch.float16, device=dev)
     max_len = int(lens.max())
-    ws = _lib.decode_workspace(mode, w.B, w.Hq, w.Hkv, cap, max_len, device=dev)
-    dargs = _lib.decode_args(mode, q, kcodes, vcodes, seq, kcb, vcb, s, out, ws, cap, max_len)
+    ws = _lib.decode_workspace(mode, w.B, w.Hq, w.Hkv, cap, max_len, device=dev, n_queries=M)
+    dargs = _lib.decode_args(mode, q.view(w.B, M * w.Hq, 128), kcodes, vcodes, seq, kcb, vcb, s, out, ws, cap,
+                             max_len)
+    dargs.Hq = w.Hq
     n_splits = _lib.vqkv_decode_num_splits(dargs)
     dec_kernels = _lib.vqkv_decode_kernel_count(dargs)
 
-    fused = mode == synth.MODE_VQ2 and not args.unfused
+    fused = mode == synth.MODE_VQ2 and not args.unfused and M == 1
+
+    def decode_only(kc, vc):
+        if M == 1:
+            _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+        else:
+            _lib.vqkv_decode_attn_multi(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
 
     def step_unfused(i, ev=None):
         kc, vc = copies[i % n_copies]
@@ -367,7 +382,7 @@ def run_ours(args):
         _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
         if ev is not None:
             ev[0].record()
-        _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+        decode_only(kc, vc)
         if ev is not None:
             ev[1].record()
 
@@ -376,7 +391,7 @@ def run_ours(args):
         if fused:
             _lib.vqkv_decode_append(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len, new_k, new_v)
         else:
-            _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+            decode_only(kc, vc)
 
     def step(i, ev=None):
         if not fused:
@@ -495,11 +510,11 @@ def run_ours(args):
     ms_total = max_over_ranks(ms_total, world, dev)
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
-    q_host = torch.from_numpy(synth.queries(w)).pin_memory()
+    q_host = q.cpu().pin_memory()
     nk_host = new_k.cpu().pin_memory()
     nv_host = new_v.cpu().pin_memory()
-    o_host = torch.empty((w.B, w.Hq, 128), dtype=torch.float16).pin_memory()
-    fp16 = None if args.profile_steps else fp16_baseline(w, kv_fp16, lens, dev, stream)
+    o_host = torch.empty(tuple(out.shape), dtype=torch.float16).pin_memory()
+    fp16 = None if args.profile_steps or M > 1 else fp16_baseline(w, kv_fp16, lens, dev, stream)
     del kv_fp16
     e2e_steps = max(20, min(args.steps, 2000))
     with torch.cuda.stream(stream):
@@ -513,7 +528,7 @@ def run_ours(args):
             else:
                 _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
                 _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
-                _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
+                decode_only(kc, vc)
             o_host.copy_(out, non_blocking=True)
             stream.synchronize()
         for i in range(10):
@@ -527,7 +542,7 @@ def run_ours(args):
     tokens = int(lens.sum())
     ms_step = ms_total / args.steps
     value = replica_throughput(tokens, ms_step, world)
-    alg = algorithmic_bytes(w, lens)
+    alg = algorithmic_bytes(w, lens) + (M - 1) * 2 * w.B * w.Hq * 128 * 2   # q and O of every query
     if fused:
         alg += 2 * w.B * w.Hkv * (128 * 2 + 128 // 4)   # the new rows read, their codes written
     peaks = {}
@@ -542,12 +557,13 @@ def run_ours(args):
     traffic = profile_traffic()[0] if headline else None
     line = {
         "metric": METRIC if headline else f"decode-attn KV tokens/s and HBM GB/s ({w.name}, "
-                                                 f"{'2' if w.mode == 0 else '1.5'}-bit)",
+                                                 f"{'2' if w.mode == 0 else '1.5'}-bit"
+                                                 f"{f', {M} queries per sequence' if M > 1 else ''})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
-                   "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits,
+                   "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits, "queries_per_sequence": M,
                    "step": ("vqkv_decode_append: 1 new K row + 1 new V row per sequence encoded into the cache "
                             "and attended in the same kernel" if fused else
                             "vqkv_encode (1 new K row per sequence), vqkv_encode (V), vqkv_decode_attn"),
