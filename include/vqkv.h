@@ -88,6 +88,7 @@ typedef enum {
 #define VQKV_DEVERR_SEQ_LEN   0x1u  /* a seq_lens[b] outside [0, max_seq_len]: clamped */
 #define VQKV_DEVERR_POSITION  0x2u  /* an encode row outside [0, cap_len): not written */
 #define VQKV_DEVERR_TIMEOUT   0x4u  /* a bounded on-chip wait gave up; that CTA's output is invalid */
+#define VQKV_DEVERR_BLOCK     0x8u  /* a block-table entry outside [0, num_blocks) (paged calls) */
 
 /*
  * vqkv_encode — smoothing, Hadamard rotation, nearest-centroid assignment and
@@ -236,6 +237,34 @@ typedef struct {
 } vqkv_decode_multi_args;
 
 vqkv_status vqkv_decode_attn_multi(const vqkv_decode_multi_args* args, void* stream);
+
+/*
+ * Paged cache: one pool of fixed-size blocks per role, shared by all
+ * sequences through a block table, as serving engines lay out their KV
+ * caches (the pages name serving-framework integration as future work,
+ * paper summary page, "Key points").
+ *
+ * In the paged calls, codes (encode) and k_codes / v_codes (decode) point to
+ * pools of num_blocks * Hkv * vqkv_code_bytes(mode, block_tokens) bytes:
+ * block n of KV head h starts at byte (n * Hkv + h) * vqkv_code_bytes(mode,
+ * block_tokens) and holds block_tokens tokens in the layout above (a stream
+ * of block_tokens tokens).  Logical token t of sequence b lives at position
+ * t % block_tokens of block block_table[b * max_blocks + t / block_tokens].
+ * cap_len must not exceed max_blocks * block_tokens.  A table entry outside
+ * [0, num_blocks) is never dereferenced: the encode skips that row, the
+ * decode reads block 0 instead (its O is then meaningless), and both set
+ * VQKV_DEVERR_BLOCK in the error word.  Everything else is as in the
+ * contiguous calls, which give the same results for the same tokens.
+ */
+typedef struct {
+  const int32_t* block_table; /* device [B][max_blocks], 4-byte aligned */
+  int32_t max_blocks;         /* entries per sequence, >= 1 */
+  int32_t block_tokens;       /* tokens per block: a positive multiple of 64 */
+  int32_t num_blocks;         /* blocks in each pool, >= 1 */
+} vqkv_paging;
+
+vqkv_status vqkv_encode_paged(const vqkv_encode_args* args, const vqkv_paging* paging, void* stream);
+vqkv_status vqkv_decode_attn_paged(const vqkv_decode_args* args, const vqkv_paging* paging, void* stream);
 
 /*
  * vqkv_decode_attn_fp16 — the same decode attention over a plain fp16 KV

@@ -39,7 +39,7 @@ def test_struct_layout_matches_header(tmp_path):
     """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
     fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs,
               "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs, "vqkv_decode_append_args": _lib.DecodeAppendArgs,
-              "vqkv_decode_multi_args": _lib.DecodeMultiArgs}
+              "vqkv_decode_multi_args": _lib.DecodeMultiArgs, "vqkv_paging": _lib.Paging}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -168,3 +168,22 @@ def test_decode_multi_validation(lib):
     a.decode = _dec(B=0, q=None, out=None)
     a.n_queries = 2
     assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 0    # empty batch: a no-op
+
+
+@pytest.mark.parametrize("kw", [dict(block_tokens=100), dict(block_tokens=0), dict(max_blocks=0),
+                                dict(num_blocks=0), dict(max_blocks=1)])   # 1 x 64 tokens < cap_len 128
+def test_paging_validation(lib, kw):
+    pg = _lib.Paging(block_table=0x1000, max_blocks=2, block_tokens=64, num_blocks=4)
+    for k, v in kw.items():
+        setattr(pg, k, v)
+    d = _dec(cap_len=128, max_seq_len=128)
+    assert lib.vqkv_decode_attn_paged(ctypes.byref(d), ctypes.byref(pg), None) == 1
+    assert lib.vqkv_encode_paged(ctypes.byref(_enc(cap_len=128)), ctypes.byref(pg), None) == 1
+
+
+def test_paging_required_and_empty_batch(lib):
+    assert lib.vqkv_decode_attn_paged(ctypes.byref(_dec()), None, None) == 1
+    assert lib.vqkv_encode_paged(ctypes.byref(_enc()), None, None) == 1
+    pg = _lib.Paging(block_table=None, max_blocks=1, block_tokens=64, num_blocks=1)
+    assert lib.vqkv_decode_attn_paged(ctypes.byref(_dec()), ctypes.byref(pg), None) == 1   # no table
+    assert lib.vqkv_decode_attn_paged(ctypes.byref(_dec(B=0, q=None, out=None)), ctypes.byref(pg), None) == 0

@@ -19,13 +19,14 @@ VQKV_ROLE_V = 1
 VQKV_DEVERR_SEQ_LEN = 0x1
 VQKV_DEVERR_POSITION = 0x2
 VQKV_DEVERR_TIMEOUT = 0x4
+VQKV_DEVERR_BLOCK = 0x8
 
 STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3: "VQKV_ERR_WORKSPACE",
           4: "VQKV_ERR_CUDA", 5: "VQKV_ERR_NO_DEVICE"}
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
             "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_multi", "vqkv_decode_append",
-            "vqkv_decode_attn_static",
+            "vqkv_decode_attn_static", "vqkv_encode_paged", "vqkv_decode_attn_paged",
             "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -61,6 +62,11 @@ class Fp16DecodeArgs(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
                 ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
+
+
+class Paging(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int32), ("block_tokens", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32)]
 
 
 class DecodeMultiArgs(ctypes.Structure):
@@ -101,6 +107,10 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_encode_paged.restype = ctypes.c_int
+        L.vqkv_encode_paged.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.POINTER(Paging), ctypes.c_void_p]
+        L.vqkv_decode_attn_paged.restype = ctypes.c_int
+        L.vqkv_decode_attn_paged.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.POINTER(Paging), ctypes.c_void_p]
         L.vqkv_decode_attn_multi.restype = ctypes.c_int
         L.vqkv_decode_attn_multi.argtypes = [ctypes.POINTER(DecodeMultiArgs), ctypes.c_void_p]
         L.vqkv_decode_append.restype = ctypes.c_int
@@ -158,6 +168,34 @@ def vqkv_encode(mode, role, x, pos, s, codebook, codes, cap_len, near_tie_count=
     st = lib().vqkv_encode(ctypes.byref(a), _stream(stream))
     if st != 0:
         raise VqkvError(st, "vqkv_encode")
+
+
+def paging(block_table, block_tokens, num_blocks) -> Paging:
+    """Block table int32 [B][max_blocks] (device) of a paged cache."""
+    return Paging(block_table=_ptr(block_table), max_blocks=block_table.shape[1], block_tokens=block_tokens,
+                  num_blocks=num_blocks)
+
+
+def vqkv_encode_paged(mode, role, x, pos, s, codebook, pool, cap_len, block_table, block_tokens, num_blocks,
+                      near_tie_count=None, error_flags=None, stream=None) -> None:
+    """vqkv_encode into a paged pool uint8 [num_blocks][Hkv][vqkv_code_bytes(mode, block_tokens)]."""
+    a = encode_args(mode, role, x, pos, s, codebook, pool, cap_len, near_tie_count, error_flags)
+    pg = paging(block_table, block_tokens, num_blocks)
+    st = lib().vqkv_encode_paged(ctypes.byref(a), ctypes.byref(pg), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_encode_paged")
+
+
+def vqkv_decode_attn_paged(mode, q, k_pool, v_pool, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,
+                           max_seq_len, block_table, block_tokens, num_blocks, softmax_scale=0.0, num_splits=0,
+                           stream=None) -> None:
+    """vqkv_decode_attn over paged pools (see vqkv_encode_paged)."""
+    a = decode_args(mode, q, k_pool, v_pool, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,
+                    max_seq_len, softmax_scale, num_splits)
+    pg = paging(block_table, block_tokens, num_blocks)
+    st = lib().vqkv_decode_attn_paged(ctypes.byref(a), ctypes.byref(pg), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_attn_paged")
 
 
 def decode_args(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_codebook, s, out, workspace, cap_len,

@@ -84,6 +84,26 @@ vqkv_status validate_decode(const vqkv_decode_args* a) {
   return VQKV_OK;
 }
 
+// Block-table arguments of the paged calls: sizes and alignment only.
+vqkv_status validate_paging(const vqkv_paging* pg, int mode, int cap_len) {
+  if (pg == nullptr) return VQKV_ERR_INVALID_ARG;
+  if (pg->max_blocks < 1 || pg->num_blocks < 1 || pg->block_tokens < 64 || pg->block_tokens % 64 != 0)
+    return VQKV_ERR_INVALID_ARG;
+  if ((long long)pg->max_blocks * pg->block_tokens < cap_len) return VQKV_ERR_INVALID_ARG;
+  if ((long long)pg->num_blocks * vqkv_code_bytes(mode, pg->block_tokens) > (1LL << 46)) return VQKV_ERR_INVALID_ARG;
+  return VQKV_OK;
+}
+
+template <typename P>
+void set_paging(P& p, const vqkv_paging* pg, int mode) {
+  if (pg == nullptr) return;
+  p.block_table = pg->block_table;
+  p.max_blocks = pg->max_blocks;
+  p.block_tiles = pg->block_tokens / (mode == VQKV_MODE_VQ2 ? 16 : 64);
+  p.num_blocks = pg->num_blocks;
+  p.block_bytes = (long long)vqkv_code_bytes(mode, pg->block_tokens);
+}
+
 }  // namespace
 size_t decode_ticket_region_bytes(int B, int Hkv);
 namespace {
@@ -197,7 +217,9 @@ vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(
 
 namespace {
 // Both decode entry points: ap == nullptr for vqkv_decode_attn.
-vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream);
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream,
+                          const vqkv_paging* pg = nullptr);
+vqkv_status encode_launch(const vqkv_encode_args* a, void* stream, const vqkv_paging* pg = nullptr);
 }  // namespace
 
 size_t decode_ticket_region_bytes(int B, int Hkv) {
@@ -259,10 +281,16 @@ vqkv_status vqkv_decode_append(const vqkv_decode_append_args* ap, void* stream) 
 namespace vqkv {
 namespace {
 
-vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream) {
+vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream,
+                          const vqkv_paging* pg) {
   if (ap != nullptr && a->mode != VQKV_MODE_VQ2) return VQKV_ERR_UNSUPPORTED;
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK) return st;
+  if (pg != nullptr) {
+    st = validate_paging(pg, a->mode, a->cap_len);
+    if (st != VQKV_OK) return st;
+    if (a->B > 0 && (!pg->block_table || !aligned(pg->block_table, 4))) return VQKV_ERR_INVALID_ARG;
+  }
   if ((long long)M * (a->Hq / a->Hkv) > 8) return VQKV_ERR_UNSUPPORTED;   // one 8-column MMA tile
   if (ap != nullptr) {
     if (a->B > 0 && (!ap->k_new || !ap->v_new || !aligned(ap->k_new, 8) || !aligned(ap->v_new, 8) ||
@@ -311,6 +339,7 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
     p.vc_w = const_cast<uint8_t*>(a->v_codes);
     p.near_tie = ap->near_tie_count;
   }
+  set_paging(p, pg, a->mode);
   const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
   if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
   if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -323,9 +352,32 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
 
 extern "C" {
 
-vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
+vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) { return encode_launch(a, stream); }
+
+vqkv_status vqkv_encode_paged(const vqkv_encode_args* a, const vqkv_paging* pg, void* stream) {
+  if (pg == nullptr) return VQKV_ERR_INVALID_ARG;
+  return encode_launch(a, stream, pg);
+}
+
+vqkv_status vqkv_decode_attn_paged(const vqkv_decode_args* a, const vqkv_paging* pg, void* stream) {
+  if (pg == nullptr) return VQKV_ERR_INVALID_ARG;
+  return decode_launch(a, nullptr, 1, stream, pg);
+}
+
+}  // extern "C"
+
+namespace vqkv {
+namespace {
+
+vqkv_status encode_launch(const vqkv_encode_args* a, void* stream, const vqkv_paging* pg) {
   vqkv_status st = validate_encode(a);
-  if (st != VQKV_OK || a->B == 0 || a->n_rows == 0) return st;
+  if (st != VQKV_OK) return st;
+  if (pg != nullptr) {
+    st = validate_paging(pg, a->mode, a->cap_len);
+    if (st != VQKV_OK) return st;
+    if (a->B > 0 && a->n_rows > 0 && (!pg->block_table || !aligned(pg->block_table, 4))) return VQKV_ERR_INVALID_ARG;
+  }
+  if (a->B == 0 || a->n_rows == 0) return st;
   DeviceInfo di;
   st = device_info(&di);
   if (st != VQKV_OK) return st;
@@ -356,10 +408,16 @@ vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) {
     if (cap < 1) cap = 1;
     blocks_x = (int)std::min(want, cap);
   }
+  set_paging(p, pg, a->mode);
   if (launch_encode(a->mode, p, blocks_x, split_rows, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VQKV_ERR_CUDA;
   return VQKV_OK;
 }
+
+}  // namespace
+}  // namespace vqkv
+
+extern "C" {
 
 size_t vqkv_fp16_decode_workspace_bytes(const vqkv_fp16_decode_args* a) {
   if (validate_fp16(a, true) != VQKV_OK) return 0;

@@ -177,6 +177,22 @@ inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// ---------------------------------------------------------------- paged cache
+// Byte offset of the first byte of tile `tile` of stream (b, kvh): in the
+// contiguous layout, or through the block table of a paged pool (P has the
+// fields of DecodeParams / EncodeParams).  A block id outside
+// [0, num_blocks) selects block 0 and sets *bad.
+template <bool PAGED, typename P>
+__device__ __forceinline__ long long tile_offset(const P& p, int b, int kvh, int tile, int tile_bytes, bool* bad) {
+  if (!PAGED) return (long long)(b * p.Hkv + kvh) * p.stream_bytes + (long long)tile * tile_bytes;
+  int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + tile / p.block_tiles);
+  if (blk < 0 || blk >= p.num_blocks) {
+    *bad = true;
+    blk = 0;
+  }
+  return ((long long)blk * p.Hkv + kvh) * p.block_bytes + (long long)(tile % p.block_tiles) * tile_bytes;
+}
+
 // ---------------------------------------------------------------- FWHT
 
 // In-warp fast Walsh-Hadamard transform of a 128-vector held 4 per lane

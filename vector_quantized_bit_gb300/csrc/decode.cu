@@ -222,8 +222,9 @@ __device__ __noinline__ void append_rows(uint2 raw, float4 s, uint8_t* k_stream,
 }
 
 // MULTI: several queries per sequence (per-column causal limits); the
-// single-query instantiation keeps one limit, L, for every column.
-template <bool MULTI>
+// single-query instantiation keeps one limit, L, for every column.  PAGED:
+// tiles are found through the block table (one bulk copy per tile).
+template <bool MULTI, bool PAGED>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
@@ -266,8 +267,6 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
-      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
       // super-tiles of V2_TPI tiles: this warp takes k = warp + j * V2_WARPS,
       // j < n_mine, starting at tile t_begin + k * V2_TPI.  The split length is
       // a multiple of V2_TPI, so a super-tile never reaches into the next split;
@@ -279,11 +278,23 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       auto issue = [&](int j) {
         const uint32_t st = (uses + j) % V2_STAGES;
         const int tile0 = t_begin + (warp + j * V2_WARPS) * V2_TPI;
-        const uint32_t n = (uint32_t)min(V2_TPI, cap_tiles - tile0) * V2_TILE_BYTES;
-        const size_t off = (size_t)tile0 * V2_TILE_BYTES;
-        mbar_expect_tx(mbar + 8 * st, 2 * n);
-        tma_load_1d(ring + st * V2_STAGE_BYTES, kbase + off, n, mbar + 8 * st);
-        tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, vbase + off, n, mbar + 8 * st);
+        const int nt = min(V2_TPI, cap_tiles - tile0);
+        mbar_expect_tx(mbar + 8 * st, 2 * (uint32_t)nt * V2_TILE_BYTES);
+        bool bad = false;
+        if (!PAGED) {   // the super-tile is contiguous
+          const long long off = tile_offset<false>(p, b, kvh, tile0, V2_TILE_BYTES, &bad);
+          tma_load_1d(ring + st * V2_STAGE_BYTES, p.kc + off, nt * V2_TILE_BYTES, mbar + 8 * st);
+          tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, p.vc + off, nt * V2_TILE_BYTES,
+                      mbar + 8 * st);
+        } else {
+          for (int i = 0; i < nt; ++i) {
+            const long long off = tile_offset<true>(p, b, kvh, tile0 + i, V2_TILE_BYTES, &bad);
+            tma_load_1d(ring + st * V2_STAGE_BYTES + i * V2_TILE_BYTES, p.kc + off, V2_TILE_BYTES, mbar + 8 * st);
+            tma_load_1d(ring + st * V2_STAGE_BYTES + (V2_TPI + i) * V2_TILE_BYTES, p.vc + off, V2_TILE_BYTES,
+                        mbar + 8 * st);
+          }
+          if (bad) atomicOr(p.err, VQKV_DEVERR_BLOCK);
+        }
       };
       // Fused append: the CTA whose split holds position L - 1 encodes the
       // new rows in its prologue and writes their codes before any copy of
@@ -384,7 +395,7 @@ __device__ __forceinline__ uint32_t pair24(uint32_t w0, uint32_t w1, uint32_t w2
   return w2 >> 8;
 }
 
-template <bool MULTI>
+template <bool MULTI, bool PAGED>
 __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint4* s_kcb = reinterpret_cast<uint4*>(smem);
@@ -417,12 +428,13 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
-      const uint8_t* kbase = p.kc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-      const uint8_t* vbase = p.vc + (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
       // this lane's 48 + 48 code bytes of `tile` into its slot
       auto copy_codes = [&](int tile) {
-        const uint8_t* kp = kbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
-        const uint8_t* vp = vbase + (size_t)tile * V15_TILE_BYTES + lane * 48;
+        bool bad = false;
+        const long long off = tile_offset<PAGED>(p, b, kvh, tile, V15_TILE_BYTES, &bad) + lane * 48;
+        if (PAGED && bad && lane == 0) atomicOr(p.err, VQKV_DEVERR_BLOCK);
+        const uint8_t* kp = p.kc + off;
+        const uint8_t* vp = p.vc + off;
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           cp_async16(slot + 16 * i, kp + 16 * i, 16);
@@ -556,29 +568,37 @@ int decode_threads(int mode) { return mode == VQKV_MODE_VQ2 ? V2_THREADS : V15_T
 
 cudaError_t decode_prepare(int mode) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaSuccess;
   if (mode == VQKV_MODE_VQ2) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_vq2_kernel<false>, a, (int)kV2Smem);
-    return e != cudaSuccess ? e : cudaFuncSetAttribute(decode_vq2_kernel<true>, a, (int)kV2Smem);
+    for (auto k : {decode_vq2_kernel<false, false>, decode_vq2_kernel<true, false>, decode_vq2_kernel<false, true>,
+                   decode_vq2_kernel<true, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV2Smem);
+    return e;
   }
-  const cudaError_t e = cudaFuncSetAttribute(decode_vq15_kernel<false>, a, (int)kV15Smem);
-  return e != cudaSuccess ? e : cudaFuncSetAttribute(decode_vq15_kernel<true>, a, (int)kV15Smem);
+  for (auto k : {decode_vq15_kernel<false, false>, decode_vq15_kernel<true, false>, decode_vq15_kernel<false, true>,
+                 decode_vq15_kernel<true, true>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV15Smem);
+  return e;
 }
 
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<false>, V2_THREADS,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<false, false>, V2_THREADS,
                                                          kV2Smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<false>, V15_THREADS,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<false, false>, V15_THREADS,
                                                        kV15Smem);
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  const bool multi = p.M > 1;
-  if (mode == VQKV_MODE_VQ2)
-    return launch_pdl(multi ? decode_vq2_kernel<true> : decode_vq2_kernel<false>, grid, dim3(V2_THREADS), kV2Smem,
-                      stream, p);
-  return launch_pdl(multi ? decode_vq15_kernel<true> : decode_vq15_kernel<false>, grid, dim3(V15_THREADS),
-                    kV15Smem, stream, p);
+  const bool multi = p.M > 1, paged = p.block_table != nullptr;
+  if (mode == VQKV_MODE_VQ2) {
+    auto k = paged ? (multi ? decode_vq2_kernel<true, true> : decode_vq2_kernel<false, true>)
+                   : (multi ? decode_vq2_kernel<true, false> : decode_vq2_kernel<false, false>);
+    return launch_pdl(k, grid, dim3(V2_THREADS), kV2Smem, stream, p);
+  }
+  auto k = paged ? (multi ? decode_vq15_kernel<true, true> : decode_vq15_kernel<false, true>)
+                 : (multi ? decode_vq15_kernel<true, false> : decode_vq15_kernel<false, false>);
+  return launch_pdl(k, grid, dim3(V15_THREADS), kV15Smem, stream, p);
 }
 
 }  // namespace vqkv

@@ -21,6 +21,21 @@ namespace {
 constexpr int ENC_WARPS = 8;
 constexpr int ENC_THREADS = ENC_WARPS * 32;
 
+// First byte of the tile holding token t of stream (b, kvh) (tiles of
+// `tile_tokens` tokens, `tile_bytes` bytes), contiguous or through the block
+// table; nullptr (and the error bit) for a block id outside the pool.
+__device__ __forceinline__ uint8_t* tile_base(const EncodeParams& p, int b, int kvh, int t, int tile_tokens,
+                                              int tile_bytes) {
+  bool bad = false;
+  const long long off = p.block_table ? tile_offset<true>(p, b, kvh, t / tile_tokens, tile_bytes, &bad)
+                                      : tile_offset<false>(p, b, kvh, t / tile_tokens, tile_bytes, &bad);
+  if (bad) {
+    if (p.err) atomicOr(p.err, VQKV_DEVERR_BLOCK);
+    return nullptr;
+  }
+  return p.codes + off;
+}
+
 // Smoothing factors of KV head kvh for keys, nullptr for values.
 __device__ __forceinline__ const float* key_s(const EncodeParams& p, int kvh) {
   return p.role == VQKV_ROLE_K ? p.s + (size_t)kvh * kHeadDim : nullptr;
@@ -64,7 +79,8 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
     Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
     if (SPLIT == 1 || warp == 0) {
       count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
-      p.codes[((long long)b * p.Hkv + kvh) * p.stream_bytes + vq2_code_offset(p.role, t, lane)] = (uint8_t)bst.i;
+      uint8_t* tb = tile_base(p, b, kvh, t, 16, 512);
+      if (tb) tb[vq2_code_offset(p.role, t & 15, lane)] = (uint8_t)bst.i;
     }
   }
 }
@@ -266,9 +282,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
     count_near_ties(p.near_tie, tie[0], lane, 0x11111111u);
     count_near_ties(p.near_tie, tie[1], lane, 0x11111111u);
     // lane (gid, tig 0) holds the pair (gid, gid+8) of this token
-    if (tig == 0)
-      store_pair(p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + vq15_pair_offset(p.role, t, gid), code[0],
-                 code[1]);
+    if (tig == 0) {
+      uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
+      if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, gid), code[0], code[1]);
+    }
   }
 }
 
@@ -404,9 +421,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
         for (int w = 1; w < TC_WARPS; ++w) m = best_merge(m, s_fin[w * 16 + j]);
       count_near_ties(p.near_tie, is_near_tie(m.d, m.s), lane, 0x0000ffffu);
       const int hi = __shfl_down_sync(0xffffffffu, m.i, 8);
-      if (lane < 8)
-        store_pair(p.codes + ((long long)b * p.Hkv + kvh) * p.stream_bytes + vq15_pair_offset(p.role, t, lane), m.i,
-                   hi);
+      if (lane < 8) {
+        uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
+        if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, lane), m.i, hi);
+      }
     }
     __syncthreads();   // s_x, s_hidden and s_fin are reused by the next row
   }

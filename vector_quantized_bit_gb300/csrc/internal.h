@@ -39,6 +39,10 @@ struct DecodeParams {
   uint8_t* kc_w = nullptr;  // the same caches as kc / vc, written by the append
   uint8_t* vc_w = nullptr;
   unsigned long long* near_tie = nullptr;
+  // Paged cache (vqkv_decode_attn_paged): block table or nullptr.
+  const int32_t* block_table = nullptr;
+  int max_blocks = 0, block_tiles = 0, num_blocks = 0;
+  long long block_bytes = 0;
 };
 
 constexpr int kPartialStride = 130;  // O[128], m, l
@@ -53,6 +57,10 @@ struct EncodeParams {
   unsigned* err;
   long long stream_bytes;
   int B, Hkv, n_rows, cap_len, role;
+  // Paged cache (vqkv_encode_paged): block table or nullptr.
+  const int32_t* block_table = nullptr;
+  int max_blocks = 0, block_tiles = 0, num_blocks = 0;
+  long long block_bytes = 0;
 };
 
 // Decode kernels (decode.cu).  tile_tokens: 16 (VQ2) / 64 (VQ15).
