@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--queries", type=int, default=1,
                     help="queries per sequence (multi-query decode, e.g. speculative decoding): a step encodes "
                          "that many new K/V rows per sequence and runs vqkv_decode_attn_multi")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_TOKENS",
+                    help="keep the cache in a pool of blocks of this many tokens behind a shuffled block table "
+                         "(vqkv_encode_paged / vqkv_decode_attn_paged)")
     ap.add_argument("--unfused", action="store_true",
                     help="2-bit: run a step as vqkv_encode (K) + vqkv_encode (V) + vqkv_decode_attn instead of "
                          "the fused vqkv_decode_append")
@@ -299,7 +302,7 @@ def run_ours(args):
     w = synth.WORKLOADS[args.workload]
     if args.mode is not None:
         w = w.with_mode(args.mode)
-    headline = args.workload == WORKLOAD_ID and w.mode == synth.MODE_VQ2 and args.queries == 1
+    headline = args.workload == WORKLOAD_ID and w.mode == synth.MODE_VQ2 and args.queries == 1 and not args.paged
     lens = synth.seq_lens(w)
     if headline:
         s_h, kcb_h, vcb_h, kv = host_workload(w)
@@ -323,14 +326,33 @@ def run_ours(args):
     s = torch.from_numpy(s_h).to(dev)
     kcb = torch.from_numpy(kcb_h).to(dev)
     vcb = torch.from_numpy(vcb_h).to(dev)
-    kcodes = torch.zeros((w.B, w.Hkv, sb), dtype=torch.uint8, device=dev)
+    BT = args.paged
+    if BT:
+        if args.queries != 1 or cap % BT:
+            raise SystemExit("--paged needs one query per sequence and a capacity that is a multiple of the block")
+        max_blocks = cap // BT
+        num_blocks = w.B * max_blocks
+        table = torch.from_numpy(np.random.default_rng([w.seed, w.config_id, 77]).permutation(num_blocks)
+                                 .reshape(w.B, max_blocks).astype(np.int32)).to(dev)
+        kcodes = torch.zeros((num_blocks, w.Hkv, _lib.vqkv_code_bytes(mode, BT)), dtype=torch.uint8, device=dev)
+    else:
+        kcodes = torch.zeros((w.B, w.Hkv, sb), dtype=torch.uint8, device=dev)
     vcodes = torch.zeros_like(kcodes)
+
+    def encode(role, x, pos_, codes):
+        cb = kcb if role == 0 else vcb
+        if BT:
+            _lib.vqkv_encode_paged(mode, role, x, pos_, s if role == 0 else None, cb, codes, cap, table, BT,
+                                   num_blocks)
+        else:
+            _lib.vqkv_encode(mode, role, x, pos_, s if role == 0 else None, cb, codes, cap)
+
     zeros = torch.zeros(w.B, dtype=torch.int32, device=dev)
     if kv is not None:
         # encode the whole cache (all KV heads, all positions) in one call per K / V
-        for role, cb, codes in ((0, kcb, kcodes), (1, vcb, vcodes)):
+        for role, codes in ((0, kcodes), (1, vcodes)):
             x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
-            _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, cb, codes, cap)
+            encode(role, x, zeros, codes)
             del x
     else:
         # other workloads: seeded uniform codes (decode cost does not depend on code values)
@@ -368,18 +390,21 @@ def run_ours(args):
     n_splits = _lib.vqkv_decode_num_splits(dargs)
     dec_kernels = _lib.vqkv_decode_kernel_count(dargs)
 
-    fused = mode == synth.MODE_VQ2 and not args.unfused and M == 1
+    fused = mode == synth.MODE_VQ2 and not args.unfused and M == 1 and not BT
 
     def decode_only(kc, vc):
-        if M == 1:
+        if BT:
+            _lib.vqkv_decode_attn_paged(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len, table, BT,
+                                        num_blocks)
+        elif M == 1:
             _lib.vqkv_decode_attn(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
         else:
             _lib.vqkv_decode_attn_multi(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len)
 
     def step_unfused(i, ev=None):
         kc, vc = copies[i % n_copies]
-        _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
-        _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
+        encode(0, new_k, pos, kc)
+        encode(1, new_v, pos, vc)
         if ev is not None:
             ev[0].record()
         decode_only(kc, vc)
@@ -514,7 +539,7 @@ def run_ours(args):
     nk_host = new_k.cpu().pin_memory()
     nv_host = new_v.cpu().pin_memory()
     o_host = torch.empty(tuple(out.shape), dtype=torch.float16).pin_memory()
-    fp16 = None if args.profile_steps or M > 1 else fp16_baseline(w, kv_fp16, lens, dev, stream)
+    fp16 = None if args.profile_steps or M > 1 or BT else fp16_baseline(w, kv_fp16, lens, dev, stream)
     del kv_fp16
     e2e_steps = max(20, min(args.steps, 2000))
     with torch.cuda.stream(stream):
@@ -526,8 +551,8 @@ def run_ours(args):
             if fused:
                 _lib.vqkv_decode_append(mode, q, kc, vc, seq, kcb, vcb, s, out, ws, cap, max_len, new_k, new_v)
             else:
-                _lib.vqkv_encode(mode, 0, new_k, pos, s, kcb, kc, cap)
-                _lib.vqkv_encode(mode, 1, new_v, pos, None, vcb, vc, cap)
+                encode(0, new_k, pos, kc)
+                encode(1, new_v, pos, vc)
                 decode_only(kc, vc)
             o_host.copy_(out, non_blocking=True)
             stream.synchronize()
@@ -558,12 +583,14 @@ def run_ours(args):
     line = {
         "metric": METRIC if headline else f"decode-attn KV tokens/s and HBM GB/s ({w.name}, "
                                                  f"{'2' if w.mode == 0 else '1.5'}-bit"
-                                                 f"{f', {M} queries per sequence' if M > 1 else ''})",
+                                                 f"{f', {M} queries per sequence' if M > 1 else ''}"
+                                                 f"{f', paged cache ({BT}-token blocks)' if BT else ''})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
                    "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits, "queries_per_sequence": M,
+                   "paged_block_tokens": BT or None,
                    "step": ("vqkv_decode_append: 1 new K row + 1 new V row per sequence encoded into the cache "
                             "and attended in the same kernel" if fused else
                             "vqkv_encode (1 new K row per sequence), vqkv_encode (V), vqkv_decode_attn"),

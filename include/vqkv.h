@@ -259,7 +259,7 @@ vqkv_status vqkv_decode_attn_multi(const vqkv_decode_multi_args* args, void* str
 typedef struct {
   const int32_t* block_table; /* device [B][max_blocks], 4-byte aligned */
   int32_t max_blocks;         /* entries per sequence, >= 1 */
-  int32_t block_tokens;       /* tokens per block: a positive multiple of 64 */
+  int32_t block_tokens;       /* tokens per block: a power of two, >= 64 */
   int32_t num_blocks;         /* blocks in each pool, >= 1 */
 } vqkv_paging;
 

@@ -170,7 +170,7 @@ def test_decode_multi_validation(lib):
     assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 0    # empty batch: a no-op
 
 
-@pytest.mark.parametrize("kw", [dict(block_tokens=100), dict(block_tokens=0), dict(max_blocks=0),
+@pytest.mark.parametrize("kw", [dict(block_tokens=100), dict(block_tokens=192), dict(block_tokens=0), dict(max_blocks=0),
                                 dict(num_blocks=0), dict(max_blocks=1)])   # 1 x 64 tokens < cap_len 128
 def test_paging_validation(lib, kw):
     pg = _lib.Paging(block_table=0x1000, max_blocks=2, block_tokens=64, num_blocks=4)

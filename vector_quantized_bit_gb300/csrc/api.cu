@@ -87,7 +87,8 @@ vqkv_status validate_decode(const vqkv_decode_args* a) {
 // Block-table arguments of the paged calls: sizes and alignment only.
 vqkv_status validate_paging(const vqkv_paging* pg, int mode, int cap_len) {
   if (pg == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (pg->max_blocks < 1 || pg->num_blocks < 1 || pg->block_tokens < 64 || pg->block_tokens % 64 != 0)
+  if (pg->max_blocks < 1 || pg->num_blocks < 1 || pg->block_tokens < 64 ||
+      (pg->block_tokens & (pg->block_tokens - 1)) != 0)
     return VQKV_ERR_INVALID_ARG;
   if ((long long)pg->max_blocks * pg->block_tokens < cap_len) return VQKV_ERR_INVALID_ARG;
   if ((long long)pg->num_blocks * vqkv_code_bytes(mode, pg->block_tokens) > (1LL << 46)) return VQKV_ERR_INVALID_ARG;
@@ -100,6 +101,8 @@ void set_paging(P& p, const vqkv_paging* pg, int mode) {
   p.block_table = pg->block_table;
   p.max_blocks = pg->max_blocks;
   p.block_tiles = pg->block_tokens / (mode == VQKV_MODE_VQ2 ? 16 : 64);
+  p.block_shift = 0;
+  while ((1 << p.block_shift) < p.block_tiles) ++p.block_shift;
   p.num_blocks = pg->num_blocks;
   p.block_bytes = (long long)vqkv_code_bytes(mode, pg->block_tokens);
 }

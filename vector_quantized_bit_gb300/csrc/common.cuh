@@ -185,12 +185,12 @@ inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
 template <bool PAGED, typename P>
 __device__ __forceinline__ long long tile_offset(const P& p, int b, int kvh, int tile, int tile_bytes, bool* bad) {
   if (!PAGED) return (long long)(b * p.Hkv + kvh) * p.stream_bytes + (long long)tile * tile_bytes;
-  int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + tile / p.block_tiles);
+  int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + (tile >> p.block_shift));
   if (blk < 0 || blk >= p.num_blocks) {
     *bad = true;
     blk = 0;
   }
-  return ((long long)blk * p.Hkv + kvh) * p.block_bytes + (long long)(tile % p.block_tiles) * tile_bytes;
+  return ((long long)blk * p.Hkv + kvh) * p.block_bytes + (long long)(tile & (p.block_tiles - 1)) * tile_bytes;
 }
 
 // ---------------------------------------------------------------- FWHT

@@ -88,7 +88,10 @@ constexpr int V15_Q_OFF = V15_SLOT_OFF + V15_SLOT_BYTES;
 // Fused append (vqkv_decode_append): per-warp partial searches.
 constexpr int V2_APP_OFF = (V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
 constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
-constexpr size_t kV2Smem = V2_APP_OFF + V2_APP_BYTES;
+// Paged cache: the block ids of the CTA's token range, read once per sequence.
+constexpr int V2_BLK_OFF = V2_APP_OFF + V2_APP_BYTES;
+constexpr int V2_BLK_CACHE = 512;
+constexpr size_t kV2Smem = V2_BLK_OFF + V2_BLK_CACHE * 4;
 static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must fit below the ring");
 // The combine area (after the tile loop) and q' (before it) overlap the
 // code slots, which are idle at those times.
@@ -273,6 +276,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // tiles past the sequence end are masked, tiles past the capacity are not
       // copied.
       const int cap_tiles = (int)(p.stream_bytes / V2_TILE_BYTES);
+      const int blk_first = PAGED ? t_begin >> p.block_shift : 0;
+      int* s_blk = reinterpret_cast<int*>(smem + V2_BLK_OFF);
       const int n_super = (t_end - t_begin + V2_TPI - 1) / V2_TPI;
       const int n_mine = warp < n_super ? (n_super - warp + V2_WARPS - 1) / V2_WARPS : 0;
       auto issue = [&](int j) {
@@ -287,15 +292,44 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, p.vc + off, nt * V2_TILE_BYTES,
                       mbar + 8 * st);
         } else {
-          for (int i = 0; i < nt; ++i) {
-            const long long off = tile_offset<true>(p, b, kvh, tile0 + i, V2_TILE_BYTES, &bad);
-            tma_load_1d(ring + st * V2_STAGE_BYTES + i * V2_TILE_BYTES, p.kc + off, V2_TILE_BYTES, mbar + 8 * st);
-            tma_load_1d(ring + st * V2_STAGE_BYTES + (V2_TPI + i) * V2_TILE_BYTES, p.vc + off, V2_TILE_BYTES,
+          // a step spans at most two blocks (nt <= 3 <= block_tiles); block ids
+          // come from the shared-memory list when this split's fit in it
+          static_assert(V2_TPI <= 4, "a step must not span more than two blocks of >= 4 tiles");
+          auto blk_off = [&](int tile) -> long long {
+            const int lb = (tile >> p.block_shift) - blk_first;
+            if (lb < V2_BLK_CACHE) return ((long long)s_blk[lb] * p.Hkv + kvh) * p.block_bytes;
+            bool bb = false;
+            const long long off = tile_offset<true>(p, b, kvh, tile & ~(p.block_tiles - 1), V2_TILE_BYTES, &bb);
+            if (bb) atomicOr(p.err, VQKV_DEVERR_BLOCK);
+            return off;
+          };
+          const int in_blk = tile0 & (p.block_tiles - 1);
+          const int n0 = min(nt, p.block_tiles - in_blk);
+          const long long off0 = blk_off(tile0) + (long long)in_blk * V2_TILE_BYTES;
+          tma_load_1d(ring + st * V2_STAGE_BYTES, p.kc + off0, n0 * V2_TILE_BYTES, mbar + 8 * st);
+          tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, p.vc + off0, n0 * V2_TILE_BYTES,
+                      mbar + 8 * st);
+          if (n0 < nt) {   // the rest starts its next block
+            const long long off1 = blk_off(tile0 + n0);
+            tma_load_1d(ring + st * V2_STAGE_BYTES + n0 * V2_TILE_BYTES, p.kc + off1, (nt - n0) * V2_TILE_BYTES,
                         mbar + 8 * st);
+            tma_load_1d(ring + st * V2_STAGE_BYTES + (V2_TPI + n0) * V2_TILE_BYTES, p.vc + off1,
+                        (nt - n0) * V2_TILE_BYTES, mbar + 8 * st);
           }
-          if (bad) atomicOr(p.err, VQKV_DEVERR_BLOCK);
         }
       };
+      if (PAGED) {   // block ids of this split's tiles, checked once
+        const int n_blk = min(((t_end - 1) >> p.block_shift) - blk_first + 1, V2_BLK_CACHE);
+        for (int i = threadIdx.x; i < n_blk; i += V2_THREADS) {
+          int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + blk_first + i);
+          if (blk < 0 || blk >= p.num_blocks) {
+            atomicOr(p.err, VQKV_DEVERR_BLOCK);
+            blk = 0;
+          }
+          s_blk[i] = blk;
+        }
+        __syncthreads();
+      }
       // Fused append: the CTA whose split holds position L - 1 encodes the
       // new rows in its prologue and writes their codes before any copy of
       // that tile is issued, so the ring reads them like any other code.

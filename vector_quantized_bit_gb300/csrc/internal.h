@@ -41,7 +41,7 @@ struct DecodeParams {
   unsigned long long* near_tie = nullptr;
   // Paged cache (vqkv_decode_attn_paged): block table or nullptr.
   const int32_t* block_table = nullptr;
-  int max_blocks = 0, block_tiles = 0, num_blocks = 0;
+  int max_blocks = 0, block_tiles = 0, block_shift = 0, num_blocks = 0;   // block_tiles = 1 << block_shift
   long long block_bytes = 0;
 };
 
@@ -59,7 +59,7 @@ struct EncodeParams {
   int B, Hkv, n_rows, cap_len, role;
   // Paged cache (vqkv_encode_paged): block table or nullptr.
   const int32_t* block_table = nullptr;
-  int max_blocks = 0, block_tiles = 0, num_blocks = 0;
+  int max_blocks = 0, block_tiles = 0, block_shift = 0, num_blocks = 0;   // block_tiles = 1 << block_shift
   long long block_bytes = 0;
 };
 
