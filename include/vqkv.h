@@ -328,6 +328,17 @@ vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* args, void* strea
  */
 vqkv_status vqkv_decode_attn_static(const vqkv_decode_args* args, void* stream);
 
+/*
+ * vqkv_test_decode_ring_timeout — test hook for the bounded on-chip waits of
+ * the 2-bit decode (not for production use).  It runs vqkv_decode_attn, but
+ * every warp withholds the first bulk copy of its code ring, and every wait
+ * gives up after max_polls polls (1..4096).  So each ring wait runs out.
+ * The call must set VQKV_DEVERR_TIMEOUT in the workspace error word and
+ * complete normally. O is then meaningless, and later calls on the same
+ * context work as usual.  2-bit mode only.
+ */
+vqkv_status vqkv_test_decode_ring_timeout(const vqkv_decode_args* args, uint32_t max_polls, void* stream);
+
 /* Static, never NULL. */
 const char* vqkv_status_string(vqkv_status status);
 

@@ -187,3 +187,10 @@ def test_paging_required_and_empty_batch(lib):
     pg = _lib.Paging(block_table=None, max_blocks=1, block_tokens=64, num_blocks=1)
     assert lib.vqkv_decode_attn_paged(ctypes.byref(_dec()), ctypes.byref(pg), None) == 1   # no table
     assert lib.vqkv_decode_attn_paged(ctypes.byref(_dec(B=0, q=None, out=None)), ctypes.byref(pg), None) == 0
+
+
+def test_ring_timeout_hook_validation(lib):
+    assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=1)), 64, None) == 2   # 2-bit only
+    assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 0, None) == 1
+    assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 5000, None) == 1
+    assert lib.vqkv_test_decode_ring_timeout(None, 64, None) == 1

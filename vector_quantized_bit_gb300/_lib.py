@@ -26,7 +26,7 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
             "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_multi", "vqkv_decode_append",
-            "vqkv_decode_attn_static", "vqkv_encode_paged", "vqkv_decode_attn_paged",
+            "vqkv_decode_attn_static", "vqkv_encode_paged", "vqkv_decode_attn_paged", "vqkv_test_decode_ring_timeout",
             "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -107,6 +107,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_encode.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.c_void_p]
         L.vqkv_decode_attn.restype = ctypes.c_int
         L.vqkv_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_test_decode_ring_timeout.restype = ctypes.c_int
+        L.vqkv_test_decode_ring_timeout.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_uint32, ctypes.c_void_p]
         L.vqkv_encode_paged.restype = ctypes.c_int
         L.vqkv_encode_paged.argtypes = [ctypes.POINTER(EncodeArgs), ctypes.POINTER(Paging), ctypes.c_void_p]
         L.vqkv_decode_attn_paged.restype = ctypes.c_int

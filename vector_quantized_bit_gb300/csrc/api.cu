@@ -221,7 +221,7 @@ vqkv_status decode_validate(const vqkv_decode_args* a) { return validate_decode(
 namespace {
 // Both decode entry points: ap == nullptr for vqkv_decode_attn.
 vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream,
-                          const vqkv_paging* pg = nullptr);
+                          const vqkv_paging* pg = nullptr, unsigned test_polls = 0);
 vqkv_status encode_launch(const vqkv_encode_args* a, void* stream, const vqkv_paging* pg = nullptr);
 }  // namespace
 
@@ -285,7 +285,7 @@ namespace vqkv {
 namespace {
 
 vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream,
-                          const vqkv_paging* pg) {
+                          const vqkv_paging* pg, unsigned test_polls) {
   if (ap != nullptr && a->mode != VQKV_MODE_VQ2) return VQKV_ERR_UNSUPPORTED;
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK) return st;
@@ -343,6 +343,10 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
     p.near_tie = ap->near_tie_count;
   }
   set_paging(p, pg, a->mode);
+  if (test_polls > 0) {
+    p.max_polls = test_polls;
+    p.withhold_first_copy = 1;
+  }
   const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
   if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
   if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -360,6 +364,12 @@ vqkv_status vqkv_encode(const vqkv_encode_args* a, void* stream) { return encode
 vqkv_status vqkv_encode_paged(const vqkv_encode_args* a, const vqkv_paging* pg, void* stream) {
   if (pg == nullptr) return VQKV_ERR_INVALID_ARG;
   return encode_launch(a, stream, pg);
+}
+
+vqkv_status vqkv_test_decode_ring_timeout(const vqkv_decode_args* a, uint32_t max_polls, void* stream) {
+  if (a == nullptr || a->mode != VQKV_MODE_VQ2) return a == nullptr ? VQKV_ERR_INVALID_ARG : VQKV_ERR_UNSUPPORTED;
+  if (max_polls < 1 || max_polls > 4096) return VQKV_ERR_INVALID_ARG;
+  return decode_launch(a, nullptr, 1, stream, nullptr, max_polls);
 }
 
 vqkv_status vqkv_decode_attn_paged(const vqkv_decode_args* a, const vqkv_paging* pg, void* stream) {

@@ -68,7 +68,6 @@ constexpr int V2_STAGE_BYTES = 2 * V2_TPI * V2_TILE_BYTES;
 constexpr int V2_RING_OFF = V2_Q_OFF + 8 * 128 * 4;
 constexpr int V2_RING_BYTES = V2_WARPS * V2_STAGES * V2_STAGE_BYTES;
 constexpr int V2_MBAR_OFF = V2_RING_OFF + V2_RING_BYTES;
-constexpr uint32_t kMaxPolls = 1u << 22;            // bounded mbarrier waits
 
 // ------------------------------------------------------------------ VQ15
 constexpr int V15_WARPS = 16;
@@ -340,7 +339,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // start the ring before the prologue so the copies overlap it (after
       // the append for the one warp whose first copies hold the new token)
       if (lane == 0 && !late_start)
-        for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
+        for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
+          if (!(p.withhold_first_copy && j == 0)) issue(j);
       // the new rows' loads overlap the codebook fill
       uint2 xraw = make_uint2(0u, 0u);
       float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -367,7 +367,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         append_rows(xraw, xs, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
                     reinterpret_cast<Best*>(smem + V2_APP_OFF));
         if (lane == 0 && late_start)
-          for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j) issue(j);
+          for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
+            if (!(p.withhold_first_copy && j == 0)) issue(j);
       }
       // A operand of the score MMA: head gid, channels 4j..4j+3 of j = 4s+tig
       uint32_t qa[8][2];
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       for (int j = 0; j < n_mine; ++j) {
         const uint32_t st = (uses + j) % V2_STAGES;
         const uint32_t par = ((uses + j) / V2_STAGES) & 1u;
-        if (!mbar_wait_bounded(mbar + 8 * st, par, kMaxPolls)) {
+        if (!mbar_wait_bounded(mbar + 8 * st, par, p.max_polls)) {
           timed_out = true;
           break;
         }
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         // ring is reused or the CTA exits, and report the failure
         for (int j = 0; j < n_mine && j < V2_STAGES; ++j) {
           const uint32_t st = (uses + n_mine - 1 - j) % V2_STAGES;
-          mbar_wait_bounded(mbar + 8 * st, ((uses + n_mine - 1 - j) / V2_STAGES) & 1u, kMaxPolls);
+          mbar_wait_bounded(mbar + 8 * st, ((uses + n_mine - 1 - j) / V2_STAGES) & 1u, p.max_polls);
         }
         if (lane == 0) atomicOr(p.err, VQKV_DEVERR_TIMEOUT);
       }

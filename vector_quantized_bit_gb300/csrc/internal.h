@@ -43,6 +43,10 @@ struct DecodeParams {
   const int32_t* block_table = nullptr;
   int max_blocks = 0, block_tiles = 0, block_shift = 0, num_blocks = 0;   // block_tiles = 1 << block_shift
   long long block_bytes = 0;
+  // Bounded waits of the 2-bit ring: polls before a wait gives up.  The
+  // timeout test withholds every warp's first bulk copy so its waits run out.
+  unsigned max_polls = 1u << 22;
+  int withhold_first_copy = 0;
 };
 
 constexpr int kPartialStride = 130;  // O[128], m, l
