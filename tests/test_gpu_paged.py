@@ -109,3 +109,44 @@ def test_block_ids_outside_the_pool_are_reported(mode):
     t.cuda.synchronize()
     assert int(ws[:4].view(t.int32).item()) & _lib.VQKV_DEVERR_BLOCK
     assert np.isfinite(out.cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("mode,block_tokens", [(0, 64), (0, 256), (1, 64)])
+def test_table_entries_past_the_sequence_are_not_read(mode, block_tokens):
+    """Serving engines leave the entries after a sequence's last block
+    unset: they must not be read (no error bit), and O must equal the
+    contiguous decode's."""
+    t = H.torch()
+    r = np.random.default_rng(40 + mode)
+    B, Hq, Hkv, cap, lens = 2, 8, 2, 1024, [700, 1]
+    E, dsub = vo.GEOMETRY[mode]
+    s, kcb, vcb = H.random_codebooks(mode, Hkv, 41)
+    max_blocks = cap // block_tokens
+    num_blocks = B * max_blocks
+    table = r.permutation(num_blocks).reshape(B, max_blocks).astype(np.int32)
+    for b in range(B):
+        table[b, -(-lens[b] // block_tokens):] = -1          # unset entries
+    kc = [[r.integers(0, E, size=(cap, 128 // dsub)) for _ in range(Hkv)] for _ in range(B)]
+    vc = [[r.integers(0, E, size=(cap, 128 // dsub)) for _ in range(Hkv)] for _ in range(B)]
+    streams = [H.pack_cache_role(mode, role, c, cap) for role, c in ((0, kc), (1, vc))]
+    bb = vo.code_bytes(mode, block_tokens)
+    pools = []
+    for st in streams:
+        pool = np.zeros((num_blocks, Hkv, bb), dtype=np.uint8)
+        for b in range(B):
+            for i in range(max_blocks):
+                if table[b, i] >= 0:
+                    pool[table[b, i]] = st[b, :, i * bb:(i + 1) * bb]
+        pools.append(H.dev(pool))
+    q = r.standard_normal((B, Hq, 128)).astype(np.float16)
+    out = t.full((B, Hq, 128), float("nan"), dtype=t.float16, device="cuda")
+    ws = _lib.decode_workspace(mode, B, Hq, Hkv, cap, cap)
+    for num_splits in (0, 7):
+        ws[:4] = 0
+        _lib.vqkv_decode_attn_paged(mode, H.dev(q), pools[0], pools[1], H.dev(np.asarray(lens, dtype=np.int32)),
+                                    H.dev(kcb), H.dev(vcb), H.dev(s), out, ws, cap, cap, H.dev(table), block_tokens,
+                                    num_blocks, num_splits=num_splits)
+        t.cuda.synchronize()
+        assert int(ws[:4].view(t.int32).item()) == 0
+        o_contig = H.gpu_decode(mode, q, streams[0], streams[1], lens, kcb, vcb, s, cap, cap, num_splits=num_splits)
+        assert np.array_equal(out.cpu().numpy(), o_contig)

@@ -276,13 +276,17 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // copied.
       const int cap_tiles = (int)(p.stream_bytes / V2_TILE_BYTES);
       const int blk_first = PAGED ? t_begin >> p.block_shift : 0;
+      // blocks of this split's tiles [t_begin, t_end) held in s_blk
+      const int n_blk = PAGED ? min(((t_end - 1) >> p.block_shift) - blk_first + 1, V2_BLK_CACHE) : 0;
       int* s_blk = reinterpret_cast<int*>(smem + V2_BLK_OFF);
       const int n_super = (t_end - t_begin + V2_TPI - 1) / V2_TPI;
       const int n_mine = warp < n_super ? (n_super - warp + V2_WARPS - 1) / V2_WARPS : 0;
       auto issue = [&](int j) {
         const uint32_t st = (uses + j) % V2_STAGES;
         const int tile0 = t_begin + (warp + j * V2_WARPS) * V2_TPI;
-        const int nt = min(V2_TPI, cap_tiles - tile0);
+        // paged: never past the sequence's last tile, whose table entries
+        // beyond it need not be valid (those slots are masked anyway)
+        const int nt = min(V2_TPI, (PAGED ? t_end : cap_tiles) - tile0);
         mbar_expect_tx(mbar + 8 * st, 2 * (uint32_t)nt * V2_TILE_BYTES);
         bool bad = false;
         if (!PAGED) {   // the super-tile is contiguous
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           static_assert(V2_TPI <= 4, "a step must not span more than two blocks of >= 4 tiles");
           auto blk_off = [&](int tile) -> long long {
             const int lb = (tile >> p.block_shift) - blk_first;
-            if (lb < V2_BLK_CACHE) return ((long long)s_blk[lb] * p.Hkv + kvh) * p.block_bytes;
+            if (lb < n_blk) return ((long long)s_blk[lb] * p.Hkv + kvh) * p.block_bytes;
             bool bb = false;
             const long long off = tile_offset<true>(p, b, kvh, tile & ~(p.block_tiles - 1), V2_TILE_BYTES, &bb);
             if (bb) atomicOr(p.err, VQKV_DEVERR_BLOCK);
@@ -318,7 +322,6 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         }
       };
       if (PAGED) {   // block ids of this split's tiles, checked once
-        const int n_blk = min(((t_end - 1) >> p.block_shift) - blk_first + 1, V2_BLK_CACHE);
         for (int i = threadIdx.x; i < n_blk; i += V2_THREADS) {
           int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + blk_first + i);
           if (blk < 0 || blk >= p.num_blocks) {

@@ -89,13 +89,15 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
 // ------------------------------------------------------------------ VQ15, tensor-core screening
 // Many rows of 1.5-bit encode: the distance search against 4096 centroids is
 // a dense contraction, run as one augmented mma.m16n8k16 per 8 centroids:
-//   A[j] = [x~_j (8 ch), 1, |x~_j|^2, 0...]   (16 subvectors of a row; x~ = fp16(x'))
-//   B[c] = [-2 c (8 ch), |c|^2, 1, 0...]
-//   D[j][c] = |x~_j|^2 + |c|^2 - 2 x~_j.c      (screened squared distance, fp32)
+//   A[j] = [x_hi (8 ch), 1, 1, 0...] and [x_lo (8 ch), 0...]  (16 subvectors
+//          of a row; x' = x_hi + x_lo in fp16 to ~2^-22)
+//   B[c] = [-2 c (8 ch), |c|^2_hi, |c|^2_lo, 0...]
+//   D[j][c] = |c|^2 - 2 x'_j.c  (two MMAs; the squared distance less the
+//          per-subvector constant |x'_j|^2, which does not change a ranking)
 // Each lane keeps the best and second-best screened distance of its
 // centroid columns.  A centroid whose screened distance is within 2*eps of
 // the best can be the exact nearest, where eps bounds the screening error
-// (fp16 rounding of x' and |c|^2, fp32 accumulation); those candidates are
+// (screen_eps); those candidates are
 // re-ranked with exact fp32 direct differences (channel order 0..7, one
 // rounding per operation), so every decision equals the exhaustive fp32
 // search's.  If a lane's second-best is also
@@ -105,6 +107,26 @@ constexpr int TC_WARPS = 16;
 constexpr int TC_THREADS = TC_WARPS * 32;
 constexpr int TC_TABLE_BYTES = 4096 * 4 * 8;                 // [centroid][tig]{b0b1, b2b3}
 constexpr size_t kTcSmem = TC_TABLE_BYTES + TC_WARPS * (128 + 16) * 4 + 16;
+
+// fp16 hi and lo parts of two fp32 values: a ~= hi.x + lo.x to about 2^-22
+// relative (lo may be subnormal: then to about 6e-8 absolute).
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const __half2 l = __floats2half2_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Bound on |screened - exact| for one candidate of a subvector with norm
+// xnorm, centroid norms <= cmax: the hi/lo splits of x and |c|^2 leave
+// ~2^-22 relative (plus fp16 subnormal steps), and the tensor-core fp32
+// accumulation and the exact search's own fp32 roundings stay well inside
+// 1.5e-5 (|x| + cmax)^2.
+__device__ __forceinline__ float screen_eps(float xnorm, float cmax) {
+  const float sc = xnorm + cmax;
+  return 9.5367431640625e-7f * xnorm * cmax + 4.76837158203125e-7f * cmax * cmax + 1e-6f * (cmax + 1.f) +
+         1.5e-5f * sc * sc;
+}
 
 __device__ __forceinline__ void top2_push(float v, int n, float& b1, float& b2, int& i1) {
   const bool lt = v < b1;
@@ -158,7 +180,8 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
       const __half2 m2 = __floats2half2_rn(-2.f * a, -2.f * b);   // exact
       s_tbl[c * 4 + t].x = *reinterpret_cast<const uint32_t*>(&m2);
     }
-    const __half2 tail = __floats2half2_rn(nn, 1.f);
+    const __half nh = __float2half_rn(nn);   // |c|^2 as fp16 hi + lo
+    const __half2 tail = __halves2half2(nh, __float2half_rn(nn - __half2float(nh)));
     s_tbl[c * 4 + 0].y = *reinterpret_cast<const uint32_t*>(&tail);
     s_tbl[c * 4 + 1].y = s_tbl[c * 4 + 2].y = s_tbl[c * 4 + 3].y = 0u;
     cmax = fmaxf(cmax, sqrtf(nn));
@@ -207,9 +230,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
     // A fragments: subvectors gid (a0a1, a4a5) and gid+8 (a2a3, a6a7)
     const float2 xa = *reinterpret_cast<const float2*>(wx + 8 * gid + 2 * tig);
     const float2 xb = *reinterpret_cast<const float2*>(wx + 8 * (gid + 8) + 2 * tig);
-    const uint32_t a0 = pack_half2(xa.x, xa.y), a1 = pack_half2(xb.x, xb.y);
-    const uint32_t a2 = tig == 0 ? pack_half2(1.f, wxn[gid]) : 0u;
-    const uint32_t a3 = tig == 0 ? pack_half2(1.f, wxn[gid + 8]) : 0u;
+    uint32_t a0, a0l, a1, a1l;
+    split_half2(xa.x, xa.y, a0, a0l);
+    split_half2(xb.x, xb.y, a1, a1l);
+    const uint32_t a2 = tig == 0 ? pack_half2(1.f, 1.f) : 0u;   // picks |c|^2 hi + lo
+    const uint32_t a3 = a2;
 
     float b1a = __int_as_float(0x7f800000), b2a = b1a, b1b = b1a, b2b = b1a;
     int i1a = 0, i1b = 0;
@@ -218,6 +243,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
       const uint2 bf = lds64(tbl_lane + n0 * 32);
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16816(d, a0, a1, a2, a3, bf.x, bf.y);
+      mma_16816(d, a0l, a1l, 0u, 0u, bf.x, bf.y);
       const int c0 = n0 + 2 * tig;
       top2_push(d[0], c0, b1a, b2a, i1a);
       top2_push(d[1], c0 + 1, b1a, b2a, i1a);
@@ -236,8 +262,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const Enc
       best = fminf(best, __shfl_xor_sync(0xffffffffu, best, 1));
       best = fminf(best, __shfl_xor_sync(0xffffffffu, best, 2));
       const float xnorm = sqrtf(wxn[j]);
-      const float sc = xnorm + Cmax;
-      const float eps = 9.765625e-4f * xnorm * Cmax + 4.8828125e-4f * Cmax * Cmax + 1.5e-5f * sc * sc;
+      const float eps = screen_eps(xnorm, Cmax);
       const float thr = best + 2.f * eps;
       const bool hidden = b2 <= thr;   // a third candidate of this lane may be within the margin
       const bool any_hidden = ((__ballot_sync(0xffffffffu, hidden) >> (4 * gid)) & 0xfu) != 0;
@@ -351,9 +376,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
     __syncthreads();
     const float2 xa = *reinterpret_cast<const float2*>(s_x + 8 * gid + 2 * tig);
     const float2 xb = *reinterpret_cast<const float2*>(s_x + 8 * (gid + 8) + 2 * tig);
-    const uint32_t a0 = pack_half2(xa.x, xa.y), a1 = pack_half2(xb.x, xb.y);
-    const uint32_t a2 = tig == 0 ? pack_half2(1.f, s_xn[gid]) : 0u;
-    const uint32_t a3 = tig == 0 ? pack_half2(1.f, s_xn[gid + 8]) : 0u;
+    uint32_t a0, a0l, a1, a1l;
+    split_half2(xa.x, xa.y, a0, a0l);
+    split_half2(xb.x, xb.y, a1, a1l);
+    const uint32_t a2 = tig == 0 ? pack_half2(1.f, 1.f) : 0u;   // picks |c|^2 hi + lo
+    const uint32_t a3 = a2;
     float b1[2] = {inf, inf}, b2[2] = {inf, inf};
     int i1[2] = {0, 0};
     const int c_lo = warp * (4096 / TC_WARPS);
@@ -362,6 +389,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
       const uint2 bf = lds64(tbl_lane + n0 * 32);
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16816(d, a0, a1, a2, a3, bf.x, bf.y);
+      mma_16816(d, a0l, a1l, 0u, 0u, bf.x, bf.y);
       const int c0 = n0 + 2 * tig;
       top2_push(d[0], c0, b1[0], b2[0], i1[0]);
       top2_push(d[1], c0 + 1, b1[0], b2[0], i1[0]);
@@ -385,8 +413,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
 #pragma unroll 4
       for (int w = 0; w < TC_WARPS; ++w) best = fminf(best, s_red[w * 16 + j]);
       const float xnorm = sqrtf(s_xn[j]);
-      const float sc = xnorm + Cmax;
-      const float eps = 9.765625e-4f * xnorm * Cmax + 4.8828125e-4f * Cmax * Cmax + 1.5e-5f * sc * sc;
+      const float eps = screen_eps(xnorm, Cmax);
       const float thr = best + 2.f * eps;
       if (b2[h] <= thr) atomicOr(&s_hidden[j], 1);   // a third candidate may hide in this slice
       cand[h] = {inf, inf, 0x7fffffff};
