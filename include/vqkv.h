@@ -225,9 +225,10 @@ vqkv_status vqkv_decode_append(const vqkv_decode_append_args* args, void* stream
  * decode.q and decode.out are fp16 [B][M][Hq][128].  Query m of sequence b
  * is the token at position L - M + m (L = seq_lens[b], clamped as in
  * vqkv_decode_attn) and attends causally: it sees the cached tokens
- * t <= L - M + m, and is a zero row when it sees none.  Each code is read
- * once for all M x (Hq / Hkv) queries of its KV head.  M * (Hq / Hkv) <= 8
- * (VQKV_ERR_UNSUPPORTED otherwise).  The workspace must hold
+ * t <= L - M + m, and is a zero row when it sees none.  The M x (Hq / Hkv)
+ * queries of a KV head are its softmax columns; each group of up to 8
+ * columns shares every code it reads (one CTA per group and token range).
+ * M * (Hq / Hkv) <= 64 (VQKV_ERR_UNSUPPORTED otherwise).  The workspace must hold
  * n_queries * vqkv_decode_workspace_bytes(&args->decode) bytes; everything
  * else is as in vqkv_decode_attn, which is this call with n_queries = 1.
  */

@@ -162,8 +162,8 @@ def test_decode_multi_validation(lib):
     a.decode = _dec(Hq=4, Hkv=1)
     a.n_queries = 0
     assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 1    # at least one query
-    a.n_queries = 3
-    assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 2    # 3 queries x 4 heads > 8 columns
+    a.n_queries = 17
+    assert lib.vqkv_decode_attn_multi(ctypes.byref(a), None) == 2    # 17 queries x 4 heads > 64 columns
     assert lib.vqkv_decode_attn_multi(None, None) == 1
     a.decode = _dec(B=0, q=None, out=None)
     a.n_queries = 2

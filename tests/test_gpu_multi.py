@@ -51,6 +51,10 @@ CASES = [
     (0, 1, 4, 1, 2, [2000], 2048, 125),        # many splits: the causal tail in one late CTA
     (1, 2, 8, 4, 4, [300, 64], 320, 0),        # 1.5 bit, several sequences per CTA (deferred merge)
     (1, 1, 1, 1, 8, [1000], 1024, 3),         # one head, 8 queries
+    (0, 1, 8, 2, 4, [1000], 1024, 0),         # 4 queries x 4 heads: two column groups of 8
+    (0, 2, 8, 2, 3, [517, 2], 768, 5),        # 12 columns: groups of 8 and 4; a sequence shorter than M
+    (1, 2, 8, 2, 4, [300, 64], 320, 0),       # 1.5 bit, two column groups, deferred merge
+    (0, 1, 32, 8, 6, [2000], 2048, 0),        # Llama-like: 6 queries x 4 heads, three groups
 ]
 
 

@@ -112,7 +112,7 @@ size_t decode_ticket_region_bytes(int B, int Hkv);
 namespace {
 
 struct DecodePlan {
-  int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1;
+  int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1, cgroups = 1;
   size_t tickets_off = 0, partials_off = 0, ws_bytes = 0;
 };
 
@@ -141,7 +141,8 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   // across sequences only when the batch alone cannot fill the GPU.
   int bpg = 1;
   if (a->mode == VQKV_MODE_VQ15 && (long long)B * a->Hkv < slots) bpg = B;
-  const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg);
+  const int cgroups = (g * a->M + 7) / 8;   // CTAs per (sequence group, KV head, split)
+  const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg) * cgroups;
   // per-CTA prologue + merge in tile units
   const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 12.0 : (a->mode == VQKV_MODE_VQ15) ? 24.0 : 4.0;
   long long best_n = 1;
@@ -166,8 +167,9 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   pl->n_splits = (int)((tiles_max + tps - 1) / tps);
   pl->bpg = bpg;
   pl->n_bgroups = (B + bpg - 1) / bpg;
+  pl->cgroups = cgroups;
   pl->tickets_off = kWsHeader;
-  pl->partials_off = decode_ticket_region_bytes(B, a->Hkv);
+  pl->partials_off = decode_ticket_region_bytes(B, a->Hkv * cgroups);
   pl->ws_bytes = pl->partials_off +
                  sizeof(float) * (size_t)B * a->Hkv * pl->n_splits * g * a->M * kPartialStride;
   return VQKV_OK;
@@ -294,7 +296,7 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
     if (st != VQKV_OK) return st;
     if (a->B > 0 && (!pg->block_table || !aligned(pg->block_table, 4))) return VQKV_ERR_INVALID_ARG;
   }
-  if ((long long)M * (a->Hq / a->Hkv) > 8) return VQKV_ERR_UNSUPPORTED;   // one 8-column MMA tile
+  if (M > 64 || (long long)M * (a->Hq / a->Hkv) > 64) return VQKV_ERR_UNSUPPORTED;   // <= 8 column groups
   if (ap != nullptr) {
     if (a->B > 0 && (!ap->k_new || !ap->v_new || !aligned(ap->k_new, 8) || !aligned(ap->v_new, 8) ||
                      (ap->near_tie_count && !aligned(ap->near_tie_count, 8))))
@@ -347,7 +349,8 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
     p.max_polls = test_polls;
     p.withhold_first_copy = 1;
   }
-  const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups);
+  p.cgroups = pl.cgroups;
+  const dim3 grid(pl.n_splits, a->Hkv, pl.n_bgroups * pl.cgroups);
   if (launch_decode(a->mode, p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VQKV_ERR_CUDA;
   if (p.defer_merge && p.n_splits > 1 && launch_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VQKV_ERR_CUDA;

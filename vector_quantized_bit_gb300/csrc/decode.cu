@@ -97,12 +97,13 @@ static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must f
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
 static_assert(V15_Q_OFF + 8 * 128 * 4 <= (int)kV15Smem, "q' must fit in the combine area");
 
-// q' of the ncols softmax columns of (b, kvh) into s_qp[c][128] (fp32,
-// scaled), by warps 0..ncols-1.
+// q' of the CTA's softmax columns col0 .. col0 + nloc - 1 of (b, kvh) into
+// s_qp[c - col0][128] (fp32, scaled), by warps 0..nloc-1.
 __device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
-                                                  int lane, float* s_qp) {
-  if (warp < p.ncols) {   // column warp: query warp / g, head warp % g
-    const int m = warp / p.g, hq = kvh * p.g + warp - m * p.g;
+                                                  int lane, float* s_qp, int col0, int nloc) {
+  if (warp < nloc) {   // column col0 + warp: query c / g, head c % g
+    const int c = col0 + warp;
+    const int m = c / p.g, hq = kvh * p.g + c - m * p.g;
     const uint2 qq = *reinterpret_cast<const uint2*>(p.q + (((size_t)b * p.M + m) * p.Hq + hq) * kHeadDim + 4 * lane);
     const float4 ss = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
     const __half2 q01 = *reinterpret_cast<const __half2*>(&qq.x);
@@ -240,8 +241,10 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int b_begin = blockIdx.z * p.bpg;
+  const int b_begin = (MULTI ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
+  // this CTA's softmax columns (column groups only with several queries)
+  const int col0 = MULTI ? cta_col0(p) : 0, nloc = MULTI ? min(8, p.ncols - col0) : p.ncols;
   const uint32_t kbyte = (uint32_t)(lane & 15) << 3;
   const uint32_t vbyte = 128u | ((uint32_t)(lane & 15) << 3);
   // this warp's ring: stage st holds the K super-tile, then the V super-tile
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     const int ntiles = (L + V2_TILE - 1) / V2_TILE;
     const int t_begin = split * p.tps;
     const int t_end = min(t_begin + p.tps, ntiles);
-    const ColumnLimits cl = MULTI ? column_limits(p, L, tig) : ColumnLimits{L, L, L};
+    const ColumnLimits cl = MULTI ? column_limits(p, L, tig, col0) : ColumnLimits{L, L, L};
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll 1
         for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
       }
-      transform_queries(p, b, kvh, warp, lane, s_qp);
+      transform_queries(p, b, kvh, warp, lane, s_qp, col0, nloc);
       __syncthreads();
       if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * s + tig;
-        if (gid < p.ncols) {
+        if (gid < nloc) {
           const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + 4 * j);
           qa[s][0] = pack_half2(v.x, v.y);
           qa[s][1] = pack_half2(v.z, v.w);
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
     stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
     __syncthreads();
-    finish_sequence<V2_WARPS>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V2_WARPS, MULTI>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
@@ -446,8 +449,10 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int b_begin = blockIdx.z * p.bpg;
+  const int b_begin = (MULTI ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
+  // this CTA's softmax columns (column groups only with several queries)
+  const int col0 = MULTI ? cta_col0(p) : 0, nloc = MULTI ? min(8, p.ncols - col0) : p.ncols;
   const uint32_t kcb_s = smem_u32(s_kcb);
   const uint32_t vcb_s = smem_u32(s_vcb);
   bool have_cb = false;
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     const int ntiles = (L + V15_TILE - 1) / V15_TILE;
     const int t_begin = split * p.tps;
     const int t_end = min(t_begin + p.tps, ntiles);
-    const ColumnLimits cl = MULTI ? column_limits(p, L, tig) : ColumnLimits{L, L, L};
+    const ColumnLimits cl = MULTI ? column_limits(p, L, tig, col0) : ColumnLimits{L, L, L};
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -492,14 +497,14 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
         }
         have_cb = true;
       }
-      transform_queries(p, b, kvh, warp, lane, s_qp);
+      transform_queries(p, b, kvh, warp, lane, s_qp, col0, nloc);
       __syncthreads();
       uint32_t qf[8][2];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * (s >> 1) + tig;     // subvector
         const int c = 8 * j + 4 * (s & 1);    // first channel of this half
-        if (gid < p.ncols) {
+        if (gid < nloc) {
           const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + c);
           qf[s][0] = pack_half2(v.x, v.y);
           qf[s][1] = pack_half2(v.z, v.w);
@@ -581,7 +586,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     __syncthreads();   // every warp is done with its code slot: the combine area overlaps them
     stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
     __syncthreads();
-    finish_sequence<V15_WARPS>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V15_WARPS, MULTI>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();
   }
 }

@@ -124,14 +124,15 @@ __device__ __forceinline__ size_t out_row(const DecodeParams& p, int b, int kvh,
   return (((size_t)b * p.M + m) * p.Hq + kvh * p.g + h) * kHeadDim;
 }
 
-// Per-lane visible-token limits of the lane's two softmax columns 2tig and
-// 2tig+1: query m of M sees tokens t < L - M + m + 1 (columns past ncols
-// are padding and see all L).  lim_min is the smallest limit of a real column.
+// Per-lane visible-token limits of the lane's two softmax columns col0 +
+// 2tig and col0 + 2tig + 1 (col0: the CTA's first column): query m of M
+// sees tokens t < L - M + m + 1 (columns past ncols are padding and see all
+// L).  lim_min is the smallest limit of any column.
 struct ColumnLimits {
   int lim0, lim1, lim_min;
 };
-__device__ __forceinline__ ColumnLimits column_limits(const DecodeParams& p, int L, int tig) {
-  const int c0 = 2 * tig, c1 = c0 + 1;
+__device__ __forceinline__ ColumnLimits column_limits(const DecodeParams& p, int L, int tig, int col0) {
+  const int c0 = col0 + 2 * tig, c1 = c0 + 1;
   return {c0 < p.ncols ? L - p.M + c0 / p.g + 1 : L, c1 < p.ncols ? L - p.M + c1 / p.g + 1 : L, L - p.M + 1};
 }
 
@@ -153,15 +154,25 @@ __device__ __forceinline__ void mask_scores(float (&sc)[4], int t0, const Column
 // happen before thread 0's acq_rel ticket increment (CTA barrier, then a
 // cumulative gpu-scope release); the last CTA's acquire and the barrier
 // after it order its partial loads after every other CTA's stores.
-template <int WARPS>
+// The CTA's columns: col0 .. col0 + nloc - 1 of the KV head's ncols
+// (column group blockIdx.z % cgroups).
+__device__ __forceinline__ int cta_col0(const DecodeParams& p) { return 8 * (int)(blockIdx.z % p.cgroups); }
+__device__ __forceinline__ int cta_bgroup(const DecodeParams& p) { return (int)(blockIdx.z / p.cgroups); }
+
+// COLGROUPS: the launch may split the columns into groups (multi-query
+// decode); otherwise the CTA holds all ncols columns.
+template <int WARPS, bool COLGROUPS>
 __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
                                                 float* s_comb, int* s_last) {
   constexpr int NO = (8 * kHeadDim + WARPS * 32 - 1) / (WARPS * 32);   // outputs per thread in the merge
   const float* wO = s_comb;
   const float* wm = s_comb + CombineSmem<WARPS>::kO;
   const float* wl = wm + WARPS * 8;
-  const int G = p.ncols;
-  float* part = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * G * kPartialStride;
+  const int col0 = COLGROUPS ? cta_col0(p) : 0;
+  const int G = COLGROUPS ? min(8, p.ncols - col0) : p.ncols;   // this CTA's columns
+  float* part = p.partials + (((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * p.ncols + col0) * kPartialStride;
+  const unsigned ticket = COLGROUPS ? (unsigned)((b * p.Hkv + kvh) * p.cgroups + blockIdx.z % p.cgroups)
+                                    : (unsigned)(b * p.Hkv + kvh);
   for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
     const int h = e >> 7, d = e & 127;
     float M = kMInit;
@@ -175,7 +186,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
       l += wl[w * 8 + h] * f;
     }
     if (p.n_splits == 1) {
-      p.out[out_row(p, b, kvh, h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+      p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
       continue;
     }
     part[h * kPartialStride + d] = o;
@@ -190,7 +201,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     unsigned prev;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                  : "=r"(prev)
-                 : "l"(p.tickets + b * p.Hkv + kvh)
+                 : "l"(p.tickets + ticket)
                  : "memory");
     *s_last = (prev == (unsigned)(p.n_splits - 1));
   }
@@ -200,14 +211,22 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     // CTA (coalesced, every load in flight at once), then each thread merges
     // one output (head, channel) with a running max.  Chunks of splits when
     // they do not all fit.
-    const float* base = p.partials + (size_t)(b * p.Hkv + kvh) * p.n_splits * G * kPartialStride;
-    const int per_split = G * kPartialStride;
+    const float* base = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits * p.ncols + col0) * kPartialStride;
+    const int per_split = G * kPartialStride;                    // this CTA's columns of one split
+    const size_t split_stride = (size_t)p.ncols * kPartialStride;
     const int chunk = max(1, min(p.n_splits, CombineSmem<WARPS>::kBytes / 4 / per_split));
     float M[NO], O[NO], Ls[NO];
     for (int k = 0; k < NO; ++k) M[k] = kMInit, O[k] = 0.f, Ls[k] = 0.f;
     for (int s0 = 0; s0 < p.n_splits; s0 += chunk) {
       const int ns = min(chunk, p.n_splits - s0);
-      for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) s_comb[i] = __ldcg(base + s0 * per_split + i);
+      if (COLGROUPS) {
+        for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) {
+          const int sp = i / per_split, r = i - sp * per_split;
+          s_comb[i] = __ldcg(base + (size_t)(s0 + sp) * split_stride + r);
+        }
+      } else {   // all columns: the chunk is contiguous
+        for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) s_comb[i] = __ldcg(base + s0 * per_split + i);
+      }
       __syncthreads();
 #pragma unroll
       for (int k = 0; k < NO; ++k) {
@@ -232,10 +251,10 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
       const int e = threadIdx.x + k * WARPS * 32;
       if (e < G * kHeadDim) {
         const int h = e >> 7, d = e & 127;
-        p.out[out_row(p, b, kvh, h) + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
+        p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
       }
     }
-    if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0u;   // ready for the next call
+    if (threadIdx.x == 0) p.tickets[ticket] = 0u;   // ready for the next call
   }
 }
 

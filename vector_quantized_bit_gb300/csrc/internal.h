@@ -27,6 +27,7 @@ struct DecodeParams {
   int B, Hq, Hkv, g;
   int M = 1;                // queries per sequence (multi-query decode)
   int ncols = 0;            // softmax columns per KV head: M * g (query m, head h -> column m * g + h)
+  int cgroups = 1;          // groups of up to 8 columns, one CTA each (grid.z = sequence groups x cgroups)
   int max_seq_len;
   int n_splits;             // CTAs per (sequence, KV head)
   int tps;                  // tiles per split
