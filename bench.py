@@ -282,6 +282,18 @@ def replica_throughput(tokens_per_replica, ms_per_step, world):
     return world * tokens_per_replica / (ms_per_step * 1e-3)
 
 
+KERNEL_SOURCES = ("decode.cu", "decode_common.cuh", "encode_common.cuh", "common.cuh", "internal.h")
+
+
+def kernel_sources_sha256():
+    """Hash of the sources the 2-bit decode kernel is compiled from; a stored
+    ncu traffic figure is used only while it matches."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "vector_quantized_bit_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def profile_traffic():
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source."""
@@ -289,8 +301,7 @@ def profile_traffic():
         prof = json.load(open(PROFILE_JSON))
     except (OSError, ValueError):
         return None, None
-    src = open(os.path.join(ROOT, "vector_quantized_bit_gb300", "csrc", "decode.cu"), "rb").read()
-    if prof.get("decode_cu_sha256") != hashlib.sha256(src).hexdigest():
+    if prof.get("kernel_sources_sha256") != kernel_sources_sha256():
         return None, prof.get("kernel")
     return prof.get("dram_bytes_per_launch"), prof.get("kernel")
 

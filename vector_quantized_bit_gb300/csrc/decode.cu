@@ -224,11 +224,14 @@ __device__ __noinline__ void append_rows(uint2 raw, float4 s, uint8_t* k_stream,
   __syncthreads();
 }
 
-// MULTI: several queries per sequence (per-column causal limits); the
-// single-query instantiation keeps one limit, L, for every column.  PAGED:
-// tiles are found through the block table (one bulk copy per tile).
-template <bool MULTI, bool PAGED>
+// Q: one query per sequence (kOneQuery: one limit, L, for every column),
+// several (kQueries: per-column causal limits, all columns in the CTA) or
+// several in column groups of up to 8, one CTA each (kQueryGroups).  PAGED:
+// tiles are found through the block table (at most two bulk copies per
+// step).
+template <int Q, bool PAGED>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
+  constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
   extern __shared__ __align__(128) unsigned char smem[];
   // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
   // c*256 + r*8, V replicas at c*256 + 128 + r*8.  Lane l reads replica
@@ -241,10 +244,10 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int b_begin = (MULTI ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
+  const int b_begin = (GROUPS ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
-  // this CTA's softmax columns (column groups only with several queries)
-  const int col0 = MULTI ? cta_col0(p) : 0, nloc = MULTI ? min(8, p.ncols - col0) : p.ncols;
+  // this CTA's softmax columns
+  const int col0 = GROUPS ? cta_col0(p) : 0, nloc = GROUPS ? min(8, p.ncols - col0) : p.ncols;
   const uint32_t kbyte = (uint32_t)(lane & 15) << 3;
   const uint32_t vbyte = 128u | ((uint32_t)(lane & 15) << 3);
   // this warp's ring: stage st holds the K super-tile, then the V super-tile
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
     stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
     __syncthreads();
-    finish_sequence<V2_WARPS, MULTI>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V2_WARPS, GROUPS>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
@@ -436,8 +439,9 @@ __device__ __forceinline__ uint32_t pair24(uint32_t w0, uint32_t w1, uint32_t w2
   return w2 >> 8;
 }
 
-template <bool MULTI, bool PAGED>
+template <int Q, bool PAGED>
 __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const DecodeParams p) {
+  constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
   extern __shared__ __align__(128) unsigned char smem[];
   uint4* s_kcb = reinterpret_cast<uint4*>(smem);
   uint4* s_vcb = reinterpret_cast<uint4*>(smem + V15_CB_BYTES);
@@ -449,10 +453,10 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int b_begin = (MULTI ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
+  const int b_begin = (GROUPS ? cta_bgroup(p) : (int)blockIdx.z) * p.bpg;
   const int b_end = min(b_begin + p.bpg, p.B);
-  // this CTA's softmax columns (column groups only with several queries)
-  const int col0 = MULTI ? cta_col0(p) : 0, nloc = MULTI ? min(8, p.ncols - col0) : p.ncols;
+  // this CTA's softmax columns
+  const int col0 = GROUPS ? cta_col0(p) : 0, nloc = GROUPS ? min(8, p.ncols - col0) : p.ncols;
   const uint32_t kcb_s = smem_u32(s_kcb);
   const uint32_t vcb_s = smem_u32(s_vcb);
   bool have_cb = false;
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     __syncthreads();   // every warp is done with its code slot: the combine area overlaps them
     stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
     __syncthreads();
-    finish_sequence<V15_WARPS, MULTI>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V15_WARPS, GROUPS>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();
   }
 }
@@ -613,35 +617,44 @@ cudaError_t decode_prepare(int mode) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e = cudaSuccess;
   if (mode == VQKV_MODE_VQ2) {
-    for (auto k : {decode_vq2_kernel<false, false>, decode_vq2_kernel<true, false>, decode_vq2_kernel<false, true>,
-                   decode_vq2_kernel<true, true>})
+    for (auto k : {decode_vq2_kernel<kOneQuery, false>, decode_vq2_kernel<kQueries, false>,
+                   decode_vq2_kernel<kQueryGroups, false>, decode_vq2_kernel<kOneQuery, true>,
+                   decode_vq2_kernel<kQueries, true>, decode_vq2_kernel<kQueryGroups, true>})
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV2Smem);
     return e;
   }
-  for (auto k : {decode_vq15_kernel<false, false>, decode_vq15_kernel<true, false>, decode_vq15_kernel<false, true>,
-                 decode_vq15_kernel<true, true>})
+  for (auto k : {decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
+                 decode_vq15_kernel<kQueryGroups, false>, decode_vq15_kernel<kOneQuery, true>,
+                 decode_vq15_kernel<kQueries, true>, decode_vq15_kernel<kQueryGroups, true>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV15Smem);
   return e;
 }
 
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<false, false>, V2_THREADS,
-                                                         kV2Smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<false, false>, V15_THREADS,
-                                                       kV15Smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<kOneQuery, false>,
+                                                         V2_THREADS, kV2Smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<kOneQuery, false>,
+                                                       V15_THREADS, kV15Smem);
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  const bool multi = p.M > 1, paged = p.block_table != nullptr;
+  const int q = p.M == 1 ? kOneQuery : p.cgroups == 1 ? kQueries : kQueryGroups;
+  const bool paged = p.block_table != nullptr;
   if (mode == VQKV_MODE_VQ2) {
-    auto k = paged ? (multi ? decode_vq2_kernel<true, true> : decode_vq2_kernel<false, true>)
-                   : (multi ? decode_vq2_kernel<true, false> : decode_vq2_kernel<false, false>);
-    return launch_pdl(k, grid, dim3(V2_THREADS), kV2Smem, stream, p);
+    using K = void (*)(DecodeParams);
+    const K ks[2][3] = {{decode_vq2_kernel<kOneQuery, false>, decode_vq2_kernel<kQueries, false>,
+                         decode_vq2_kernel<kQueryGroups, false>},
+                        {decode_vq2_kernel<kOneQuery, true>, decode_vq2_kernel<kQueries, true>,
+                         decode_vq2_kernel<kQueryGroups, true>}};
+    return launch_pdl(ks[paged][q], grid, dim3(V2_THREADS), kV2Smem, stream, p);
   }
-  auto k = paged ? (multi ? decode_vq15_kernel<true, true> : decode_vq15_kernel<false, true>)
-                 : (multi ? decode_vq15_kernel<true, false> : decode_vq15_kernel<false, false>);
-  return launch_pdl(k, grid, dim3(V15_THREADS), kV15Smem, stream, p);
+  using K = void (*)(DecodeParams);
+  const K ks[2][3] = {{decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
+                       decode_vq15_kernel<kQueryGroups, false>},
+                      {decode_vq15_kernel<kOneQuery, true>, decode_vq15_kernel<kQueries, true>,
+                       decode_vq15_kernel<kQueryGroups, true>}};
+  return launch_pdl(ks[paged][q], grid, dim3(V15_THREADS), kV15Smem, stream, p);
 }
 
 }  // namespace vqkv

@@ -154,6 +154,10 @@ __device__ __forceinline__ void mask_scores(float (&sc)[4], int t0, const Column
 // happen before thread 0's acq_rel ticket increment (CTA barrier, then a
 // cumulative gpu-scope release); the last CTA's acquire and the barrier
 // after it order its partial loads after every other CTA's stores.
+// Query layout a decode kernel is compiled for: one query per sequence,
+// several with all columns in one CTA, or several in column groups.
+enum QueryLayout : int { kOneQuery = 0, kQueries = 1, kQueryGroups = 2 };
+
 // The CTA's columns: col0 .. col0 + nloc - 1 of the KV head's ncols
 // (column group blockIdx.z % cgroups).
 __device__ __forceinline__ int cta_col0(const DecodeParams& p) { return 8 * (int)(blockIdx.z % p.cgroups); }
