@@ -83,7 +83,7 @@ constexpr int V15_SLOT_BYTES = V15_THREADS * 96;  // 48 KB
 constexpr int V15_Q_OFF = V15_SLOT_OFF + V15_SLOT_BYTES;
 
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
-// codebook and q' region after the tile loop.
+// codebook, q' and ring region after the tile loop.
 // Fused append (vqkv_decode_append): per-warp partial searches.
 constexpr int V2_APP_OFF = (V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
 constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
@@ -91,7 +91,7 @@ constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
 constexpr int V2_BLK_OFF = V2_APP_OFF + V2_APP_BYTES;
 constexpr int V2_BLK_CACHE = 512;
 constexpr size_t kV2Smem = V2_BLK_OFF + V2_BLK_CACHE * 4;
-static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_RING_OFF, "combine area must fit below the ring");
+static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_MBAR_OFF, "combine area must fit below the ring barriers");
 // The combine area (after the tile loop) and q' (before it) overlap the
 // code slots, which are idle at those times.
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
     stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
     __syncthreads();
-    finish_sequence<V2_WARPS, GROUPS>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V2_WARPS, GROUPS, Vq2Dim>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     __syncthreads();   // every warp is done with its code slot: the combine area overlaps them
     stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
     __syncthreads();
-    finish_sequence<V15_WARPS, GROUPS>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V15_WARPS, GROUPS, Vq15Dim>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();
   }
 }

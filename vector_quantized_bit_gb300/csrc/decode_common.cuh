@@ -16,10 +16,16 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // never see inf - inf; masked scores are -inf and give p = 0.
 constexpr float kMInit = -1e30f;
 
+// Combine area (floats), used after the tile loop: each warp's O rows (one
+// per softmax column, pitch kPitch: 128 channels after a per-column skew of
+// up to 31 floats that spreads the stash stores over the banks), then the
+// warps' m, l, their scale factors and the CTA's max per column.
 template <int WARPS>
 struct CombineSmem {
-  static constexpr int kO = WARPS * 8 * 128;     // floats
-  static constexpr int kBytes = (kO + 2 * WARPS * 8) * 4;
+  static constexpr int kPitch = kHeadDim + 32;   // a multiple of 32: the pitch itself is bank-neutral
+  static constexpr int kO = WARPS * 8 * kPitch;
+  static constexpr int kM = kO, kL = kM + WARPS * 8, kF = kL + WARPS * 8, kMax = kF + WARPS * 8;
+  static constexpr int kBytes = (kMax + 8) * 4;
 };
 
 // Clamp the sequence length to [0, max_seq_len]; report out-of-range once.
@@ -164,40 +170,51 @@ __device__ __forceinline__ int cta_col0(const DecodeParams& p) { return 8 * (int
 __device__ __forceinline__ int cta_bgroup(const DecodeParams& p) { return (int)(blockIdx.z / p.cgroups); }
 
 // COLGROUPS: the launch may split the columns into groups (multi-query
-// decode); otherwise the CTA holds all ncols columns.
-template <int WARPS, bool COLGROUPS>
+// decode); otherwise the CTA holds all ncols columns.  DimOf: the stash
+// layout (row skew).
+template <int WARPS, bool COLGROUPS, typename DimOf>
 __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
                                                 float* s_comb, int* s_last) {
-  constexpr int NO = (8 * kHeadDim + WARPS * 32 - 1) / (WARPS * 32);   // outputs per thread in the merge
+  using C = CombineSmem<WARPS>;
   const float* wO = s_comb;
-  const float* wm = s_comb + CombineSmem<WARPS>::kO;
-  const float* wl = wm + WARPS * 8;
+  const float* wm = s_comb + C::kM;
+  const float* wl = s_comb + C::kL;
+  float* wf = s_comb + C::kF;
+  float* wM = s_comb + C::kMax;
   const int col0 = COLGROUPS ? cta_col0(p) : 0;
   const int G = COLGROUPS ? min(8, p.ncols - col0) : p.ncols;   // this CTA's columns
   float* part = p.partials + (((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * p.ncols + col0) * kPartialStride;
   const unsigned ticket = COLGROUPS ? (unsigned)((b * p.Hkv + kvh) * p.cgroups + blockIdx.z % p.cgroups)
                                     : (unsigned)(b * p.Hkv + kvh);
-  for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
-    const int h = e >> 7, d = e & 127;
+  // each warp's scale against the CTA's max of the column, once per (warp,
+  // column) rather than once per output
+  for (int i = threadIdx.x; i < WARPS * 8; i += WARPS * 32) {
+    const int h = i & 7;
     float M = kMInit;
 #pragma unroll 4
     for (int w = 0; w < WARPS; ++w) M = fmaxf(M, wm[w * 8 + h]);
-    float o = 0.f, l = 0.f;
+    wf[i] = fast_exp2(wm[i] - M);
+    if (i < 8) wM[h] = M;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * kHeadDim; e += WARPS * 32) {
+    const int h = e >> 7, d = e & 127;
+    const float* col = wO + h * C::kPitch + DimOf::skew(h) + d;
+    float o = 0.f;
 #pragma unroll 4
-    for (int w = 0; w < WARPS; ++w) {
-      const float f = fast_exp2(wm[w * 8 + h] - M);
-      o += wO[(w * 8 + h) * kHeadDim + d] * f;
-      l += wl[w * 8 + h] * f;
-    }
-    if (p.n_splits == 1) {
-      p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
-      continue;
-    }
-    part[h * kPartialStride + d] = o;
-    if (d == 0) {
-      part[h * kPartialStride + 128] = M;
+    for (int w = 0; w < WARPS; ++w) o += col[w * 8 * C::kPitch] * wf[w * 8 + h];
+    if (p.n_splits == 1 || d == 0) {
+      float l = 0.f;
+#pragma unroll 4
+      for (int w = 0; w < WARPS; ++w) l += wl[w * 8 + h] * wf[w * 8 + h];
+      if (p.n_splits == 1) {
+        p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
+        continue;
+      }
+      part[h * kPartialStride + 128] = wM[h];
       part[h * kPartialStride + 129] = l;
     }
+    part[h * kPartialStride + d] = o;
   }
   if (p.n_splits == 1 || p.defer_merge) return;
   __syncthreads();
@@ -211,51 +228,96 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
   }
   __syncthreads();
   if (*s_last) {
-    // All split partials of (b, kvh) are staged in shared memory by the whole
-    // CTA (coalesced, every load in flight at once), then each thread merges
-    // one output (head, channel) with a running max.  Chunks of splits when
-    // they do not all fit.
+    // Thread t merges 8 channels of one column (item t % items) over every
+    // R-th split (t / items), straight from the partials: a batch of splits
+    // has all its loads in flight at once and one rescale; the R threads of
+    // an item then meet in shared memory.
+    constexpr int THREADS = WARPS * 32, BATCH = 6;
     const float* base = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits * p.ncols + col0) * kPartialStride;
-    const int per_split = G * kPartialStride;                    // this CTA's columns of one split
     const size_t split_stride = (size_t)p.ncols * kPartialStride;
-    const int chunk = max(1, min(p.n_splits, CombineSmem<WARPS>::kBytes / 4 / per_split));
-    float M[NO], O[NO], Ls[NO];
-    for (int k = 0; k < NO; ++k) M[k] = kMInit, O[k] = 0.f, Ls[k] = 0.f;
-    for (int s0 = 0; s0 < p.n_splits; s0 += chunk) {
-      const int ns = min(chunk, p.n_splits - s0);
-      if (COLGROUPS) {
-        for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) {
-          const int sp = i / per_split, r = i - sp * per_split;
-          s_comb[i] = __ldcg(base + (size_t)(s0 + sp) * split_stride + r);
-        }
-      } else {   // all columns: the chunk is contiguous
-        for (int i = threadIdx.x; i < ns * per_split; i += WARPS * 32) s_comb[i] = __ldcg(base + s0 * per_split + i);
-      }
-      __syncthreads();
+    const int items = G * (kHeadDim / 8), R = THREADS / items;
+    const int item = threadIdx.x % items, r = threadIdx.x / items;
+    const int h = item / (kHeadDim / 8), d8 = (item % (kHeadDim / 8)) * 8;
+    float M = kMInit, Ls = 0.f, O[8];
 #pragma unroll
-      for (int k = 0; k < NO; ++k) {
-        const int e = threadIdx.x + k * WARPS * 32;
-        if (e < G * kHeadDim) {
-          const int h = e >> 7, d = e & 127;
-          for (int s = 0; s < ns; ++s) {
-            const float* ph = s_comb + s * per_split + h * kPartialStride;
-            const float ms = ph[128];
-            const float n = fmaxf(M[k], ms);
-            const float fa = fast_exp2(M[k] - n), fb = fast_exp2(ms - n);
-            O[k] = O[k] * fa + ph[d] * fb;
-            Ls[k] = Ls[k] * fa + ph[129] * fb;
-            M[k] = n;
+    for (int i = 0; i < 8; ++i) O[i] = 0.f;
+    if (r < R) {
+      const float* col = base + h * kPartialStride;
+      for (int s0 = r; s0 < p.n_splits; s0 += BATCH * R) {
+        float2 ml[BATCH];
+        float4 oa[BATCH], ob[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+          const int sp = s0 + j * R;
+          if (sp < p.n_splits) {
+            const float* ph = col + (size_t)sp * split_stride;
+            ml[j] = __ldcg(reinterpret_cast<const float2*>(ph + 128));
+            oa[j] = __ldcg(reinterpret_cast<const float4*>(ph + d8));
+            ob[j] = __ldcg(reinterpret_cast<const float4*>(ph + d8 + 4));
+          } else {
+            ml[j] = make_float2(kMInit, 0.f);
+            oa[j] = ob[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
+        float n = M;
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) n = fmaxf(n, ml[j].x);
+        const float fa = fast_exp2(M - n);
+        Ls *= fa;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) O[i] *= fa;
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+          const float f = fast_exp2(ml[j].x - n);
+          Ls += ml[j].y * f;
+          O[0] += oa[j].x * f, O[1] += oa[j].y * f, O[2] += oa[j].z * f, O[3] += oa[j].w * f;
+          O[4] += ob[j].x * f, O[5] += ob[j].y * f, O[6] += ob[j].z * f, O[7] += ob[j].w * f;
+        }
+        M = n;
+      }
+    }
+    if (R > 1) {   // [R][items] states of 12 floats (m, l, O[8], pad)
+      float* xs = s_comb + (size_t)threadIdx.x * 12;
+      if (r < R) {
+        *reinterpret_cast<float4*>(xs) = make_float4(M, Ls, 0.f, 0.f);
+        *reinterpret_cast<float4*>(xs + 4) = make_float4(O[0], O[1], O[2], O[3]);
+        *reinterpret_cast<float4*>(xs + 8) = make_float4(O[4], O[5], O[6], O[7]);
       }
       __syncthreads();
+      if (r == 0) {
+        for (int q = 1; q < R; ++q) {
+          const float* ys = s_comb + (size_t)(q * items + item) * 12;
+          const float4 y0 = *reinterpret_cast<const float4*>(ys);
+          const float4 y1 = *reinterpret_cast<const float4*>(ys + 4);
+          const float4 y2 = *reinterpret_cast<const float4*>(ys + 8);
+          const float n = fmaxf(M, y0.x);
+          const float fa = fast_exp2(M - n), fb = fast_exp2(y0.x - n);
+          Ls = Ls * fa + y0.y * fb;
+          O[0] = O[0] * fa + y1.x * fb, O[1] = O[1] * fa + y1.y * fb;
+          O[2] = O[2] * fa + y1.z * fb, O[3] = O[3] * fa + y1.w * fb;
+          O[4] = O[4] * fa + y2.x * fb, O[5] = O[5] * fa + y2.y * fb;
+          O[6] = O[6] * fa + y2.z * fb, O[7] = O[7] * fa + y2.w * fb;
+          M = n;
+        }
+      }
     }
+    if (r == 0) {
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      uint4 packed;
+      packed.x = pack_half2(O[0] * inv, O[1] * inv);
+      packed.y = pack_half2(O[2] * inv, O[3] * inv);
+      packed.z = pack_half2(O[4] * inv, O[5] * inv);
+      packed.w = pack_half2(O[6] * inv, O[7] * inv);
+      __half* dst = p.out + out_row(p, b, kvh, col0 + h) + d8;
+      if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {   // out needs only 2-byte alignment
+        *reinterpret_cast<uint4*>(dst) = packed;
+      } else {
+        const uint32_t w[4] = {packed.x, packed.y, packed.z, packed.w};
 #pragma unroll
-    for (int k = 0; k < NO; ++k) {
-      const int e = threadIdx.x + k * WARPS * 32;
-      if (e < G * kHeadDim) {
-        const int h = e >> 7, d = e & 127;
-        p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(Ls[k] > 0.f ? O[k] / Ls[k] : 0.f);
+        for (int i = 0; i < 4; ++i) {
+          dst[2 * i] = __ushort_as_half((unsigned short)(w[i] & 0xffffu));
+          dst[2 * i + 1] = __ushort_as_half((unsigned short)(w[i] >> 16));
+        }
       }
     }
     if (threadIdx.x == 0) p.tickets[ticket] = 0u;   // ready for the next call
@@ -296,45 +358,64 @@ __device__ __forceinline__ void combine_splits(const DecodeParams& p) {
 }
 
 // Store one warp's (m, l, O) into the combine area.  acc holds O^T fragments:
-// acc[mt] = rows {gid, gid+8} (channels dim0(mt), dim0(mt)+1) x heads {2tig, 2tig+1}.
+// acc[mt] = rows {gid, gid+8} (channels dim_of(mt, gid), dim_of(mt, gid+8))
+// x heads {2tig, 2tig+1}.  Row h of the warp starts DimOf::skew(h) floats
+// into its pitch; with that skew the stores of a warp fall on distinct banks.
 template <int WARPS, int NMT, typename DimOf>
 __device__ __forceinline__ void stash_warp(float* s_comb, int warp, int lane, const float (&acc)[NMT][4],
                                            float m0, float m1, float l0, float l1, DimOf dim_of) {
+  using C = CombineSmem<WARPS>;
   const int gid = lane >> 2, tig = lane & 3;
-  float* wO = s_comb;
-  float* wm = s_comb + CombineSmem<WARPS>::kO;
-  float* wl = wm + WARPS * 8;
+  float* wm = s_comb + C::kM;
+  float* wl = s_comb + C::kL;
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
-  const int h0 = warp * 8 + 2 * tig;
+  const int h0 = 2 * tig;
+  float* r0 = s_comb + (warp * 8 + h0) * C::kPitch + DimOf::skew(h0);
+  float* r1 = s_comb + (warp * 8 + h0 + 1) * C::kPitch + DimOf::skew(h0 + 1);
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt) {
     const int d0 = dim_of(mt, gid), d1 = dim_of(mt, gid + 8);
-    wO[h0 * kHeadDim + d0] = acc[mt][0];
-    wO[(h0 + 1) * kHeadDim + d0] = acc[mt][1];
-    wO[h0 * kHeadDim + d1] = acc[mt][2];
-    wO[(h0 + 1) * kHeadDim + d1] = acc[mt][3];
+    if (DimOf::kPairs) {   // d1 == d0 + 1, d0 even
+      *reinterpret_cast<float2*>(r0 + d0) = make_float2(acc[mt][0], acc[mt][2]);
+      *reinterpret_cast<float2*>(r1 + d0) = make_float2(acc[mt][1], acc[mt][3]);
+    } else {
+      r0[d0] = acc[mt][0];
+      r1[d0] = acc[mt][1];
+      r0[d1] = acc[mt][2];
+      r1[d1] = acc[mt][3];
+    }
   }
   if (gid == 0) {
-    wm[h0] = m0;
-    wm[h0 + 1] = m1;
-    wl[h0] = l0;
-    wl[h0 + 1] = l1;
+    wm[warp * 8 + h0] = m0;
+    wm[warp * 8 + h0 + 1] = m1;
+    wl[warp * 8 + h0] = l0;
+    wl[warp * 8 + h0 + 1] = l1;
   }
 }
 
-// Channel held by row r (0..15) of P.V M-tile mt, per kernel's row order.
-struct Vq2Dim {
+// Channel held by row r (0..15) of P.V M-tile mt, per kernel's row order,
+// and the skew of stashed row h.
+//   kPairs: rows gid and gid+8 hold two adjacent channels (stored as float2);
+//   the skews make a half-warp's float2 stores (or a warp's scalar stores)
+//   cover the 32 banks once.
+struct Vq2Dim {   // channel pair offset 4*gid
+  static constexpr bool kPairs = true;
   __device__ int operator()(int mt, int r) const { return 4 * (8 * (mt >> 1) + (r & 7)) + 2 * (mt & 1) + (r >> 3); }
+  __device__ static int skew(int h) { const int t = (h >> 1) & 3; return 2 * (t & 1) + 16 * (t >> 1); }
 };
-struct Vq15Dim {
+struct Vq15Dim {   // channel pair offset 8*gid
+  static constexpr bool kPairs = true;
   __device__ int operator()(int mt, int r) const { return 8 * (8 * (mt >> 2) + (r & 7)) + 2 * (mt & 3) + (r >> 3); }
+  __device__ static int skew(int h) { return 2 * ((h >> 1) & 3); }
 };
-struct NaturalDim {
+struct NaturalDim {   // channel offset gid, rows gid+8 eight channels on
+  static constexpr bool kPairs = false;
   __device__ int operator()(int mt, int r) const { return 16 * mt + r; }
+  __device__ static int skew(int h) { return 8 * ((h >> 1) & 3); }
 };
 
 }  // namespace

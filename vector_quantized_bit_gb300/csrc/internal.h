@@ -50,7 +50,7 @@ struct DecodeParams {
   int withhold_first_copy = 0;
 };
 
-constexpr int kPartialStride = 130;  // O[128], m, l
+constexpr int kPartialStride = 132;  // O[128], m, l, pad (rows 16-byte aligned)
 
 struct EncodeParams {
   const __half* x;          // [B][Hkv][n_rows][128]
