@@ -97,23 +97,42 @@ static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_MBAR_OFF, "combine area must f
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
 static_assert(V15_Q_OFF + 8 * 128 * 4 <= (int)kV15Smem, "q' must fit in the combine area");
 
-// q' of the CTA's softmax columns col0 .. col0 + nloc - 1 of (b, kvh) into
-// s_qp[c - col0][128] (fp32, scaled), by warps 0..nloc-1.
-__device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
-                                                  int lane, float* s_qp, int col0, int nloc) {
-  if (warp < nloc) {   // column col0 + warp: query c / g, head c % g
+// The lane's 4 channels of query column col0 + warp (query c / g, head
+// c % g) and their smoothing factors, for warps 0..nloc-1.
+struct QueryLoad {
+  uint2 q;
+  float4 s;
+};
+__device__ __forceinline__ QueryLoad load_query(const DecodeParams& p, int b, int kvh, int warp, int lane, int col0,
+                                                int nloc) {
+  QueryLoad r{make_uint2(0u, 0u), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (warp < nloc) {
     const int c = col0 + warp;
     const int m = c / p.g, hq = kvh * p.g + c - m * p.g;
-    const uint2 qq = *reinterpret_cast<const uint2*>(p.q + (((size_t)b * p.M + m) * p.Hq + hq) * kHeadDim + 4 * lane);
-    const float4 ss = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
-    const __half2 q01 = *reinterpret_cast<const __half2*>(&qq.x);
-    const __half2 q23 = *reinterpret_cast<const __half2*>(&qq.y);
-    float v[4] = {__low2float(q01) * ss.x, __high2float(q01) * ss.y, __low2float(q23) * ss.z,
-                  __high2float(q23) * ss.w};
+    r.q = *reinterpret_cast<const uint2*>(p.q + (((size_t)b * p.M + m) * p.Hq + hq) * kHeadDim + 4 * lane);
+    r.s = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+  }
+  return r;
+}
+
+// q' of the CTA's softmax column col0 + warp into s_qp[warp][128] (fp32,
+// scaled), by warps 0..nloc-1.
+__device__ __forceinline__ void transform_query(const DecodeParams& p, const QueryLoad& r, int warp, int lane,
+                                                float* s_qp, int nloc) {
+  if (warp < nloc) {
+    const __half2 q01 = *reinterpret_cast<const __half2*>(&r.q.x);
+    const __half2 q23 = *reinterpret_cast<const __half2*>(&r.q.y);
+    float v[4] = {__low2float(q01) * r.s.x, __high2float(q01) * r.s.y, __low2float(q23) * r.s.z,
+                  __high2float(q23) * r.s.w};
     fwht128_f32(v, lane);
     float4 o = make_float4(v[0] * p.qscale, v[1] * p.qscale, v[2] * p.qscale, v[3] * p.qscale);
     *reinterpret_cast<float4*>(s_qp + warp * kHeadDim + 4 * lane) = o;
   }
+}
+
+__device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
+                                                  int lane, float* s_qp, int col0, int nloc) {
+  transform_query(p, load_query(p, b, kvh, warp, lane, col0, nloc), warp, lane, s_qp, nloc);
 }
 
 // Shared-memory offset of a gathered centroid: one byte permute puts code
@@ -188,22 +207,21 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
 }
 
 // Encode of the new K row (warps 0-7) and V row (warps 8-15) of one
-// (sequence, KV head) for the fused append, from the lane's 4 channels of its
-// row (raw) and smoothing factors (s, keys): each warp searches 32 of the 256
+// (sequence, KV head) for the fused append, from the lane's 4 transformed
+// channels x of its row: each warp searches 32 of the 256
 // candidates (replica 0 of the shared codebook, one broadcast per load), the
 // slices are merged as in the encode kernel, and lane j of warps 0 / 8 writes
 // the code of subvector j to the cache at token t_new.  The writes are made
 // visible to the bulk copies (async proxy) that the CTA issues after the
 // closing barrier.  Called by every thread of the CTA after the codebook is
 // in shared memory.
-__device__ __noinline__ void append_rows(uint2 raw, float4 s, uint8_t* k_stream, uint8_t* v_stream,
+__device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* v_stream,
                                          unsigned long long* near_tie, int t_new, const unsigned char* s_cb,
                                          Best* s_part) {
   static_assert(V2_WARPS == 16, "two roles x 8 candidate slices");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int role = warp >> 3, slice = warp & 7;
-  float x[4];
-  transform_loaded(raw, role == 0, s, lane, x);
+  const float x[4] = {xv.x, xv.y, xv.z, xv.w};
   const unsigned char* cb_role = s_cb + role * 128;
   const Best part = vq2_search(x, slice * 32, slice * 32 + 32, [&](int c) {
     const uint2 raw = *reinterpret_cast<const uint2*>(cb_role + c * 256);
@@ -264,6 +282,19 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   bool timed_out = false;
 
   for (int b = b_begin; b < b_end; ++b) {
+    // Every input load of the prologue is issued before the first one is
+    // used (the sequence length decides the rest): this warp's codebook
+    // entry, its query column, and the new K / V row of a fused append.
+    const uint2 cb_entry = __ldg(reinterpret_cast<const uint2*>((threadIdx.x >> 8) ? p.vcb : p.kcb) +
+                                 (size_t)kvh * 256 + (threadIdx.x & 255));
+    const QueryLoad qload = load_query(p, b, kvh, warp, lane, col0, nloc);
+    uint2 xraw = make_uint2(0u, 0u);
+    float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (p.k_new != nullptr) {
+      const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
+      xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
+      if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+    }
     const int L = load_len(p, b);
     const int ntiles = (L + V2_TILE - 1) / V2_TILE;
     const int t_begin = split * p.tps;
@@ -350,30 +381,30 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       if (lane == 0 && !late_start)
         for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
           if (!(p.withhold_first_copy && j == 0)) issue(j);
-      // the new rows' loads overlap the codebook fill
-      uint2 xraw = make_uint2(0u, 0u);
-      float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
+      // the new row's transform (warps 0-7: smoothed, rotated key) before
+      // the codebook fill, which only the search needs
+      float4 xnew = make_float4(0.f, 0.f, 0.f, 0.f);
       if (append) {
-        const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
-        xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
-        if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
+        float x[4];
+        transform_loaded(xraw, warp < 8, xs, lane, x);
+        xnew = make_float4(x[0], x[1], x[2], x[3]);
       }
       {
-        // thread t loads centroid t & 255 of K (t < 256) or V (t >= 256) once and
-        // writes its 16 replicas; replica (i + lane) % 16 at step i keeps the 16
-        // lanes of each half-warp on 16 different bank pairs
+        // thread t writes the 16 replicas of centroid t & 255 of K (t < 256)
+        // or V (t >= 256), loaded above; replica (i + lane) % 16 at step i
+        // keeps the 16 lanes of each half-warp on 16 different bank pairs
         static_assert(V2_THREADS == 512, "one thread per K and V centroid");
         const int c = threadIdx.x & 255, role = threadIdx.x >> 8;
-        const uint2 e = __ldg(reinterpret_cast<const uint2*>(role ? p.vcb : p.kcb) + (size_t)kvh * 256 + c);
+        const uint2 e = cb_entry;
         uint2* row = reinterpret_cast<uint2*>(smem + c * 256 + role * 128);
 #pragma unroll 1
         for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
       }
-      transform_queries(p, b, kvh, warp, lane, s_qp, col0, nloc);
+      transform_query(p, qload, warp, lane, s_qp, nloc);
       __syncthreads();
       if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-        append_rows(xraw, xs, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
+        append_rows(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
                     reinterpret_cast<Best*>(smem + V2_APP_OFF));
         if (lane == 0 && late_start)
           for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
