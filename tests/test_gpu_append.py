@@ -95,10 +95,16 @@ def test_fused_step_against_oracle_and_unfused(B, Hq, Hkv, lens, cap, num_splits
             vc[b].append(vo.unpack_stream_fast(vb[b, h], 0, 1, L))
     ref_o = vo.decode_attention(q, kc, vc, kcb, vcb, s, lens)
     assert vo.o_error(o, ref_o).max() <= H.O_TOL
-    # the unfused calls give the same cache and the same O
+    # the unfused calls give the same cache, and the same O under the same
+    # split plan; the fused call's own plan may shorten the split that holds
+    # the new token, which only regroups the fp32 partial sums
     o2, kb2, vb2 = _unfused(q, kbuf, vbuf, lens, kcb, vcb, s, cap, k_new, v_new, num_splits)
     assert np.array_equal(kb, kb2) and np.array_equal(vb, vb2)
-    assert np.array_equal(o, o2)
+    if num_splits > 0:
+        assert np.array_equal(o, o2)
+    else:
+        diff = np.abs(o.astype(np.float32) - o2.astype(np.float32))
+        assert diff.max() <= 2e-3 * max(1.0, float(np.abs(o.astype(np.float32)).max()))
 
 
 def test_near_tie_counter_counts_both_rows():

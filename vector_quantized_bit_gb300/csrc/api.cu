@@ -125,6 +125,11 @@ struct PlanInput {
   int mode;   // VQKV_MODE_VQ2, VQKV_MODE_VQ15 or kModeFp16
   int B, Hq, Hkv, max_seq_len, num_splits;
   int M = 1;  // queries per sequence
+  // Tiles' worth of extra work in the CTA whose split holds a sequence's
+  // last token (the fused append encodes the new rows there first).  When
+  // every CTA of the plan runs at once, the splits are sized for
+  // max_seq_len + credit_tiles, so that split comes out this much shorter.
+  int credit_tiles = 0;
 };
 
 vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
@@ -162,7 +167,9 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
     }
   }
   const long long unit = unit_tiles;
-  const long long tps = ((tiles_max + best_n - 1) / best_n + unit - 1) / unit * unit;
+  const bool one_wave = pairs * best_n <= slots;
+  const long long credit = (a->num_splits == 0 && one_wave) ? a->credit_tiles : 0;
+  const long long tps = ((tiles_max + credit + best_n - 1) / best_n + unit - 1) / unit * unit;
   pl->tps = (int)tps;
   pl->n_splits = (int)((tiles_max + tps - 1) / tps);
   pl->bpg = bpg;
@@ -306,6 +313,10 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
   DecodePlan pl;
   PlanInput in = plan_input(a);
   in.M = M;
+  // the fused append costs its CTA about 60 tiles of streaming (2-bit, one
+  // CTA per SM); a split of at most the plain plan's size, so the workspace
+  // of vqkv_decode_workspace_bytes still covers it
+  if (ap != nullptr) in.credit_tiles = 60;
   st = plan_decode(&in, &pl);
   if (st != VQKV_OK) return st;
   if (a->workspace == nullptr || a->workspace_bytes < pl.ws_bytes) return VQKV_ERR_WORKSPACE;
