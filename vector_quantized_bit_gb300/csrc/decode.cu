@@ -62,10 +62,14 @@ constexpr int V2_TILE_BYTES = 512;
 constexpr int V2_REPL = 16;                         // replicas of each centroid (bank spreading)
 static_assert(V2_REPL * 8 == 128, "one 128-byte half row per codebook");
 constexpr int V2_CB_BYTES = 256 * 256;              // [code][K replicas (128 B) | V replicas (128 B)]
-constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][128]) after the codebooks
+// q' rows (fp32, 128 channels) at a pitch that keeps the 8 lanes of each
+// quarter-warp on distinct 16-byte bank groups when the MMA fragments are
+// read (lane (gid, tig) reads 4 floats at gid * pitch + 4 tig + 16 s).
+constexpr int V2_Q_PITCH = 144;
+constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][V2_Q_PITCH]) after the codebooks
 constexpr int V2_STAGES = VQKV_V2_STAGES;           // per-warp ring of super-tiles (K then V)
 constexpr int V2_STAGE_BYTES = 2 * V2_TPI * V2_TILE_BYTES;
-constexpr int V2_RING_OFF = V2_Q_OFF + 8 * 128 * 4;
+constexpr int V2_RING_OFF = V2_Q_OFF + 8 * V2_Q_PITCH * 4;
 constexpr int V2_RING_BYTES = V2_WARPS * V2_STAGES * V2_STAGE_BYTES;
 constexpr int V2_MBAR_OFF = V2_RING_OFF + V2_RING_BYTES;
 
@@ -81,6 +85,7 @@ constexpr int V15_CB_BYTES = 4096 * 16;          // 64 KB per codebook
 constexpr int V15_SLOT_OFF = 2 * V15_CB_BYTES;
 constexpr int V15_SLOT_BYTES = V15_THREADS * 96;  // 48 KB
 constexpr int V15_Q_OFF = V15_SLOT_OFF + V15_SLOT_BYTES;
+constexpr int V15_Q_PITCH = 128;   // read once per sequence; a padded pitch measured no better
 
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
 // codebook, q' and ring region after the tile loop.
@@ -95,7 +100,7 @@ static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_MBAR_OFF, "combine area must f
 // The combine area (after the tile loop) and q' (before it) overlap the
 // code slots, which are idle at those times.
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
-static_assert(V15_Q_OFF + 8 * 128 * 4 <= (int)kV15Smem, "q' must fit in the combine area");
+static_assert(V15_Q_OFF + 8 * V15_Q_PITCH * 4 <= (int)kV15Smem, "q' must fit in the combine area");
 
 // The lane's 4 channels of query column col0 + warp (query c / g, head
 // c % g) and their smoothing factors, for warps 0..nloc-1.
@@ -115,10 +120,10 @@ __device__ __forceinline__ QueryLoad load_query(const DecodeParams& p, int b, in
   return r;
 }
 
-// q' of the CTA's softmax column col0 + warp into s_qp[warp][128] (fp32,
-// scaled), by warps 0..nloc-1.
+// q' of the CTA's softmax column col0 + warp into row `warp` of s_qp (fp32,
+// scaled, rows `pitch` floats apart), by warps 0..nloc-1.
 __device__ __forceinline__ void transform_query(const DecodeParams& p, const QueryLoad& r, int warp, int lane,
-                                                float* s_qp, int nloc) {
+                                                float* s_qp, int pitch, int nloc) {
   if (warp < nloc) {
     const __half2 q01 = *reinterpret_cast<const __half2*>(&r.q.x);
     const __half2 q23 = *reinterpret_cast<const __half2*>(&r.q.y);
@@ -126,13 +131,13 @@ __device__ __forceinline__ void transform_query(const DecodeParams& p, const Que
                   __high2float(q23) * r.s.w};
     fwht128_f32(v, lane);
     float4 o = make_float4(v[0] * p.qscale, v[1] * p.qscale, v[2] * p.qscale, v[3] * p.qscale);
-    *reinterpret_cast<float4*>(s_qp + warp * kHeadDim + 4 * lane) = o;
+    *reinterpret_cast<float4*>(s_qp + warp * pitch + 4 * lane) = o;
   }
 }
 
 __device__ __forceinline__ void transform_queries(const DecodeParams& p, int b, int kvh, int warp,
-                                                  int lane, float* s_qp, int col0, int nloc) {
-  transform_query(p, load_query(p, b, kvh, warp, lane, col0, nloc), warp, lane, s_qp, nloc);
+                                                  int lane, float* s_qp, int pitch, int col0, int nloc) {
+  transform_query(p, load_query(p, b, kvh, warp, lane, col0, nloc), warp, lane, s_qp, pitch, nloc);
 }
 
 // Shared-memory offset of a gathered centroid: one byte permute puts code
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll 1
         for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
       }
-      transform_query(p, qload, warp, lane, s_qp, nloc);
+      transform_query(p, qload, warp, lane, s_qp, V2_Q_PITCH, nloc);
       __syncthreads();
       if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       for (int s = 0; s < 8; ++s) {
         const int j = 4 * s + tig;
         if (gid < nloc) {
-          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + 4 * j);
+          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH + 4 * j);
           qa[s][0] = pack_half2(v.x, v.y);
           qa[s][1] = pack_half2(v.z, v.w);
         } else {
@@ -532,7 +537,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
         }
         have_cb = true;
       }
-      transform_queries(p, b, kvh, warp, lane, s_qp, col0, nloc);
+      transform_queries(p, b, kvh, warp, lane, s_qp, V15_Q_PITCH, col0, nloc);
       __syncthreads();
       uint32_t qf[8][2];
 #pragma unroll
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
         const int j = 4 * (s >> 1) + tig;     // subvector
         const int c = 8 * j + 4 * (s & 1);    // first channel of this half
         if (gid < nloc) {
-          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * kHeadDim + c);
+          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V15_Q_PITCH + c);
           qf[s][0] = pack_half2(v.x, v.y);
           qf[s][1] = pack_half2(v.z, v.w);
         } else {
