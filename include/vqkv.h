@@ -340,6 +340,106 @@ vqkv_status vqkv_decode_attn_static(const vqkv_decode_args* args, void* stream);
  */
 vqkv_status vqkv_test_decode_ring_timeout(const vqkv_decode_args* args, uint32_t max_polls, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Offline calibration: the key smoothing vector, the key transform variants
+ * and K-Means codebook training.  These produce the s and codebook inputs of
+ * the calls above; they are not part of a decode step.  VecInfer trains its
+ * codebooks offline with K-Means on the smoothed, rotated key subvectors
+ * (and on raw value subvectors) (paper summary page, "Summary"), and its
+ * ablation compares smoothing, the rotation, both, and their order ("Key
+ * points").  Readings where the pages are silent: s_c = sqrt(max_t |K[t][c]|)
+ * with 0 -> 1; K-Means is Lloyd's algorithm seeded by k-means++ (Arthur and
+ * Vassilvitskii), with the random draws passed in.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * vqkv_smoothing — s[c] = sqrt(max over the n_rows rows of |rows[t][c]|),
+ * correctly rounded fp32, and 1 where that maximum is 0, for the 128
+ * channels.  rows: device [n_rows][128], fp16 (dtype 0) or fp32 (dtype 1),
+ * 16-byte aligned; s: device fp32 [128], 16-byte aligned, written only by
+ * this call (it is also the call's scratch).  n_rows >= 0 (0 gives all 1).
+ * Errors: VQKV_ERR_INVALID_ARG for a NULL or misaligned pointer, a negative
+ * n_rows or another dtype.
+ */
+vqkv_status vqkv_smoothing(const void* rows, int32_t dtype, int64_t n_rows, float* s, void* stream);
+
+/*
+ * vqkv_calib_transform — out[t] = R(x[t] / s_pre) / s_post for the n_rows
+ * rows of 128 channels: R is the normalised Hadamard rotation x . Hn (Hn =
+ * H / sqrt(128), H[i][k] = (-1)^popcount(i & k)) when rotate is nonzero,
+ * else the identity; s_pre / s_post (device fp32 [128]) may each be NULL
+ * (no division).  fp32 arithmetic (one rounding per division, a fast
+ * Walsh-Hadamard transform for R).  x: device [n_rows][128] fp16 (dtype 0)
+ * or fp32 (dtype 1); out: device fp32 [n_rows][128] (may equal x when
+ * dtype is 1).  All pointers 16-byte aligned.  The variants of the
+ * ablation: none (no s, no R), smooth (s_pre), Hadamard (R), both (s_pre,
+ * R: the decode path's key transform), rotate-then-smooth (R, then s_post =
+ * vqkv_smoothing of the rotated rows).
+ */
+vqkv_status vqkv_calib_transform(const void* x, int32_t dtype, int64_t n_rows, const float* s_pre,
+                                 int32_t rotate, const float* s_post, float* out, void* stream);
+
+/*
+ * K-Means on n points of dim (2, 4 or 8) fp32 coordinates into k centroids.
+ *   - Seeding (k-means++): centre 0 is point floor(u[0] * n); centre i is the
+ *     first point (index order) whose running sum of D^2 exceeds
+ *     u[i] * sum D^2, D(x) the distance of x to its nearest chosen centre
+ *     (floor(u[i] * n) when every D^2 is 0).  D^2 is fp32 (the assignment's
+ *     arithmetic), the sums fp64.
+ *   - Assignment: nearest centroid by fp32 squared distance from direct
+ *     differences; ties go to the lowest index.
+ *   - Update: each centroid becomes the fp64 mean of its points rounded to
+ *     fp32; an empty cluster keeps its centroid.  Every step is
+ *     deterministic: the same inputs give the same bits on every run.
+ *   - vqkv_kmeans runs the seeding, then `iters` (assignment, update) steps,
+ *     and writes the fp32 centroids and, if requested, their fp16 rounding.
+ */
+typedef struct {
+  int32_t n;               /* points, >= 1 */
+  int32_t dim;             /* 2, 4 or 8 */
+  int32_t k;               /* centroids, 1 <= k <= min(n, 4096) */
+  int32_t iters;           /* Lloyd steps, 0..1000 */
+  const float* points;     /* device fp32 [n][dim], 16-byte aligned */
+  const float* uniforms;   /* device fp32 [k], draws in [0, 1) */
+  float* centroids;        /* device fp32 [k][dim] out, 16-byte aligned */
+  uint16_t* codebook;      /* device fp16 [k][dim] out, or NULL */
+  int32_t* seeds;          /* device int32 [k] out: the seeding's picks, or NULL */
+  int32_t* assign;         /* device int32 [n] out: the last step's assignment (made
+                              before the last update), or NULL; untouched when iters = 0 */
+  void* workspace;         /* device, >= vqkv_kmeans_workspace_bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} vqkv_kmeans_args;
+
+/* Workspace of vqkv_kmeans (0 for invalid sizes). */
+size_t vqkv_kmeans_workspace_bytes(const vqkv_kmeans_args* args);
+
+/* The whole training.  Errors: VQKV_ERR_INVALID_ARG (sizes, NULL or
+ * misaligned pointers), VQKV_ERR_WORKSPACE, VQKV_ERR_CUDA. */
+vqkv_status vqkv_kmeans(const vqkv_kmeans_args* args, void* stream);
+
+/* The seeding alone: writes args->seeds (required here) and sets
+ * args->centroids to the picked points.  Uses the workspace like
+ * vqkv_kmeans; args->iters, codebook and assign are ignored. */
+vqkv_status vqkv_kmeans_seed(const vqkv_kmeans_args* args, void* stream);
+
+/* One assignment: assign[i] = nearest centroid of point i (int32), and, if
+ * dist is not NULL, its fp32 squared distance.  points / centroids 16-byte
+ * aligned; 1 <= k <= 4096; n >= 0. */
+vqkv_status vqkv_kmeans_assign(const float* points, int32_t n, int32_t dim, const float* centroids, int32_t k,
+                               int32_t* assign, float* dist, void* stream);
+
+/* One update: c_out[c] = fp64 mean of the points with assign == c rounded to
+ * fp32, c_in[c] when there is none.  Assignments outside [0, k) count for no
+ * centroid.  c_out must not overlap c_in.  The points are brought into
+ * cluster order by a stable counting sort in the workspace (device, 256-byte
+ * aligned, >= vqkv_kmeans_update_workspace_bytes(n, k); 0 for invalid
+ * sizes), and each cluster is summed in point order: the result does not
+ * depend on scheduling. */
+size_t vqkv_kmeans_update_workspace_bytes(int32_t n, int32_t k);
+vqkv_status vqkv_kmeans_update(const float* points, int32_t n, int32_t dim, const int32_t* assign, int32_t k,
+                               const float* c_in, float* c_out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* Static, never NULL. */
 const char* vqkv_status_string(vqkv_status status);
 

@@ -39,7 +39,8 @@ def test_struct_layout_matches_header(tmp_path):
     """ctypes mirrors of the argument structs have the C layout (gcc offsetof)."""
     fields = {"vqkv_encode_args": _lib.EncodeArgs, "vqkv_decode_args": _lib.DecodeArgs,
               "vqkv_fp16_decode_args": _lib.Fp16DecodeArgs, "vqkv_decode_append_args": _lib.DecodeAppendArgs,
-              "vqkv_decode_multi_args": _lib.DecodeMultiArgs, "vqkv_paging": _lib.Paging}
+              "vqkv_decode_multi_args": _lib.DecodeMultiArgs, "vqkv_paging": _lib.Paging,
+              "vqkv_kmeans_args": _lib.KmeansArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "vqkv.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -194,3 +195,60 @@ def test_ring_timeout_hook_validation(lib):
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 0, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 5000, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(None, 64, None) == 1
+
+
+def _km(**kw):
+    base = dict(n=1000, dim=4, k=256, iters=20, points=0x1000, uniforms=0x2000, centroids=0x3000,
+                workspace=0x10000, workspace_bytes=1 << 24)
+    base.update(kw)
+    return _lib.KmeansArgs(**base)
+
+
+@pytest.mark.parametrize("kw", [dict(n=0), dict(dim=3), dict(dim=16), dict(k=0), dict(k=4097), dict(k=1001),
+                                dict(iters=-1), dict(iters=1001)])
+def test_kmeans_size_validation(lib, kw):
+    a = _km(**kw)
+    assert lib.vqkv_kmeans_workspace_bytes(ctypes.byref(a)) == 0
+    assert lib.vqkv_kmeans(ctypes.byref(a), None) == 1
+
+
+def test_kmeans_workspace_layout(lib):
+    # D^2 [n] fp32 | assignment [n] int32 | second centroid buffer [k][dim], each padded to 256 bytes
+    # ... then the update's sort scratch: H [k][blocks of 1024] | start [k + 1] | perm [n] | tot [k] int32, + 256
+    upd = lambda n, k: (4 * (k * max(1, -(-n // 1024)) + k + 1 + n + k) + 256 + 255) // 256 * 256
+    assert lib.vqkv_kmeans_update_workspace_bytes(1000, 256) == upd(1000, 256)
+    assert lib.vqkv_kmeans_workspace_bytes(ctypes.byref(_km(n=1000, dim=4, k=256))) == 3 * 4096 + upd(1000, 256)
+    assert lib.vqkv_kmeans_workspace_bytes(ctypes.byref(_km(n=65536, dim=8, k=4096))) == (
+        2 * 262144 + 131072 + upd(65536, 4096))
+    assert lib.vqkv_kmeans_update_workspace_bytes(10, 0) == 0
+
+
+def test_kmeans_pointer_and_workspace_validation(lib):
+    assert lib.vqkv_kmeans(ctypes.byref(_km(points=None)), None) == 1
+    assert lib.vqkv_kmeans(ctypes.byref(_km(points=0x1004)), None) == 1          # 16-byte alignment
+    assert lib.vqkv_kmeans(ctypes.byref(_km(workspace_bytes=100)), None) == 3    # VQKV_ERR_WORKSPACE
+    assert lib.vqkv_kmeans(ctypes.byref(_km(workspace=0x10010)), None) == 1      # 256-byte alignment
+    assert lib.vqkv_kmeans_seed(ctypes.byref(_km(seeds=None)), None) == 1        # seeding needs its picks
+    assert lib.vqkv_kmeans(None, None) == 1
+
+
+def test_kmeans_step_validation(lib):
+    assert lib.vqkv_kmeans_assign(0x1000, 10, 5, 0x2000, 4, 0x3000, None, None) == 1      # dim
+    assert lib.vqkv_kmeans_assign(0x1000, 10, 4, 0x2000, 0, 0x3000, None, None) == 1      # k
+    assert lib.vqkv_kmeans_assign(0x1008, 10, 4, 0x2000, 4, 0x3000, None, None) == 1      # alignment
+    assert lib.vqkv_kmeans_assign(None, 0, 4, None, 4, None, None, None) == 0              # nothing to do
+    ws = 0x100000
+    assert lib.vqkv_kmeans_update(0x1000, 10, 4, 0x3000, 4, 0x2000, 0x2020, ws, 1 << 20, None) == 1   # overlap
+    assert lib.vqkv_kmeans_update(0x1000, 10, 4, 0x3000, 5000, 0x2000, 0x90000, ws, 1 << 20, None) == 1
+    assert lib.vqkv_kmeans_update(0x1000, 10, 4, 0x3000, 4, 0x2000, 0x9000, ws, 8, None) == 3        # workspace
+    assert lib.vqkv_kmeans_update(0x1000, 10, 4, 0x3000, 4, 0x2000, 0x9000, ws + 8, 1 << 20, None) == 1
+
+
+def test_calibration_validation(lib):
+    assert lib.vqkv_smoothing(0x1000, 2, 10, 0x2000, None) == 1        # dtype
+    assert lib.vqkv_smoothing(0x1000, 0, -1, 0x2000, None) == 1        # n_rows
+    assert lib.vqkv_smoothing(0x1000, 0, 10, None, None) == 1          # s
+    assert lib.vqkv_smoothing(0x1000, 0, 10, 0x2004, None) == 1        # s alignment
+    assert lib.vqkv_calib_transform(0x1000, 0, 10, None, 1, None, 0x2008, None) == 1   # out alignment
+    assert lib.vqkv_calib_transform(0x1000, 3, 10, None, 1, None, 0x2000, None) == 1   # dtype
+    assert lib.vqkv_calib_transform(None, 0, 0, None, 1, None, None, None) == 0        # no rows

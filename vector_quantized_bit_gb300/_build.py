@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvqkv.so")
-SOURCES = ["api.cu", "decode.cu", "decode_fp16.cu", "decode_static.cu", "encode.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_fp16.cu", "decode_static.cu", "encode.cu", "kmeans.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

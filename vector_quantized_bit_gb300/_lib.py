@@ -27,7 +27,9 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
             "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_multi", "vqkv_decode_append",
             "vqkv_decode_attn_static", "vqkv_encode_paged", "vqkv_decode_attn_paged", "vqkv_test_decode_ring_timeout",
-            "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_status_string"]
+            "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_smoothing", "vqkv_calib_transform",
+            "vqkv_kmeans_workspace_bytes", "vqkv_kmeans", "vqkv_kmeans_seed", "vqkv_kmeans_assign",
+            "vqkv_kmeans_update_workspace_bytes", "vqkv_kmeans_update", "vqkv_status_string"]
 STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -71,6 +73,13 @@ class Paging(ctypes.Structure):
 
 class DecodeMultiArgs(ctypes.Structure):
     _fields_ = [("decode", DecodeArgs), ("n_queries", ctypes.c_int32)]
+
+
+class KmeansArgs(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("dim", ctypes.c_int32), ("k", ctypes.c_int32), ("iters", ctypes.c_int32),
+                ("points", ctypes.c_void_p), ("uniforms", ctypes.c_void_p), ("centroids", ctypes.c_void_p),
+                ("codebook", ctypes.c_void_p), ("seeds", ctypes.c_void_p), ("assign", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class DecodeAppendArgs(ctypes.Structure):
@@ -123,6 +132,26 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_fp16_decode_workspace_bytes.argtypes = [ctypes.POINTER(Fp16DecodeArgs)]
         L.vqkv_decode_attn_fp16.restype = ctypes.c_int
         L.vqkv_decode_attn_fp16.argtypes = [ctypes.POINTER(Fp16DecodeArgs), ctypes.c_void_p]
+        L.vqkv_smoothing.restype = ctypes.c_int
+        L.vqkv_smoothing.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+        L.vqkv_calib_transform.restype = ctypes.c_int
+        L.vqkv_calib_transform.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                           ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.vqkv_kmeans_workspace_bytes.restype = ctypes.c_size_t
+        L.vqkv_kmeans_workspace_bytes.argtypes = [ctypes.POINTER(KmeansArgs)]
+        for name in ("vqkv_kmeans", "vqkv_kmeans_seed"):
+            getattr(L, name).restype = ctypes.c_int
+            getattr(L, name).argtypes = [ctypes.POINTER(KmeansArgs), ctypes.c_void_p]
+        L.vqkv_kmeans_assign.restype = ctypes.c_int
+        L.vqkv_kmeans_assign.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.vqkv_kmeans_update_workspace_bytes.restype = ctypes.c_size_t
+        L.vqkv_kmeans_update_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        L.vqkv_kmeans_update.restype = ctypes.c_int
+        L.vqkv_kmeans_update.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]
         L.vqkv_status_string.restype = ctypes.c_char_p
         L.vqkv_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -318,3 +347,88 @@ def fp16_decode_workspace(B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device
     if n == 0:
         raise VqkvError(1, "vqkv_fp16_decode_workspace_bytes")
     return torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- calibration
+
+def _check(st: int, what: str) -> None:
+    if st != 0:
+        raise VqkvError(st, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return 0
+    if t.dtype == torch.float32:
+        return 1
+    raise TypeError(f"rows must be fp16 or fp32, not {t.dtype}")
+
+
+def vqkv_smoothing(rows, s, stream=None) -> None:
+    """s fp32 [128] <- sqrt(max_t |rows[t]|) (0 -> 1); rows fp16 or fp32 [n][128] (device)."""
+    _check(lib().vqkv_smoothing(_ptr(rows), _dtype_code(rows), rows.shape[0], _ptr(s), _stream(stream)),
+           "vqkv_smoothing")
+
+
+def vqkv_calib_transform(x, out, s_pre=None, rotate=False, s_post=None, stream=None) -> None:
+    """out fp32 [n][128] <- R(x / s_pre) / s_post (R: the normalised Hadamard rotation if ``rotate``)."""
+    _check(lib().vqkv_calib_transform(_ptr(x), _dtype_code(x), x.shape[0], _ptr(s_pre), int(bool(rotate)),
+                                      _ptr(s_post), _ptr(out), _stream(stream)), "vqkv_calib_transform")
+
+
+def kmeans_args(points, uniforms, centroids, iters=0, codebook=None, seeds=None, assign=None, workspace=None):
+    n, dim = points.shape
+    a = KmeansArgs(n=n, dim=dim, k=centroids.shape[0], iters=iters, points=_ptr(points), uniforms=_ptr(uniforms),
+                   centroids=_ptr(centroids), codebook=_ptr(codebook), seeds=_ptr(seeds), assign=_ptr(assign))
+    if workspace is not None:
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def kmeans_workspace(n, dim, k, device="cuda"):
+    """A workspace tensor of the size vqkv_kmeans needs."""
+    import torch
+    a = KmeansArgs(n=n, dim=dim, k=k)
+    nbytes = int(lib().vqkv_kmeans_workspace_bytes(ctypes.byref(a)))
+    if nbytes == 0:
+        raise VqkvError(1, "vqkv_kmeans_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def vqkv_kmeans(points, uniforms, centroids, iters, codebook=None, seeds=None, assign=None, workspace=None,
+                stream=None) -> None:
+    """k-means++ seeding and ``iters`` Lloyd steps: points fp32 [n][dim] -> centroids fp32 [k][dim]
+    (codebook fp16 [k][dim], seeds int32 [k], assign int32 [n] optional)."""
+    if workspace is None:
+        workspace = kmeans_workspace(points.shape[0], points.shape[1], centroids.shape[0], points.device)
+    a = kmeans_args(points, uniforms, centroids, iters, codebook, seeds, assign, workspace)
+    _check(lib().vqkv_kmeans(ctypes.byref(a), _stream(stream)), "vqkv_kmeans")
+
+
+def vqkv_kmeans_seed(points, uniforms, centroids, seeds, workspace=None, stream=None) -> None:
+    """k-means++ seeding only: seeds int32 [k], centroids fp32 [k][dim] = the picked points."""
+    if workspace is None:
+        workspace = kmeans_workspace(points.shape[0], points.shape[1], centroids.shape[0], points.device)
+    a = kmeans_args(points, uniforms, centroids, 0, None, seeds, None, workspace)
+    _check(lib().vqkv_kmeans_seed(ctypes.byref(a), _stream(stream)), "vqkv_kmeans_seed")
+
+
+def vqkv_kmeans_assign(points, centroids, assign, dist=None, stream=None) -> None:
+    """assign int32 [n] (and dist fp32 [n]) <- nearest centroid of each point."""
+    n, dim = points.shape
+    _check(lib().vqkv_kmeans_assign(_ptr(points), n, dim, _ptr(centroids), centroids.shape[0], _ptr(assign),
+                                    _ptr(dist), _stream(stream)), "vqkv_kmeans_assign")
+
+
+def vqkv_kmeans_update(points, assign, c_in, c_out, workspace=None, stream=None) -> None:
+    """c_out <- per-cluster fp64 means of the points (c_in for empty clusters)."""
+    import torch
+    n, dim = points.shape
+    k = c_in.shape[0]
+    if workspace is None:
+        nbytes = int(lib().vqkv_kmeans_update_workspace_bytes(n, k))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=c_in.device)
+    _check(lib().vqkv_kmeans_update(_ptr(points), n, dim, _ptr(assign), k, _ptr(c_in), _ptr(c_out),
+                                    _ptr(workspace), workspace.numel(), _stream(stream)), "vqkv_kmeans_update")
