@@ -63,6 +63,10 @@ def parse():
     ap.add_argument("--profile-fp16", type=int, default=0,
                     help="run this many fp16-KV comparison decodes of the workload (eager) and exit: the "
                          "command the fp16 kernel's ncu summary is taken with")
+    ap.add_argument("--calib", action="store_true",
+                    help="time the offline calibration stage (smoothing, key transform, K-Means training) instead")
+    ap.add_argument("--ablation", action="store_true",
+                    help="codebook utilisation and reconstruction error of the five key transforms instead")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
@@ -745,10 +749,195 @@ def fp16_baseline(w, kv, lens, dev, stream, launches=60, reps=5):
             "how": "graph of 60 launches x 5 replays, CUDA events; fp16 K/V of the same synthetic cache"}
 
 
+# ------------------------------------------------------------- calibration stage
+
+CALIB_POINTS = 65536          # sampled subvectors a codebook is trained on
+CALIB_ITERS = 20              # Lloyd steps after k-means++
+CALIB_SHAPES = ((256, 4), (4096, 8))
+
+
+def _calib_rows(w, kvh=0):
+    """Key rows (fp16 [L][128]) of one KV head of the workload, as generated for its cache."""
+    return synth.keys(w, 0, kvh, 0, w.seq_len)
+
+
+def _time_cuda(fn, reps, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _sample_points(xt, dim, n_points, rng):
+    """n_points subvectors of dim channels from randomly chosen rows of xt (fp32 [L][128], device)."""
+    import torch
+    rows = n_points * dim // 128
+    idx = np.sort(rng.choice(xt.shape[0], size=rows, replace=False))
+    return xt[torch.from_numpy(idx).to(xt.device)].reshape(-1, dim).contiguous()
+
+
+def run_calibration(args):
+    """The offline stage on one KV head of the Llama-shaped workload: key
+    smoothing over its 196,608 rows, the smooth + rotate transform, and
+    K-Means training (k-means++ then 20 Lloyd steps) of a 256 x 4 and a
+    4096 x 8 codebook from 65,536 sampled subvectors.  Headline: the Lloyd
+    assignment rate of the 4096 x 8 codebook (distance evaluations per second)
+    against the fp32 ALU roofline."""
+    import torch
+    from vector_quantized_bit_gb300 import _lib
+    w = synth.WORKLOADS[1]
+    dev = torch.device("cuda")
+    rows = torch.from_numpy(_calib_rows(w)).to(dev)
+    L = rows.shape[0]
+    s = torch.empty(128, dtype=torch.float32, device=dev)
+    xt = torch.empty((L, 128), dtype=torch.float32, device=dev)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    t_smooth = _time_cuda(lambda: _lib.vqkv_smoothing(rows, s), 20)
+    t_xf = _time_cuda(lambda: _lib.vqkv_calib_transform(rows, xt, s_pre=s, rotate=True), 20)
+    rng = np.random.default_rng(0)
+    shapes = {}
+    for k, dim in CALIB_SHAPES:
+        pts = _sample_points(xt, dim, CALIB_POINTS, rng)
+        u = torch.from_numpy(rng.random(k).astype(np.float32)).to(dev)
+        cent = torch.empty((k, dim), dtype=torch.float32, device=dev)
+        cent2 = torch.empty_like(cent)
+        seeds = torch.empty(k, dtype=torch.int32, device=dev)
+        idx = torch.empty(CALIB_POINTS, dtype=torch.int32, device=dev)
+        ws = _lib.kmeans_workspace(CALIB_POINTS, dim, k)
+        t_seed = _time_cuda(lambda: _lib.vqkv_kmeans_seed(pts, u, cent, seeds, workspace=ws), 3, 1)
+        t_assign = _time_cuda(lambda: _lib.vqkv_kmeans_assign(pts, cent, idx), 50)
+        t_update = _time_cuda(lambda: _lib.vqkv_kmeans_update(pts, idx, cent, cent2), 50)
+        t_train = _time_cuda(lambda: _lib.vqkv_kmeans(pts, u, cent, CALIB_ITERS, workspace=ws), 3, 1)
+        evals = CALIB_POINTS * k
+        shapes[f"{k}x{dim}"] = {"seed_ms": t_seed, "assign_us": t_assign * 1e3, "update_us": t_update * 1e3,
+                                "train_ms": t_train, "assign_evals_per_s": evals / (t_assign * 1e-3)}
+    clocks = clk.stop()
+    props = torch.cuda.get_device_properties(dev)
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    ops = 2 * 8 + 3   # per evaluation at dim 8: 8 sub, 1 mul, 7 fma, compare + 2 selects
+    peak = props.multi_processor_count * 128 * mhz * 1e6 / ops
+    head = shapes["4096x8"]
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import kmeans_oracle as ko
+        p_np = _sample_points(xt, 8, CALIB_POINTS, np.random.default_rng(1)).cpu().numpy()[:1024]
+        c_np = p_np[:512].copy()
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            ko.assign(p_np, c_np)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * 1024 * 512 / dt, "unit": "distance evals/s", "cores": 1, "kind": "oracle",
+               "sample": f"oracle assignment of 1024 points x 512 centroids (dim 8), {reps} passes, {dt:.1f} s"}
+    print(json.dumps({
+        "metric": "K-Means Lloyd assignment distance evaluations/s (4096 x 8 codebook, 65,536 subvectors)",
+        "value": head["assign_evals_per_s"], "unit": "evals/s", "higher_is_better": True, "n_gpus": 1,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "calibration_llama8b_kvh0_l196608", "rows": L, "points": CALIB_POINTS,
+                   "iters": CALIB_ITERS, "l2": "points (2 MB) stay in L2: the assignment is ALU-bound"},
+        "roofline": {"bound": "alu", "achieved": head["assign_evals_per_s"] / 1e12, "peak": peak / 1e12,
+                     "unit": "T evals/s", "frac": head["assign_evals_per_s"] / peak, "traffic": None,
+                     "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 lanes x {mhz:.0f} MHz / "
+                                    f"{ops} ops per evaluation"},
+        "stages": {"smoothing_us": t_smooth * 1e3, "smoothing_GB_per_s": L * 256 / (t_smooth * 1e-3) / 1e9,
+                   "transform_us": t_xf * 1e3, "transform_GB_per_s": L * (256 + 512) / (t_xf * 1e-3) / 1e9,
+                   **{f"kmeans_{key}": val for key, val in shapes.items()}},
+        "cpu_baseline": cpu, "clocks": clocks}))
+
+
+ABLATION_VARIANTS = ("none", "smooth", "hadamard", "smooth_hadamard", "hadamard_smooth")
+
+
+def run_ablation(args):
+    """Codebook utilisation and key reconstruction error of the five key
+    transforms, for the 256 x 4 and 4096 x 8 codebooks, on one KV head of the
+    Llama-shaped outlier keys (196,608 rows).  On the GPU: smoothing, the
+    transform, k-means++ + 20 Lloyd steps on 65,536 sampled subvectors, and
+    the assignment of every subvector of every row.  On the host (measurement
+    only): the reconstruction from the codes, its relative error against the
+    original keys, and the relative error of q.k scores for 16 random
+    queries."""
+    import scipy.linalg
+    import torch
+    from vector_quantized_bit_gb300 import _lib
+    w = synth.WORKLOADS[1]
+    dev = torch.device("cuda")
+    k_np = _calib_rows(w)
+    rows = torch.from_numpy(k_np).to(dev)
+    L = rows.shape[0]
+    k64 = k_np.astype(np.float64)
+    hn = scipy.linalg.hadamard(128).astype(np.float64) / np.sqrt(128.0)
+    q = np.random.default_rng(5).standard_normal((16, 128))
+    scores = k64 @ q.T
+    out = {}
+    for variant in ABLATION_VARIANTS:
+        xt = torch.empty((L, 128), dtype=torch.float32, device=dev)
+        s = torch.empty(128, dtype=torch.float32, device=dev)
+        if variant == "none":
+            _lib.vqkv_calib_transform(rows, xt)
+        elif variant in ("smooth", "smooth_hadamard"):
+            _lib.vqkv_smoothing(rows, s)
+            _lib.vqkv_calib_transform(rows, xt, s_pre=s, rotate=variant == "smooth_hadamard")
+        elif variant == "hadamard":
+            _lib.vqkv_calib_transform(rows, xt, rotate=True)
+        else:
+            rot = torch.empty_like(xt)
+            _lib.vqkv_calib_transform(rows, rot, rotate=True)
+            _lib.vqkv_smoothing(rot, s)
+            _lib.vqkv_calib_transform(rot, xt, s_post=s)
+        s_np = s.cpu().numpy().astype(np.float64)
+        res = {}
+        for k, dim in CALIB_SHAPES:
+            rng = np.random.default_rng(k)
+            pts = _sample_points(xt, dim, CALIB_POINTS, rng)
+            u = torch.from_numpy(rng.random(k).astype(np.float32)).to(dev)
+            cent = torch.empty((k, dim), dtype=torch.float32, device=dev)
+            cb = torch.empty((k, dim), dtype=torch.float16, device=dev)
+            _lib.vqkv_kmeans(pts, u, cent, CALIB_ITERS, codebook=cb)
+            allp = xt.reshape(-1, dim)
+            codes = torch.empty(allp.shape[0], dtype=torch.int32, device=dev)
+            _lib.vqkv_kmeans_assign(allp, cb.float().contiguous(), codes)
+            c = codes.cpu().numpy()
+            rec = cb.float().cpu().numpy().astype(np.float64)[c].reshape(L, 128)
+            if variant == "smooth":
+                rec = rec * s_np
+            elif variant == "hadamard":
+                rec = rec @ hn.T
+            elif variant == "smooth_hadamard":
+                rec = (rec @ hn.T) * s_np
+            elif variant == "hadamard_smooth":
+                rec = (rec * s_np) @ hn.T
+            err = rec - k64
+            counts = np.bincount(c, minlength=k).astype(np.float64)
+            pr = counts[counts > 0] / counts.sum()
+            res[f"{k}x{dim}"] = {
+                "key_rel_mse": float((err * err).sum() / (k64 * k64).sum()),
+                "score_rel_err": float(np.linalg.norm(rec @ q.T - scores) / np.linalg.norm(scores)),
+                "used_fraction": float((counts > 0).mean()), "code_entropy_bits": float(-(pr * np.log2(pr)).sum())}
+        out[variant] = res
+    print(json.dumps({"metric": "key transform ablation: codebook utilisation and reconstruction error",
+                      "data": "synthetic", "config": {"workload": "llama8b_kvh0_l196608_outlier_keys", "rows": L,
+                                                      "points": CALIB_POINTS, "iters": CALIB_ITERS},
+                      "ablation": out}))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.calib:
+        run_calibration(args)
+    elif args.ablation:
+        run_ablation(args)
     else:
         run_ours(args)
 
