@@ -35,14 +35,17 @@ import numpy as np
 HEAD_DIM = 128
 MODE_VQ2 = 0
 MODE_VQ15 = 1
+MODE_VQ4 = 2
 ROLE_K = 0
 ROLE_V = 1
 
 # (entries, subvector dims) per mode [P1 Key points: 2^8 x 4 and 2^12 x 8]
-GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8)}
+# and, within the pages' 1.25-4 bit range [P1 Summary], 4 bit = 2^8 x 2
+GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2)}
 # tokens per layout tile and bytes per tile of one cache stream
-TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64}
-TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536}
+TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64, MODE_VQ4: 16}
+TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536, MODE_VQ4: 1024}
+BYTE_CODE_MODES = (MODE_VQ2, MODE_VQ4)   # one byte per code
 
 
 # ----------------------------------------------------------------------------
@@ -176,6 +179,20 @@ def vq2_offset(role: int, t: int, j: int) -> int:
     return 512 * tile + 16 * lane + 4 * (j // 8) + 2 * (r // 8) + (r % 2)
 
 
+def vq4_offset(role: int, t: int, j: int) -> int:
+    """Byte holding the 8-bit code of subvector j (0..63, channels 2j, 2j+1) of token t."""
+    tile, r = divmod(t, 16)
+    if role == ROLE_K:
+        lane = 4 * (r % 8) + (j % 4)
+        return 1024 * tile + 32 * lane + 16 * (r // 8) + 2 * (j // 8) + (j // 4) % 2
+    lane = 4 * (j % 8) + (r % 8) // 2
+    return 1024 * tile + 32 * lane + 4 * (j // 8) + 2 * (r // 8) + (r % 2)
+
+
+def byte_offset(mode: int, role: int, t: int, j: int) -> int:
+    return vq2_offset(role, t, j) if mode == MODE_VQ2 else vq4_offset(role, t, j)
+
+
 def vq15_offset(role: int, t: int, pair: int) -> int:
     """First of the 3 bytes holding the code pair (pair, pair+8) of token t."""
     tile, rem = divmod(t, 64)
@@ -201,10 +218,10 @@ def pack_stream(codes: np.ndarray, mode: int, role: int, cap_len: int,
     """codes int [L][n_sub] (token t at row t) -> uint8 stream of code_bytes."""
     buf = np.zeros(code_bytes(mode, cap_len), dtype=np.uint8) if out is None else out
     L = codes.shape[0]
-    if mode == MODE_VQ2:
+    if mode in BYTE_CODE_MODES:
         for t in range(L):
-            for j in range(32):
-                buf[vq2_offset(role, t, j)] = int(codes[t, j])
+            for j in range(codes.shape[1]):
+                buf[byte_offset(mode, role, t, j)] = int(codes[t, j])
     else:
         for t in range(L):
             for p in range(8):
@@ -215,11 +232,12 @@ def pack_stream(codes: np.ndarray, mode: int, role: int, cap_len: int,
 
 def unpack_stream(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
     """uint8 stream -> codes int64 [L][n_sub]."""
-    if mode == MODE_VQ2:
-        out = np.empty((L, 32), dtype=np.int64)
+    if mode in BYTE_CODE_MODES:
+        nsub = HEAD_DIM // GEOMETRY[mode][1]
+        out = np.empty((L, nsub), dtype=np.int64)
         for t in range(L):
-            for j in range(32):
-                out[t, j] = buf[vq2_offset(role, t, j)]
+            for j in range(nsub):
+                out[t, j] = buf[byte_offset(mode, role, t, j)]
         return out
     out = np.empty((L, 16), dtype=np.int64)
     for t in range(L):
@@ -230,9 +248,16 @@ def unpack_stream(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
 
 
 def offset_table(mode: int, role: int, L: int) -> np.ndarray:
-    """Byte offset of every code (VQ2) or code pair (VQ15) of tokens [0, L):
-    a vectorised form of the offset functions above, for large streams."""
+    """Byte offset of every code (VQ2, VQ4) or code pair (VQ15) of tokens
+    [0, L): a vectorised form of the offset functions above, for large
+    streams."""
     t = np.arange(L)[:, None]
+    if mode == MODE_VQ4:
+        j = np.arange(64)[None, :]
+        tile, r = t // 16, t % 16
+        if role == ROLE_K:
+            return 1024 * tile + 32 * (4 * (r % 8) + j % 4) + 16 * (r // 8) + 2 * (j // 8) + (j // 4) % 2
+        return 1024 * tile + 32 * (4 * (j % 8) + (r % 8) // 2) + 4 * (j // 8) + 2 * (r // 8) + r % 2
     if mode == MODE_VQ2:
         j = np.arange(32)[None, :]
         tile, r = t // 16, t % 16
@@ -250,7 +275,7 @@ def offset_table(mode: int, role: int, L: int) -> np.ndarray:
 def pack_stream_fast(codes: np.ndarray, mode: int, role: int, cap_len: int) -> np.ndarray:
     buf = np.zeros(code_bytes(mode, cap_len), dtype=np.uint8)
     off = offset_table(mode, role, codes.shape[0])
-    if mode == MODE_VQ2:
+    if mode in BYTE_CODE_MODES:
         buf[off] = codes.astype(np.uint8)
     else:
         lo, hi = codes[:, :8].astype(np.int64), codes[:, 8:].astype(np.int64)
@@ -262,7 +287,7 @@ def pack_stream_fast(codes: np.ndarray, mode: int, role: int, cap_len: int) -> n
 
 def unpack_stream_fast(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
     off = offset_table(mode, role, L)
-    if mode == MODE_VQ2:
+    if mode in BYTE_CODE_MODES:
         return buf[off].astype(np.int64)
     b0, b1, b2 = (buf[off + k].astype(np.int64) for k in range(3))
     return np.concatenate([b0 | ((b1 & 0xF) << 8), (b1 >> 4) | (b2 << 4)], axis=1)

@@ -151,10 +151,13 @@ def test_near_tie_rule():
 def check_bits():
     assert vo.bits_per_element(vo.MODE_VQ2) == 2.0
     assert vo.bits_per_element(vo.MODE_VQ15) == 1.5
-    for mode, cap in ((vo.MODE_VQ2, 16), (vo.MODE_VQ2, 196608), (vo.MODE_VQ15, 64), (vo.MODE_VQ15, 65536)):
+    assert vo.bits_per_element(vo.MODE_VQ4) == 4.0
+    for mode, cap in ((vo.MODE_VQ2, 16), (vo.MODE_VQ2, 196608), (vo.MODE_VQ15, 64), (vo.MODE_VQ15, 65536),
+                      (vo.MODE_VQ4, 16), (vo.MODE_VQ4, 16384)):
         assert vo.code_bytes(mode, cap) * 8 / (cap * 128) == vo.bits_per_element(mode)
     assert vo.code_bytes(vo.MODE_VQ2, 17) == 1024      # rounded up to whole tiles
     assert vo.code_bytes(vo.MODE_VQ15, 65) == 3072
+    assert vo.code_bytes(vo.MODE_VQ4, 17) == 2048
 
 
 def check_layout_golden():
@@ -162,6 +165,10 @@ def check_layout_golden():
         role, t, j, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
         assert vo.vq2_offset(r, int(t), int(j)) == int(off), line
+    for line in golden_lines("layout_vq4.txt"):
+        role, t, j, off = line.split()
+        r = vo.ROLE_K if role == "K" else vo.ROLE_V
+        assert vo.vq4_offset(r, int(t), int(j)) == int(off), line
     for line in golden_lines("layout_vq15.txt"):
         role, t, p, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
@@ -173,15 +180,19 @@ def check_layout_golden():
 
 
 def check_layout_bijective():
-    for mode, role in ((0, 0), (0, 1), (1, 0), (1, 1)):
+    for mode, role in ((0, 0), (0, 1), (1, 0), (1, 1), (2, 0), (2, 1)):
         T = vo.TILE_TOKENS[mode]
-        if mode == vo.MODE_VQ2:
+        if mode == vo.MODE_VQ4:
+            offs = [vo.vq4_offset(role, t, j) for t in range(2 * T) for j in range(64)]
+        elif mode == vo.MODE_VQ2:
             offs = [vo.vq2_offset(role, t, j) for t in range(2 * T) for j in range(32)]
         else:
             offs = [vo.vq15_offset(role, t, p) + k for t in range(2 * T) for p in range(8) for k in range(3)]
         assert sorted(offs) == list(range(2 * vo.TILE_BYTES[mode]))
         tab = vo.offset_table(mode, role, 2 * T)
-        if mode == vo.MODE_VQ2:
+        if mode == vo.MODE_VQ4:
+            ref = [[vo.vq4_offset(role, t, j) for j in range(64)] for t in range(2 * T)]
+        elif mode == vo.MODE_VQ2:
             ref = [[vo.vq2_offset(role, t, j) for j in range(32)] for t in range(2 * T)]
         else:
             ref = [[vo.vq15_offset(role, t, p) for p in range(8)] for t in range(2 * T)]
@@ -202,7 +213,7 @@ def test_layout_bijective():
 
 def test_pack_roundtrip():
     r = np.random.default_rng(1)
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             L = 150
@@ -219,7 +230,7 @@ def test_pack_roundtrip():
 
 def test_append_does_not_touch_neighbours():
     """Writing token t changes only token t's bytes (token-local packing)."""
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             codes = np.zeros((64, 128 // dsub), dtype=np.int64)
@@ -431,6 +442,14 @@ def test_planted_layout(monkeypatch):
     real = vo.vq2_offset
     monkeypatch.setattr(vo, "vq2_offset",
                         lambda role, t, j: real(1 - role, t, j))
+    assert _fails(check_layout_golden)
+
+
+def test_planted_vq4_half_order(monkeypatch):
+    """Swapping the two subvectors a K lane's byte pair holds must fail a pin."""
+    real = vo.vq4_offset
+    monkeypatch.setattr(vo, "vq4_offset",
+                        lambda role, t, j: real(role, t, j ^ 4) if role == vo.ROLE_K else real(role, t, j))
     assert _fails(check_layout_golden)
 
 
