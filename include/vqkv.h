@@ -48,12 +48,19 @@
  *     u = (t % 64) / 16 and r = t % 16, the first byte of pair p of token t is
  *       K: 1536*(t/64) + 48*(4*(r%8) + p%4) + 12*u + 6*(r/8) + 3*(p/4)
  *       V: 1536*(t/64) + 48*(4*p + (r%8)/2) + 12*u + 3*((r%2) + 2*(r/8))
- *   Both layouts are token-local: writing token t changes no byte of any other
- *   token.  Bits per element: 512*8/(16*128) = 2 and 1536*8/(64*128) = 1.5.
+ *   VQKV_MODE_VQ4 (256 entries x 2 dims, 8-bit codes, 64 codes per token;
+ *   within the 1.25-4 bit range the paper's summary page covers, "Summary"):
+ *     TILE = 16 tokens, 1024 bytes.  With r = t % 16 and subvector j (0..63,
+ *     channels 2j, 2j+1):
+ *       K: byte 1024*(t/16) + 32*(4*(r%8) + j%4) + 16*(r/8) + 2*(j/8) + (j/4)%2
+ *       V: byte 1024*(t/16) + 32*(4*(j%8) + (r%8)/2) + 4*(j/8) + 2*(r/8) + r%2
+ *   All three layouts are token-local: writing token t changes no byte of any
+ *   other token.  Bits per element: 512*8/(16*128) = 2, 1536*8/(64*128) = 1.5
+ *   and 1024*8/(16*128) = 4.
  *   (The layouts place, for each of the 32 lanes of a warp, the codes that
- *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2)
- *   or 48-byte (VQ15) run, so a warp reads a tile with coalesced 128-bit
- *   loads.)
+ *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2),
+ *   48-byte (VQ15) or 32-byte (VQ4) run, so a warp reads a tile with
+ *   coalesced 128-bit loads.)
  */
 #ifndef VQKV_H
 #define VQKV_H
@@ -76,7 +83,9 @@ typedef enum {
 
 typedef enum {
   VQKV_MODE_VQ2 = 0,   /* 2 bit:   2^8 entries x 4 dims, 8-bit codes  */
-  VQKV_MODE_VQ15 = 1   /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
+  VQKV_MODE_VQ15 = 1,  /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
+  VQKV_MODE_VQ4 = 2    /* 4 bit:   2^8 entries x 2 dims, 8-bit codes (decode, encode, multi-query,
+                          paged; not the fused append) */
 } vqkv_mode;
 
 typedef enum {

@@ -60,6 +60,8 @@ def test_struct_layout_matches_header(tmp_path):
 
 
 def test_code_bytes(lib):
+    assert lib.vqkv_code_bytes(2, 16384) == 16384 * 64
+    assert lib.vqkv_code_bytes(2, 17) == 2048
     assert lib.vqkv_code_bytes(0, 196608) == 196608 * 32
     assert lib.vqkv_code_bytes(1, 65536) == 65536 * 24
     assert lib.vqkv_code_bytes(0, 1) == 512
@@ -114,7 +116,7 @@ def test_null_args(lib):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(head_dim=256), 2), (dict(mode=2), 2), (dict(role=2), 1), (dict(Hkv=0), 1), (dict(n_rows=-1), 1),
+    (dict(head_dim=256), 2), (dict(mode=3), 2), (dict(role=2), 1), (dict(Hkv=0), 1), (dict(n_rows=-1), 1),
     (dict(cap_len=0), 1), (dict(x=None), 1), (dict(pos=None), 1), (dict(codebook=None), 1),
     (dict(codes=None), 1), (dict(s=None), 1), (dict(x=0x1004), 1), (dict(codebook=0x4008), 1),
 ])
@@ -149,6 +151,8 @@ def test_decode_append_validation(lib):
     a = _lib.DecodeAppendArgs()
     a.decode = _dec(mode=1)
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # 2-bit only
+    a.decode = _dec(mode=2)
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2
     a.decode = _dec()
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1    # no new rows
     a.k_new, a.v_new = 0x10000, 0x10004                             # v_new not 8-byte aligned
@@ -192,6 +196,7 @@ def test_paging_required_and_empty_batch(lib):
 
 def test_ring_timeout_hook_validation(lib):
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=1)), 64, None) == 2   # 2-bit only
+    assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=2)), 64, None) == 2
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 0, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 5000, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(None, 64, None) == 1

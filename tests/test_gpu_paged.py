@@ -41,6 +41,7 @@ def _gather(pool, table, mode, block_tokens, cap):
     (0, 2, 4, 1, [700, 1], 768, 64, 7),       # small blocks: a 48-token step spans two blocks
     (1, 2, 10, 2, [300, 190], 384, 128, 0),   # 1.5 bit, several sequences per CTA
     (1, 1, 4, 1, [1024], 1024, 64, 3),
+    (2, 2, 8, 2, [1000, 300], 1024, 64, 5),   # 4 bit: a 32-token step spans two 64-token blocks
 ])
 def test_paged_equals_contiguous_and_oracle(mode, B, Hq, Hkv, lens, cap, block_tokens, num_splits):
     t = H.torch()
@@ -82,7 +83,7 @@ def test_paged_equals_contiguous_and_oracle(mode, B, Hq, Hkv, lens, cap, block_t
     assert vo.o_error(o, vo.decode_attention(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_block_ids_outside_the_pool_are_reported(mode):
     t = H.torch()
     s, kcb, vcb = H.random_codebooks(mode, 1, 4)

@@ -17,8 +17,8 @@ constexpr size_t kWsHeader = 256;   // word 0: device error flags
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int decode_bpsm[3] = {0, 0, 0};   // resident decode CTAs per SM: VQ2, VQ15, fp16
-  int encode_bpsm[2] = {0, 0};
+  int decode_bpsm[4] = {0, 0, 0, 0};   // resident decode CTAs per SM: VQ2, VQ15, VQ4, fp16
+  int encode_bpsm[3] = {0, 0, 0};
 };
 
 std::mutex g_mu;
@@ -32,7 +32,7 @@ vqkv_status device_info(DeviceInfo* out) {
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return VQKV_ERR_NO_DEVICE;
-    for (int m = 0; m < 2; ++m) {
+    for (int m = 0; m < kCodeModes; ++m) {
       if (decode_prepare(m) != cudaSuccess || encode_prepare(m) != cudaSuccess) return VQKV_ERR_CUDA;
       if (decode_occupancy(m, &d.decode_bpsm[m]) != cudaSuccess) return VQKV_ERR_CUDA;
       if (encode_occupancy(m, &d.encode_bpsm[m]) != cudaSuccess) return VQKV_ERR_CUDA;
@@ -54,7 +54,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Sizes only (what the split plan and the workspace size depend on).
 vqkv_status validate_decode_sizes(const vqkv_decode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
@@ -66,7 +66,7 @@ vqkv_status validate_decode_sizes(const vqkv_decode_args* a) {
 
 vqkv_status validate_decode(const vqkv_decode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
@@ -100,7 +100,7 @@ void set_paging(P& p, const vqkv_paging* pg, int mode) {
   if (pg == nullptr) return;
   p.block_table = pg->block_table;
   p.max_blocks = pg->max_blocks;
-  p.block_tiles = pg->block_tokens / (mode == VQKV_MODE_VQ2 ? 16 : 64);
+  p.block_tiles = pg->block_tokens / decode_tile_tokens(mode);
   p.block_shift = 0;
   while ((1 << p.block_shift) < p.block_tiles) ++p.block_shift;
   p.num_blocks = pg->num_blocks;
@@ -149,7 +149,7 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   const int cgroups = (g * a->M + 7) / 8;   // CTAs per (sequence group, KV head, split)
   const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg) * cgroups;
   // per-CTA prologue + merge in tile units
-  const double setup_tiles = (a->mode == VQKV_MODE_VQ2) ? 12.0 : (a->mode == VQKV_MODE_VQ15) ? 24.0 : 4.0;
+  const double setup_tiles = (a->mode == VQKV_MODE_VQ15) ? 24.0 : (a->mode == kModeFp16) ? 4.0 : 12.0;
   long long best_n = 1;
   double best_cost = 1e300;
   if (a->num_splits > 0) {
@@ -184,7 +184,7 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
 
 vqkv_status validate_encode(const vqkv_encode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15) return VQKV_ERR_UNSUPPORTED;
+  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
   if (a->role != VQKV_ROLE_K && a->role != VQKV_ROLE_V) return VQKV_ERR_INVALID_ARG;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hkv < 1 || a->n_rows < 0 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
@@ -248,6 +248,7 @@ size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
   if (cap_len < 0) return 0;
   if (mode == VQKV_MODE_VQ2) return (size_t)((cap_len + 15) / 16) * 512;
   if (mode == VQKV_MODE_VQ15) return (size_t)((cap_len + 63) / 64) * 1536;
+  if (mode == VQKV_MODE_VQ4) return (size_t)((cap_len + 15) / 16) * 1024;
   return 0;
 }
 

@@ -36,6 +36,8 @@
 //              M-tiles 2p, 2p+1; VQ15: J = 8p+gid over M-tiles 4p..4p+3),
 //              k = the four tokens above; centroid halves are paired across
 //              tokens with byte permutes.
+#include <type_traits>
+
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "encode_common.cuh"
@@ -58,9 +60,6 @@ constexpr int V2_WARPS = VQKV_V2_WARPS;             // one CTA per SM
 constexpr int V2_TPI = VQKV_V2_TPI;                 // 16-token tiles per step (a "super-tile")
 constexpr int V2_THREADS = V2_WARPS * 32;
 constexpr int V2_TILE = 16;
-constexpr int V2_TILE_BYTES = 512;
-constexpr int V2_REPL = 16;                         // replicas of each centroid (bank spreading)
-static_assert(V2_REPL * 8 == 128, "one 128-byte half row per codebook");
 constexpr int V2_CB_BYTES = 256 * 256;              // [code][K replicas (128 B) | V replicas (128 B)]
 // q' rows (fp32, 128 channels) at a pitch that keeps the 8 lanes of each
 // quarter-warp on distinct 16-byte bank groups when the MMA fragments are
@@ -68,10 +67,22 @@ constexpr int V2_CB_BYTES = 256 * 256;              // [code][K replicas (128 B)
 constexpr int V2_Q_PITCH = 144;
 constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][V2_Q_PITCH]) after the codebooks
 constexpr int V2_STAGES = VQKV_V2_STAGES;           // per-warp ring of super-tiles (K then V)
-constexpr int V2_STAGE_BYTES = 2 * V2_TPI * V2_TILE_BYTES;
 constexpr int V2_RING_OFF = V2_Q_OFF + 8 * V2_Q_PITCH * 4;
-constexpr int V2_RING_BYTES = V2_WARPS * V2_STAGES * V2_STAGE_BYTES;
-constexpr int V2_MBAR_OFF = V2_RING_OFF + V2_RING_BYTES;
+
+// Geometry of the byte-code decode: DSUB = 4 is the 2-bit mode (256 x 4, 32
+// codes per token), DSUB = 2 the 4-bit mode (256 x 2, 64 codes per token).
+// Both keep the 64-KB replicated codebook and q' prefix; the 4-bit tile is
+// twice as long, so its steps are two tiles.
+template <int DSUB>
+struct V2Geo {
+  static constexpr int TILE_BYTES = 16 * (kHeadDim / DSUB);    // 16 tokens x one byte per subvector
+  static constexpr int LANE_WORDS = TILE_BYTES / 32 / 16;      // a lane's 128-bit code words per tile and role
+  static constexpr int TPI = DSUB == 4 ? V2_TPI : 2;           // tiles per step
+  static constexpr int STAGE_BYTES = 2 * TPI * TILE_BYTES;
+  static constexpr int RING_OFF = V2_RING_OFF;
+  static constexpr int MBAR_OFF = RING_OFF + V2_WARPS * V2_STAGES * STAGE_BYTES;
+  static constexpr int REPL = 128 / (2 * DSUB);                // replicas of a centroid per 128-byte half row
+};
 
 // ------------------------------------------------------------------ VQ15
 constexpr int V15_WARPS = 16;
@@ -90,13 +101,19 @@ constexpr int V15_Q_PITCH = 128;   // read once per sequence; a padded pitch mea
 // Codebooks, q', code ring, ring barriers; the combine area reuses the
 // codebook, q' and ring region after the tile loop.
 // Fused append (vqkv_decode_append): per-warp partial searches.
-constexpr int V2_APP_OFF = (V2_MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
 constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
 // Paged cache: the block ids of the CTA's token range, read once per sequence.
-constexpr int V2_BLK_OFF = V2_APP_OFF + V2_APP_BYTES;
 constexpr int V2_BLK_CACHE = 512;
-constexpr size_t kV2Smem = V2_BLK_OFF + V2_BLK_CACHE * 4;
-static_assert(CombineSmem<V2_WARPS>::kBytes <= V2_MBAR_OFF, "combine area must fit below the ring barriers");
+template <int DSUB>
+struct V2Smem {
+  static constexpr int APP_OFF = (V2Geo<DSUB>::MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
+  static constexpr int BLK_OFF = APP_OFF + V2_APP_BYTES;
+  static constexpr size_t BYTES = BLK_OFF + V2_BLK_CACHE * 4;
+};
+constexpr size_t kV2Smem = V2Smem<4>::BYTES;
+constexpr size_t kV4Smem = V2Smem<2>::BYTES;
+static_assert(kV4Smem <= 227 * 1024, "4-bit decode shared memory");
+static_assert(CombineSmem<V2_WARPS>::kBytes <= V2Geo<4>::MBAR_OFF, "combine area must fit below the ring barriers");
 // The combine area (after the tile loop) and q' (before it) overlap the
 // code slots, which are idle at those times.
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
@@ -153,36 +170,63 @@ __device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
   return *reinterpret_cast<const T*>(base + off);
 }
 
-// One step of the 2-bit path over T consecutive 16-token tiles.
+// 32-bit word w of a 128-bit code word.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// One step of the byte-code path over T consecutive 16-token tiles.
 //
-// Scores: tokens are the MMA rows, heads the 8 columns.  The A operand of
-// k-step s is two 8-byte centroid gathers (tokens gid and gid+8, channels
-// 4j..4j+3 of subvector j = 4s+tig), B is q' (qa), so a 16-token tile takes
-// 8 score MMAs.  movmatrix turns the scores into the P.V B operand.
-//   kq[i]: this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig)
-//   vq[i]: this lane's 16 value-code bytes (word p: tokens 2tig, 2tig+1,
-//          2tig+8, 2tig+9 of subvector 8p+gid)
+// Scores: tokens are the MMA rows, heads the 8 columns; B is q' (qa).
+//   2 bit (DSUB 4): the A operand of k-step s is two 8-byte centroid gathers
+//     (tokens gid and gid+8, channels 4j..4j+3 of subvector j = 4s+tig);
+//     kq[i][0]: this lane's 16 key-code bytes (tokens gid, gid+8 x
+//     subvectors 4s+tig).
+//   4 bit (DSUB 2): four 4-byte gathers (tokens gid and gid+8 x subvectors
+//     8s+tig and 8s+4+tig, i.e. channels 16s+k in k order); kq[i][0] / [1]:
+//     tokens gid / gid+8, byte 2s / 2s+1 = subvector 8s+tig / 8s+4+tig.
+// A 16-token tile takes 8 score MMAs.  movmatrix turns the scores into the
+// P.V B operand.  P.V: A = gathered V centroids, channels x tokens (2tig,
+// 2tig+1, 2tig+8, 2tig+9), paired by byte permutes; vq word p holds those
+// four tokens' codes of subvector 8p+gid (2 bit: channels 4j..4j+3 over two
+// M-tiles; 4 bit: channels 2j, 2j+1 in one M-tile).
 // Softmax state m0/l0, m1/l1 belongs to heads 2tig, 2tig+1, the columns of
 // this lane's O^T fragments.
-template <int T>
+template <int T, int DSUB>
 __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
-                                            const uint32_t (&qa)[8][2], const uint4 (&kq)[T],
-                                            const uint4 (&vq)[T], int tile0, const ColumnLimits& cl, int lane, float& m0,
-                                            float& m1, float& l0, float& l1, float (&acc)[8][4]) {
+                                         const uint32_t (&qa)[8][2], const uint4 (&kq)[T][V2Geo<DSUB>::LANE_WORDS],
+                                         const uint4 (&vq)[T][V2Geo<DSUB>::LANE_WORDS], int tile0,
+                                         const ColumnLimits& cl, int lane, float& m0, float& m1, float& l0, float& l1,
+                                         float (&acc)[8][4]) {
   const int gid = lane >> 2;
   float sc[T][4];
 #pragma unroll
   for (int i = 0; i < T; ++i) {
     float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
-#define VQKV_SCORE_STEP(S, ACC)                                                              \
-  {                                                                                          \
-    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i].x : kq[i].y, kbyte)); \
-    const uint2 d = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i].z : kq[i].w, kbyte)); \
-    mma_16816(ACC, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);                                   \
+    if constexpr (DSUB == 4) {
+#define VQKV_SCORE_STEP(S, ACC)                                                                     \
+  {                                                                                                 \
+    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i][0].x : kq[i][0].y, kbyte)); \
+    const uint2 d = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i][0].z : kq[i][0].w, kbyte)); \
+    mma_16816(ACC, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);                                          \
   }
-    VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
-    VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
+      VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
+      VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
 #undef VQKV_SCORE_STEP
+    } else {
+#define VQKV_SCORE_STEP4(S, ACC)                                                          \
+  {                                                                                       \
+    const uint32_t wg = word_of(kq[i][0], (S) >> 1), wh = word_of(kq[i][1], (S) >> 1);    \
+    const uint32_t ag = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2>(wg, kbyte));        \
+    const uint32_t bg = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2 + 1>(wg, kbyte));    \
+    const uint32_t ah = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2>(wh, kbyte));        \
+    const uint32_t bh = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2 + 1>(wh, kbyte));    \
+    mma_16816(ACC, ag, ah, bg, bh, qa[S][0], qa[S][1]);                                   \
+  }
+      VQKV_SCORE_STEP4(0, da) VQKV_SCORE_STEP4(1, db) VQKV_SCORE_STEP4(2, da) VQKV_SCORE_STEP4(3, db)
+      VQKV_SCORE_STEP4(4, da) VQKV_SCORE_STEP4(5, db) VQKV_SCORE_STEP4(6, da) VQKV_SCORE_STEP4(7, db)
+#undef VQKV_SCORE_STEP4
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) sc[i][e] = da[e] + db[e];
   }
@@ -194,6 +238,7 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   softmax_tiles<T, 8>(sc, m0, m1, l0, l1, acc, bP);
 #pragma unroll
   for (int i = 0; i < T; ++i) {
+    if constexpr (DSUB == 4) {
 #define VQKV_PV_STEP(PP, W)                                                                    \
   {                                                                                            \
     const uint2 R0 = lds_at<uint2>(s_cb, cb_offset<0>(W, vbyte));                              \
@@ -206,8 +251,21 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
               __byte_perm(R0.y, R1.y, 0x7632), __byte_perm(R2.y, R3.y, 0x5410),                \
               __byte_perm(R2.y, R3.y, 0x7632), bP[i][0], bP[i][1]);                            \
   }
-    VQKV_PV_STEP(0, vq[i].x) VQKV_PV_STEP(1, vq[i].y) VQKV_PV_STEP(2, vq[i].z) VQKV_PV_STEP(3, vq[i].w)
+      VQKV_PV_STEP(0, vq[i][0].x) VQKV_PV_STEP(1, vq[i][0].y) VQKV_PV_STEP(2, vq[i][0].z)
+      VQKV_PV_STEP(3, vq[i][0].w)
 #undef VQKV_PV_STEP
+    } else {
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        const uint32_t w = word_of(vq[i][pp >> 2], pp & 3);
+        const uint32_t R0 = lds_at<uint32_t>(s_cb, cb_offset<0>(w, vbyte));
+        const uint32_t R1 = lds_at<uint32_t>(s_cb, cb_offset<1>(w, vbyte));
+        const uint32_t R2 = lds_at<uint32_t>(s_cb, cb_offset<2>(w, vbyte));
+        const uint32_t R3 = lds_at<uint32_t>(s_cb, cb_offset<3>(w, vbyte));
+        mma_16816(acc[pp], __byte_perm(R0, R1, 0x5410), __byte_perm(R0, R1, 0x7632), __byte_perm(R2, R3, 0x5410),
+                  __byte_perm(R2, R3, 0x7632), bP[i][0], bP[i][1]);
+      }
+    }
   }
 }
 
@@ -252,13 +310,17 @@ __device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* 
 // several in column groups of up to 8, one CTA each (kQueryGroups).  PAGED:
 // tiles are found through the block table (at most two bulk copies per
 // step).
-template <int Q, bool PAGED>
+template <int Q, bool PAGED, int DSUB>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
+  using G = V2Geo<DSUB>;
+  using Sm = V2Smem<DSUB>;
+  using Dim = typename std::conditional<DSUB == 4, Vq2Dim, Vq4Dim>::type;
   extern __shared__ __align__(128) unsigned char smem[];
-  // Codebooks: centroid c at row c (256 bytes): K replicas 0..15 at
-  // c*256 + r*8, V replicas at c*256 + 128 + r*8.  Lane l reads replica
-  // l % 16, so each half-warp phase of a 64-bit gather hits 16 bank pairs.
+  // Codebooks: centroid c at row c (256 bytes): K replicas at c*256 + r*2*DSUB,
+  // V replicas at c*256 + 128 + r*2*DSUB.  2 bit: lane l reads replica l % 16
+  // (8 bytes), so each half-warp phase of a 64-bit gather hits 16 bank pairs;
+  // 4 bit: lane l reads replica l (4 bytes), one bank per lane.
   const unsigned char* s_cb = smem;
   float* s_qp = reinterpret_cast<float*>(smem + V2_Q_OFF);
   float* s_comb = reinterpret_cast<float*>(smem);   // after the tile loop only
@@ -271,11 +333,11 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int b_end = min(b_begin + p.bpg, p.B);
   // this CTA's softmax columns
   const int col0 = GROUPS ? cta_col0(p) : 0, nloc = GROUPS ? min(8, p.ncols - col0) : p.ncols;
-  const uint32_t kbyte = (uint32_t)(lane & 15) << 3;
-  const uint32_t vbyte = 128u | ((uint32_t)(lane & 15) << 3);
+  const uint32_t kbyte = DSUB == 4 ? (uint32_t)(lane & 15) << 3 : (uint32_t)lane << 2;
+  const uint32_t vbyte = 128u | kbyte;
   // this warp's ring: stage st holds the K super-tile, then the V super-tile
-  const uint32_t ring = smem_u32(smem + V2_RING_OFF) + warp * (V2_STAGES * V2_STAGE_BYTES);
-  const uint32_t mbar = smem_u32(smem + V2_MBAR_OFF) + warp * (V2_STAGES * 8);
+  const uint32_t ring = smem_u32(smem + G::RING_OFF) + warp * (V2_STAGES * G::STAGE_BYTES);
+  const uint32_t mbar = smem_u32(smem + G::MBAR_OFF) + warp * (V2_STAGES * 8);
   if (lane == 0) {
     for (int st = 0; st < V2_STAGES; ++st) mbar_init(mbar + 8 * st, 1);
     mbar_init_fence();
@@ -290,12 +352,13 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     // Every input load of the prologue is issued before the first one is
     // used (the sequence length decides the rest): this warp's codebook
     // entry, its query column, and the new K / V row of a fused append.
-    const uint2 cb_entry = __ldg(reinterpret_cast<const uint2*>((threadIdx.x >> 8) ? p.vcb : p.kcb) +
-                                 (size_t)kvh * 256 + (threadIdx.x & 255));
+    using CbEntry = typename std::conditional<DSUB == 4, uint2, uint32_t>::type;
+    const CbEntry cb_entry = __ldg(reinterpret_cast<const CbEntry*>((threadIdx.x >> 8) ? p.vcb : p.kcb) +
+                                   (size_t)kvh * 256 + (threadIdx.x & 255));
     const QueryLoad qload = load_query(p, b, kvh, warp, lane, col0, nloc);
     uint2 xraw = make_uint2(0u, 0u);
     float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (p.k_new != nullptr) {
+    if (DSUB == 4 && p.k_new != nullptr) {
       const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
       xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
       if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
@@ -311,55 +374,55 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     float m0 = kMInit, m1 = kMInit, l0 = 0.f, l1 = 0.f;
 
     if (t_begin < t_end) {
-      // super-tiles of V2_TPI tiles: this warp takes k = warp + j * V2_WARPS,
-      // j < n_mine, starting at tile t_begin + k * V2_TPI.  The split length is
-      // a multiple of V2_TPI, so a super-tile never reaches into the next split;
+      // super-tiles of G::TPI tiles: this warp takes k = warp + j * V2_WARPS,
+      // j < n_mine, starting at tile t_begin + k * G::TPI.  The split length is
+      // a multiple of G::TPI, so a super-tile never reaches into the next split;
       // tiles past the sequence end are masked, tiles past the capacity are not
       // copied.
-      const int cap_tiles = (int)(p.stream_bytes / V2_TILE_BYTES);
+      const int cap_tiles = (int)(p.stream_bytes / G::TILE_BYTES);
       const int blk_first = PAGED ? t_begin >> p.block_shift : 0;
       // blocks of this split's tiles [t_begin, t_end) held in s_blk
       const int n_blk = PAGED ? min(((t_end - 1) >> p.block_shift) - blk_first + 1, V2_BLK_CACHE) : 0;
-      int* s_blk = reinterpret_cast<int*>(smem + V2_BLK_OFF);
-      const int n_super = (t_end - t_begin + V2_TPI - 1) / V2_TPI;
+      int* s_blk = reinterpret_cast<int*>(smem + Sm::BLK_OFF);
+      const int n_super = (t_end - t_begin + G::TPI - 1) / G::TPI;
       const int n_mine = warp < n_super ? (n_super - warp + V2_WARPS - 1) / V2_WARPS : 0;
       auto issue = [&](int j) {
         const uint32_t st = (uses + j) % V2_STAGES;
-        const int tile0 = t_begin + (warp + j * V2_WARPS) * V2_TPI;
+        const int tile0 = t_begin + (warp + j * V2_WARPS) * G::TPI;
         // paged: never past the sequence's last tile, whose table entries
         // beyond it need not be valid (those slots are masked anyway)
-        const int nt = min(V2_TPI, (PAGED ? t_end : cap_tiles) - tile0);
-        mbar_expect_tx(mbar + 8 * st, 2 * (uint32_t)nt * V2_TILE_BYTES);
+        const int nt = min(G::TPI, (PAGED ? t_end : cap_tiles) - tile0);
+        mbar_expect_tx(mbar + 8 * st, 2 * (uint32_t)nt * G::TILE_BYTES);
         bool bad = false;
         if (!PAGED) {   // the super-tile is contiguous
-          const long long off = tile_offset<false>(p, b, kvh, tile0, V2_TILE_BYTES, &bad);
-          tma_load_1d(ring + st * V2_STAGE_BYTES, p.kc + off, nt * V2_TILE_BYTES, mbar + 8 * st);
-          tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, p.vc + off, nt * V2_TILE_BYTES,
+          const long long off = tile_offset<false>(p, b, kvh, tile0, G::TILE_BYTES, &bad);
+          tma_load_1d(ring + st * G::STAGE_BYTES, p.kc + off, nt * G::TILE_BYTES, mbar + 8 * st);
+          tma_load_1d(ring + st * G::STAGE_BYTES + G::TPI * G::TILE_BYTES, p.vc + off, nt * G::TILE_BYTES,
                       mbar + 8 * st);
         } else {
           // a step spans at most two blocks (nt <= 3 <= block_tiles); block ids
           // come from the shared-memory list when this split's fit in it
-          static_assert(V2_TPI <= 4, "a step must not span more than two blocks of >= 4 tiles");
+          static_assert(G::TPI <= 4, "a step must not span more than two blocks of >= 4 tiles");
           auto blk_off = [&](int tile) -> long long {
             const int lb = (tile >> p.block_shift) - blk_first;
             if (lb < n_blk) return ((long long)s_blk[lb] * p.Hkv + kvh) * p.block_bytes;
             bool bb = false;
-            const long long off = tile_offset<true>(p, b, kvh, tile & ~(p.block_tiles - 1), V2_TILE_BYTES, &bb);
+            const long long off = tile_offset<true>(p, b, kvh, tile & ~(p.block_tiles - 1), G::TILE_BYTES, &bb);
             if (bb) atomicOr(p.err, VQKV_DEVERR_BLOCK);
             return off;
           };
           const int in_blk = tile0 & (p.block_tiles - 1);
           const int n0 = min(nt, p.block_tiles - in_blk);
-          const long long off0 = blk_off(tile0) + (long long)in_blk * V2_TILE_BYTES;
-          tma_load_1d(ring + st * V2_STAGE_BYTES, p.kc + off0, n0 * V2_TILE_BYTES, mbar + 8 * st);
-          tma_load_1d(ring + st * V2_STAGE_BYTES + V2_TPI * V2_TILE_BYTES, p.vc + off0, n0 * V2_TILE_BYTES,
+          const long long off0 = blk_off(tile0) + (long long)in_blk * G::TILE_BYTES;
+          tma_load_1d(ring + st * G::STAGE_BYTES, p.kc + off0, n0 * G::TILE_BYTES, mbar + 8 * st);
+          tma_load_1d(ring + st * G::STAGE_BYTES + G::TPI * G::TILE_BYTES, p.vc + off0, n0 * G::TILE_BYTES,
                       mbar + 8 * st);
           if (n0 < nt) {   // the rest starts its next block
             const long long off1 = blk_off(tile0 + n0);
-            tma_load_1d(ring + st * V2_STAGE_BYTES + n0 * V2_TILE_BYTES, p.kc + off1, (nt - n0) * V2_TILE_BYTES,
+            tma_load_1d(ring + st * G::STAGE_BYTES + n0 * G::TILE_BYTES, p.kc + off1, (nt - n0) * G::TILE_BYTES,
                         mbar + 8 * st);
-            tma_load_1d(ring + st * V2_STAGE_BYTES + (V2_TPI + n0) * V2_TILE_BYTES, p.vc + off1,
-                        (nt - n0) * V2_TILE_BYTES, mbar + 8 * st);
+            tma_load_1d(ring + st * G::STAGE_BYTES + (G::TPI + n0) * G::TILE_BYTES, p.vc + off1,
+                        (nt - n0) * G::TILE_BYTES, mbar + 8 * st);
           }
         }
       };
@@ -378,8 +441,9 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // new rows in its prologue and writes their codes before any copy of
       // that tile is issued, so the ring reads them like any other code.
       const int t_new = L - 1;
-      const bool append = p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
-      const int k_new = append ? ((t_new >> 4) - t_begin) / V2_TPI : 0;   // super-tile of the new token
+      const bool append =
+          DSUB == 4 && p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
+      const int k_new = append ? ((t_new >> 4) - t_begin) / G::TPI : 0;   // super-tile of the new token
       const bool late_start = append && k_new % V2_WARPS == warp && k_new / V2_WARPS < V2_STAGES - 1;
       // start the ring before the prologue so the copies overlap it (after
       // the append for the one warp whose first copies hold the new token)
@@ -395,35 +459,41 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         xnew = make_float4(x[0], x[1], x[2], x[3]);
       }
       {
-        // thread t writes the 16 replicas of centroid t & 255 of K (t < 256)
-        // or V (t >= 256), loaded above; replica (i + lane) % 16 at step i
-        // keeps the 16 lanes of each half-warp on 16 different bank pairs
+        // thread t writes the G::REPL replicas of centroid t & 255 of K
+        // (t < 256) or V (t >= 256), loaded above; replica (i + lane) % REPL
+        // at step i keeps the lanes of each store phase on distinct banks
         static_assert(V2_THREADS == 512, "one thread per K and V centroid");
         const int c = threadIdx.x & 255, role = threadIdx.x >> 8;
-        const uint2 e = cb_entry;
-        uint2* row = reinterpret_cast<uint2*>(smem + c * 256 + role * 128);
+        CbEntry* row = reinterpret_cast<CbEntry*>(smem + c * 256 + role * 128);
 #pragma unroll 1
-        for (int i = 0; i < V2_REPL; ++i) row[(i + lane) & (V2_REPL - 1)] = e;
+        for (int i = 0; i < G::REPL; ++i) row[(i + lane) & (G::REPL - 1)] = cb_entry;
       }
       transform_query(p, qload, warp, lane, s_qp, V2_Q_PITCH, nloc);
       __syncthreads();
       if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
         append_rows(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
-                    reinterpret_cast<Best*>(smem + V2_APP_OFF));
+                    reinterpret_cast<Best*>(smem + Sm::APP_OFF));
         if (lane == 0 && late_start)
           for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
             if (!(p.withhold_first_copy && j == 0)) issue(j);
       }
-      // A operand of the score MMA: head gid, channels 4j..4j+3 of j = 4s+tig
+      // B operand of the score MMA: head gid; 2 bit: channels 4j..4j+3 of
+      // j = 4s+tig; 4 bit: channels 16s+2tig, +1 and 16s+8+2tig, +1
       uint32_t qa[8][2];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const int j = 4 * s + tig;
         if (gid < nloc) {
-          const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH + 4 * j);
-          qa[s][0] = pack_half2(v.x, v.y);
-          qa[s][1] = pack_half2(v.z, v.w);
+          if constexpr (DSUB == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH + 4 * (4 * s + tig));
+            qa[s][0] = pack_half2(v.x, v.y);
+            qa[s][1] = pack_half2(v.z, v.w);
+          } else {
+            const float2 v0 = *reinterpret_cast<const float2*>(s_qp + gid * V2_Q_PITCH + 16 * s + 2 * tig);
+            const float2 v1 = *reinterpret_cast<const float2*>(s_qp + gid * V2_Q_PITCH + 16 * s + 8 + 2 * tig);
+            qa[s][0] = pack_half2(v0.x, v0.y);
+            qa[s][1] = pack_half2(v1.x, v1.y);
+          }
         } else {
           qa[s][0] = qa[s][1] = 0u;
         }
@@ -436,17 +506,21 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           timed_out = true;
           break;
         }
-        uint4 kq[V2_TPI], vq[V2_TPI];
+        uint4 kq[G::TPI][G::LANE_WORDS], vq[G::TPI][G::LANE_WORDS];
 #pragma unroll
-        for (int i = 0; i < V2_TPI; ++i) {
-          kq[i] = lds128(ring + st * V2_STAGE_BYTES + i * V2_TILE_BYTES + lane * 16);
-          vq[i] = lds128(ring + st * V2_STAGE_BYTES + (V2_TPI + i) * V2_TILE_BYTES + lane * 16);
+        for (int i = 0; i < G::TPI; ++i) {
+#pragma unroll
+          for (int w = 0; w < G::LANE_WORDS; ++w) {
+            const uint32_t lo = lane * 16 * G::LANE_WORDS + 16 * w;
+            kq[i][w] = lds128(ring + st * G::STAGE_BYTES + i * G::TILE_BYTES + lo);
+            vq[i][w] = lds128(ring + st * G::STAGE_BYTES + (G::TPI + i) * G::TILE_BYTES + lo);
+          }
         }
         __syncwarp();
         // refill the stage this warp finished with in the previous step
         if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
-        vq2_step<V2_TPI>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * V2_TPI, cl, lane, m0,
-                         m1, l0, l1, acc);
+        vq2_step<G::TPI, DSUB>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
+                               lane, m0, m1, l0, l1, acc);
       }
       if (timed_out) {
         // give the copies already issued a bounded chance to land before the
@@ -460,9 +534,9 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       uses += n_mine;
     }
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
-    stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq2Dim());
+    stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Dim());
     __syncthreads();
-    finish_sequence<V2_WARPS, GROUPS, Vq2Dim>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V2_WARPS, GROUPS, Dim>(p, b, kvh, split, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
@@ -644,53 +718,59 @@ cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
   return launch_pdl(decode_combine_kernel, dim3(p.Hkv * p.ncols, p.B), dim3(kHeadDim), 0, stream, p);
 }
 
-int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TILE : V15_TILE; }
-int decode_tiles_per_step(int mode) { return mode == VQKV_MODE_VQ2 ? V2_TPI : 1; }
-size_t decode_smem_bytes(int mode) { return mode == VQKV_MODE_VQ2 ? kV2Smem : kV15Smem; }
-int decode_threads(int mode) { return mode == VQKV_MODE_VQ2 ? V2_THREADS : V15_THREADS; }
+int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ15 ? V15_TILE : V2_TILE; }
+int decode_tiles_per_step(int mode) {
+  return mode == VQKV_MODE_VQ2 ? V2Geo<4>::TPI : mode == VQKV_MODE_VQ4 ? V2Geo<2>::TPI : 1;
+}
+size_t decode_smem_bytes(int mode) {
+  return mode == VQKV_MODE_VQ2 ? kV2Smem : mode == VQKV_MODE_VQ4 ? kV4Smem : kV15Smem;
+}
+int decode_threads(int mode) { return mode == VQKV_MODE_VQ15 ? V15_THREADS : V2_THREADS; }
+
+namespace {
+using DecodeKernel = void (*)(DecodeParams);
+
+// [paged][query layout] instantiations of one mode's decode kernel.
+template <int DSUB>
+struct ByteCodeKernels {
+  static constexpr DecodeKernel k[2][3] = {
+      {decode_vq2_kernel<kOneQuery, false, DSUB>, decode_vq2_kernel<kQueries, false, DSUB>,
+       decode_vq2_kernel<kQueryGroups, false, DSUB>},
+      {decode_vq2_kernel<kOneQuery, true, DSUB>, decode_vq2_kernel<kQueries, true, DSUB>,
+       decode_vq2_kernel<kQueryGroups, true, DSUB>}};
+};
+struct Vq15Kernels {
+  static constexpr DecodeKernel k[2][3] = {
+      {decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
+       decode_vq15_kernel<kQueryGroups, false>},
+      {decode_vq15_kernel<kOneQuery, true>, decode_vq15_kernel<kQueries, true>,
+       decode_vq15_kernel<kQueryGroups, true>}};
+};
+
+const DecodeKernel (*kernels_of(int mode))[3] {
+  return mode == VQKV_MODE_VQ2 ? ByteCodeKernels<4>::k : mode == VQKV_MODE_VQ4 ? ByteCodeKernels<2>::k : Vq15Kernels::k;
+}
+}  // namespace
 
 cudaError_t decode_prepare(int mode) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const auto ks = kernels_of(mode);
   cudaError_t e = cudaSuccess;
-  if (mode == VQKV_MODE_VQ2) {
-    for (auto k : {decode_vq2_kernel<kOneQuery, false>, decode_vq2_kernel<kQueries, false>,
-                   decode_vq2_kernel<kQueryGroups, false>, decode_vq2_kernel<kOneQuery, true>,
-                   decode_vq2_kernel<kQueries, true>, decode_vq2_kernel<kQueryGroups, true>})
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV2Smem);
-    return e;
-  }
-  for (auto k : {decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
-                 decode_vq15_kernel<kQueryGroups, false>, decode_vq15_kernel<kOneQuery, true>,
-                 decode_vq15_kernel<kQueries, true>, decode_vq15_kernel<kQueryGroups, true>})
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, a, (int)kV15Smem);
+  for (int pg = 0; pg < 2; ++pg)
+    for (int q = 0; q < 3; ++q)
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(ks[pg][q], a, (int)decode_smem_bytes(mode));
   return e;
 }
 
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
-  if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq2_kernel<kOneQuery, false>,
-                                                         V2_THREADS, kV2Smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_vq15_kernel<kOneQuery, false>,
-                                                       V15_THREADS, kV15Smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernels_of(mode)[0][kOneQuery],
+                                                       decode_threads(mode), decode_smem_bytes(mode));
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   const int q = p.M == 1 ? kOneQuery : p.cgroups == 1 ? kQueries : kQueryGroups;
   const bool paged = p.block_table != nullptr;
-  if (mode == VQKV_MODE_VQ2) {
-    using K = void (*)(DecodeParams);
-    const K ks[2][3] = {{decode_vq2_kernel<kOneQuery, false>, decode_vq2_kernel<kQueries, false>,
-                         decode_vq2_kernel<kQueryGroups, false>},
-                        {decode_vq2_kernel<kOneQuery, true>, decode_vq2_kernel<kQueries, true>,
-                         decode_vq2_kernel<kQueryGroups, true>}};
-    return launch_pdl(ks[paged][q], grid, dim3(V2_THREADS), kV2Smem, stream, p);
-  }
-  using K = void (*)(DecodeParams);
-  const K ks[2][3] = {{decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
-                       decode_vq15_kernel<kQueryGroups, false>},
-                      {decode_vq15_kernel<kOneQuery, true>, decode_vq15_kernel<kQueries, true>,
-                       decode_vq15_kernel<kQueryGroups, true>}};
-  return launch_pdl(ks[paged][q], grid, dim3(V15_THREADS), kV15Smem, stream, p);
+  return launch_pdl(kernels_of(mode)[paged][q], grid, dim3(decode_threads(mode)), decode_smem_bytes(mode), stream, p);
 }
 
 }  // namespace vqkv

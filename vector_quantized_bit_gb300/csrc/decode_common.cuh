@@ -407,6 +407,11 @@ struct Vq2Dim {   // channel pair offset 4*gid
   __device__ int operator()(int mt, int r) const { return 4 * (8 * (mt >> 1) + (r & 7)) + 2 * (mt & 1) + (r >> 3); }
   __device__ static int skew(int h) { const int t = (h >> 1) & 3; return 2 * (t & 1) + 16 * (t >> 1); }
 };
+struct Vq4Dim {   // the two channels of subvector 8mt + r%8 (rows gid, gid+8); channel pair offset 2*gid
+  static constexpr bool kPairs = true;
+  __device__ int operator()(int mt, int r) const { return 2 * (8 * mt + (r & 7)) + (r >> 3); }
+  __device__ static int skew(int h) { return 8 * ((h >> 1) & 3); }
+};
 struct Vq15Dim {   // channel pair offset 8*gid
   static constexpr bool kPairs = true;
   __device__ int operator()(int mt, int r) const { return 8 * (8 * (mt >> 2) + (r & 7)) + 2 * (mt & 3) + (r >> 3); }

@@ -11,6 +11,8 @@
 // vector handed to the nearest-centroid search is the correctly rounded fp32
 // value of the exact transform.  Distances are fp32 direct differences; the
 // argmin keeps the lowest index on equal distances.
+#include <type_traits>
+
 #include "common.cuh"
 #include "encode_common.cuh"
 #include "internal.h"
@@ -41,23 +43,33 @@ __device__ __forceinline__ const float* key_s(const EncodeParams& p, int kvh) {
   return p.role == VQKV_ROLE_K ? p.s + (size_t)kvh * kHeadDim : nullptr;
 }
 
-// ------------------------------------------------------------------ VQ2
-// SPLIT = 1: one warp per row, lane = subvector, 256 candidates per lane.
+// ------------------------------------------------------------------ VQ2 / VQ4
+// 256-entry codebooks, one byte per code.  DSUB = 4 (2 bit): lane l holds
+// subvector l (channels 4l..4l+3); DSUB = 2 (4 bit): lane l holds
+// subvectors 2l and 2l+1 (channels 4l, 4l+1 and 4l+2, 4l+3).
+// SPLIT = 1: one warp per row, 256 candidates per lane.
 // SPLIT = 8: the CTA's 8 warps share one row, 32 candidates each (few rows,
 // e.g. a decode-step append: latency instead of throughput).
-template <int SPLIT>
+template <int SPLIT, int DSUB>
 __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodeParams p) {
-  __shared__ float4 s_cb[256];
+  using Centroid = typename std::conditional<DSUB == 4, float4, float2>::type;
+  constexpr int kTileBytes = 16 * (kHeadDim / DSUB);
+  __shared__ Centroid s_cb[256];
   __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_dependents_launch();
   for (int c = threadIdx.x; c < 256; c += ENC_THREADS) {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * 256 + c);
-    const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
-    s_cb[c] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+    if constexpr (DSUB == 4) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * 256 + c);
+      const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
+      const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
+      s_cb[c] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+    } else {
+      const __half2 a = __ldg(reinterpret_cast<const __half2*>(p.cb) + (size_t)kvh * 256 + c);
+      s_cb[c] = make_float2(__low2float(a), __high2float(a));
+    }
   }
   __syncthreads();
   const int rows = p.B * p.n_rows;
@@ -74,13 +86,28 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
     }
     float x[4];
     transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
-    // lane = subvector j (channels 4j..4j+3)
-    const Best part = vq2_search(x, c_lo, c_hi, [&](int c) { return s_cb[c]; });
-    Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
-    if (SPLIT == 1 || warp == 0) {
-      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
-      uint8_t* tb = tile_base(p, b, kvh, t, 16, 512);
-      if (tb) tb[vq2_code_offset(p.role, t & 15, lane)] = (uint8_t)bst.i;
+    if constexpr (DSUB == 4) {   // lane = subvector j (channels 4j..4j+3)
+      const Best part = vq2_search(x, c_lo, c_hi, [&](int c) { return s_cb[c]; });
+      Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
+      if (SPLIT == 1 || warp == 0) {
+        count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+        uint8_t* tb = tile_base(p, b, kvh, t, 16, kTileBytes);
+        if (tb) tb[vq2_code_offset(p.role, t & 15, lane)] = (uint8_t)bst.i;
+      }
+    } else {   // lane = subvectors 2l, 2l+1
+      Best pa, pb;
+      vq4_search(x, c_lo, c_hi, [&](int c) { return s_cb[c]; }, pa, pb);
+      Best ba = merge_warps<SPLIT>(pa, warp, lane, s_part);
+      Best bb = merge_warps<SPLIT>(pb, warp, lane, s_part);
+      if (SPLIT == 1 || warp == 0) {
+        count_near_ties(p.near_tie, is_near_tie(ba.d, ba.s), lane, 0xffffffffu);
+        count_near_ties(p.near_tie, is_near_tie(bb.d, bb.s), lane, 0xffffffffu);
+        uint8_t* tb = tile_base(p, b, kvh, t, 16, kTileBytes);
+        if (tb) {
+          tb[vq4_code_offset(p.role, t & 15, 2 * lane)] = (uint8_t)ba.i;
+          tb[vq4_code_offset(p.role, t & 15, 2 * lane + 1)] = (uint8_t)bb.i;
+        }
+      }
     }
   }
 }
@@ -476,7 +503,9 @@ cudaError_t encode_prepare(int mode) {
 
 cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1>, ENC_THREADS, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 4>, ENC_THREADS, 0);
+  if (mode == VQKV_MODE_VQ4)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 2>, ENC_THREADS, 0);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_tc_kernel, TC_THREADS, kTcSmem);
 }
 
@@ -484,8 +513,12 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
 cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool split_rows, cudaStream_t stream) {
   const dim3 grid(blocks_x, p.Hkv);
   if (mode == VQKV_MODE_VQ2) {
-    if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), 0, stream, p);
-    return launch_pdl(encode_vq2_kernel<1>, grid, dim3(ENC_THREADS), 0, stream, p);
+    if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 4>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_vq2_kernel<1, 4>, grid, dim3(ENC_THREADS), 0, stream, p);
+  }
+  if (mode == VQKV_MODE_VQ4) {
+    if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_vq2_kernel<1, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
   }
   if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
   return launch_pdl(encode_vq15_tc_kernel, grid, dim3(TC_THREADS), kTcSmem, stream, p);

@@ -196,6 +196,42 @@ __device__ __forceinline__ long long vq2_code_offset(int role, int t, int j) {
              : 512LL * tile + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
 }
 
+// 4-bit search of the lane's two subvectors (channels (x0, x1) and (x2, x3))
+// over candidates [c_lo, c_hi) (an even count): fp32 direct differences,
+// even / odd chains per subvector, merged.  load(c) returns centroid c as a
+// float2.
+template <typename Load>
+__device__ __forceinline__ void vq4_search(const float (&x)[4], int c_lo, int c_hi, Load load, Best& a, Best& b) {
+  Best ae = best_init(), ao = best_init(), be = best_init(), bo = best_init();
+#pragma unroll 4
+  for (int c = c_lo; c < c_hi; c += 2) {
+    const float2 ca = load(c), cb = load(c + 1);
+    float u = __fsub_rn(x[0], ca.x), d = __fmul_rn(u, u);
+    u = __fsub_rn(x[1], ca.y), d = __fmaf_rn(u, u, d);
+    best_push(ae, d, c);
+    u = __fsub_rn(x[0], cb.x), d = __fmul_rn(u, u);
+    u = __fsub_rn(x[1], cb.y), d = __fmaf_rn(u, u, d);
+    best_push(ao, d, c + 1);
+    u = __fsub_rn(x[2], ca.x), d = __fmul_rn(u, u);
+    u = __fsub_rn(x[3], ca.y), d = __fmaf_rn(u, u, d);
+    best_push(be, d, c);
+    u = __fsub_rn(x[2], cb.x), d = __fmul_rn(u, u);
+    u = __fsub_rn(x[3], cb.y), d = __fmaf_rn(u, u, d);
+    best_push(bo, d, c + 1);
+  }
+  a = best_merge(ae, ao);
+  b = best_merge(be, bo);
+}
+
+// Byte offset of the 4-bit code (one byte) of subvector j (0..63) of token
+// t in a K or V stream (the layout of include/vqkv.h).
+__device__ __forceinline__ long long vq4_code_offset(int role, int t, int j) {
+  const int tile = t >> 4, rr = t & 15;
+  return (role == VQKV_ROLE_K)
+             ? 1024LL * tile + 32 * (4 * (rr & 7) + (j & 3)) + 16 * (rr >> 3) + 2 * (j >> 3) + ((j >> 2) & 1)
+             : 1024LL * tile + 32 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
+}
+
 // Byte offset of the first byte of 1.5-bit pair `pair` (subvectors pair and
 // pair + 8) of token t in a K or V stream (the layout of include/vqkv.h).
 __device__ __forceinline__ long long vq15_pair_offset(int role, int t, int pair) {

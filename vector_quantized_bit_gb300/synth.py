@@ -30,9 +30,10 @@ _S_Q, _S_K, _S_V, _S_OUTLIER, _S_SEQLEN, _S_CODES, _S_CALIB, _S_KMEANS, _S_APPEN
 
 MODE_VQ2 = 0
 MODE_VQ15 = 1
+MODE_VQ4 = 2
 
 # codebook geometry per mode: (entries, subvector dims)
-MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8)}
+MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -41,7 +42,7 @@ class Workload:
 
     config_id: int
     name: str
-    mode: int              # MODE_VQ2 or MODE_VQ15
+    mode: int              # MODE_VQ2, MODE_VQ15 or MODE_VQ4
     B: int
     Hq: int
     Hkv: int
