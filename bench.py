@@ -37,6 +37,7 @@ WORKLOAD_ID = 1
 GRAPH_STEPS = 100           # steps captured per CUDA graph
 SOAK_S = 0.5                # untimed load on each side of the timed region for clock sampling
 PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_vq2_llama8b_196k.json")
+BITS = {0: 2, 1: 1.5, 2: 4}   # bits per element of each code mode
 
 
 def parse():
@@ -49,8 +50,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[1, 2, 3, 4],
                     help="1: Llama-3.1-8B 196k 2-bit (default); 2: ragged batch of 32; "
                          "3: Qwen2.5-14B 1.5-bit; 4: Mistral-7B encode + decode")
-    ap.add_argument("--mode", type=int, default=None, choices=[0, 1],
-                    help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit)")
+    ap.add_argument("--mode", type=int, default=None, choices=[0, 1, 2],
+                    help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit, 2: 4-bit)")
     ap.add_argument("--queries", type=int, default=1,
                     help="queries per sequence (multi-query decode, e.g. speculative decoding): a step encodes "
                          "that many new K/V rows per sequence and runs vqkv_decode_attn_multi")
@@ -597,14 +598,14 @@ def run_ours(args):
     traffic = profile_traffic()[0] if headline else None
     line = {
         "metric": METRIC if headline else f"decode-attn KV tokens/s and HBM GB/s ({w.name}, "
-                                                 f"{'2' if w.mode == 0 else '1.5'}-bit"
+                                                 f"{BITS[w.mode]}-bit"
                                                  f"{f', {M} queries per sequence' if M > 1 else ''}"
                                                  f"{f', paged cache ({BT}-token blocks)' if BT else ''})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 operands, f32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "seq_len": int(lens[0]),
-                   "bits": 2 if w.mode == 0 else 1.5, "splits_per_kv_head": n_splits, "queries_per_sequence": M,
+                   "bits": BITS[w.mode], "splits_per_kv_head": n_splits, "queries_per_sequence": M,
                    "paged_block_tokens": BT or None,
                    "step": ("vqkv_decode_append: 1 new K row + 1 new V row per sequence encoded into the cache "
                             "and attended in the same kernel" if fused else
@@ -617,7 +618,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "decode_vq2_kernel" if w.mode == 0 else "decode_vq15_kernel",
+                     "kernel": "decode_vq15_kernel" if w.mode == synth.MODE_VQ15 else "decode_vq2_kernel",
                      "launch_ms": dec_avg_ms, "algorithmic_bytes": alg,
                      "how": f"graph of {g_steps} back-to-back {'vqkv_decode_append' if fused else 'vqkv_decode_attn'} "
                             f"calls ({dec_kernels} kernel(s) each) over the rotating cache copies, CUDA events on "

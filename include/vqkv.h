@@ -52,15 +52,16 @@
  *   within the 1.25-4 bit range the paper's summary page covers, "Summary"):
  *     TILE = 16 tokens, 1024 bytes.  With r = t % 16 and subvector j (0..63,
  *     channels 2j, 2j+1):
- *       K: byte 1024*(t/16) + 32*(4*(r%8) + j%4) + 16*(r/8) + 2*(j/8) + (j/4)%2
- *       V: byte 1024*(t/16) + 32*(4*(j%8) + (r%8)/2) + 4*(j/8) + 2*(r/8) + r%2
+ *       K: byte 1024*(t/16) + 512*(r/8) + 16*(4*(r%8) + j%4) + 2*(j/8) + (j/4)%2
+ *       V: byte 1024*(t/16) + 512*(j/32) + 16*(4*(j%8) + (r%8)/2) + 4*((j/8)%4)
+ *            + 2*(r/8) + r%2
  *   All three layouts are token-local: writing token t changes no byte of any
  *   other token.  Bits per element: 512*8/(16*128) = 2, 1536*8/(64*128) = 1.5
  *   and 1024*8/(16*128) = 4.
  *   (The layouts place, for each of the 32 lanes of a warp, the codes that
- *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2),
- *   48-byte (VQ15) or 32-byte (VQ4) run, so a warp reads a tile with
- *   coalesced 128-bit loads.)
+ *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2)
+ *   or 48-byte (VQ15) run, or two 16-byte runs 512 bytes apart (VQ4), so a
+ *   warp reads a tile with coalesced 128-bit loads.)
  */
 #ifndef VQKV_H
 #define VQKV_H

@@ -184,9 +184,9 @@ def vq4_offset(role: int, t: int, j: int) -> int:
     tile, r = divmod(t, 16)
     if role == ROLE_K:
         lane = 4 * (r % 8) + (j % 4)
-        return 1024 * tile + 32 * lane + 16 * (r // 8) + 2 * (j // 8) + (j // 4) % 2
+        return 1024 * tile + 512 * (r // 8) + 16 * lane + 2 * (j // 8) + (j // 4) % 2
     lane = 4 * (j % 8) + (r % 8) // 2
-    return 1024 * tile + 32 * lane + 4 * (j // 8) + 2 * (r // 8) + (r % 2)
+    return 1024 * tile + 512 * (j // 32) + 16 * lane + 4 * ((j // 8) % 4) + 2 * (r // 8) + (r % 2)
 
 
 def byte_offset(mode: int, role: int, t: int, j: int) -> int:
@@ -256,8 +256,9 @@ def offset_table(mode: int, role: int, L: int) -> np.ndarray:
         j = np.arange(64)[None, :]
         tile, r = t // 16, t % 16
         if role == ROLE_K:
-            return 1024 * tile + 32 * (4 * (r % 8) + j % 4) + 16 * (r // 8) + 2 * (j // 8) + (j // 4) % 2
-        return 1024 * tile + 32 * (4 * (j % 8) + (r % 8) // 2) + 4 * (j // 8) + 2 * (r // 8) + r % 2
+            return 1024 * tile + 512 * (r // 8) + 16 * (4 * (r % 8) + j % 4) + 2 * (j // 8) + (j // 4) % 2
+        return (1024 * tile + 512 * (j // 32) + 16 * (4 * (j % 8) + (r % 8) // 2) + 4 * ((j // 8) % 4)
+                + 2 * (r // 8) + r % 2)
     if mode == MODE_VQ2:
         j = np.arange(32)[None, :]
         tile, r = t // 16, t % 16

@@ -185,6 +185,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
 //   4 bit (DSUB 2): four 4-byte gathers (tokens gid and gid+8 x subvectors
 //     8s+tig and 8s+4+tig, i.e. channels 16s+k in k order); kq[i][0] / [1]:
 //     tokens gid / gid+8, byte 2s / 2s+1 = subvector 8s+tig / 8s+4+tig.
+//     A tile holds every lane's word 0, then every lane's word 1, so the
+//     two 128-bit reads of a warp are each one contiguous 512-byte run.
 // A 16-token tile takes 8 score MMAs.  movmatrix turns the scores into the
 // P.V B operand.  P.V: A = gathered V centroids, channels x tokens (2tig,
 // 2tig+1, 2tig+8, 2tig+9), paired by byte permutes; vq word p holds those
@@ -510,8 +512,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll
         for (int i = 0; i < G::TPI; ++i) {
 #pragma unroll
-          for (int w = 0; w < G::LANE_WORDS; ++w) {
-            const uint32_t lo = lane * 16 * G::LANE_WORDS + 16 * w;
+          for (int w = 0; w < G::LANE_WORDS; ++w) {   // word w of every lane: 512 contiguous bytes
+            const uint32_t lo = 512 * w + lane * 16;
             kq[i][w] = lds128(ring + st * G::STAGE_BYTES + i * G::TILE_BYTES + lo);
             vq[i][w] = lds128(ring + st * G::STAGE_BYTES + (G::TPI + i) * G::TILE_BYTES + lo);
           }

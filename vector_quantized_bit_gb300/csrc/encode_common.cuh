@@ -228,8 +228,9 @@ __device__ __forceinline__ void vq4_search(const float (&x)[4], int c_lo, int c_
 __device__ __forceinline__ long long vq4_code_offset(int role, int t, int j) {
   const int tile = t >> 4, rr = t & 15;
   return (role == VQKV_ROLE_K)
-             ? 1024LL * tile + 32 * (4 * (rr & 7) + (j & 3)) + 16 * (rr >> 3) + 2 * (j >> 3) + ((j >> 2) & 1)
-             : 1024LL * tile + 32 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * (j >> 3) + 2 * (rr >> 3) + (rr & 1);
+             ? 1024LL * tile + 512 * (rr >> 3) + 16 * (4 * (rr & 7) + (j & 3)) + 2 * (j >> 3) + ((j >> 2) & 1)
+             : 1024LL * tile + 512 * (j >> 5) + 16 * (4 * (j & 7) + ((rr & 7) >> 1)) + 4 * ((j >> 3) & 3) +
+                   2 * (rr >> 3) + (rr & 1);
 }
 
 // Byte offset of the first byte of 1.5-bit pair `pair` (subvectors pair and
