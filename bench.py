@@ -406,7 +406,7 @@ def run_ours(args):
     n_splits = _lib.vqkv_decode_num_splits(dargs)
     dec_kernels = _lib.vqkv_decode_kernel_count(dargs)
 
-    fused = mode == synth.MODE_VQ2 and not args.unfused and M == 1 and not BT
+    fused = mode in (synth.MODE_VQ2, synth.MODE_VQ4) and not args.unfused and M == 1 and not BT
 
     def decode_only(kc, vc):
         if BT:

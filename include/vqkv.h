@@ -85,8 +85,7 @@ typedef enum {
 typedef enum {
   VQKV_MODE_VQ2 = 0,   /* 2 bit:   2^8 entries x 4 dims, 8-bit codes  */
   VQKV_MODE_VQ15 = 1,  /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
-  VQKV_MODE_VQ4 = 2    /* 4 bit:   2^8 entries x 2 dims, 8-bit codes (decode, encode, multi-query,
-                          paged; not the fused append) */
+  VQKV_MODE_VQ4 = 2    /* 4 bit:   2^8 entries x 2 dims, 8-bit codes */
 } vqkv_mode;
 
 typedef enum {
@@ -214,8 +213,8 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
  * arguments over the L tokens including the new one.  Inside the kernel the
  * CTA that holds position L - 1 writes the new codes before it starts
  * streaming that tile, so one kernel does the whole step.  Workspace, error
- * word, alignment and failure rules are those of vqkv_decode_attn.  2-bit
- * mode only (VQKV_ERR_UNSUPPORTED otherwise).
+ * word, alignment and failure rules are those of vqkv_decode_attn.  2-bit and
+ * 4-bit modes (VQKV_ERR_UNSUPPORTED for 1.5 bit).
  */
 typedef struct {
   vqkv_decode_args decode;    /* as for vqkv_decode_attn (seq_lens include the new token) */

@@ -152,7 +152,7 @@ def test_decode_append_validation(lib):
     a.decode = _dec(mode=1)
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # 2-bit only
     a.decode = _dec(mode=2)
-    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1    # 4 bit too: no new rows
     a.decode = _dec()
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1    # no new rows
     a.k_new, a.v_new = 0x10000, 0x10004                             # v_new not 8-byte aligned

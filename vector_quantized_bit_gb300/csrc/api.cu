@@ -296,7 +296,7 @@ namespace {
 
 vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_args* ap, int M, void* stream,
                           const vqkv_paging* pg, unsigned test_polls) {
-  if (ap != nullptr && a->mode != VQKV_MODE_VQ2) return VQKV_ERR_UNSUPPORTED;
+  if (ap != nullptr && a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
   vqkv_status st = validate_decode(a);
   if (st != VQKV_OK) return st;
   if (pg != nullptr) {

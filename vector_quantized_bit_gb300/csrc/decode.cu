@@ -271,15 +271,30 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   }
 }
 
+// Merged search state of this lane's subvector over the 8 warps of its role
+// (valid in the role's first warp).
+__device__ __forceinline__ Best merge_role_slices(Best part, int warp, int lane, int slice, Best* s_part) {
+  s_part[warp * 32 + lane] = part;
+  __syncthreads();
+  Best bst = part;
+  if (slice == 0) {
+#pragma unroll
+    for (int w = 1; w < 8; ++w) bst = best_merge(bst, s_part[(warp + w) * 32 + lane]);
+  }
+  __syncthreads();   // s_part is reused
+  return bst;
+}
+
 // Encode of the new K row (warps 0-7) and V row (warps 8-15) of one
 // (sequence, KV head) for the fused append, from the lane's 4 transformed
-// channels x of its row: each warp searches 32 of the 256
-// candidates (replica 0 of the shared codebook, one broadcast per load), the
-// slices are merged as in the encode kernel, and lane j of warps 0 / 8 writes
-// the code of subvector j to the cache at token t_new.  The writes are made
-// visible to the bulk copies (async proxy) that the CTA issues after the
-// closing barrier.  Called by every thread of the CTA after the codebook is
-// in shared memory.
+// channels x of its row: each warp searches 32 of the 256 candidates
+// (replica 0 of the shared codebook, one broadcast per load), the slices are
+// merged as in the encode kernel, and warps 0 / 8 write the codes to the
+// cache at token t_new (2 bit: lane j writes subvector j; 4 bit: lane j
+// writes subvectors 2j and 2j+1).  The writes are made visible to the bulk
+// copies (async proxy) that the CTA issues after the closing barrier.
+// Called by every thread of the CTA after the codebook is in shared memory.
+template <int DSUB>
 __device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* v_stream,
                                          unsigned long long* near_tie, int t_new, const unsigned char* s_cb,
                                          Best* s_part) {
@@ -288,21 +303,35 @@ __device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* 
   const int role = warp >> 3, slice = warp & 7;
   const float x[4] = {xv.x, xv.y, xv.z, xv.w};
   const unsigned char* cb_role = s_cb + role * 128;
-  const Best part = vq2_search(x, slice * 32, slice * 32 + 32, [&](int c) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(cb_role + c * 256);
-    const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
-    return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
-  });
-  s_part[warp * 32 + lane] = part;
-  __syncthreads();
-  if (slice == 0) {
-    Best bst = part;
-#pragma unroll
-    for (int w = 1; w < 8; ++w) bst = best_merge(bst, s_part[(warp + w) * 32 + lane]);
-    count_near_ties(near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
-    (role ? v_stream : k_stream)[vq2_code_offset(role, t_new, lane)] = (uint8_t)bst.i;
-    fence_proxy_async_global();
+  uint8_t* stream = role ? v_stream : k_stream;
+  if constexpr (DSUB == 4) {
+    const Best part = vq2_search(x, slice * 32, slice * 32 + 32, [&](int c) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(cb_role + c * 256);
+      const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
+      const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
+      return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+    });
+    const Best bst = merge_role_slices(part, warp, lane, slice, s_part);
+    if (slice == 0) {
+      count_near_ties(near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+      stream[vq2_code_offset(role, t_new, lane)] = (uint8_t)bst.i;
+      fence_proxy_async_global();
+    }
+  } else {
+    Best pa, pb;
+    vq4_search(x, slice * 32, slice * 32 + 32, [&](int c) {
+      const __half2 v = *reinterpret_cast<const __half2*>(cb_role + c * 256);
+      return make_float2(__low2float(v), __high2float(v));
+    }, pa, pb);
+    const Best ba = merge_role_slices(pa, warp, lane, slice, s_part);
+    const Best bb = merge_role_slices(pb, warp, lane, slice, s_part);
+    if (slice == 0) {
+      count_near_ties(near_tie, is_near_tie(ba.d, ba.s), lane, 0xffffffffu);
+      count_near_ties(near_tie, is_near_tie(bb.d, bb.s), lane, 0xffffffffu);
+      stream[vq4_code_offset(role, t_new, 2 * lane)] = (uint8_t)ba.i;
+      stream[vq4_code_offset(role, t_new, 2 * lane + 1)] = (uint8_t)bb.i;
+      fence_proxy_async_global();
+    }
   }
   __syncthreads();
 }
@@ -360,7 +389,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     const QueryLoad qload = load_query(p, b, kvh, warp, lane, col0, nloc);
     uint2 xraw = make_uint2(0u, 0u);
     float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (DSUB == 4 && p.k_new != nullptr) {
+    if (p.k_new != nullptr) {
       const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
       xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
       if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
@@ -443,8 +472,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // new rows in its prologue and writes their codes before any copy of
       // that tile is issued, so the ring reads them like any other code.
       const int t_new = L - 1;
-      const bool append =
-          DSUB == 4 && p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
+      const bool append = p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
       const int k_new = append ? ((t_new >> 4) - t_begin) / G::TPI : 0;   // super-tile of the new token
       const bool late_start = append && k_new % V2_WARPS == warp && k_new / V2_WARPS < V2_STAGES - 1;
       // start the ring before the prologue so the copies overlap it (after
@@ -474,7 +502,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       __syncthreads();
       if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-        append_rows(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
+        append_rows<DSUB>(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
                     reinterpret_cast<Best*>(smem + Sm::APP_OFF));
         if (lane == 0 && late_start)
           for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
