@@ -36,15 +36,17 @@ HEAD_DIM = 128
 MODE_VQ2 = 0
 MODE_VQ15 = 1
 MODE_VQ4 = 2
+MODE_VQ3 = 3
 ROLE_K = 0
 ROLE_V = 1
 
 # (entries, subvector dims) per mode [P1 Key points: 2^8 x 4 and 2^12 x 8]
-# and, within the pages' 1.25-4 bit range [P1 Summary], 4 bit = 2^8 x 2
-GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2)}
+# and, within the pages' 1.25-4 bit range [P1 Summary], 4 bit = 2^8 x 2 and
+# 3 bit = 2^12 x 4
+GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4)}
 # tokens per layout tile and bytes per tile of one cache stream
-TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64, MODE_VQ4: 16}
-TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536, MODE_VQ4: 1024}
+TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64, MODE_VQ4: 16, MODE_VQ3: 16}
+TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536, MODE_VQ4: 1024, MODE_VQ3: 768}
 BYTE_CODE_MODES = (MODE_VQ2, MODE_VQ4)   # one byte per code
 
 
@@ -193,6 +195,22 @@ def byte_offset(mode: int, role: int, t: int, j: int) -> int:
     return vq2_offset(role, t, j) if mode == MODE_VQ2 else vq4_offset(role, t, j)
 
 
+def vq3_byte(role: int, t: int, pair: int, k: int) -> int:
+    """Byte k (0..2) of the 3-byte code pair (pair, pair+16) (pair 0..15) of token t.
+
+    A tile is 32 lanes' 24-byte runs stored as two planes: run bytes 0..15 of
+    lane L at 16*L, run bytes 16..23 at 512 + 8*L.  K: lane 4*(r%8) + pair%4,
+    run byte 12*(r/8) + 3*(pair/4) + k.  V: lane 4*(pair%8) + (r%8)/2, run
+    byte 6*(2*(r/8) + r%2) + 3*(pair/8) + k.
+    """
+    tile, r = divmod(t, 16)
+    if role == ROLE_K:
+        lane, b = 4 * (r % 8) + pair % 4, 12 * (r // 8) + 3 * (pair // 4) + k
+    else:
+        lane, b = 4 * (pair % 8) + (r % 8) // 2, 6 * (2 * (r // 8) + r % 2) + 3 * (pair // 8) + k
+    return 768 * tile + (16 * lane + b if b < 16 else 512 + 8 * lane + b - 16)
+
+
 def vq15_offset(role: int, t: int, pair: int) -> int:
     """First of the 3 bytes holding the code pair (pair, pair+8) of token t."""
     tile, rem = divmod(t, 64)
@@ -222,6 +240,11 @@ def pack_stream(codes: np.ndarray, mode: int, role: int, cap_len: int,
         for t in range(L):
             for j in range(codes.shape[1]):
                 buf[byte_offset(mode, role, t, j)] = int(codes[t, j])
+    elif mode == MODE_VQ3:
+        for t in range(L):
+            for p in range(16):
+                for k, byte in enumerate(pack_pair(int(codes[t, p]), int(codes[t, p + 16]))):
+                    buf[vq3_byte(role, t, p, k)] = byte
     else:
         for t in range(L):
             for p in range(8):
@@ -239,6 +262,12 @@ def unpack_stream(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
             for j in range(nsub):
                 out[t, j] = buf[byte_offset(mode, role, t, j)]
         return out
+    if mode == MODE_VQ3:
+        out = np.empty((L, 32), dtype=np.int64)
+        for t in range(L):
+            for p in range(16):
+                out[t, p], out[t, p + 16] = unpack_pair(*(int(buf[vq3_byte(role, t, p, k)]) for k in range(3)))
+        return out
     out = np.empty((L, 16), dtype=np.int64)
     for t in range(L):
         for p in range(8):
@@ -252,6 +281,16 @@ def offset_table(mode: int, role: int, L: int) -> np.ndarray:
     [0, L): a vectorised form of the offset functions above, for large
     streams."""
     t = np.arange(L)[:, None]
+    if mode == MODE_VQ3:   # [L][16 pairs][3 bytes]
+        p = np.arange(16)[None, :, None]
+        k = np.arange(3)[None, None, :]
+        tt = t[:, :, None]
+        tile, r = tt // 16, tt % 16
+        if role == ROLE_K:
+            lane, b = 4 * (r % 8) + p % 4, 12 * (r // 8) + 3 * (p // 4) + k
+        else:
+            lane, b = 4 * (p % 8) + (r % 8) // 2, 6 * (2 * (r // 8) + r % 2) + 3 * (p // 8) + k
+        return 768 * tile + np.where(b < 16, 16 * lane + b, 512 + 8 * lane + b - 16)
     if mode == MODE_VQ4:
         j = np.arange(64)[None, :]
         tile, r = t // 16, t % 16
@@ -278,6 +317,11 @@ def pack_stream_fast(codes: np.ndarray, mode: int, role: int, cap_len: int) -> n
     off = offset_table(mode, role, codes.shape[0])
     if mode in BYTE_CODE_MODES:
         buf[off] = codes.astype(np.uint8)
+    elif mode == MODE_VQ3:
+        lo, hi = codes[:, :16].astype(np.int64), codes[:, 16:].astype(np.int64)
+        buf[off[..., 0]] = lo & 0xFF
+        buf[off[..., 1]] = (lo >> 8) | ((hi & 0xF) << 4)
+        buf[off[..., 2]] = hi >> 4
     else:
         lo, hi = codes[:, :8].astype(np.int64), codes[:, 8:].astype(np.int64)
         buf[off] = lo & 0xFF
@@ -290,6 +334,9 @@ def unpack_stream_fast(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndar
     off = offset_table(mode, role, L)
     if mode in BYTE_CODE_MODES:
         return buf[off].astype(np.int64)
+    if mode == MODE_VQ3:
+        b0, b1, b2 = (buf[off[..., k]].astype(np.int64) for k in range(3))
+        return np.concatenate([b0 | ((b1 & 0xF) << 8), (b1 >> 4) | (b2 << 4)], axis=1)
     b0, b1, b2 = (buf[off + k].astype(np.int64) for k in range(3))
     return np.concatenate([b0 | ((b1 & 0xF) << 8), (b1 >> 4) | (b2 << 4)], axis=1)
 

@@ -152,8 +152,9 @@ def check_bits():
     assert vo.bits_per_element(vo.MODE_VQ2) == 2.0
     assert vo.bits_per_element(vo.MODE_VQ15) == 1.5
     assert vo.bits_per_element(vo.MODE_VQ4) == 4.0
+    assert vo.bits_per_element(vo.MODE_VQ3) == 3.0
     for mode, cap in ((vo.MODE_VQ2, 16), (vo.MODE_VQ2, 196608), (vo.MODE_VQ15, 64), (vo.MODE_VQ15, 65536),
-                      (vo.MODE_VQ4, 16), (vo.MODE_VQ4, 16384)):
+                      (vo.MODE_VQ4, 16), (vo.MODE_VQ4, 16384), (vo.MODE_VQ3, 16), (vo.MODE_VQ3, 65536)):
         assert vo.code_bytes(mode, cap) * 8 / (cap * 128) == vo.bits_per_element(mode)
     assert vo.code_bytes(vo.MODE_VQ2, 17) == 1024      # rounded up to whole tiles
     assert vo.code_bytes(vo.MODE_VQ15, 65) == 3072
@@ -169,6 +170,10 @@ def check_layout_golden():
         role, t, j, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
         assert vo.vq4_offset(r, int(t), int(j)) == int(off), line
+    for line in golden_lines("layout_vq3.txt"):
+        role, t, p, k, off = line.split()
+        r = vo.ROLE_K if role == "K" else vo.ROLE_V
+        assert vo.vq3_byte(r, int(t), int(p), int(k)) == int(off), line
     for line in golden_lines("layout_vq15.txt"):
         role, t, p, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
@@ -180,6 +185,12 @@ def check_layout_golden():
 
 
 def check_layout_bijective():
+    for role in (0, 1):   # VQ3: byte by byte
+        offs = [vo.vq3_byte(role, t, p, k) for t in range(32) for p in range(16) for k in range(3)]
+        assert sorted(offs) == list(range(2 * vo.TILE_BYTES[vo.MODE_VQ3]))
+        tab = vo.offset_table(vo.MODE_VQ3, role, 32)
+        ref = [[[vo.vq3_byte(role, t, p, k) for k in range(3)] for p in range(16)] for t in range(32)]
+        assert np.array_equal(tab, np.array(ref))
     for mode, role in ((0, 0), (0, 1), (1, 0), (1, 1), (2, 0), (2, 1)):
         T = vo.TILE_TOKENS[mode]
         if mode == vo.MODE_VQ4:
@@ -213,7 +224,7 @@ def test_layout_bijective():
 
 def test_pack_roundtrip():
     r = np.random.default_rng(1)
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             L = 150
@@ -230,7 +241,7 @@ def test_pack_roundtrip():
 
 def test_append_does_not_touch_neighbours():
     """Writing token t changes only token t's bytes (token-local packing)."""
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             codes = np.zeros((64, 128 // dsub), dtype=np.int64)
@@ -450,6 +461,19 @@ def test_planted_vq4_half_order(monkeypatch):
     real = vo.vq4_offset
     monkeypatch.setattr(vo, "vq4_offset",
                         lambda role, t, j: real(role, t, j ^ 4) if role == vo.ROLE_K else real(role, t, j))
+    assert _fails(check_layout_golden)
+
+
+def test_planted_vq3_plane_split(monkeypatch):
+    """Storing a run in one 24-byte block instead of two planes must fail a pin."""
+    def flat(role, t, pair, k):
+        tile, r = divmod(t, 16)
+        if role == vo.ROLE_K:
+            lane, b = 4 * (r % 8) + pair % 4, 12 * (r // 8) + 3 * (pair // 4) + k
+        else:
+            lane, b = 4 * (pair % 8) + (r % 8) // 2, 6 * (2 * (r // 8) + r % 2) + 3 * (pair // 8) + k
+        return 768 * tile + 24 * lane + b
+    monkeypatch.setattr(vo, "vq3_byte", flat)
     assert _fails(check_layout_golden)
 
 
