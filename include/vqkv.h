@@ -55,13 +55,22 @@
  *       K: byte 1024*(t/16) + 512*(r/8) + 16*(4*(r%8) + j%4) + 2*(j/8) + (j/4)%2
  *       V: byte 1024*(t/16) + 512*(j/32) + 16*(4*(j%8) + (r%8)/2) + 4*((j/8)%4)
  *            + 2*(r/8) + r%2
- *   All three layouts are token-local: writing token t changes no byte of any
- *   other token.  Bits per element: 512*8/(16*128) = 2, 1536*8/(64*128) = 1.5
- *   and 1024*8/(16*128) = 4.
+ *   VQKV_MODE_VQ3 (4096 entries x 4 dims, 12-bit codes, 32 codes per token;
+ *   the same 1.25-4 bit range): the codes of subvectors p and p+16 (p =
+ *   0..15, channels 4p..4p+3 and 4p+64..4p+67) form a pair stored in 3 bytes
+ *   as in VQ15.  TILE = 16 tokens, 768 bytes: 32 lanes' 24-byte runs, run
+ *   bytes 0..15 of lane L at 16*L and bytes 16..23 at 512 + 8*L.  With
+ *   r = t % 16, byte k (0..2) of pair p of token t is run byte n of lane L:
+ *       K: L = 4*(r%8) + p%4,      n = 12*(r/8) + 3*(p/4) + k
+ *       V: L = 4*(p%8) + (r%8)/2,  n = 6*(2*(r/8) + r%2) + 3*(p/8) + k
+ *   All four layouts are token-local: writing token t changes no byte of any
+ *   other token.  Bits per element: 512*8/(16*128) = 2, 1536*8/(64*128) = 1.5,
+ *   1024*8/(16*128) = 4 and 768*8/(16*128) = 3.
  *   (The layouts place, for each of the 32 lanes of a warp, the codes that
  *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2)
- *   or 48-byte (VQ15) run, or two 16-byte runs 512 bytes apart (VQ4), so a
- *   warp reads a tile with coalesced 128-bit loads.)
+ *   or 48-byte (VQ15) run, in two 16-byte runs 512 bytes apart (VQ4), or in
+ *   a 16-byte and an 8-byte run (VQ3), so a warp reads a tile with
+ *   coalesced 128-bit (and 64-bit) loads.)
  */
 #ifndef VQKV_H
 #define VQKV_H
@@ -85,7 +94,8 @@ typedef enum {
 typedef enum {
   VQKV_MODE_VQ2 = 0,   /* 2 bit:   2^8 entries x 4 dims, 8-bit codes  */
   VQKV_MODE_VQ15 = 1,  /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
-  VQKV_MODE_VQ4 = 2    /* 4 bit:   2^8 entries x 2 dims, 8-bit codes */
+  VQKV_MODE_VQ4 = 2,   /* 4 bit:   2^8 entries x 2 dims, 8-bit codes */
+  VQKV_MODE_VQ3 = 3    /* 3 bit:   2^12 entries x 4 dims, 12-bit codes */
 } vqkv_mode;
 
 typedef enum {
@@ -109,7 +119,7 @@ typedef enum {
  *   role K: y = x / s[h] (per channel), x' = y . Hn with Hn = H/sqrt(128),
  *           H[i][k] = (-1)^popcount(i & k), x' rounded to fp32;
  *   role V: x' = x.
- *   For each subvector j of x' (d_sub = 4 or 8 channels) the code is
+ *   For each subvector j of x' (d_sub = 2, 4 or 8 channels) the code is
  *   argmin_c sum_i (x'_{j,i} - C[h][c][i])^2 over the KV head's codebook C,
  *   decided on fp32 distances with ties to the lowest index, and is written
  *   at cache position pos[b] + n of stream (b, h) in the layout above.

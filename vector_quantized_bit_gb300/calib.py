@@ -100,8 +100,8 @@ def calibrate_head(w: synth.Workload, kvh: int, *, sample_tokens: int | None = N
     kr = _rotated_key_rows(k_all[idx], s).reshape(-1, dsub)
     v_rows = synth.values(w, b, kvh, 0, L)[idx].astype(np.float32).reshape(-1, dsub)
     if iters is None:
-        iters = 4 if w.mode == synth.MODE_VQ15 else 20
-    init = "points" if w.mode == synth.MODE_VQ15 else "++"
+        iters = 4 if E == 4096 else 20
+    init = "points" if E == 4096 else "++"
     kcb = kmeans(kr, E, iters, synth.kmeans_rng(w, kvh, 0), init)
     vcb = kmeans(v_rows, E, iters, synth.kmeans_rng(w, kvh, 1), init)
     return s, kcb, vcb

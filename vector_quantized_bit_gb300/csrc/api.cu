@@ -17,8 +17,8 @@ constexpr size_t kWsHeader = 256;   // word 0: device error flags
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int decode_bpsm[4] = {0, 0, 0, 0};   // resident decode CTAs per SM: VQ2, VQ15, VQ4, fp16
-  int encode_bpsm[3] = {0, 0, 0};
+  int decode_bpsm[kCodeModes + 1] = {};   // resident decode CTAs per SM: each code mode, then fp16
+  int encode_bpsm[kCodeModes] = {};
 };
 
 std::mutex g_mu;
@@ -48,13 +48,16 @@ vqkv_status device_info(DeviceInfo* out) {
   return VQKV_OK;
 }
 
+bool is_code_mode(int m) {
+  return m == VQKV_MODE_VQ2 || m == VQKV_MODE_VQ15 || m == VQKV_MODE_VQ4 || m == VQKV_MODE_VQ3;
+}
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Sizes only (what the split plan and the workspace size depend on).
 vqkv_status validate_decode_sizes(const vqkv_decode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
+  if (!is_code_mode(a->mode)) return VQKV_ERR_UNSUPPORTED;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
@@ -66,7 +69,7 @@ vqkv_status validate_decode_sizes(const vqkv_decode_args* a) {
 
 vqkv_status validate_decode(const vqkv_decode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
+  if (!is_code_mode(a->mode)) return VQKV_ERR_UNSUPPORTED;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return VQKV_ERR_INVALID_ARG;
@@ -122,7 +125,7 @@ struct DecodePlan {
 // per-CTA setup cost), assuming full-length sequences; short sequences make
 // some CTAs finish early, which the hardware scheduler backfills.
 struct PlanInput {
-  int mode;   // VQKV_MODE_VQ2, VQKV_MODE_VQ15 or kModeFp16
+  int mode;   // a code mode or kModeFp16
   int B, Hq, Hkv, max_seq_len, num_splits;
   int M = 1;  // queries per sequence
   // Tiles' worth of extra work in the CTA whose split holds a sequence's
@@ -184,7 +187,7 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
 
 vqkv_status validate_encode(const vqkv_encode_args* a) {
   if (a == nullptr) return VQKV_ERR_INVALID_ARG;
-  if (a->mode != VQKV_MODE_VQ2 && a->mode != VQKV_MODE_VQ15 && a->mode != VQKV_MODE_VQ4) return VQKV_ERR_UNSUPPORTED;
+  if (!is_code_mode(a->mode)) return VQKV_ERR_UNSUPPORTED;
   if (a->role != VQKV_ROLE_K && a->role != VQKV_ROLE_V) return VQKV_ERR_INVALID_ARG;
   if (a->head_dim != 128) return VQKV_ERR_UNSUPPORTED;
   if (a->B < 0 || a->Hkv < 1 || a->n_rows < 0 || a->cap_len < 1) return VQKV_ERR_INVALID_ARG;
@@ -249,6 +252,7 @@ size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
   if (mode == VQKV_MODE_VQ2) return (size_t)((cap_len + 15) / 16) * 512;
   if (mode == VQKV_MODE_VQ15) return (size_t)((cap_len + 63) / 64) * 1536;
   if (mode == VQKV_MODE_VQ4) return (size_t)((cap_len + 15) / 16) * 1024;
+  if (mode == VQKV_MODE_VQ3) return (size_t)((cap_len + 15) / 16) * 768;
   return 0;
 }
 

@@ -69,19 +69,24 @@ constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][V2_Q_PITCH])
 constexpr int V2_STAGES = VQKV_V2_STAGES;           // per-warp ring of super-tiles (K then V)
 constexpr int V2_RING_OFF = V2_Q_OFF + 8 * V2_Q_PITCH * 4;
 
-// Geometry of the byte-code decode: DSUB = 4 is the 2-bit mode (256 x 4, 32
-// codes per token), DSUB = 2 the 4-bit mode (256 x 2, 64 codes per token).
-// Both keep the 64-KB replicated codebook and q' prefix; the 4-bit tile is
-// twice as long, so its steps are two tiles.
-template <int DSUB>
+// Geometry of the tile-ring decode, per code mode: 2 bit (256 x 4, one byte
+// per code), 4 bit (256 x 2, one byte per code) and 3 bit (4096 x 4, 12-bit
+// codes in 3-byte pairs).  All keep the 64-KB codebook and q' prefix: the
+// 256-entry codebooks replicated across banks, the 4096-entry ones once.  A
+// lane's code words of a tile: 2 bit one 16-byte word; 4 bit two 16-byte
+// words in planes 512 bytes apart; 3 bit a 16-byte and an 8-byte word
+// (planes at 0 and 512).
+template <int MODE>
 struct V2Geo {
-  static constexpr int TILE_BYTES = 16 * (kHeadDim / DSUB);    // 16 tokens x one byte per subvector
-  static constexpr int LANE_WORDS = TILE_BYTES / 32 / 16;      // a lane's 128-bit code words per tile and role
-  static constexpr int TPI = DSUB == 4 ? V2_TPI : 2;           // tiles per step
+  static constexpr int DSUB = MODE == VQKV_MODE_VQ4 ? 2 : 4;
+  static constexpr bool PAIRS = MODE == VQKV_MODE_VQ3;          // 12-bit codes in 3-byte pairs
+  static constexpr int TILE_BYTES = PAIRS ? 768 : 16 * (kHeadDim / DSUB);
+  static constexpr int LW = TILE_BYTES / 32 / 4;                  // a lane's 32-bit code words per tile and role
+  static constexpr int TPI = MODE == VQKV_MODE_VQ4 ? 2 : V2_TPI;  // tiles per step
   static constexpr int STAGE_BYTES = 2 * TPI * TILE_BYTES;
   static constexpr int RING_OFF = V2_RING_OFF;
   static constexpr int MBAR_OFF = RING_OFF + V2_WARPS * V2_STAGES * STAGE_BYTES;
-  static constexpr int REPL = 128 / (2 * DSUB);                // replicas of a centroid per 128-byte half row
+  static constexpr int REPL = PAIRS ? 1 : 128 / (2 * DSUB);     // replicas of a 256-entry codebook's centroid
 };
 
 // ------------------------------------------------------------------ VQ15
@@ -104,16 +109,18 @@ constexpr int V15_Q_PITCH = 128;   // read once per sequence; a padded pitch mea
 constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
 // Paged cache: the block ids of the CTA's token range, read once per sequence.
 constexpr int V2_BLK_CACHE = 512;
-template <int DSUB>
+template <int MODE>
 struct V2Smem {
-  static constexpr int APP_OFF = (V2Geo<DSUB>::MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
+  static constexpr int APP_OFF = (V2Geo<MODE>::MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
   static constexpr int BLK_OFF = APP_OFF + V2_APP_BYTES;
   static constexpr size_t BYTES = BLK_OFF + V2_BLK_CACHE * 4;
 };
-constexpr size_t kV2Smem = V2Smem<4>::BYTES;
-constexpr size_t kV4Smem = V2Smem<2>::BYTES;
-static_assert(kV4Smem <= 227 * 1024, "4-bit decode shared memory");
-static_assert(CombineSmem<V2_WARPS>::kBytes <= V2Geo<4>::MBAR_OFF, "combine area must fit below the ring barriers");
+constexpr size_t kV2Smem = V2Smem<VQKV_MODE_VQ2>::BYTES;
+constexpr size_t kV4Smem = V2Smem<VQKV_MODE_VQ4>::BYTES;
+constexpr size_t kV3Smem = V2Smem<VQKV_MODE_VQ3>::BYTES;
+static_assert(kV4Smem <= 227 * 1024 && kV3Smem <= 227 * 1024, "4-bit / 3-bit decode shared memory");
+static_assert(CombineSmem<V2_WARPS>::kBytes <= V2Geo<VQKV_MODE_VQ2>::MBAR_OFF,
+              "combine area must fit below the ring barriers");
 // The combine area (after the tile loop) and q' (before it) overlap the
 // code slots, which are idle at those times.
 constexpr size_t kV15Smem = 2 * V15_CB_BYTES + CombineSmem<V15_WARPS>::kBytes;
@@ -170,34 +177,39 @@ __device__ __forceinline__ T lds_at(const unsigned char* base, uint32_t off) {
   return *reinterpret_cast<const T*>(base + off);
 }
 
-// 32-bit word w of a 128-bit code word.
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
-  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+// 24-bit code pair at byte b (a multiple of 3) of a lane's run of words.
+template <int LW>
+__device__ __forceinline__ uint32_t pair_at(const uint32_t (&w)[LW], int b) {
+  const int i = b >> 2, sh = (b & 3) * 8;
+  return (sh <= 8 ? (w[i] >> sh) : __funnelshift_r(w[i], w[i + 1], sh)) & 0xffffffu;
 }
 
-// One step of the byte-code path over T consecutive 16-token tiles.
+// One step of the tile-ring decode over T consecutive 16-token tiles.
 //
 // Scores: tokens are the MMA rows, heads the 8 columns; B is q' (qa).
-//   2 bit (DSUB 4): the A operand of k-step s is two 8-byte centroid gathers
-//     (tokens gid and gid+8, channels 4j..4j+3 of subvector j = 4s+tig);
-//     kq[i][0]: this lane's 16 key-code bytes (tokens gid, gid+8 x
-//     subvectors 4s+tig).
-//   4 bit (DSUB 2): four 4-byte gathers (tokens gid and gid+8 x subvectors
-//     8s+tig and 8s+4+tig, i.e. channels 16s+k in k order); kq[i][0] / [1]:
+//   2 bit: the A operand of k-step s is two 8-byte centroid gathers (tokens
+//     gid and gid+8, channels 4j..4j+3 of subvector j = 4s+tig); kw[i]:
+//     this lane's 16 key-code bytes (tokens gid, gid+8 x subvectors 4s+tig).
+//   3 bit: the same gathers; kw[i]: the 3-byte pairs (j, j+16) of tokens gid
+//     (bytes 0..11) and gid+8 (bytes 12..23) for j = tig, 4+tig, 8+tig,
+//     12+tig, so subvector 4s+tig is pair s%4, low code for s < 4.
+//   4 bit: four 4-byte gathers (tokens gid and gid+8 x subvectors 8s+tig and
+//     8s+4+tig, i.e. channels 16s+k in k order); kw[i][0..3] / [4..7]:
 //     tokens gid / gid+8, byte 2s / 2s+1 = subvector 8s+tig / 8s+4+tig.
-//     A tile holds every lane's word 0, then every lane's word 1, so the
-//     two 128-bit reads of a warp are each one contiguous 512-byte run.
 // A 16-token tile takes 8 score MMAs.  movmatrix turns the scores into the
 // P.V B operand.  P.V: A = gathered V centroids, channels x tokens (2tig,
-// 2tig+1, 2tig+8, 2tig+9), paired by byte permutes; vq word p holds those
-// four tokens' codes of subvector 8p+gid (2 bit: channels 4j..4j+3 over two
-// M-tiles; 4 bit: channels 2j, 2j+1 in one M-tile).
+// 2tig+1, 2tig+8, 2tig+9), paired by byte permutes: for subvector 8p+gid, the
+// four tokens' codes are vw word p (2 and 4 bit), or pair (gid + 8(p%2))
+// of each token's 6-byte slot, low code for p < 2 (3 bit); 2 and 3 bit:
+// channels 4j..4j+3 over two M-tiles; 4 bit: channels 2j, 2j+1 in one.
+// kbyte / vbyte: the lane's replica offset in the K / V half row (2 and 4
+// bit), or the byte offset of the K / V codebook (3 bit).
 // Softmax state m0/l0, m1/l1 belongs to heads 2tig, 2tig+1, the columns of
 // this lane's O^T fragments.
-template <int T, int DSUB>
+template <int T, int MODE>
 __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
-                                         const uint32_t (&qa)[8][2], const uint4 (&kq)[T][V2Geo<DSUB>::LANE_WORDS],
-                                         const uint4 (&vq)[T][V2Geo<DSUB>::LANE_WORDS], int tile0,
+                                         const uint32_t (&qa)[8][2], const uint32_t (&kw)[T][V2Geo<MODE>::LW],
+                                         const uint32_t (&vw)[T][V2Geo<MODE>::LW], int tile0,
                                          const ColumnLimits& cl, int lane, float& m0, float& m1, float& l0, float& l1,
                                          float (&acc)[8][4]) {
   const int gid = lane >> 2;
@@ -205,20 +217,29 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
 #pragma unroll
   for (int i = 0; i < T; ++i) {
     float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (DSUB == 4) {
-#define VQKV_SCORE_STEP(S, ACC)                                                                     \
-  {                                                                                                 \
-    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i][0].x : kq[i][0].y, kbyte)); \
-    const uint2 d = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kq[i][0].z : kq[i][0].w, kbyte)); \
-    mma_16816(ACC, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);                                          \
+    if constexpr (MODE == VQKV_MODE_VQ2) {
+#define VQKV_SCORE_STEP(S, ACC)                                                                        \
+  {                                                                                                    \
+    const uint2 c = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kw[i][0] : kw[i][1], kbyte));         \
+    const uint2 d = lds_at<uint2>(s_cb, cb_offset<(S)&3>((S) < 4 ? kw[i][2] : kw[i][3], kbyte));         \
+    mma_16816(ACC, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);                                             \
   }
       VQKV_SCORE_STEP(0, da) VQKV_SCORE_STEP(1, db) VQKV_SCORE_STEP(2, da) VQKV_SCORE_STEP(3, db)
       VQKV_SCORE_STEP(4, da) VQKV_SCORE_STEP(5, db) VQKV_SCORE_STEP(6, da) VQKV_SCORE_STEP(7, db)
 #undef VQKV_SCORE_STEP
+    } else if constexpr (MODE == VQKV_MODE_VQ3) {
+#pragma unroll
+      for (int S = 0; S < 8; ++S) {
+        const uint32_t pg = pair_at(kw[i], 3 * (S & 3)), ph = pair_at(kw[i], 12 + 3 * (S & 3));
+        const uint32_t cg = S < 4 ? (pg & 0xfffu) : (pg >> 12), ch = S < 4 ? (ph & 0xfffu) : (ph >> 12);
+        const uint2 c = lds_at<uint2>(s_cb, kbyte + (cg << 3));
+        const uint2 d = lds_at<uint2>(s_cb, kbyte + (ch << 3));
+        mma_16816((S & 1) ? db : da, c.x, d.x, c.y, d.y, qa[S][0], qa[S][1]);
+      }
     } else {
 #define VQKV_SCORE_STEP4(S, ACC)                                                          \
   {                                                                                       \
-    const uint32_t wg = word_of(kq[i][0], (S) >> 1), wh = word_of(kq[i][1], (S) >> 1);    \
+    const uint32_t wg = kw[i][(S) >> 1], wh = kw[i][4 + ((S) >> 1)];                      \
     const uint32_t ag = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2>(wg, kbyte));        \
     const uint32_t bg = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2 + 1>(wg, kbyte));    \
     const uint32_t ah = lds_at<uint32_t>(s_cb, cb_offset<((S)&1) * 2>(wh, kbyte));        \
@@ -240,26 +261,10 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   softmax_tiles<T, 8>(sc, m0, m1, l0, l1, acc, bP);
 #pragma unroll
   for (int i = 0; i < T; ++i) {
-    if constexpr (DSUB == 4) {
-#define VQKV_PV_STEP(PP, W)                                                                    \
-  {                                                                                            \
-    const uint2 R0 = lds_at<uint2>(s_cb, cb_offset<0>(W, vbyte));                              \
-    const uint2 R1 = lds_at<uint2>(s_cb, cb_offset<1>(W, vbyte));                              \
-    const uint2 R2 = lds_at<uint2>(s_cb, cb_offset<2>(W, vbyte));                              \
-    const uint2 R3 = lds_at<uint2>(s_cb, cb_offset<3>(W, vbyte));                              \
-    mma_16816(acc[2 * (PP)], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632), \
-              __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP[i][0], bP[i][1]); \
-    mma_16816(acc[2 * (PP) + 1], __byte_perm(R0.y, R1.y, 0x5410),                              \
-              __byte_perm(R0.y, R1.y, 0x7632), __byte_perm(R2.y, R3.y, 0x5410),                \
-              __byte_perm(R2.y, R3.y, 0x7632), bP[i][0], bP[i][1]);                            \
-  }
-      VQKV_PV_STEP(0, vq[i][0].x) VQKV_PV_STEP(1, vq[i][0].y) VQKV_PV_STEP(2, vq[i][0].z)
-      VQKV_PV_STEP(3, vq[i][0].w)
-#undef VQKV_PV_STEP
-    } else {
+    if constexpr (MODE == VQKV_MODE_VQ4) {
 #pragma unroll
       for (int pp = 0; pp < 8; ++pp) {
-        const uint32_t w = word_of(vq[i][pp >> 2], pp & 3);
+        const uint32_t w = vw[i][pp];
         const uint32_t R0 = lds_at<uint32_t>(s_cb, cb_offset<0>(w, vbyte));
         const uint32_t R1 = lds_at<uint32_t>(s_cb, cb_offset<1>(w, vbyte));
         const uint32_t R2 = lds_at<uint32_t>(s_cb, cb_offset<2>(w, vbyte));
@@ -267,6 +272,36 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
         mma_16816(acc[pp], __byte_perm(R0, R1, 0x5410), __byte_perm(R0, R1, 0x7632), __byte_perm(R2, R3, 0x5410),
                   __byte_perm(R2, R3, 0x7632), bP[i][0], bP[i][1]);
       }
+    } else {
+#define VQKV_PV_PAIR(PP, R0, R1, R2, R3)                                                           \
+  {                                                                                                \
+    mma_16816(acc[2 * (PP)], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632),     \
+              __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP[i][0], bP[i][1]); \
+    mma_16816(acc[2 * (PP) + 1], __byte_perm(R0.y, R1.y, 0x5410), __byte_perm(R0.y, R1.y, 0x7632), \
+              __byte_perm(R2.y, R3.y, 0x5410), __byte_perm(R2.y, R3.y, 0x7632), bP[i][0], bP[i][1]); \
+  }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        if constexpr (MODE == VQKV_MODE_VQ2) {
+          const uint32_t w = vw[i][pp];
+          const uint2 R0 = lds_at<uint2>(s_cb, cb_offset<0>(w, vbyte));
+          const uint2 R1 = lds_at<uint2>(s_cb, cb_offset<1>(w, vbyte));
+          const uint2 R2 = lds_at<uint2>(s_cb, cb_offset<2>(w, vbyte));
+          const uint2 R3 = lds_at<uint2>(s_cb, cb_offset<3>(w, vbyte));
+          VQKV_PV_PAIR(pp, R0, R1, R2, R3)
+        } else {
+          auto code = [&](int k) {   // the code of slot k's token (pair byte 6k + 3(pp%2))
+            const uint32_t pr = pair_at(vw[i], 6 * k + 3 * (pp & 1));
+            return pp < 2 ? (pr & 0xfffu) : (pr >> 12);
+          };
+          const uint2 R0 = lds_at<uint2>(s_cb, vbyte + (code(0) << 3));
+          const uint2 R1 = lds_at<uint2>(s_cb, vbyte + (code(1) << 3));
+          const uint2 R2 = lds_at<uint2>(s_cb, vbyte + (code(2) << 3));
+          const uint2 R3 = lds_at<uint2>(s_cb, vbyte + (code(3) << 3));
+          VQKV_PV_PAIR(pp, R0, R1, R2, R3)
+        }
+      }
+#undef VQKV_PV_PAIR
     }
   }
 }
@@ -341,17 +376,19 @@ __device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* 
 // several in column groups of up to 8, one CTA each (kQueryGroups).  PAGED:
 // tiles are found through the block table (at most two bulk copies per
 // step).
-template <int Q, bool PAGED, int DSUB>
+template <int Q, bool PAGED, int MODE>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
-  using G = V2Geo<DSUB>;
-  using Sm = V2Smem<DSUB>;
-  using Dim = typename std::conditional<DSUB == 4, Vq2Dim, Vq4Dim>::type;
+  using G = V2Geo<MODE>;
+  using Sm = V2Smem<MODE>;
+  using Dim = typename std::conditional<MODE == VQKV_MODE_VQ4, Vq4Dim, Vq2Dim>::type;
+  constexpr bool APPEND = !G::PAIRS;   // the fused append encodes one-byte codes only
   extern __shared__ __align__(128) unsigned char smem[];
-  // Codebooks: centroid c at row c (256 bytes): K replicas at c*256 + r*2*DSUB,
-  // V replicas at c*256 + 128 + r*2*DSUB.  2 bit: lane l reads replica l % 16
-  // (8 bytes), so each half-warp phase of a 64-bit gather hits 16 bank pairs;
-  // 4 bit: lane l reads replica l (4 bytes), one bank per lane.
+  // Codebooks.  256 entries: centroid c at row c (256 bytes), K replicas at
+  // c*256 + r*2*DSUB, V replicas at c*256 + 128 + r*2*DSUB; 2 bit: lane l
+  // reads replica l % 16 (8 bytes), so each half-warp phase of a 64-bit
+  // gather hits 16 bank pairs; 4 bit: lane l reads replica l (4 bytes), one
+  // bank per lane.  4096 entries (3 bit): K centroid c at 8c, V at 32768 + 8c.
   const unsigned char* s_cb = smem;
   float* s_qp = reinterpret_cast<float*>(smem + V2_Q_OFF);
   float* s_comb = reinterpret_cast<float*>(smem);   // after the tile loop only
@@ -364,8 +401,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int b_end = min(b_begin + p.bpg, p.B);
   // this CTA's softmax columns
   const int col0 = GROUPS ? cta_col0(p) : 0, nloc = GROUPS ? min(8, p.ncols - col0) : p.ncols;
-  const uint32_t kbyte = DSUB == 4 ? (uint32_t)(lane & 15) << 3 : (uint32_t)lane << 2;
-  const uint32_t vbyte = 128u | kbyte;
+  const uint32_t kbyte = G::PAIRS ? 0u : G::DSUB == 4 ? (uint32_t)(lane & 15) << 3 : (uint32_t)lane << 2;
+  const uint32_t vbyte = G::PAIRS ? 32768u : 128u | kbyte;
   // this warp's ring: stage st holds the K super-tile, then the V super-tile
   const uint32_t ring = smem_u32(smem + G::RING_OFF) + warp * (V2_STAGES * G::STAGE_BYTES);
   const uint32_t mbar = smem_u32(smem + G::MBAR_OFF) + warp * (V2_STAGES * 8);
@@ -383,13 +420,23 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     // Every input load of the prologue is issued before the first one is
     // used (the sequence length decides the rest): this warp's codebook
     // entry, its query column, and the new K / V row of a fused append.
-    using CbEntry = typename std::conditional<DSUB == 4, uint2, uint32_t>::type;
-    const CbEntry cb_entry = __ldg(reinterpret_cast<const CbEntry*>((threadIdx.x >> 8) ? p.vcb : p.kcb) +
-                                   (size_t)kvh * 256 + (threadIdx.x & 255));
+    // (4096 entries: eight 16-byte pieces of the two 32-KB codebooks per thread)
+    using CbEntry = typename std::conditional<G::PAIRS, uint4[8],
+                                              typename std::conditional<G::DSUB == 4, uint2, uint32_t>::type>::type;
+    CbEntry cb_entry;
+    if constexpr (G::PAIRS) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        cb_entry[i] = __ldg(reinterpret_cast<const uint4*>(i < 4 ? p.kcb : p.vcb) + (size_t)kvh * 2048 +
+                            (i & 3) * V2_THREADS + threadIdx.x);
+    } else {
+      cb_entry = __ldg(reinterpret_cast<const CbEntry*>((threadIdx.x >> 8) ? p.vcb : p.kcb) + (size_t)kvh * 256 +
+                       (threadIdx.x & 255));
+    }
     const QueryLoad qload = load_query(p, b, kvh, warp, lane, col0, nloc);
     uint2 xraw = make_uint2(0u, 0u);
     float4 xs = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (p.k_new != nullptr) {
+    if (APPEND && p.k_new != nullptr) {
       const size_t row = ((size_t)b * p.Hkv + kvh) * kHeadDim + 4 * lane;
       xraw = *reinterpret_cast<const uint2*>((warp < 8 ? p.k_new : p.v_new) + row);
       if (warp < 8) xs = *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane);
@@ -472,7 +519,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       // new rows in its prologue and writes their codes before any copy of
       // that tile is issued, so the ring reads them like any other code.
       const int t_new = L - 1;
-      const bool append = p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
+      const bool append = APPEND && p.k_new != nullptr && t_new >= 0 && (t_new >> 4) >= t_begin && (t_new >> 4) < t_end;
       const int k_new = append ? ((t_new >> 4) - t_begin) / G::TPI : 0;   // super-tile of the new token
       const bool late_start = append && k_new % V2_WARPS == warp && k_new / V2_WARPS < V2_STAGES - 1;
       // start the ring before the prologue so the copies overlap it (after
@@ -488,7 +535,10 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         transform_loaded(xraw, warp < 8, xs, lane, x);
         xnew = make_float4(x[0], x[1], x[2], x[3]);
       }
-      {
+      if constexpr (G::PAIRS) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) reinterpret_cast<uint4*>(smem)[i * V2_THREADS + threadIdx.x] = cb_entry[i];
+      } else {
         // thread t writes the G::REPL replicas of centroid t & 255 of K
         // (t < 256) or V (t >= 256), loaded above; replica (i + lane) % REPL
         // at step i keeps the lanes of each store phase on distinct banks
@@ -500,9 +550,9 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
       }
       transform_query(p, qload, warp, lane, s_qp, V2_Q_PITCH, nloc);
       __syncthreads();
-      if (append) {
+      if constexpr (APPEND) if (append) {
         const size_t stream = (size_t)(b * p.Hkv + kvh) * p.stream_bytes;
-        append_rows<DSUB>(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
+        append_rows<G::DSUB>(xnew, p.kc_w + stream, p.vc_w + stream, p.near_tie, t_new, smem,
                     reinterpret_cast<Best*>(smem + Sm::APP_OFF));
         if (lane == 0 && late_start)
           for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
@@ -514,7 +564,7 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         if (gid < nloc) {
-          if constexpr (DSUB == 4) {
+          if constexpr (G::DSUB == 4) {
             const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH + 4 * (4 * s + tig));
             qa[s][0] = pack_half2(v.x, v.y);
             qa[s][1] = pack_half2(v.z, v.w);
@@ -536,20 +586,29 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           timed_out = true;
           break;
         }
-        uint4 kq[G::TPI][G::LANE_WORDS], vq[G::TPI][G::LANE_WORDS];
+        // the lane's code words: plane w (every lane's 16- or 8-byte piece
+        // of it, contiguous) at 512 w
+        uint32_t kq[G::TPI][G::LW], vq[G::TPI][G::LW];
 #pragma unroll
         for (int i = 0; i < G::TPI; ++i) {
+          const uint32_t kt = ring + st * G::STAGE_BYTES + i * G::TILE_BYTES;
+          const uint32_t vt = kt + G::TPI * G::TILE_BYTES;
 #pragma unroll
-          for (int w = 0; w < G::LANE_WORDS; ++w) {   // word w of every lane: 512 contiguous bytes
-            const uint32_t lo = 512 * w + lane * 16;
-            kq[i][w] = lds128(ring + st * G::STAGE_BYTES + i * G::TILE_BYTES + lo);
-            vq[i][w] = lds128(ring + st * G::STAGE_BYTES + (G::TPI + i) * G::TILE_BYTES + lo);
+          for (int w = 0; w < G::LW / 4; ++w) {
+            const uint4 a = lds128(kt + 512 * w + lane * 16), c = lds128(vt + 512 * w + lane * 16);
+            kq[i][4 * w] = a.x, kq[i][4 * w + 1] = a.y, kq[i][4 * w + 2] = a.z, kq[i][4 * w + 3] = a.w;
+            vq[i][4 * w] = c.x, vq[i][4 * w + 1] = c.y, vq[i][4 * w + 2] = c.z, vq[i][4 * w + 3] = c.w;
+          }
+          if constexpr (G::LW % 4 != 0) {
+            const uint2 a = lds64(kt + 512 + lane * 8), c = lds64(vt + 512 + lane * 8);
+            kq[i][G::LW - 2] = a.x, kq[i][G::LW - 1] = a.y;
+            vq[i][G::LW - 2] = c.x, vq[i][G::LW - 1] = c.y;
           }
         }
         __syncwarp();
         // refill the stage this warp finished with in the previous step
         if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
-        vq2_step<G::TPI, DSUB>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
+        vq2_step<G::TPI, MODE>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
                                lane, m0, m1, l0, l1, acc);
       }
       if (timed_out) {
@@ -750,10 +809,13 @@ cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
 
 int decode_tile_tokens(int mode) { return mode == VQKV_MODE_VQ15 ? V15_TILE : V2_TILE; }
 int decode_tiles_per_step(int mode) {
-  return mode == VQKV_MODE_VQ2 ? V2Geo<4>::TPI : mode == VQKV_MODE_VQ4 ? V2Geo<2>::TPI : 1;
+  return mode == VQKV_MODE_VQ2   ? V2Geo<VQKV_MODE_VQ2>::TPI
+         : mode == VQKV_MODE_VQ4 ? V2Geo<VQKV_MODE_VQ4>::TPI
+         : mode == VQKV_MODE_VQ3 ? V2Geo<VQKV_MODE_VQ3>::TPI
+                                 : 1;
 }
 size_t decode_smem_bytes(int mode) {
-  return mode == VQKV_MODE_VQ2 ? kV2Smem : mode == VQKV_MODE_VQ4 ? kV4Smem : kV15Smem;
+  return mode == VQKV_MODE_VQ2 ? kV2Smem : mode == VQKV_MODE_VQ4 ? kV4Smem : mode == VQKV_MODE_VQ3 ? kV3Smem : kV15Smem;
 }
 int decode_threads(int mode) { return mode == VQKV_MODE_VQ15 ? V15_THREADS : V2_THREADS; }
 
@@ -761,13 +823,13 @@ namespace {
 using DecodeKernel = void (*)(DecodeParams);
 
 // [paged][query layout] instantiations of one mode's decode kernel.
-template <int DSUB>
+template <int MODE>
 struct ByteCodeKernels {
   static constexpr DecodeKernel k[2][3] = {
-      {decode_vq2_kernel<kOneQuery, false, DSUB>, decode_vq2_kernel<kQueries, false, DSUB>,
-       decode_vq2_kernel<kQueryGroups, false, DSUB>},
-      {decode_vq2_kernel<kOneQuery, true, DSUB>, decode_vq2_kernel<kQueries, true, DSUB>,
-       decode_vq2_kernel<kQueryGroups, true, DSUB>}};
+      {decode_vq2_kernel<kOneQuery, false, MODE>, decode_vq2_kernel<kQueries, false, MODE>,
+       decode_vq2_kernel<kQueryGroups, false, MODE>},
+      {decode_vq2_kernel<kOneQuery, true, MODE>, decode_vq2_kernel<kQueries, true, MODE>,
+       decode_vq2_kernel<kQueryGroups, true, MODE>}};
 };
 struct Vq15Kernels {
   static constexpr DecodeKernel k[2][3] = {
@@ -778,7 +840,10 @@ struct Vq15Kernels {
 };
 
 const DecodeKernel (*kernels_of(int mode))[3] {
-  return mode == VQKV_MODE_VQ2 ? ByteCodeKernels<4>::k : mode == VQKV_MODE_VQ4 ? ByteCodeKernels<2>::k : Vq15Kernels::k;
+  return mode == VQKV_MODE_VQ2   ? ByteCodeKernels<VQKV_MODE_VQ2>::k
+         : mode == VQKV_MODE_VQ4 ? ByteCodeKernels<VQKV_MODE_VQ4>::k
+         : mode == VQKV_MODE_VQ3 ? ByteCodeKernels<VQKV_MODE_VQ3>::k
+                                 : Vq15Kernels::k;
 }
 }  // namespace
 

@@ -3,8 +3,8 @@
 // a Hadamard rotation of the keys, K-Means codebook; arXiv summary page,
 // "方法详解", stages 1-2).
 //
-// 2-bit: one warp per row (or one CTA per row when rows are few); lane l
-// holds channels 4l..4l+3.  1.5-bit: tensor-core screening with an exact
+// 2-, 3- and 4-bit: one warp per row (or one CTA per row when rows are few);
+// lane l holds channels 4l..4l+3.  1.5-bit: tensor-core screening with an exact
 // re-rank (below).  For keys the transform
 // x' = (x / s) . H / sqrt(128) is carried in double-float arithmetic (pairs
 // of fp32 with error-free sums and products) and rounded to fp32 once, so the
@@ -112,6 +112,98 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
   }
 }
 
+// ------------------------------------------------------------------ VQ3
+// 4096-entry codebooks of 4-channel subvectors, 12-bit codes in 3-byte
+// pairs (j, j+16).  Lane l holds subvector l (channels 4l..4l+3) and scans
+// the whole codebook (SPLIT = 1, 8 warps, one row per warp) or a slice of
+// 4096 / SPLIT candidates (SPLIT = 16 warps sharing one row per CTA), with
+// the fp32 codebook (or each warp's slice of it) in shared memory (64 KB,
+// read by broadcast).  Lanes 0..15 then write pair l from their own code
+// and lane l + 16's.
+constexpr size_t kEnc3Smem = 4096 * sizeof(float4);
+constexpr int ENC3_SPLIT = 16;
+
+// Search of one subvector over candidates [c_lo, c_hi) (a multiple of 4):
+// fp32 direct differences, four chains over the candidates of each residue
+// mod 4 (independent latency chains), merged by distance, then index.
+template <typename Load>
+__device__ __forceinline__ Best vq3_search(const float (&x)[4], int c_lo, int c_hi, Load load) {
+  Best ch[4] = {best_init(), best_init(), best_init(), best_init()};
+#pragma unroll 2
+  for (int c = c_lo; c < c_hi; c += 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 cv = load(c + k);
+      float u = __fsub_rn(x[0], cv.x), d = __fmul_rn(u, u);
+      u = __fsub_rn(x[1], cv.y); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[2], cv.z); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[3], cv.w); d = __fmaf_rn(u, u, d);
+      best_push(ch[k], d, c + k);
+    }
+  }
+  return best_merge(best_merge(ch[0], ch[1]), best_merge(ch[2], ch[3]));
+}
+
+template <int SPLIT>
+__global__ void __launch_bounds__(SPLIT == 1 ? ENC_THREADS : SPLIT * 32) encode_vq3_kernel(const EncodeParams p) {
+  constexpr int kThreads = SPLIT == 1 ? ENC_THREADS : SPLIT * 32;
+  constexpr int kWarps = kThreads / 32;
+  extern __shared__ __align__(16) unsigned char enc_smem[];
+  float4* s_cb = reinterpret_cast<float4*>(enc_smem);
+  __shared__ Best s_part[SPLIT > 1 ? SPLIT * 32 : 1];
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c_lo = (SPLIT == 1) ? 0 : warp * (4096 / SPLIT);
+  const int c_hi = c_lo + 4096 / SPLIT;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  {
+    // the whole codebook (SPLIT = 1, by the CTA) or this warp's slice
+    // (SPLIT > 1, by the warp): every load in flight before the first store
+    constexpr int kPer = SPLIT == 1 ? 4096 / kThreads : 4096 / SPLIT / 32;
+    const int first = SPLIT == 1 ? threadIdx.x : c_lo + lane;
+    const int stride = SPLIT == 1 ? kThreads : 32;
+    const uint2* g = reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * 4096 + first;
+    uint2 raw[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) raw[i] = __ldg(g + i * stride);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const __half2 a = *reinterpret_cast<const __half2*>(&raw[i].x);
+      const __half2 b = *reinterpret_cast<const __half2*>(&raw[i].y);
+      s_cb[first + i * stride] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+    }
+  }
+  if (SPLIT == 1)
+    __syncthreads();
+  else
+    __syncwarp();
+  const int rows = p.B * p.n_rows;
+  const int r0 = (SPLIT == 1) ? blockIdx.x * kWarps + warp : blockIdx.x;
+  const int rstep = (SPLIT == 1) ? gridDim.x * kWarps : gridDim.x;
+  for (int r = r0; r < rows; r += rstep) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    const int t = p.pos[b] + n;
+    if (t < 0 || t >= p.cap_len) {
+      if (lane == 0 && (SPLIT == 1 || warp == 0) && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      continue;
+    }
+    float x[4];
+    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
+    const Best part = vq3_search(x, c_lo, c_hi, [&](int c) { return s_cb[c]; });
+    const Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
+    if (SPLIT == 1 || warp == 0) {
+      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffffffu);
+      const int hi = __shfl_down_sync(0xffffffffu, bst.i, 16);
+      uint8_t* tb = tile_base(p, b, kvh, t, 16, 768);
+      if (tb && lane < 16) {
+        tb[vq3_byte_offset(p.role, t & 15, lane, 0)] = (uint8_t)(bst.i & 0xff);
+        tb[vq3_byte_offset(p.role, t & 15, lane, 1)] = (uint8_t)(((bst.i >> 8) & 0xf) | ((hi & 0xf) << 4));
+        tb[vq3_byte_offset(p.role, t & 15, lane, 2)] = (uint8_t)(hi >> 4);
+      }
+    }
+  }
+}
 
 // ------------------------------------------------------------------ VQ15, tensor-core screening
 // Many rows of 1.5-bit encode: the distance search against 4096 centroids is
@@ -489,6 +581,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
 int encode_warps_per_cta() { return ENC_WARPS; }
 
 cudaError_t encode_prepare(int mode) {
+  if (mode == VQKV_MODE_VQ3) {
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(encode_vq3_kernel<1>, a, (int)kEnc3Smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(encode_vq3_kernel<ENC3_SPLIT>, a, (int)kEnc3Smem);
+    return e;
+  }
   if (mode != VQKV_MODE_VQ15) return cudaSuccess;
   {
     const cudaError_t e0 = cudaFuncSetAttribute(encode_vq15_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -506,6 +604,9 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 4>, ENC_THREADS, 0);
   if (mode == VQKV_MODE_VQ4)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 2>, ENC_THREADS, 0);
+  if (mode == VQKV_MODE_VQ3)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq3_kernel<1>, ENC_THREADS,
+                                                         kEnc3Smem);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_tc_kernel, TC_THREADS, kTcSmem);
 }
 
@@ -519,6 +620,11 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
   if (mode == VQKV_MODE_VQ4) {
     if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
     return launch_pdl(encode_vq2_kernel<1, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
+  }
+  if (mode == VQKV_MODE_VQ3) {
+    if (split_rows)
+      return launch_pdl(encode_vq3_kernel<ENC3_SPLIT>, grid, dim3(ENC3_SPLIT * 32), kEnc3Smem, stream, p);
+    return launch_pdl(encode_vq3_kernel<1>, grid, dim3(ENC_THREADS), kEnc3Smem, stream, p);
   }
   if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
   return launch_pdl(encode_vq15_tc_kernel, grid, dim3(TC_THREADS), kTcSmem, stream, p);

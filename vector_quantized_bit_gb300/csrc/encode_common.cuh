@@ -242,6 +242,17 @@ __device__ __forceinline__ long long vq15_pair_offset(int role, int t, int pair)
              : 1536LL * tile + 48 * (4 * pair + ((rr & 7) >> 1)) + 12 * u + 3 * ((rr & 1) + 2 * (rr >> 3));
 }
 
+// Byte offset of byte k (0..2) of 3-bit pair `pair` (subvectors pair and
+// pair + 16) of token t in a K or V stream (the layout of include/vqkv.h:
+// each lane's 24-byte run split into a 16-byte and an 8-byte plane).
+__device__ __forceinline__ long long vq3_byte_offset(int role, int t, int pair, int k) {
+  const int tile = t >> 4, rr = t & 15;
+  const int lane = (role == VQKV_ROLE_K) ? 4 * (rr & 7) + (pair & 3) : 4 * (pair & 7) + ((rr & 7) >> 1);
+  const int n = (role == VQKV_ROLE_K) ? 12 * (rr >> 3) + 3 * (pair >> 2) + k
+                                      : 6 * (2 * (rr >> 3) + (rr & 1)) + 3 * (pair >> 3) + k;
+  return 768LL * tile + (n < 16 ? 16 * lane + n : 512 + 8 * lane + n - 16);
+}
+
 // Writes codes lo (subvector pair) and hi (pair + 8) as 3 bytes.
 __device__ __forceinline__ void store_pair(uint8_t* dst, int lo, int hi) {
   dst[0] = (uint8_t)(lo & 0xff);

@@ -31,9 +31,10 @@ _S_Q, _S_K, _S_V, _S_OUTLIER, _S_SEQLEN, _S_CODES, _S_CALIB, _S_KMEANS, _S_APPEN
 MODE_VQ2 = 0
 MODE_VQ15 = 1
 MODE_VQ4 = 2
+MODE_VQ3 = 3
 
 # codebook geometry per mode: (entries, subvector dims)
-MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2)}
+MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -42,7 +43,7 @@ class Workload:
 
     config_id: int
     name: str
-    mode: int              # MODE_VQ2, MODE_VQ15 or MODE_VQ4
+    mode: int              # MODE_VQ2, MODE_VQ15, MODE_VQ4 or MODE_VQ3
     B: int
     Hq: int
     Hkv: int
