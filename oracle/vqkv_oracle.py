@@ -37,16 +37,18 @@ MODE_VQ2 = 0
 MODE_VQ15 = 1
 MODE_VQ4 = 2
 MODE_VQ3 = 3
+MODE_VQ125 = 4
 ROLE_K = 0
 ROLE_V = 1
 
 # (entries, subvector dims) per mode [P1 Key points: 2^8 x 4 and 2^12 x 8]
-# and, within the pages' 1.25-4 bit range [P1 Summary], 4 bit = 2^8 x 2 and
-# 3 bit = 2^12 x 4
-GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4)}
+# and, within the pages' 1.25-4 bit range [P1 Summary], 4 bit = 2^8 x 2,
+# 3 bit = 2^12 x 4 and 1.25 bit = 2^10 x 8
+GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4),
+            MODE_VQ125: (1024, 8)}
 # tokens per layout tile and bytes per tile of one cache stream
-TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64, MODE_VQ4: 16, MODE_VQ3: 16}
-TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536, MODE_VQ4: 1024, MODE_VQ3: 768}
+TILE_TOKENS = {MODE_VQ2: 16, MODE_VQ15: 64, MODE_VQ4: 16, MODE_VQ3: 16, MODE_VQ125: 16}
+TILE_BYTES = {MODE_VQ2: 512, MODE_VQ15: 1536, MODE_VQ4: 1024, MODE_VQ3: 768, MODE_VQ125: 320}
 BYTE_CODE_MODES = (MODE_VQ2, MODE_VQ4)   # one byte per code
 
 
@@ -211,6 +213,29 @@ def vq3_byte(role: int, t: int, pair: int, k: int) -> int:
     return 768 * tile + (16 * lane + b if b < 16 else 512 + 8 * lane + b - 16)
 
 
+def vq125_bit(role: int, t: int, j: int, b: int) -> int:
+    """Stream bit address (8 * byte + bit, LSB first) of bit b (0..9) of the
+    10-bit code of subvector j (0..15, channels 8j..8j+7) of token t.
+
+    A 320-byte tile of 16 tokens is a set of runs, each stored as two planes
+    (plane 0 from byte 0, plane 1 from byte 256); run bits are numbered from
+    the least significant bit of the run's first byte.  K: 32 runs of 10
+    bytes (plane 0: 8 bytes at 8*L, plane 1: 2 bytes at 256 + 2*L), run
+    L = 4*(r%8) + j%4, run bit 40*(r/8) + 10*(j/4) + b.  V: 16 runs of 20
+    bytes (plane 0: 16 bytes at 16*R, plane 1: 4 bytes at 256 + 4*R), run
+    R = 4*((j%8)/2) + (r%8)/2, run bit 40*(2*(r/8) + r%2) + 10*(j%2 + 2*(j/8))
+    + b.  Each token's bits of a run fill 5 whole bytes.
+    """
+    tile, r = divmod(t, 16)
+    if role == ROLE_K:
+        run, rb, p0, p1 = 4 * (r % 8) + j % 4, 40 * (r // 8) + 10 * (j // 4) + b, 8, 2
+    else:
+        run, rb, p0, p1 = 4 * ((j % 8) // 2) + (r % 8) // 2, 40 * (2 * (r // 8) + r % 2) + 10 * (j % 2 + 2 * (j // 8)) + b, 16, 4
+    n, bit = divmod(rb, 8)
+    byte = p0 * run + n if n < p0 else 256 + p1 * run + n - p0
+    return 8 * (320 * tile + byte) + bit
+
+
 def vq15_offset(role: int, t: int, pair: int) -> int:
     """First of the 3 bytes holding the code pair (pair, pair+8) of token t."""
     tile, rem = divmod(t, 64)
@@ -245,6 +270,15 @@ def pack_stream(codes: np.ndarray, mode: int, role: int, cap_len: int,
             for p in range(16):
                 for k, byte in enumerate(pack_pair(int(codes[t, p]), int(codes[t, p + 16]))):
                     buf[vq3_byte(role, t, p, k)] = byte
+    elif mode == MODE_VQ125:
+        for t in range(L):
+            for j in range(16):
+                for b in range(10):
+                    a = vq125_bit(role, t, j, b)
+                    if (int(codes[t, j]) >> b) & 1:
+                        buf[a // 8] |= 1 << (a % 8)
+                    else:
+                        buf[a // 8] &= ~(1 << (a % 8)) & 0xFF
     else:
         for t in range(L):
             for p in range(8):
@@ -268,6 +302,14 @@ def unpack_stream(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
             for p in range(16):
                 out[t, p], out[t, p + 16] = unpack_pair(*(int(buf[vq3_byte(role, t, p, k)]) for k in range(3)))
         return out
+    if mode == MODE_VQ125:
+        out = np.zeros((L, 16), dtype=np.int64)
+        for t in range(L):
+            for j in range(16):
+                for b in range(10):
+                    a = vq125_bit(role, t, j, b)
+                    out[t, j] |= ((int(buf[a // 8]) >> (a % 8)) & 1) << b
+        return out
     out = np.empty((L, 16), dtype=np.int64)
     for t in range(L):
         for p in range(8):
@@ -277,10 +319,23 @@ def unpack_stream(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndarray:
 
 
 def offset_table(mode: int, role: int, L: int) -> np.ndarray:
-    """Byte offset of every code (VQ2, VQ4) or code pair (VQ15) of tokens
-    [0, L): a vectorised form of the offset functions above, for large
-    streams."""
+    """Byte offset of every code (VQ2, VQ4) or code pair (VQ15; VQ3: of each
+    of its 3 bytes, [L][16][3]) of tokens [0, L), or the stream bit address
+    of every code bit (VQ125, [L][16][10]): a vectorised form of the offset
+    functions above, for large streams."""
     t = np.arange(L)[:, None]
+    if mode == MODE_VQ125:   # [L][16 subvectors][10 bits]: bit addresses
+        j = np.arange(16)[None, :, None]
+        b = np.arange(10)[None, None, :]
+        tt = t[:, :, None]
+        tile, r = tt // 16, tt % 16
+        if role == ROLE_K:
+            run, rb, p0, p1 = 4 * (r % 8) + j % 4, 40 * (r // 8) + 10 * (j // 4) + b, 8, 2
+        else:
+            run, rb, p0, p1 = (4 * ((j % 8) // 2) + (r % 8) // 2,
+                               40 * (2 * (r // 8) + r % 2) + 10 * (j % 2 + 2 * (j // 8)) + b, 16, 4)
+        n, bit = rb // 8, rb % 8
+        return 8 * (320 * tile + np.where(n < p0, p0 * run + n, 256 + p1 * run + n - p0)) + bit
     if mode == MODE_VQ3:   # [L][16 pairs][3 bytes]
         p = np.arange(16)[None, :, None]
         k = np.arange(3)[None, None, :]
@@ -317,6 +372,9 @@ def pack_stream_fast(codes: np.ndarray, mode: int, role: int, cap_len: int) -> n
     off = offset_table(mode, role, codes.shape[0])
     if mode in BYTE_CODE_MODES:
         buf[off] = codes.astype(np.uint8)
+    elif mode == MODE_VQ125:
+        bits = ((codes.astype(np.int64)[..., None] >> np.arange(10)) & 1) << (off & 7)
+        np.bitwise_or.at(buf, off >> 3, bits.astype(np.uint8))
     elif mode == MODE_VQ3:
         lo, hi = codes[:, :16].astype(np.int64), codes[:, 16:].astype(np.int64)
         buf[off[..., 0]] = lo & 0xFF
@@ -337,6 +395,9 @@ def unpack_stream_fast(buf: np.ndarray, mode: int, role: int, L: int) -> np.ndar
     if mode == MODE_VQ3:
         b0, b1, b2 = (buf[off[..., k]].astype(np.int64) for k in range(3))
         return np.concatenate([b0 | ((b1 & 0xF) << 8), (b1 >> 4) | (b2 << 4)], axis=1)
+    if mode == MODE_VQ125:
+        bits = (buf[off >> 3].astype(np.int64) >> (off & 7)) & 1
+        return (bits << np.arange(10)).sum(axis=2)
     b0, b1, b2 = (buf[off + k].astype(np.int64) for k in range(3))
     return np.concatenate([b0 | ((b1 & 0xF) << 8), (b1 >> 4) | (b2 << 4)], axis=1)
 

@@ -153,12 +153,15 @@ def check_bits():
     assert vo.bits_per_element(vo.MODE_VQ15) == 1.5
     assert vo.bits_per_element(vo.MODE_VQ4) == 4.0
     assert vo.bits_per_element(vo.MODE_VQ3) == 3.0
+    assert vo.bits_per_element(vo.MODE_VQ125) == 1.25
     for mode, cap in ((vo.MODE_VQ2, 16), (vo.MODE_VQ2, 196608), (vo.MODE_VQ15, 64), (vo.MODE_VQ15, 65536),
-                      (vo.MODE_VQ4, 16), (vo.MODE_VQ4, 16384), (vo.MODE_VQ3, 16), (vo.MODE_VQ3, 65536)):
+                      (vo.MODE_VQ4, 16), (vo.MODE_VQ4, 16384), (vo.MODE_VQ3, 16), (vo.MODE_VQ3, 65536),
+                      (vo.MODE_VQ125, 16), (vo.MODE_VQ125, 65536)):
         assert vo.code_bytes(mode, cap) * 8 / (cap * 128) == vo.bits_per_element(mode)
     assert vo.code_bytes(vo.MODE_VQ2, 17) == 1024      # rounded up to whole tiles
     assert vo.code_bytes(vo.MODE_VQ15, 65) == 3072
     assert vo.code_bytes(vo.MODE_VQ4, 17) == 2048
+    assert vo.code_bytes(vo.MODE_VQ125, 17) == 640
 
 
 def check_layout_golden():
@@ -174,6 +177,10 @@ def check_layout_golden():
         role, t, p, k, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
         assert vo.vq3_byte(r, int(t), int(p), int(k)) == int(off), line
+    for line in golden_lines("layout_vq125.txt"):
+        role, t, j, b, addr = line.split()
+        r = vo.ROLE_K if role == "K" else vo.ROLE_V
+        assert vo.vq125_bit(r, int(t), int(j), int(b)) == int(addr), line
     for line in golden_lines("layout_vq15.txt"):
         role, t, p, off = line.split()
         r = vo.ROLE_K if role == "K" else vo.ROLE_V
@@ -185,6 +192,12 @@ def check_layout_golden():
 
 
 def check_layout_bijective():
+    for role in (0, 1):   # VQ125: bit by bit
+        addrs = [vo.vq125_bit(role, t, j, b) for t in range(32) for j in range(16) for b in range(10)]
+        assert sorted(addrs) == list(range(8 * 2 * vo.TILE_BYTES[vo.MODE_VQ125]))
+        tab = vo.offset_table(vo.MODE_VQ125, role, 32)
+        ref = [[[vo.vq125_bit(role, t, j, b) for b in range(10)] for j in range(16)] for t in range(32)]
+        assert np.array_equal(tab, np.array(ref))
     for role in (0, 1):   # VQ3: byte by byte
         offs = [vo.vq3_byte(role, t, p, k) for t in range(32) for p in range(16) for k in range(3)]
         assert sorted(offs) == list(range(2 * vo.TILE_BYTES[vo.MODE_VQ3]))
@@ -224,7 +237,7 @@ def test_layout_bijective():
 
 def test_pack_roundtrip():
     r = np.random.default_rng(1)
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3, vo.MODE_VQ125):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             L = 150
@@ -241,7 +254,7 @@ def test_pack_roundtrip():
 
 def test_append_does_not_touch_neighbours():
     """Writing token t changes only token t's bytes (token-local packing)."""
-    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3):
+    for mode in (vo.MODE_VQ2, vo.MODE_VQ15, vo.MODE_VQ4, vo.MODE_VQ3, vo.MODE_VQ125):
         E, dsub = vo.GEOMETRY[mode]
         for role in (vo.ROLE_K, vo.ROLE_V):
             codes = np.zeros((64, 128 // dsub), dtype=np.int64)
@@ -475,6 +488,44 @@ def test_planted_vq3_plane_split(monkeypatch):
         return 768 * tile + 24 * lane + b
     monkeypatch.setattr(vo, "vq3_byte", flat)
     assert _fails(check_layout_golden)
+
+
+def test_planted_vq125_single_plane(monkeypatch):
+    """Storing each K run as one 10-byte block instead of two planes must fail a pin."""
+    real = vo.vq125_bit
+
+    def flat(role, t, j, b):
+        if role != vo.ROLE_K:
+            return real(role, t, j, b)
+        tile, r = divmod(t, 16)
+        return 8 * (320 * tile + 10 * (4 * (r % 8) + j % 4)) + 40 * (r // 8) + 10 * (j // 4) + b
+    monkeypatch.setattr(vo, "vq125_bit", flat)
+    assert _fails(check_layout_golden)
+
+
+def test_planted_vq125_slot_order(monkeypatch):
+    """Giving V slots 1 and 2 (tokens 2i+1 and 2i+8) each other's bits must fail a pin."""
+    real = vo.vq125_bit
+
+    def swapped(role, t, j, b):
+        if role == vo.ROLE_V and t % 16 in (1, 8, 3, 10, 5, 12, 7, 14):
+            t = t + 7 if t % 2 else t - 7
+        return real(role, t, j, b)
+    monkeypatch.setattr(vo, "vq125_bit", swapped)
+    assert _fails(check_layout_golden)
+
+
+def test_vq125_token_bits_fill_whole_bytes():
+    """Each token's bits of a run occupy 5 whole bytes that hold no other token's bits."""
+    for role in (0, 1):
+        owner = {}
+        for t in range(16):
+            for j in range(16):
+                for b in range(10):
+                    owner.setdefault(vo.vq125_bit(role, t, j, b) // 8, set()).add(t)
+        assert all(len(v) == 1 for v in owner.values())
+        per_token = np.bincount([next(iter(v)) for v in owner.values()], minlength=16)
+        assert (per_token == 20).all()
 
 
 def test_planted_pair_order(monkeypatch):
