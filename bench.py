@@ -37,7 +37,7 @@ WORKLOAD_ID = 1
 GRAPH_STEPS = 100           # steps captured per CUDA graph
 SOAK_S = 0.5                # untimed load on each side of the timed region for clock sampling
 PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_vq2_llama8b_196k.json")
-BITS = {0: 2, 1: 1.5, 2: 4, 3: 3}   # bits per element of each code mode
+BITS = {0: 2, 1: 1.5, 2: 4, 3: 3, 4: 1.25}   # bits per element of each code mode
 
 
 def parse():
@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[1, 2, 3, 4],
                     help="1: Llama-3.1-8B 196k 2-bit (default); 2: ragged batch of 32; "
                          "3: Qwen2.5-14B 1.5-bit; 4: Mistral-7B encode + decode")
-    ap.add_argument("--mode", type=int, default=None, choices=[0, 1, 2, 3],
+    ap.add_argument("--mode", type=int, default=None, choices=[0, 1, 2, 3, 4],
                     help="override the workload's bit-width (0: 2-bit, 1: 1.5-bit, 2: 4-bit)")
     ap.add_argument("--queries", type=int, default=1,
                     help="queries per sequence (multi-query decode, e.g. speculative decoding): a step encodes "

@@ -63,14 +63,27 @@
  *   r = t % 16, byte k (0..2) of pair p of token t is run byte n of lane L:
  *       K: L = 4*(r%8) + p%4,      n = 12*(r/8) + 3*(p/4) + k
  *       V: L = 4*(p%8) + (r%8)/2,  n = 6*(2*(r/8) + r%2) + 3*(p/8) + k
- *   All four layouts are token-local: writing token t changes no byte of any
+ *   VQKV_MODE_VQ125 (1024 entries x 8 dims, 10-bit codes, 16 codes per
+ *   token; the low end of the same range): TILE = 16 tokens, 320 bytes, a
+ *   set of runs stored in two planes (plane 0 from byte 0, plane 1 from byte
+ *   256).  Run bits are numbered from the least significant bit of the run's
+ *   first byte; a code's bit b (LSB first) of subvector j (channels
+ *   8j..8j+7) of token t, r = t % 16, is run bit B of run L / R:
+ *       K: 32 runs of 10 bytes (8 at 8*L, 2 at 256 + 2*L),
+ *          L = 4*(r%8) + j%4,        B = 40*(r/8) + 10*(j/4) + b
+ *       V: 16 runs of 20 bytes (16 at 16*R, 4 at 256 + 4*R),
+ *          R = 4*((j%8)/2) + (r%8)/2, B = 40*(2*(r/8) + r%2) + 10*(j%2 + 2*(j/8)) + b
+ *     and run byte n = B/8 lies at the plane-0 offset + n while n is below
+ *     the plane-0 length, else at the plane-1 offset + n - (plane-0 length).
+ *   All five layouts are token-local: writing token t changes no byte of any
  *   other token.  Bits per element: 512*8/(16*128) = 2, 1536*8/(64*128) = 1.5,
- *   1024*8/(16*128) = 4 and 768*8/(16*128) = 3.
+ *   1024*8/(16*128) = 4, 768*8/(16*128) = 3 and 320*8/(16*128) = 1.25.
  *   (The layouts place, for each of the 32 lanes of a warp, the codes that
  *   lane needs for its tensor-core fragments in one contiguous 16-byte (VQ2)
  *   or 48-byte (VQ15) run, in two 16-byte runs 512 bytes apart (VQ4), or in
  *   a 16-byte and an 8-byte run (VQ3), so a warp reads a tile with
- *   coalesced 128-bit (and 64-bit) loads.)
+ *   coalesced 128-bit (and 64-bit) loads; VQ125 V runs are each read by the
+ *   two lanes that share their four tokens.)
  */
 #ifndef VQKV_H
 #define VQKV_H
@@ -95,7 +108,8 @@ typedef enum {
   VQKV_MODE_VQ2 = 0,   /* 2 bit:   2^8 entries x 4 dims, 8-bit codes  */
   VQKV_MODE_VQ15 = 1,  /* 1.5 bit: 2^12 entries x 8 dims, 12-bit codes */
   VQKV_MODE_VQ4 = 2,   /* 4 bit:   2^8 entries x 2 dims, 8-bit codes */
-  VQKV_MODE_VQ3 = 3    /* 3 bit:   2^12 entries x 4 dims, 12-bit codes */
+  VQKV_MODE_VQ3 = 3,   /* 3 bit:   2^12 entries x 4 dims, 12-bit codes */
+  VQKV_MODE_VQ125 = 4  /* 1.25 bit: 2^10 entries x 8 dims, 10-bit codes */
 } vqkv_mode;
 
 typedef enum {

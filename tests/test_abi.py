@@ -68,6 +68,8 @@ def test_code_bytes(lib):
     assert lib.vqkv_code_bytes(1, 65) == 3072
     assert lib.vqkv_code_bytes(3, 65536) == 65536 * 48
     assert lib.vqkv_code_bytes(3, 17) == 1536
+    assert lib.vqkv_code_bytes(4, 65536) == 65536 * 20
+    assert lib.vqkv_code_bytes(4, 17) == 640
     assert lib.vqkv_code_bytes(7, 16) == 0
     assert lib.vqkv_code_bytes(0, -1) == 0
 
@@ -91,7 +93,7 @@ def _enc(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(head_dim=64), 2), (dict(mode=4), 2), (dict(Hq=36, Hkv=4), 2), (dict(Hq=6, Hkv=4), 1),
+    (dict(head_dim=64), 2), (dict(mode=5), 2), (dict(Hq=36, Hkv=4), 2), (dict(Hq=6, Hkv=4), 1),
     (dict(Hkv=0), 1), (dict(B=-1), 1), (dict(max_seq_len=65), 1), (dict(max_seq_len=-1), 1),
     (dict(cap_len=0, max_seq_len=0), 1), (dict(q=None), 1), (dict(k_codes=None), 1), (dict(s=None), 1),
     (dict(out=None), 1), (dict(k_codes=0x2008), 1), (dict(k_codebook=0x5004), 1), (dict(q=0x1002), 1),
@@ -118,7 +120,7 @@ def test_null_args(lib):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(head_dim=256), 2), (dict(mode=4), 2), (dict(role=2), 1), (dict(Hkv=0), 1), (dict(n_rows=-1), 1),
+    (dict(head_dim=256), 2), (dict(mode=5), 2), (dict(role=2), 1), (dict(Hkv=0), 1), (dict(n_rows=-1), 1),
     (dict(cap_len=0), 1), (dict(x=None), 1), (dict(pos=None), 1), (dict(codebook=None), 1),
     (dict(codes=None), 1), (dict(s=None), 1), (dict(x=0x1004), 1), (dict(codebook=0x4008), 1),
 ])
@@ -155,6 +157,8 @@ def test_decode_append_validation(lib):
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # 2-bit only
     a.decode = _dec(mode=3)
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # nor 3 bit (12-bit code pairs)
+    a.decode = _dec(mode=4)
+    assert lib.vqkv_decode_append(ctypes.byref(a), None) == 2    # nor 1.25 bit (10-bit codes)
     a.decode = _dec(mode=2)
     assert lib.vqkv_decode_append(ctypes.byref(a), None) == 1    # 4 bit too: no new rows
     a.decode = _dec()
@@ -202,6 +206,7 @@ def test_ring_timeout_hook_validation(lib):
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=1)), 64, None) == 2   # 2-bit only
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=2)), 64, None) == 2
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=3)), 64, None) == 2
+    assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec(mode=4)), 64, None) == 2
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 0, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(ctypes.byref(_dec()), 5000, None) == 1
     assert lib.vqkv_test_decode_ring_timeout(None, 64, None) == 1

@@ -50,6 +50,11 @@ CASES = [
     (3, 1, 32, 8, [1000], 1024),
     (3, 2, 16, 2, [16, 15], 16),
     (3, 1, 8, 1, [257], 260),
+    (4, 3, 8, 2, [1, 17, 300], 320),
+    (4, 2, 5, 1, [64, 33], 64),
+    (4, 1, 32, 8, [1000], 1024),
+    (4, 2, 16, 2, [16, 15], 16),
+    (4, 1, 8, 1, [257], 260),
 ]
 
 
@@ -84,7 +89,7 @@ def test_tiny_config_full_pipeline_codes_from_oracle():
     assert vo.o_error(o, ref).max() <= H.O_TOL
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_zero_length_rows_and_empty_cache(mode):
     q, kc, vc, kcb, vcb, s = random_case(mode, 3, 4, 2, [0, 5, 0], 64, seed=7)
     kbuf, vbuf = H.pack_cache_role(mode, 0, kc, 64), H.pack_cache_role(mode, 1, vc, 64)
@@ -105,7 +110,7 @@ def test_empty_batch_is_a_no_op():
     _lib.vqkv_decode_attn(0, q, None, None, None, kcb, kcb, None, out, None, 16, 16)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_single_token_is_its_value_row(mode):
     q, kc, vc, kcb, vcb, s = random_case(mode, 1, 4, 1, [1], 16, seed=3)
     kbuf, vbuf = H.pack_cache_role(mode, 0, kc, 16), H.pack_cache_role(mode, 1, vc, 16)
@@ -115,7 +120,7 @@ def test_single_token_is_its_value_row(mode):
         assert np.array_equal(o[0, h], want)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_constant_value_codes(mode):
     q, kc, vc, kcb, vcb, s = random_case(mode, 1, 8, 2, [333], 400, seed=5)
     vc = [[np.full_like(vc[0][h], 11) for h in range(2)]]

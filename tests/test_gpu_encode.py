@@ -49,7 +49,7 @@ def test_tiny_config_keys_and_values():
         assert fails == 0, (role, ties, fails)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("role", [0, 1])
 @pytest.mark.parametrize("n", [37, 3])   # 3 rows: the few-rows launch (candidates split over warps)
 def test_ragged_positions_multi_head(mode, role, n):
@@ -70,6 +70,8 @@ def test_ragged_positions_multi_head(mode, role, n):
         for h in range(2):
             L = vo.TILE_TOKENS[mode] * (-(-cap // vo.TILE_TOKENS[mode]))
             off = vo.offset_table(mode, role, L)
+            if mode == vo.MODE_VQ125:   # bit addresses -> bytes
+                off = off >> 3
             if mode != vo.MODE_VQ15:   # every code byte (VQ3: every pair byte) is listed
                 touched = off[pos[b]:pos[b] + n].reshape(-1)
             else:
@@ -79,7 +81,7 @@ def test_ragged_positions_multi_head(mode, role, n):
             assert np.array_equal(buf[b, h][mask], prefill[b, h][mask])
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_positions_out_of_range_are_skipped_and_reported(mode):
     s, kcb, vcb = H.random_codebooks(mode, 1, 3)
     x = np.random.default_rng(1).standard_normal((2, 1, 4, 128)).astype(np.float16)
@@ -93,11 +95,13 @@ def test_positions_out_of_range_are_skipped_and_reported(mode):
     assert H.check_codes(got0[62:64], ref0[:2], d0[:2])[1] == 0
     changed = np.flatnonzero(buf[1, 0] != 0xA5)
     off = vo.offset_table(mode, 0, 1)
+    if mode == vo.MODE_VQ125:   # bit addresses -> bytes
+        off = off >> 3
     allowed = off.reshape(-1) if mode != vo.MODE_VQ15 else (off[..., None] + np.arange(3)).reshape(-1)
     assert set(changed.tolist()) <= set(allowed.tolist())
 
 
-@pytest.mark.parametrize("mode", [0, 2, 3])
+@pytest.mark.parametrize("mode", [0, 2, 3, 4])
 def test_encode_then_decode_matches_oracle_pipeline(mode):
     """GPU encode + GPU decode against oracle encode + oracle decode."""
     w = synth.WORKLOADS[1].with_mode(mode).scaled(seq_len=3000, cap_len=3008)

@@ -59,6 +59,8 @@ CASES = [
     (2, 2, 8, 2, 3, [517, 2], 768, 5),        # 4 bit, two column groups
     (3, 1, 8, 2, 2, [1000], 1024, 0),         # 3 bit, 2 queries fill the 8 columns
     (3, 2, 8, 2, 3, [517, 2], 768, 5),        # 3 bit, two column groups
+    (4, 1, 8, 2, 2, [1000], 1024, 0),         # 1.25 bit, 2 queries fill the 8 columns
+    (4, 2, 8, 2, 3, [517, 2], 768, 5),        # 1.25 bit, two column groups
 ]
 
 
@@ -77,7 +79,7 @@ def test_multi_query_against_oracle(mode, B, Hq, Hkv, M, lens, cap, num_splits):
                 assert np.all(o[b, m] == 0)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_one_query_equals_single_query_decode(mode):
     q, kc, vc, s, kcb, vcb = _case(mode, 2, 8, 2, 1, [700, 129], 768, seed=31 + mode)
     o = _gpu_multi(mode, q, kc, vc, s, kcb, vcb, [700, 129], 768)

@@ -43,6 +43,7 @@ def _gather(pool, table, mode, block_tokens, cap):
     (1, 1, 4, 1, [1024], 1024, 64, 3),
     (2, 2, 8, 2, [1000, 300], 1024, 64, 5),   # 4 bit: a 32-token step spans two 64-token blocks
     (3, 2, 8, 2, [1000, 300], 1024, 64, 5),   # 3 bit: a 48-token step spans two 64-token blocks
+    (4, 2, 8, 2, [1000, 300], 1024, 64, 5),   # 1.25 bit, the same
 ])
 def test_paged_equals_contiguous_and_oracle(mode, B, Hq, Hkv, lens, cap, block_tokens, num_splits):
     t = H.torch()
@@ -84,7 +85,7 @@ def test_paged_equals_contiguous_and_oracle(mode, B, Hq, Hkv, lens, cap, block_t
     assert vo.o_error(o, vo.decode_attention(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_block_ids_outside_the_pool_are_reported(mode):
     t = H.torch()
     s, kcb, vcb = H.random_codebooks(mode, 1, 4)
@@ -113,7 +114,7 @@ def test_block_ids_outside_the_pool_are_reported(mode):
     assert np.isfinite(out.cpu().numpy()).all()
 
 
-@pytest.mark.parametrize("mode,block_tokens", [(0, 64), (0, 256), (1, 64), (3, 64)])
+@pytest.mark.parametrize("mode,block_tokens", [(0, 64), (0, 256), (1, 64), (3, 64), (4, 64)])
 def test_table_entries_past_the_sequence_are_not_read(mode, block_tokens):
     """Serving engines leave the entries after a sequence's last block
     unset: they must not be read (no error bit), and O must equal the

@@ -8,6 +8,7 @@ C ABI in ``include/vqkv.h``); this package only marshals arguments to it
 from ._lib import (  # noqa: F401
     VQKV_MODE_VQ2,
     VQKV_MODE_VQ15,
+    VQKV_MODE_VQ125,
     VQKV_MODE_VQ3,
     VQKV_MODE_VQ4,
     VQKV_ROLE_K,

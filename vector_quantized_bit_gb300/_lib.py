@@ -16,6 +16,7 @@ VQKV_MODE_VQ2 = 0
 VQKV_MODE_VQ15 = 1
 VQKV_MODE_VQ4 = 2
 VQKV_MODE_VQ3 = 3
+VQKV_MODE_VQ125 = 4
 VQKV_ROLE_K = 0
 VQKV_ROLE_V = 1
 VQKV_DEVERR_SEQ_LEN = 0x1

@@ -49,7 +49,8 @@ vqkv_status device_info(DeviceInfo* out) {
 }
 
 bool is_code_mode(int m) {
-  return m == VQKV_MODE_VQ2 || m == VQKV_MODE_VQ15 || m == VQKV_MODE_VQ4 || m == VQKV_MODE_VQ3;
+  return m == VQKV_MODE_VQ2 || m == VQKV_MODE_VQ15 || m == VQKV_MODE_VQ4 || m == VQKV_MODE_VQ3 ||
+         m == VQKV_MODE_VQ125;
 }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -253,6 +254,7 @@ size_t vqkv_code_bytes(int32_t mode, int32_t cap_len) {
   if (mode == VQKV_MODE_VQ15) return (size_t)((cap_len + 63) / 64) * 1536;
   if (mode == VQKV_MODE_VQ4) return (size_t)((cap_len + 15) / 16) * 1024;
   if (mode == VQKV_MODE_VQ3) return (size_t)((cap_len + 15) / 16) * 768;
+  if (mode == VQKV_MODE_VQ125) return (size_t)((cap_len + 15) / 16) * 320;
   return 0;
 }
 

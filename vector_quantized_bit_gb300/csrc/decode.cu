@@ -60,33 +60,36 @@ constexpr int V2_WARPS = VQKV_V2_WARPS;             // one CTA per SM
 constexpr int V2_TPI = VQKV_V2_TPI;                 // 16-token tiles per step (a "super-tile")
 constexpr int V2_THREADS = V2_WARPS * 32;
 constexpr int V2_TILE = 16;
-constexpr int V2_CB_BYTES = 256 * 256;              // [code][K replicas (128 B) | V replicas (128 B)]
 // q' rows (fp32, 128 channels) at a pitch that keeps the 8 lanes of each
 // quarter-warp on distinct 16-byte bank groups when the MMA fragments are
 // read (lane (gid, tig) reads 4 floats at gid * pitch + 4 tig + 16 s).
 constexpr int V2_Q_PITCH = 144;
-constexpr int V2_Q_OFF = V2_CB_BYTES;               // q' (fp32 [8][V2_Q_PITCH]) after the codebooks
 constexpr int V2_STAGES = VQKV_V2_STAGES;           // per-warp ring of super-tiles (K then V)
-constexpr int V2_RING_OFF = V2_Q_OFF + 8 * V2_Q_PITCH * 4;
 
 // Geometry of the tile-ring decode, per code mode: 2 bit (256 x 4, one byte
-// per code), 4 bit (256 x 2, one byte per code) and 3 bit (4096 x 4, 12-bit
-// codes in 3-byte pairs).  All keep the 64-KB codebook and q' prefix: the
-// 256-entry codebooks replicated across banks, the 4096-entry ones once.  A
-// lane's code words of a tile: 2 bit one 16-byte word; 4 bit two 16-byte
-// words in planes 512 bytes apart; 3 bit a 16-byte and an 8-byte word
-// (planes at 0 and 512).
+// per code), 4 bit (256 x 2, one byte per code), 3 bit (4096 x 4, 12-bit
+// codes in 3-byte pairs) and 1.25 bit (1024 x 8, 10-bit codes).  Shared
+// memory starts with the codebooks (64 KB: the 256-entry ones replicated
+// across banks, the 4096-entry ones once; 128 KB: the 1024-entry ones in
+// four interleaved copies), then q'.  A lane's code words of a tile: 2 bit
+// one 16-byte word; 4 bit two 16-byte words in planes 512 bytes apart; 3 bit
+// a 16-byte and an 8-byte word (planes at 0 and 512); 1.25 bit: K an 8-byte
+// and a 2-byte word, V a 16-byte and a 4-byte word (planes at 0 and 256).
 template <int MODE>
 struct V2Geo {
-  static constexpr int DSUB = MODE == VQKV_MODE_VQ4 ? 2 : 4;
   static constexpr bool PAIRS = MODE == VQKV_MODE_VQ3;          // 12-bit codes in 3-byte pairs
-  static constexpr int TILE_BYTES = PAIRS ? 768 : 16 * (kHeadDim / DSUB);
-  static constexpr int LW = TILE_BYTES / 32 / 4;                  // a lane's 32-bit code words per tile and role
+  static constexpr bool TEN = MODE == VQKV_MODE_VQ125;          // 10-bit codes in bit runs
+  static constexpr int DSUB = MODE == VQKV_MODE_VQ4 ? 2 : TEN ? 8 : 4;
+  static constexpr int TILE_BYTES = PAIRS ? 768 : TEN ? 320 : 16 * (kHeadDim / DSUB);
+  static constexpr int LW = TILE_BYTES / 32 / 4;                  // byte and pair codes: a lane's 32-bit words
+  static constexpr int KW = TEN ? 3 : LW, VW = TEN ? 5 : LW;      // words a lane reads per tile, K and V
   static constexpr int TPI = MODE == VQKV_MODE_VQ4 ? 2 : V2_TPI;  // tiles per step
   static constexpr int STAGE_BYTES = 2 * TPI * TILE_BYTES;
-  static constexpr int RING_OFF = V2_RING_OFF;
+  static constexpr int CB_BYTES = TEN ? 2 * 65536 : 65536;
+  static constexpr int Q_OFF = CB_BYTES;                          // q' (fp32 [8][V2_Q_PITCH])
+  static constexpr int RING_OFF = Q_OFF + 8 * V2_Q_PITCH * 4;
   static constexpr int MBAR_OFF = RING_OFF + V2_WARPS * V2_STAGES * STAGE_BYTES;
-  static constexpr int REPL = PAIRS ? 1 : 128 / (2 * DSUB);     // replicas of a 256-entry codebook's centroid
+  static constexpr int REPL = PAIRS ? 1 : TEN ? 4 : 128 / (2 * DSUB);   // codebook copies (byte codes use it)
 };
 
 // ------------------------------------------------------------------ VQ15
@@ -118,7 +121,9 @@ struct V2Smem {
 constexpr size_t kV2Smem = V2Smem<VQKV_MODE_VQ2>::BYTES;
 constexpr size_t kV4Smem = V2Smem<VQKV_MODE_VQ4>::BYTES;
 constexpr size_t kV3Smem = V2Smem<VQKV_MODE_VQ3>::BYTES;
-static_assert(kV4Smem <= 227 * 1024 && kV3Smem <= 227 * 1024, "4-bit / 3-bit decode shared memory");
+constexpr size_t kV125Smem = V2Smem<VQKV_MODE_VQ125>::BYTES;
+static_assert(kV4Smem <= 227 * 1024 && kV3Smem <= 227 * 1024 && kV125Smem <= 227 * 1024,
+              "4-bit / 3-bit / 1.25-bit decode shared memory");
 static_assert(CombineSmem<V2_WARPS>::kBytes <= V2Geo<VQKV_MODE_VQ2>::MBAR_OFF,
               "combine area must fit below the ring barriers");
 // The combine area (after the tile loop) and q' (before it) overlap the
@@ -208,8 +213,8 @@ __device__ __forceinline__ uint32_t pair_at(const uint32_t (&w)[LW], int b) {
 // this lane's O^T fragments.
 template <int T, int MODE>
 __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
-                                         const uint32_t (&qa)[8][2], const uint32_t (&kw)[T][V2Geo<MODE>::LW],
-                                         const uint32_t (&vw)[T][V2Geo<MODE>::LW], int tile0,
+                                         const uint32_t (&qa)[8][2], const uint32_t (&kw)[T][V2Geo<MODE>::KW],
+                                         const uint32_t (&vw)[T][V2Geo<MODE>::VW], int tile0,
                                          const ColumnLimits& cl, int lane, float& m0, float& m1, float& l0, float& l1,
                                          float (&acc)[8][4]) {
   const int gid = lane >> 2;
@@ -306,6 +311,79 @@ __device__ __forceinline__ void vq2_step(const unsigned char* s_cb, uint32_t kby
   }
 }
 
+// 10-bit code at bit b of a lane's run words (b is a constant after
+// unrolling, so the word indices are too).
+template <int N>
+__device__ __forceinline__ uint32_t bits10(const uint32_t (&w)[N], int b) {
+  const int i = b >> 5, sh = b & 31;
+  return (i + 1 < N ? __funnelshift_r(w[i], w[i + 1], sh) : w[i] >> sh) & 0x3ffu;
+}
+
+// Byte offset of centroid c in copy `rep` of a 1024-entry codebook whose four
+// copies are interleaved in 128-byte rows: copy r holds its even / odd
+// entries in 16-byte bank groups 2r / 2r+1.
+__device__ __forceinline__ uint32_t cb10_offset(uint32_t c) { return ((c >> 1) << 7) | ((c & 1u) << 4); }
+
+// One step of the 1.25-bit decode over T consecutive 16-token tiles.
+// Scores: a 16-byte gather is channels 8j..8j+7 of subvector j = 4 s2 + tig
+// (s2 = 0..3) for token gid (X) and gid+8 (Y), the A operand of two MMAs
+// (qa[2 s2], qa[2 s2 + 1]); kw: the lane's 80-bit K run, token gid's 4 codes
+// at bits 10 s2, token gid+8's at 40 + 10 s2.  P.V: subvector 8 pp + gid of
+// the four tokens (2tig, 2tig+1, 2tig+8, 2tig+9) = slots 0..3 of the V run,
+// code at bit 40 slot + 20 pp once the run is shifted right by vshift
+// (10 bits for odd gid); each gather feeds four M-tiles (channel pairs).
+// kbyte / vbyte: this lane's codebook copy (tig) in the K / V table.
+template <int T>
+__device__ __forceinline__ void vq125_step(const unsigned char* s_cb, uint32_t kbyte, uint32_t vbyte,
+                                           const uint32_t (&qa)[8][2], const uint32_t (&kw)[T][3],
+                                           const uint32_t (&vw)[T][5], uint32_t vshift, int tile0,
+                                           const ColumnLimits& cl, int lane, float& m0, float& m1, float& l0,
+                                           float& l1, float (&acc)[8][4]) {
+  const int gid = lane >> 2;
+  float sc[T][4];
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+      const uint4 X = lds_at<uint4>(s_cb, kbyte + cb10_offset(bits10(kw[i], 10 * s2)));
+      const uint4 Y = lds_at<uint4>(s_cb, kbyte + cb10_offset(bits10(kw[i], 40 + 10 * s2)));
+      mma_16816(da, X.x, Y.x, X.y, Y.y, qa[2 * s2][0], qa[2 * s2][1]);
+      mma_16816(db, X.z, Y.z, X.w, Y.w, qa[2 * s2 + 1][0], qa[2 * s2 + 1][1]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[i][e] = da[e] + db[e];
+  }
+  if ((tile0 + T) * V2_TILE > cl.lim_min) {   // tail of the sequence
+#pragma unroll
+    for (int i = 0; i < T; ++i) mask_scores(sc[i], (tile0 + i) * V2_TILE + gid, cl);
+  }
+  uint32_t bP[T][2];
+  softmax_tiles<T, 8>(sc, m0, m1, l0, l1, acc, bP);
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    uint32_t v[5];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) v[m] = __funnelshift_r(vw[i][m], vw[i][m + 1], vshift);
+    v[4] = vw[i][4] >> vshift;
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+      const uint4 R0 = lds_at<uint4>(s_cb, vbyte + cb10_offset(bits10(v, 20 * pp)));
+      const uint4 R1 = lds_at<uint4>(s_cb, vbyte + cb10_offset(bits10(v, 40 + 20 * pp)));
+      const uint4 R2 = lds_at<uint4>(s_cb, vbyte + cb10_offset(bits10(v, 80 + 20 * pp)));
+      const uint4 R3 = lds_at<uint4>(s_cb, vbyte + cb10_offset(bits10(v, 120 + 20 * pp)));
+      mma_16816(acc[4 * pp + 0], __byte_perm(R0.x, R1.x, 0x5410), __byte_perm(R0.x, R1.x, 0x7632),
+                __byte_perm(R2.x, R3.x, 0x5410), __byte_perm(R2.x, R3.x, 0x7632), bP[i][0], bP[i][1]);
+      mma_16816(acc[4 * pp + 1], __byte_perm(R0.y, R1.y, 0x5410), __byte_perm(R0.y, R1.y, 0x7632),
+                __byte_perm(R2.y, R3.y, 0x5410), __byte_perm(R2.y, R3.y, 0x7632), bP[i][0], bP[i][1]);
+      mma_16816(acc[4 * pp + 2], __byte_perm(R0.z, R1.z, 0x5410), __byte_perm(R0.z, R1.z, 0x7632),
+                __byte_perm(R2.z, R3.z, 0x5410), __byte_perm(R2.z, R3.z, 0x7632), bP[i][0], bP[i][1]);
+      mma_16816(acc[4 * pp + 3], __byte_perm(R0.w, R1.w, 0x5410), __byte_perm(R0.w, R1.w, 0x7632),
+                __byte_perm(R2.w, R3.w, 0x5410), __byte_perm(R2.w, R3.w, 0x7632), bP[i][0], bP[i][1]);
+    }
+  }
+}
+
 // Merged search state of this lane's subvector over the 8 warps of its role
 // (valid in the role's first warp).
 __device__ __forceinline__ Best merge_role_slices(Best part, int warp, int lane, int slice, Best* s_part) {
@@ -381,16 +459,19 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
   using G = V2Geo<MODE>;
   using Sm = V2Smem<MODE>;
-  using Dim = typename std::conditional<MODE == VQKV_MODE_VQ4, Vq4Dim, Vq2Dim>::type;
-  constexpr bool APPEND = !G::PAIRS;   // the fused append encodes one-byte codes only
+  using Dim = typename std::conditional<MODE == VQKV_MODE_VQ4, Vq4Dim,
+                                        typename std::conditional<G::TEN, Vq15Dim, Vq2Dim>::type>::type;
+  constexpr bool APPEND = !G::PAIRS && !G::TEN;   // the fused append encodes one-byte codes only
   extern __shared__ __align__(128) unsigned char smem[];
   // Codebooks.  256 entries: centroid c at row c (256 bytes), K replicas at
   // c*256 + r*2*DSUB, V replicas at c*256 + 128 + r*2*DSUB; 2 bit: lane l
   // reads replica l % 16 (8 bytes), so each half-warp phase of a 64-bit
   // gather hits 16 bank pairs; 4 bit: lane l reads replica l (4 bytes), one
   // bank per lane.  4096 entries (3 bit): K centroid c at 8c, V at 32768 + 8c.
+  // 1024 entries (1.25 bit): K copy r of centroid c at cb10_offset(c) + 32 r,
+  // V at 65536 + the same; lane (gid, tig) reads copy tig.
   const unsigned char* s_cb = smem;
-  float* s_qp = reinterpret_cast<float*>(smem + V2_Q_OFF);
+  float* s_qp = reinterpret_cast<float*>(smem + G::Q_OFF);
   float* s_comb = reinterpret_cast<float*>(smem);   // after the tile loop only
   __shared__ int s_last;
 
@@ -401,8 +482,11 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   const int b_end = min(b_begin + p.bpg, p.B);
   // this CTA's softmax columns
   const int col0 = GROUPS ? cta_col0(p) : 0, nloc = GROUPS ? min(8, p.ncols - col0) : p.ncols;
-  const uint32_t kbyte = G::PAIRS ? 0u : G::DSUB == 4 ? (uint32_t)(lane & 15) << 3 : (uint32_t)lane << 2;
-  const uint32_t vbyte = G::PAIRS ? 32768u : 128u | kbyte;
+  const uint32_t kbyte = G::PAIRS ? 0u
+                        : G::TEN   ? (uint32_t)tig << 5
+                        : G::DSUB == 4 ? (uint32_t)(lane & 15) << 3
+                                       : (uint32_t)lane << 2;
+  const uint32_t vbyte = G::PAIRS ? 32768u : G::TEN ? 65536u + kbyte : 128u | kbyte;
   // this warp's ring: stage st holds the K super-tile, then the V super-tile
   const uint32_t ring = smem_u32(smem + G::RING_OFF) + warp * (V2_STAGES * G::STAGE_BYTES);
   const uint32_t mbar = smem_u32(smem + G::MBAR_OFF) + warp * (V2_STAGES * 8);
@@ -421,10 +505,18 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     // used (the sequence length decides the rest): this warp's codebook
     // entry, its query column, and the new K / V row of a fused append.
     // (4096 entries: eight 16-byte pieces of the two 32-KB codebooks per thread)
-    using CbEntry = typename std::conditional<G::PAIRS, uint4[8],
-                                              typename std::conditional<G::DSUB == 4, uint2, uint32_t>::type>::type;
+    // (1024 entries: four 16-byte centroids of the two codebooks per thread)
+    using CbEntry = typename std::conditional<
+        G::PAIRS, uint4[8],
+        typename std::conditional<G::TEN, uint4[4],
+                                  typename std::conditional<G::DSUB == 4, uint2, uint32_t>::type>::type>::type;
     CbEntry cb_entry;
-    if constexpr (G::PAIRS) {
+    if constexpr (G::TEN) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        cb_entry[i] = __ldg(reinterpret_cast<const uint4*>(i < 2 ? p.kcb : p.vcb) + (size_t)kvh * 1024 +
+                            (i & 1) * V2_THREADS + threadIdx.x);
+    } else if constexpr (G::PAIRS) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         cb_entry[i] = __ldg(reinterpret_cast<const uint4*>(i < 4 ? p.kcb : p.vcb) + (size_t)kvh * 2048 +
@@ -535,7 +627,18 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         transform_loaded(xraw, warp < 8, xs, lane, x);
         xnew = make_float4(x[0], x[1], x[2], x[3]);
       }
-      if constexpr (G::PAIRS) {
+      if constexpr (G::TEN) {
+        // the four copies of each centroid; copy (k + c/2) % 4 at step k keeps
+        // the 8 lanes of each store phase on distinct 16-byte bank groups
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t c = (uint32_t)((i & 1) * V2_THREADS + threadIdx.x);
+          unsigned char* row = smem + (i >> 1) * 65536 + cb10_offset(c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(row + 32 * ((k + (c >> 1)) & 3)) = cb_entry[i];
+        }
+      } else if constexpr (G::PAIRS) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) reinterpret_cast<uint4*>(smem)[i * V2_THREADS + threadIdx.x] = cb_entry[i];
       } else {
@@ -558,13 +661,19 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           for (int j = 0; j < min(V2_STAGES - 1, n_mine); ++j)
             if (!(p.withhold_first_copy && j == 0)) issue(j);
       }
-      // B operand of the score MMA: head gid; 2 bit: channels 4j..4j+3 of
-      // j = 4s+tig; 4 bit: channels 16s+2tig, +1 and 16s+8+2tig, +1
+      // B operand of the score MMA: head gid; 2 and 3 bit: channels
+      // 4j..4j+3 of j = 4s+tig; 4 bit: channels 16s+2tig, +1 and
+      // 16s+8+2tig, +1; 1.25 bit: channels 8j + 4(s%2) .. +3 of j = 4(s/2)+tig
       uint32_t qa[8][2];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         if (gid < nloc) {
-          if constexpr (G::DSUB == 4) {
+          if constexpr (G::TEN) {
+            const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH +
+                                                              8 * (4 * (s >> 1) + tig) + 4 * (s & 1));
+            qa[s][0] = pack_half2(v.x, v.y);
+            qa[s][1] = pack_half2(v.z, v.w);
+          } else if constexpr (G::DSUB == 4) {
             const float4 v = *reinterpret_cast<const float4*>(s_qp + gid * V2_Q_PITCH + 4 * (4 * s + tig));
             qa[s][0] = pack_half2(v.x, v.y);
             qa[s][1] = pack_half2(v.z, v.w);
@@ -587,29 +696,42 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           break;
         }
         // the lane's code words: plane w (every lane's 16- or 8-byte piece
-        // of it, contiguous) at 512 w
-        uint32_t kq[G::TPI][G::LW], vq[G::TPI][G::LW];
+        // of it, contiguous) at 512 w; 1.25 bit: planes at 0 and 256, V run
+        // 4 (gid / 2) + tig shared by the lanes gid and gid ^ 1
+        uint32_t kq[G::TPI][G::KW], vq[G::TPI][G::VW];
 #pragma unroll
         for (int i = 0; i < G::TPI; ++i) {
           const uint32_t kt = ring + st * G::STAGE_BYTES + i * G::TILE_BYTES;
           const uint32_t vt = kt + G::TPI * G::TILE_BYTES;
+          if constexpr (G::TEN) {
+            const uint2 a = lds64(kt + 8 * lane);
+            kq[i][0] = a.x, kq[i][1] = a.y, kq[i][2] = lds16(kt + 256 + 2 * lane);
+            const uint32_t run = 4 * (gid >> 1) + tig;
+            const uint4 c = lds128(vt + 16 * run);
+            vq[i][0] = c.x, vq[i][1] = c.y, vq[i][2] = c.z, vq[i][3] = c.w, vq[i][4] = lds32(vt + 256 + 4 * run);
+          } else {
 #pragma unroll
-          for (int w = 0; w < G::LW / 4; ++w) {
-            const uint4 a = lds128(kt + 512 * w + lane * 16), c = lds128(vt + 512 * w + lane * 16);
-            kq[i][4 * w] = a.x, kq[i][4 * w + 1] = a.y, kq[i][4 * w + 2] = a.z, kq[i][4 * w + 3] = a.w;
-            vq[i][4 * w] = c.x, vq[i][4 * w + 1] = c.y, vq[i][4 * w + 2] = c.z, vq[i][4 * w + 3] = c.w;
-          }
-          if constexpr (G::LW % 4 != 0) {
-            const uint2 a = lds64(kt + 512 + lane * 8), c = lds64(vt + 512 + lane * 8);
-            kq[i][G::LW - 2] = a.x, kq[i][G::LW - 1] = a.y;
-            vq[i][G::LW - 2] = c.x, vq[i][G::LW - 1] = c.y;
+            for (int w = 0; w < G::LW / 4; ++w) {
+              const uint4 a = lds128(kt + 512 * w + lane * 16), c = lds128(vt + 512 * w + lane * 16);
+              kq[i][4 * w] = a.x, kq[i][4 * w + 1] = a.y, kq[i][4 * w + 2] = a.z, kq[i][4 * w + 3] = a.w;
+              vq[i][4 * w] = c.x, vq[i][4 * w + 1] = c.y, vq[i][4 * w + 2] = c.z, vq[i][4 * w + 3] = c.w;
+            }
+            if constexpr (G::LW % 4 != 0) {
+              const uint2 a = lds64(kt + 512 + lane * 8), c = lds64(vt + 512 + lane * 8);
+              kq[i][G::LW - 2] = a.x, kq[i][G::LW - 1] = a.y;
+              vq[i][G::LW - 2] = c.x, vq[i][G::LW - 1] = c.y;
+            }
           }
         }
         __syncwarp();
         // refill the stage this warp finished with in the previous step
         if (lane == 0 && j + V2_STAGES - 1 < n_mine) issue(j + V2_STAGES - 1);
-        vq2_step<G::TPI, MODE>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
-                               lane, m0, m1, l0, l1, acc);
+        if constexpr (G::TEN)
+          vq125_step<G::TPI>(s_cb, kbyte, vbyte, qa, kq, vq, 10u * (gid & 1), t_begin + (warp + j * V2_WARPS) * G::TPI,
+                             cl, lane, m0, m1, l0, l1, acc);
+        else
+          vq2_step<G::TPI, MODE>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
+                                 lane, m0, m1, l0, l1, acc);
       }
       if (timed_out) {
         // give the copies already issued a bounded chance to land before the
@@ -812,10 +934,15 @@ int decode_tiles_per_step(int mode) {
   return mode == VQKV_MODE_VQ2   ? V2Geo<VQKV_MODE_VQ2>::TPI
          : mode == VQKV_MODE_VQ4 ? V2Geo<VQKV_MODE_VQ4>::TPI
          : mode == VQKV_MODE_VQ3 ? V2Geo<VQKV_MODE_VQ3>::TPI
+         : mode == VQKV_MODE_VQ125 ? V2Geo<VQKV_MODE_VQ125>::TPI
                                  : 1;
 }
 size_t decode_smem_bytes(int mode) {
-  return mode == VQKV_MODE_VQ2 ? kV2Smem : mode == VQKV_MODE_VQ4 ? kV4Smem : mode == VQKV_MODE_VQ3 ? kV3Smem : kV15Smem;
+  return mode == VQKV_MODE_VQ2     ? kV2Smem
+         : mode == VQKV_MODE_VQ4   ? kV4Smem
+         : mode == VQKV_MODE_VQ3   ? kV3Smem
+         : mode == VQKV_MODE_VQ125 ? kV125Smem
+                                   : kV15Smem;
 }
 int decode_threads(int mode) { return mode == VQKV_MODE_VQ15 ? V15_THREADS : V2_THREADS; }
 
@@ -843,6 +970,7 @@ const DecodeKernel (*kernels_of(int mode))[3] {
   return mode == VQKV_MODE_VQ2   ? ByteCodeKernels<VQKV_MODE_VQ2>::k
          : mode == VQKV_MODE_VQ4 ? ByteCodeKernels<VQKV_MODE_VQ4>::k
          : mode == VQKV_MODE_VQ3 ? ByteCodeKernels<VQKV_MODE_VQ3>::k
+         : mode == VQKV_MODE_VQ125 ? ByteCodeKernels<VQKV_MODE_VQ125>::k
                                  : Vq15Kernels::k;
 }
 }  // namespace

@@ -3,8 +3,8 @@
 // a Hadamard rotation of the keys, K-Means codebook; arXiv summary page,
 // "方法详解", stages 1-2).
 //
-// 2-, 3- and 4-bit: one warp per row (or one CTA per row when rows are few);
-// lane l holds channels 4l..4l+3.  1.5-bit: tensor-core screening with an exact
+// 1.25-, 2-, 3- and 4-bit: one warp per row (or one CTA per row when rows
+// are few); lane l holds channels 4l..4l+3.  1.5-bit: tensor-core screening with an exact
 // re-rank (below).  For keys the transform
 // x' = (x / s) . H / sqrt(128) is carried in double-float arithmetic (pairs
 // of fp32 with error-free sums and products) and rounded to fp32 once, so the
@@ -200,6 +200,111 @@ __global__ void __launch_bounds__(SPLIT == 1 ? ENC_THREADS : SPLIT * 32) encode_
         tb[vq3_byte_offset(p.role, t & 15, lane, 0)] = (uint8_t)(bst.i & 0xff);
         tb[vq3_byte_offset(p.role, t & 15, lane, 1)] = (uint8_t)(((bst.i >> 8) & 0xf) | ((hi & 0xf) << 4));
         tb[vq3_byte_offset(p.role, t & 15, lane, 2)] = (uint8_t)(hi >> 4);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ VQ125
+// 1024-entry codebooks of 8-channel subvectors, 10-bit codes.  Lane l
+// searches subvector l % 16 (channels 8j..8j+7, taken from lanes 2j and
+// 2j+1) over half l / 16 of its warp's candidates (the whole codebook for
+// SPLIT = 1, 1024 / SPLIT per warp otherwise); the halves merge across
+// lanes l and l + 16.  Lanes 0..3 then pack the row's four 40-bit groups
+// (K: subvectors g, g+4, g+8, g+12; V: 2g, 2g+1, 2g+8, 2g+9) and write 5
+// bytes each.
+
+// Search of one 8-channel subvector over candidates [c_lo, c_hi) (a multiple
+// of 4): fp32 direct differences in channel order, four chains over the
+// candidates of each residue mod 4, merged by distance, then index.
+// s_cb: centroid c as two float4 at 2c (channels 0..3) and 2c+1 (4..7).
+__device__ __forceinline__ Best vq125_search(const float (&x)[8], int c_lo, int c_hi, const float4* s_cb) {
+  Best ch[4] = {best_init(), best_init(), best_init(), best_init()};
+#pragma unroll 2
+  for (int c = c_lo; c < c_hi; c += 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 a = s_cb[2 * (c + k)], b = s_cb[2 * (c + k) + 1];
+      float u = __fsub_rn(x[0], a.x), d = __fmul_rn(u, u);
+      u = __fsub_rn(x[1], a.y); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[2], a.z); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[3], a.w); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[4], b.x); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[5], b.y); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[6], b.z); d = __fmaf_rn(u, u, d);
+      u = __fsub_rn(x[7], b.w); d = __fmaf_rn(u, u, d);
+      best_push(ch[k], d, c + k);
+    }
+  }
+  return best_merge(best_merge(ch[0], ch[1]), best_merge(ch[2], ch[3]));
+}
+
+template <int SPLIT>
+__global__ void __launch_bounds__(ENC_THREADS) encode_vq125_kernel(const EncodeParams p) {
+  __shared__ float4 s_cb[2 * 1024];
+  __shared__ Best s_part[SPLIT > 1 ? ENC_WARPS * 32 : 1];
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kSpan = 1024 / SPLIT;   // candidates of one warp
+  const int c_lo = (SPLIT == 1 ? 0 : warp * kSpan) + (lane >> 4) * (kSpan / 2);
+  const int c_hi = c_lo + kSpan / 2;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  {
+    // every codebook load in flight before the first store
+    constexpr int kPer = 1024 / ENC_THREADS;
+    const uint4* g = reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 1024 + threadIdx.x;
+    uint4 raw[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) raw[i] = __ldg(g + i * ENC_THREADS);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int c = threadIdx.x + i * ENC_THREADS;
+      const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
+      s_cb[2 * c] = make_float4(__low2float(h[0]), __high2float(h[0]), __low2float(h[1]), __high2float(h[1]));
+      s_cb[2 * c + 1] = make_float4(__low2float(h[2]), __high2float(h[2]), __low2float(h[3]), __high2float(h[3]));
+    }
+  }
+  __syncthreads();
+  const bool key = p.role == VQKV_ROLE_K;
+  const int rows = p.B * p.n_rows;
+  const int r0 = (SPLIT == 1) ? blockIdx.x * ENC_WARPS + warp : blockIdx.x;
+  const int rstep = (SPLIT == 1) ? gridDim.x * ENC_WARPS : gridDim.x;
+  for (int r = r0; r < rows; r += rstep) {
+    const int b = r / p.n_rows, n = r - b * p.n_rows;
+    const int t = p.pos[b] + n;
+    if (t < 0 || t >= p.cap_len) {
+      if (lane == 0 && (SPLIT == 1 || warp == 0) && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
+      continue;
+    }
+    float x[4];
+    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
+    const int j = lane & 15;
+    float xs[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      xs[k] = __shfl_sync(0xffffffffu, x[k], 2 * j);
+      xs[4 + k] = __shfl_sync(0xffffffffu, x[k], 2 * j + 1);
+    }
+    Best part = vq125_search(xs, c_lo, c_hi, s_cb);
+    part = best_merge(part, best_shfl_xor(part, 16));
+    const Best bst = merge_warps<SPLIT>(part, warp, lane, s_part);
+    if (SPLIT == 1 || warp == 0) {
+      count_near_ties(p.near_tie, is_near_tie(bst.d, bst.s), lane, 0xffffu);
+      const int g = lane & 3;
+      const uint32_t c0 = __shfl_sync(0xffffffffu, bst.i, key ? g : 2 * g);
+      const uint32_t c1 = __shfl_sync(0xffffffffu, bst.i, key ? g + 4 : 2 * g + 1);
+      const uint32_t c2 = __shfl_sync(0xffffffffu, bst.i, key ? g + 8 : 2 * g + 8);
+      const uint32_t c3 = __shfl_sync(0xffffffffu, bst.i, key ? g + 12 : 2 * g + 9);
+      const unsigned long long grp =
+          (unsigned long long)(c0 | (c1 << 10) | (c2 << 20)) | ((unsigned long long)c3 << 30);
+      uint8_t* tb = tile_base(p, b, kvh, t, 16, 320);
+      if (tb && lane < 4) {
+        const int rr = t & 15;
+        const int run = key ? 4 * (rr & 7) + g : 4 * g + ((rr & 7) >> 1);
+        const int n0 = key ? 5 * (rr >> 3) : 5 * (2 * (rr >> 3) + (rr & 1));
+#pragma unroll
+        for (int q = 0; q < 5; ++q) tb[vq125_run_byte(p.role, run, n0 + q)] = (uint8_t)(grp >> (8 * q));
       }
     }
   }
@@ -607,6 +712,8 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ3)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq3_kernel<1>, ENC_THREADS,
                                                          kEnc3Smem);
+  if (mode == VQKV_MODE_VQ125)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq125_kernel<1>, ENC_THREADS, 0);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_tc_kernel, TC_THREADS, kTcSmem);
 }
 
@@ -620,6 +727,10 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
   if (mode == VQKV_MODE_VQ4) {
     if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
     return launch_pdl(encode_vq2_kernel<1, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
+  }
+  if (mode == VQKV_MODE_VQ125) {
+    if (split_rows) return launch_pdl(encode_vq125_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_vq125_kernel<1>, grid, dim3(ENC_THREADS), 0, stream, p);
   }
   if (mode == VQKV_MODE_VQ3) {
     if (split_rows)

@@ -253,6 +253,14 @@ __device__ __forceinline__ long long vq3_byte_offset(int role, int t, int pair, 
   return 768LL * tile + (n < 16 ? 16 * lane + n : 512 + 8 * lane + n - 16);
 }
 
+// Byte offset within a 1.25-bit tile of byte n of K run L (10 bytes: 8 in
+// plane 0, 2 in plane 1) or V run R (20 bytes: 16 + 4) (the layout of
+// include/vqkv.h).
+__device__ __forceinline__ int vq125_run_byte(int role, int run, int n) {
+  return (role == VQKV_ROLE_K) ? (n < 8 ? 8 * run + n : 256 + 2 * run + n - 8)
+                               : (n < 16 ? 16 * run + n : 256 + 4 * run + n - 16);
+}
+
 // Writes codes lo (subvector pair) and hi (pair + 8) as 3 bytes.
 __device__ __forceinline__ void store_pair(uint8_t* dst, int lo, int hi) {
   dst[0] = (uint8_t)(lo & 0xff);

@@ -82,7 +82,7 @@ cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
 
 // fp16-KV comparison kernel (decode_fp16.cu); DecodeParams.kc / .vc point to
 // the fp16 K / V caches, stream_bytes = cap_len * 256.
-constexpr int kCodeModes = 4;  // VQKV_MODE_VQ2, VQKV_MODE_VQ15, VQKV_MODE_VQ4, VQKV_MODE_VQ3
+constexpr int kCodeModes = 5;  // VQKV_MODE_VQ2, VQKV_MODE_VQ15, VQKV_MODE_VQ4, VQKV_MODE_VQ3, VQKV_MODE_VQ125
 constexpr int kModeFp16 = kCodeModes;   // plan index after the code modes
 size_t decode_fp16_smem_bytes();
 int decode_fp16_threads();

@@ -32,9 +32,11 @@ MODE_VQ2 = 0
 MODE_VQ15 = 1
 MODE_VQ4 = 2
 MODE_VQ3 = 3
+MODE_VQ125 = 4
 
 # codebook geometry per mode: (entries, subvector dims)
-MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4)}
+MODE_GEOMETRY = {MODE_VQ2: (256, 4), MODE_VQ15: (4096, 8), MODE_VQ4: (256, 2), MODE_VQ3: (4096, 4),
+                 MODE_VQ125: (1024, 8)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -43,7 +45,7 @@ class Workload:
 
     config_id: int
     name: str
-    mode: int              # MODE_VQ2, MODE_VQ15, MODE_VQ4 or MODE_VQ3
+    mode: int              # MODE_VQ2, MODE_VQ15, MODE_VQ4, MODE_VQ3 or MODE_VQ125
     B: int
     Hq: int
     Hkv: int
