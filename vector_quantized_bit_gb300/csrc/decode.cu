@@ -11,10 +11,13 @@
 //   O[d][h] += sum_t V[t][d] P[t][h]              (tensor cores, V gathered
 //                                                  from the smem codebook)
 // Dequantisation happens only in registers: the cache layout puts each
-// lane's codes for its MMA fragments in one contiguous 16-byte (2-bit) or
-// 48-byte (1.5-bit) run; 2-bit codes reach shared memory through a per-warp
-// ring of TMA bulk copies, 1.5-bit codes come with 128-bit loads straight
-// into registers; centroids are gathered from shared memory.
+// lane's codes for its MMA fragments in one run (16 bytes at 2 bit, two
+// 16-byte planes at 4 bit, 16 + 8 bytes at 3 bit, 8 + 2 bytes of K and a
+// 16 + 4-byte V run shared by two lanes at 1.25 bit, 48 bytes at 1.5 bit).
+// The 2-, 3-, 4- and 1.25-bit codes reach shared memory through a per-warp
+// ring of TMA bulk copies (the tile-ring kernel, decode_vq2_kernel); the
+// 1.5-bit codes reach a per-lane shared-memory slot through cp.async;
+// centroids are gathered from shared memory.
 //
 // The per-query transform is q' = (q * s) . Hn, so q'.K'^T = q.K^T
 // (VecInfer paper summary page, "Summary": matching inverse operations on
@@ -25,15 +28,17 @@
 //
 // Fragment maps (mma.m16n8k16, lane = 4*gid + tig):
 //   score MMA  A = K' tile: rows = tokens {gid, gid+8}, k = the 4 channels of
-//              one subvector (VQ2: j = 4s+tig at k-step s; VQ15: half of
-//              subvector j = 4s'+tig at k-steps 2s', 2s'+1), so one 8/16-byte
-//              centroid load fills a0a1|a4a5 (token gid) or a2a3|a6a7;
+//              one subvector (VQ2, VQ3: j = 4s+tig at k-step s; VQ15, VQ125:
+//              half of subvector j = 4s'+tig at k-steps 2s', 2s'+1; VQ4: two
+//              2-channel subvectors), so one 8/16-byte centroid load fills
+//              a0a1|a4a5 (token gid) or a2a3|a6a7;
 //              B = q' (k = channels, n = heads, columns >= g are zero);
 //              D: tokens {gid, gid+8} x heads {2tig, 2tig+1}.
 //   P          D -> fp16 -> movmatrix.trans -> B operand of the P.V MMA
 //              (k = tokens {2tig, 2tig+1, 2tig+8, 2tig+9}, n = head gid).
-//   P.V MMA    A = V^T: rows = channels of subvector J (VQ2: J = 8p+gid over
-//              M-tiles 2p, 2p+1; VQ15: J = 8p+gid over M-tiles 4p..4p+3),
+//   P.V MMA    A = V^T: rows = channels of subvector J (VQ2, VQ3: J = 8p+gid
+//              over M-tiles 2p, 2p+1; VQ15, VQ125: J = 8p+gid over M-tiles
+//              4p..4p+3; VQ4: J = 8p+gid in M-tile p),
 //              k = the four tokens above; centroid halves are paired across
 //              tokens with byte permutes.
 #include <type_traits>
@@ -46,7 +51,7 @@
 namespace vqkv {
 namespace {
 
-// ------------------------------------------------------------------ VQ2
+// ------------------------------------------------------------------ tile ring (VQ2, VQ4, VQ3, VQ125)
 #ifndef VQKV_V2_WARPS
 #define VQKV_V2_WARPS 16
 #endif
