@@ -372,9 +372,10 @@ def pack_stream_fast(codes: np.ndarray, mode: int, role: int, cap_len: int) -> n
     off = offset_table(mode, role, codes.shape[0])
     if mode in BYTE_CODE_MODES:
         buf[off] = codes.astype(np.uint8)
-    elif mode == MODE_VQ125:
+    elif mode == MODE_VQ125:   # no two code bits share a stream bit, so summing is or-ing
         bits = ((codes.astype(np.int64)[..., None] >> np.arange(10)) & 1) << (off & 7)
-        np.bitwise_or.at(buf, off >> 3, bits.astype(np.uint8))
+        n = int(off.max() >> 3) + 1 if off.size else 0
+        buf[:n] = np.bincount((off >> 3).ravel(), weights=bits.ravel(), minlength=n).astype(np.uint8)
     elif mode == MODE_VQ3:
         lo, hi = codes[:, :16].astype(np.int64), codes[:, 16:].astype(np.int64)
         buf[off[..., 0]] = lo & 0xFF

@@ -206,6 +206,28 @@ def pack_parallel(mode, role, codes, cap):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("mode", [2, 3, 4])
+def test_full_size_other_bit_widths_sampled_heads(mode):
+    """The 196k-token Llama-shaped workload at 4, 3 and 1.25 bit, launched as
+    bench.py --mode launches it; the oracle recomputes a few heads."""
+    w = synth.WORKLOADS[1].with_mode(mode)
+    kw = {} if mode == 2 else dict(sample_tokens=2048, iters=2)
+    s, kcb, vcb = H.calibrate(w, **kw)
+    kc, vc, lens = full_size_uniform_codes(w)
+    kbuf = pack_parallel(w.mode, 0, kc, w.cap_len)
+    vbuf = pack_parallel(w.mode, 1, vc, w.cap_len)
+    q = synth.queries(w)
+    o = H.gpu_decode(w.mode, q, kbuf, vbuf, lens, kcb, vcb, s, w.cap_len, int(lens.max()))
+    assert np.isfinite(o).all()
+    r = np.random.default_rng(10 + mode)
+    heads = [(0, int(r.integers(w.Hq))) for _ in range(3)] + [(0, w.Hq - 1)]
+    ref = vo.decode_attention(q, kc, vc, kcb, vcb, s, lens, heads=heads)
+    for b, h in heads:
+        e = vo.o_error(o[b, h], ref[b, h])
+        assert e <= H.O_TOL, (b, h, e)
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("cfg", [1, 2, 3])
 def test_full_size_sampled_heads(cfg):
     """The benchmarked workloads at full size, launched exactly as bench.py
