@@ -38,6 +38,9 @@ def _case(mode, B, Hq, Hkv, lens, cap, seed):
 @pytest.mark.parametrize("mode,B,Hq,Hkv,lens,cap", [
     (0, 2, 8, 2, [900, 517], 1024),
     (1, 2, 10, 2, [300, 64], 320),
+    (2, 2, 8, 2, [900, 517], 1024),
+    (3, 2, 8, 2, [900, 517], 1024),
+    (4, 2, 8, 2, [900, 517], 1024),
 ])
 def test_static_scratch_matches_workspace_entry_on_two_calls(mode, B, Hq, Hkv, lens, cap):
     t, qs, torch = _case(mode, B, Hq, Hkv, lens, cap, seed=21 + mode)
