@@ -238,7 +238,8 @@ vqkv_status vqkv_decode_attn(const vqkv_decode_args* args, void* stream);
  * CTA that holds position L - 1 writes the new codes before it starts
  * streaming that tile, so one kernel does the whole step.  Workspace, error
  * word, alignment and failure rules are those of vqkv_decode_attn.  2-bit and
- * 4-bit modes (VQKV_ERR_UNSUPPORTED for 1.5 bit).
+ * 4-bit modes (VQKV_ERR_UNSUPPORTED for the 1.5-, 3- and 1.25-bit modes,
+ * whose multi-byte codes the in-kernel encode does not write).
  */
 typedef struct {
   vqkv_decode_args decode;    /* as for vqkv_decode_attn (seq_lens include the new token) */
