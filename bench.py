@@ -8,7 +8,13 @@ workload is the Llama-3.1-8B-shaped 2-bit decode at 196,608 cached tokens
 (batch 1, 32 query heads over 8 KV heads, head_dim 128); its cache is
 produced by the library's own GPU encoder from seeded synthetic K/V.
 
-Prints one JSON line (see README of the result keys in the design doc).
+Prints one JSON line: the contract's keys (metric, value, unit, n_gpus,
+steps, warmup, ms_per_step, config, ...) plus "roofline" (the decode
+kernel's algorithmic bytes per launch over its back-to-back launch time,
+against the measured HBM copy bandwidth), "cpu_baseline" (the CPU oracle on
+a bounded sample), "e2e" (through the public binding with host buffers),
+"near_ties" (near-tie counts of the encodes the run made) and
+"fp16_kv_decode" (the fp16-KV comparison kernel on the same shape).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (weak scaling).
 """
@@ -177,28 +183,27 @@ _ORACLE_INPUTS = {}
 
 
 def _oracle_setup(max_tokens):
-    """Inputs of the oracle sample (built once per worker, not timed)."""
+    """Inputs of the oracle runs (built once per worker, not timed): every KV
+    head's codebooks and s (a small calibration), the queries, and seeded
+    uniform codes of the first max_tokens tokens of each KV head."""
     w = synth.WORKLOADS[WORKLOAD_ID]
-    s, kcb, vcb = calib.calibrate_head(w, 0, sample_tokens=512, iters=2)
+    cal = [calib.calibrate_head(w, h, sample_tokens=512, iters=2) for h in range(w.Hkv)]
     _ORACLE_INPUTS.update(
-        s=s[None], kcb=kcb[None], vcb=vcb[None], q=synth.queries(w)[:, :w.g],
-        kc=synth.uniform_codes(w, 0, 0, 0, max_tokens), vc=synth.uniform_codes(w, 0, 0, 1, max_tokens))
+        s=np.stack([c[0] for c in cal]), kcb=np.stack([c[1] for c in cal]), vcb=np.stack([c[2] for c in cal]),
+        q=synth.queries(w),
+        kc=[[synth.uniform_codes(w, 0, h, 0, max_tokens) for h in range(w.Hkv)]],
+        vc=[[synth.uniform_codes(w, 0, h, 1, max_tokens) for h in range(w.Hkv)]])
     return True
 
 
-def _oracle_decode_sample(n_tokens):
-    """Seconds the oracle takes for the g query heads of KV head 0 over n tokens."""
+def _oracle_decode_step(n_tokens):
+    """Seconds the oracle takes for one decode step of the workload cut to its
+    first n_tokens tokens: all 32 query heads over all 8 KV heads."""
     import oracle
     d = _ORACLE_INPUTS
     t0 = time.perf_counter()
-    oracle.decode_attention(d["q"], [[d["kc"][:n_tokens]]], [[d["vc"][:n_tokens]]], d["kcb"], d["vcb"], d["s"],
-                            np.array([n_tokens]))
+    oracle.decode_attention(d["q"], d["kc"], d["vc"], d["kcb"], d["vcb"], d["s"], np.array([n_tokens]))
     return time.perf_counter() - t0
-
-
-def _oracle_decode_passes(n_tokens, passes):
-    """Seconds for `passes` repetitions of the sample above."""
-    return sum(_oracle_decode_sample(n_tokens) for _ in range(passes))
 
 
 def _oracle_worker(max_tokens):
@@ -212,59 +217,62 @@ def _oracle_worker(max_tokens):
     return ex, cores
 
 
-def _size_sample(ex, seconds, lo=256, hi=196608):
-    t = ex.submit(_oracle_decode_sample, 2048).result()
-    n = int(min(hi, max(lo, 2048 * seconds / max(t, 1e-4))))
+def _size_step(ex, seconds, lo=16, hi=196608):
+    """Tokens per oracle step so that one step takes about `seconds`."""
+    t = ex.submit(_oracle_decode_step, 1024).result()
+    n = int(min(hi, max(lo, 1024 * seconds / max(t, 1e-4))))
     return max(16, n // 16 * 16)
 
 
-def cpu_baseline(budget_s=12.0):
+def cpu_baseline(budget_s=15.0):
     """The oracle as it stands (fp64 numpy, the plain original-domain path) on
-    a bounded sample of the same workload: KV head 0's 4 query heads over the
-    first n tokens, n sized to about budget_s of host work."""
+    a bounded sample of the same workload: whole decode steps (all 32 query
+    heads over the 8 KV heads) over the first n tokens, n sized so the run
+    takes about budget_s of host work."""
     ex, cores = _oracle_worker(196608)
     with ex:
-        n = _size_sample(ex, budget_s)
-        t1 = ex.submit(_oracle_decode_sample, n).result()
-        passes = max(1, int(round(budget_s / max(t1, 1e-3))))
-        t = ex.submit(_oracle_decode_passes, n, passes).result()
-    tok_s = n * passes / (t * 8)    # each pass covers 1 of the 8 KV heads of each token
-    return {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"KV head 0 of 8 (its 4 query heads), first {n} of 196608 tokens, {passes} passes "
-                      f"({passes / 8:.1f} full steps of work), {t:.1f} s; tokens/s scaled to all 8 KV heads"}
+        n = _size_step(ex, budget_s / 3)
+        ex.submit(_oracle_decode_step, n).result()   # warm-up
+        times = [ex.submit(_oracle_decode_step, n).result() for _ in range(2)]
+    t = sum(times) / len(times)
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"2 timed decode steps (all 32 query heads, 8 KV heads) over the first {n} of 196608 "
+                      f"tokens, {t:.2f} s each; tokens/s = {n} / step seconds"}
 
 
 # ------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    """The reference arm: the CPU oracle timed on the host cores, each step a
-    bounded sample of the workload, the whole run kept to about 90 s."""
+    """The reference arm: the CPU oracle timed on the host cores.  Each step
+    is one decode step of the workload (all 32 query heads over the 8 KV
+    heads) over the first n tokens of the cache, n = all 196,608 when the
+    whole run fits in about two minutes, else fewer; ms_per_step is the
+    measured time of that step and value = n / step seconds."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = synth.WORKLOADS[WORKLOAD_ID]
-    lens = synth.seq_lens(w)
     total = args.steps + args.warmup
-    per_step = 90.0 / max(total, 1)
+    per_step = 120.0 / max(total, 1)
     ex, cores = _oracle_worker(196608)
     with ex:
-        n = _size_sample(ex, per_step, lo=16)
+        n = _size_step(ex, per_step)
         times = []
         for i in range(total):
-            dt = ex.submit(_oracle_decode_sample, n).result()
+            dt = ex.submit(_oracle_decode_step, n).result()
             if i >= args.warmup:
                 times.append(dt)
     step_s = sum(times) / len(times)
-    value = n / (step_s * 8)
-    full_step_ms = 1e3 * int(lens.sum()) / value
+    value = n / step_s
+    sample = ("the whole step" if n == w.seq_len else f"the first {n} of {w.seq_len} tokens") + \
+        " of all 32 query heads over the 8 KV heads per step"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_step_ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": f"first {n} tokens of KV head 0 (4 query heads) per step; "
-                                                 f"tokens/s scaled to the full 8-KV-head step"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"KV head 0 (4 query heads), {n} tokens per step"},
+        "config": {"workload": w.name, "sample": sample, "tokens_per_step": n,
+                   "timing": "wall clock around each oracle step on the host"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -364,12 +372,18 @@ def run_ours(args):
             _lib.vqkv_encode(mode, role, x, pos_, s if role == 0 else None, cb, codes, cap)
 
     zeros = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    near_ties = None
     if kv is not None:
-        # encode the whole cache (all KV heads, all positions) in one call per K / V
+        # encode the whole cache (all KV heads, all positions) in one call per K / V,
+        # counting near-ties (best two fp32 distances within 1e-6 relative)
+        cnt = torch.zeros(2, dtype=torch.int64, device=dev)
         for role, codes in ((0, kcodes), (1, vcodes)):
             x = torch.from_numpy(np.stack([kv[h][role] for h in range(w.Hkv)])[None]).to(dev)
-            encode(role, x, zeros, codes)
+            _lib.vqkv_encode(mode, role, x, zeros, s if role == 0 else None, kcb if role == 0 else vcb, codes, cap,
+                             near_tie_count=cnt[role:role + 1])
             del x
+        n_codes = w.B * w.Hkv * w.seq_len * (128 // w.d_sub)
+        near_ties = {"cache_encode": {"K": int(cnt[0].item()), "V": int(cnt[1].item()), "codes_per_role": n_codes}}
     else:
         # other workloads: seeded uniform codes (decode cost does not depend on code values)
         gen = torch.Generator(device=dev)
@@ -443,6 +457,13 @@ def run_ours(args):
         if ev is not None:
             ev[1].record()
 
+    if fused and near_ties is not None:
+        # the step's own encode of the new rows, counted once outside the timed region
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        kc0, vc0 = copies[0]
+        _lib.vqkv_decode_append(mode, q, kc0, vc0, seq, kcb, vcb, s, out, ws, cap, max_len, new_k, new_v,
+                                near_tie_count=cnt)
+        near_ties["append_step"] = {"near_ties": int(cnt.item()), "codes": 2 * w.B * w.Hkv * (128 // w.d_sub)}
     if args.profile_fp16:
         fp16_profile_run(w, lens, dev, args.profile_fp16)
         return
@@ -464,12 +485,17 @@ def run_ours(args):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(g_steps):
                 step(i)
-        one = []
-        for i in range(g_steps):
-            g1 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g1, stream=stream):
-                step(i)
-            one.append(g1)
+        # the timed region is exactly args.steps steps: whole graphs of g_steps
+        # steps, then one graph of the remaining steps (back to back, each
+        # step's kernels chained to the previous step's by programmatic
+        # dependent launch inside a graph)
+        rest_steps = args.steps % g_steps
+        graph_rest = None
+        if rest_steps:
+            graph_rest = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rest, stream=stream):
+                for i in range(rest_steps):
+                    step(i)
         # instrumented graph: events around every decode launch
         evs = [(torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(g_steps)]
@@ -481,18 +507,18 @@ def run_ours(args):
         torch.cuda.synchronize()
 
         def run_steps(k):
-            full, rest = divmod(k, g_steps)
-            for _ in range(full):
+            for _ in range(k // g_steps):
                 graph.replay()
-            for i in range(rest):
-                one[i].replay()
+            if k % g_steps:
+                assert graph_rest is not None and k % g_steps == rest_steps
+                graph_rest.replay()
 
         # time one replay to size the soak
         t0 = time.perf_counter()
         graph.replay()
         torch.cuda.synchronize()
         per_step = (time.perf_counter() - t0) / g_steps
-        soak = max(1, int(SOAK_S / per_step))
+        soak = max(1, int(SOAK_S / per_step)) // g_steps * g_steps or g_steps
 
         clocks = ClockSampler(local)
         clocks.start()
@@ -614,7 +640,10 @@ def run_ours(args):
                              else "seeded uniform codes (decode cost does not depend on code values)"),
                    "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB > "
                          f"{l2 / 1e6:.0f} MB L2)",
-                   "timing": f"CUDA graphs of {g_steps} steps, CUDA events on the launch stream",
+                   "timing": (f"timed region = exactly {args.steps} steps: {args.steps // g_steps} replays of a "
+                              f"CUDA graph of {g_steps} back-to-back steps"
+                              + (f" + one graph of {args.steps % g_steps} steps" if args.steps % g_steps else "")
+                              + "; CUDA events on the launch stream"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
@@ -632,6 +661,8 @@ def run_ours(args):
                        + ("vqkv_decode_append" if fused else "2 encodes, decode") + ", D2H O, sync"},
         "gpu_launches": (dec_kernels if fused else 2 + dec_kernels) * args.steps,
     }
+    if near_ties is not None:
+        line["near_ties"] = near_ties
     if unfused_ms is not None:
         line["unfused_step_ms"] = unfused_ms
     if cpu is not None:
@@ -672,7 +703,9 @@ def encode_prefill_bench(w, dev, reps=3):
             x = x.half()
             call = lambda: _lib.vqkv_encode(mode, role, x, pos, s if role == 0 else None,  # noqa: E731
                                             kcb if role == 0 else vcb, codes, w.cap_len)
-            call()
+            cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+            _lib.vqkv_encode(mode, role, x, pos, s if role == 0 else None, kcb if role == 0 else vcb, codes,
+                             w.cap_len, near_tie_count=cnt)   # untimed: the near-tie count of this encode
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -681,7 +714,9 @@ def encode_prefill_bench(w, dev, reps=3):
             e1.record()
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / reps
-            out["K" if role == 0 else "V"] = {"ms": ms, "rows_per_s": w.B * w.Hkv * w.prefill / (ms * 1e-3)}
+            out["K" if role == 0 else "V"] = {"ms": ms, "rows_per_s": w.B * w.Hkv * w.prefill / (ms * 1e-3),
+                                              "near_ties": int(cnt.item()),
+                                              "codes": w.B * w.Hkv * w.prefill * (128 // wm.d_sub)}
             del x
         res["2-bit" if mode == 0 else "1.5-bit"] = out
     return res

@@ -120,8 +120,19 @@ typedef enum {
 /* Bits of the device error word (see error_flags / workspace word 0). */
 #define VQKV_DEVERR_SEQ_LEN   0x1u  /* a seq_lens[b] outside [0, max_seq_len]: clamped */
 #define VQKV_DEVERR_POSITION  0x2u  /* an encode row outside [0, cap_len): not written */
-#define VQKV_DEVERR_TIMEOUT   0x4u  /* a bounded on-chip wait gave up; that CTA's output is invalid */
+#define VQKV_DEVERR_TIMEOUT   0x4u  /* a bounded on-chip wait gave up: see below */
 #define VQKV_DEVERR_BLOCK     0x8u  /* a block-table entry outside [0, num_blocks) (paged calls) */
+/*
+ * VQKV_DEVERR_TIMEOUT: every on-chip wait of the decode kernels (the bulk
+ * copies of the 2-bit code ring) gives up after a bounded number of polls
+ * instead of hanging.  The CTA then waits, again bounded, for the copies it
+ * still has in flight, sets this bit and finishes.  After it is set, the
+ * launch's output O (and the shared memory of that CTA, which a late copy
+ * may still write) are undefined.  A wait runs out only when a copy did not
+ * complete in about 10^6 polls, which points at a fault outside the
+ * library: treat the context as suspect, and do not trust later results on
+ * it without checking them.
+ */
 
 /*
  * vqkv_encode — smoothing, Hadamard rotation, nearest-centroid assignment and
@@ -351,17 +362,33 @@ vqkv_status vqkv_decode_attn_fp16(const vqkv_fp16_decode_args* args, void* strea
  *     plan needs more scratch than VQKV_STATIC_SCRATCH_BYTES
  *     (vqkv_decode_workspace_bytes(args) tells how much), the call returns
  *     VQKV_ERR_WORKSPACE and enqueues nothing.
- *   - The first call on a device looks up the array's device address (with
- *     that device current, once per device); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (cudaGetSymbolAddress, which allocates nothing), so
+ *     the address stays right after a context is torn down and rebuilt.  The
+ *     first call in a context may load the library's device code into it:
+ *     make that first call before any stream capture.
  *   - Each call clears the scratch's error word and tickets with
  *     cudaMemsetAsync on `stream`, then launches.  The array is shared by
  *     every call on a device and keeps the last call's contents: calls whose
  *     execution overlaps on the GPU (different streams, not ordered) race on
- *     it and must be serialised by the caller.  Device-side error bits are
- *     not reported back by this entry point (lengths are still clamped).
+ *     it and must be serialised by the caller.  The device error bits of the
+ *     last call (VQKV_DEVERR_SEQ_LEN, VQKV_DEVERR_TIMEOUT) stay in the
+ *     scratch's error word until the next call clears it:
+ *     vqkv_decode_static_error reads them.
  */
 vqkv_status vqkv_decode_attn_static(const vqkv_decode_args* args, void* stream);
+
+/*
+ * vqkv_decode_static_error — the device error word of the last
+ * vqkv_decode_attn_static call on the current device (VQKV_DEVERR_* bits,
+ * 0 when none was raised).  Enqueues a 4-byte copy from the scratch array to
+ * *host_flags (host memory, pageable or pinned) on `stream` after the work
+ * already queued there, then waits for `stream`; allocates nothing.  Call it
+ * on the stream of the decode call it should observe.  Returns
+ * VQKV_ERR_INVALID_ARG for a NULL host_flags, VQKV_ERR_CUDA when the copy or
+ * the wait fails.
+ */
+vqkv_status vqkv_decode_static_error(uint32_t* host_flags, void* stream);
 
 /*
  * vqkv_test_decode_ring_timeout — test hook for the bounded on-chip waits of

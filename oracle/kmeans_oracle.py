@@ -11,7 +11,7 @@ Sources (cited as page title + section):
        trained offline with K-Means; section "Key points": 2^8 x 4 and
        2^12 x 8 codebook shapes, and the transform ablation (smoothing or
        the rotation alone helps less than both; their order matters little).
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent (each also in the readings table):
   * the smoothing factor of key channel c is s_c = sqrt(max_t |K[t, c]|)
     (SmoothQuant's per-channel factor with migration strength 1/2;
     SmoothQuant is in the page's reference list), computed in fp64 and

@@ -14,7 +14,7 @@ What the pages fix:
     the index of a K-Means centroid; 2-bit = 2^8 entries x 4 dims, 1.5-bit =
     2^12 entries x 8 dims [P1 Key points];
   * attention is computed over the dequantised cache [P1 Summary, P2 方法详解].
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent (each also in the readings table):
   * smoothing divides keys by s and multiplies queries by s;
   * the rotation is the normalised Sylvester matrix Hn = H/sqrt(128) with
     H[i][k] = (-1)^popcount(i & k); values are not transformed;

@@ -29,3 +29,13 @@ def golden_lines(name):
 @pytest.fixture
 def golden():
     return golden_lines
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Near-tie counts of the code-parity tests (tests/tie_log.py)."""
+    from tests import tie_log
+    lines = tie_log.summary_lines()
+    if lines:
+        terminalreporter.section("near-tie counts (GPU codes vs oracle codes)")
+        for line in lines:
+            terminalreporter.write_line(line)

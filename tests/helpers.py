@@ -122,5 +122,21 @@ def check_codes(gpu_codes, ref_codes, d32):
     return ties, len(bad) - ties
 
 
+def check_and_record_codes(name, gpu_codes, ref_codes, d32, device_count=None, bounded=True):
+    """check_codes, recorded in the near-tie log (tests/tie_log.py), with the
+    failing count asserted zero and, for natural data, the near-tie count
+    bounded.  Returns the number of near-tie mismatches."""
+    from tests import tie_log
+    ties, fails = check_codes(gpu_codes, ref_codes, d32)
+    n = int(np.asarray(gpu_codes).size)
+    tie_log.record(name, n, ties, fails, device_count)
+    assert fails == 0, (name, ties, fails)
+    if bounded:
+        assert ties <= tie_log.bound(n), (name, ties, n)
+        if device_count is not None:
+            assert device_count <= tie_log.bound(n), (name, device_count, n)
+    return ties
+
+
 def library_loaded() -> bool:
     return os.path.exists(_build.LIB)

@@ -23,18 +23,21 @@ def unpack_all(mode, role, buf, L):
     return [[vo.unpack_stream_fast(buf[b, h], mode, role, L) for h in range(Hkv)] for b in range(B)]
 
 
-def compare(mode, role, x, s, cb, gpu_buf, pos, n_rows):
-    """Oracle-encode every row and compare with the GPU stream bytes."""
+def compare(name, mode, role, x, s, cb, gpu_buf, pos, n_rows, device_count=None):
+    """Oracle-encode every row and compare with the GPU stream bytes: no
+    failing mismatch, near-ties recorded and bounded.  Returns the number of
+    near-tie mismatches."""
     B, Hkv = x.shape[:2]
-    ties = fails = 0
+    got_all, ref_all, d_all = [], [], []
     for b in range(B):
         for h in range(Hkv):
             ref, d32 = vo.encode_rows(x[b, h], role, s[h] if s is not None else None, cb[h])
             got = vo.unpack_stream_fast(gpu_buf[b, h], mode, role, pos[b] + n_rows)[pos[b]:pos[b] + n_rows]
-            t, f = H.check_codes(got, ref, d32)
-            ties += t
-            fails += f
-    return ties, fails
+            got_all.append(got.reshape(-1))
+            ref_all.append(ref.reshape(-1))
+            d_all.append(d32.reshape(ref.size, -1))
+    return H.check_and_record_codes(name, np.concatenate(got_all), np.concatenate(ref_all), np.concatenate(d_all),
+                                    device_count)
 
 
 def test_tiny_config_keys_and_values():
@@ -45,8 +48,7 @@ def test_tiny_config_keys_and_values():
     for role, x, cb in ((vo.ROLE_K, k, kcb), (vo.ROLE_V, v, vcb)):
         buf, nties, err = H.gpu_encode(0, role, x, [0], s if role == 0 else None, cb, w.cap_len, with_ties=True)
         assert err == 0
-        ties, fails = compare(0, role, x, s if role == 0 else None, cb, buf, [0], w.seq_len)
-        assert fails == 0, (role, ties, fails)
+        compare(f"tiny config, role {role}", 0, role, x, s if role == 0 else None, cb, buf, [0], w.seq_len, nties)
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
@@ -62,9 +64,10 @@ def test_ragged_positions_multi_head(mode, role, n):
     pos = [0, 5, 130]
     cap = 200
     prefill = np.random.default_rng(0).integers(0, 256, size=(3, 2, vo.code_bytes(mode, cap)), dtype=np.uint8)
-    buf = H.gpu_encode(mode, role, x, pos, s if role == 0 else None, cb, cap, codes=prefill)
-    ties, fails = compare(mode, role, x, s if role == 0 else None, cb, buf, pos, n)
-    assert fails == 0, (ties, fails)
+    buf, nties, _ = H.gpu_encode(mode, role, x, pos, s if role == 0 else None, cb, cap, codes=prefill,
+                                 with_ties=True)
+    compare(f"ragged positions, mode {mode}, role {role}, {n} rows", mode, role, x, s if role == 0 else None, cb,
+            buf, pos, n, nties)
     # bytes of tokens outside [pos, pos+n) are untouched
     for b in range(3):
         for h in range(2):
@@ -92,7 +95,7 @@ def test_positions_out_of_range_are_skipped_and_reported(mode):
     # sequence 0: rows at 62, 63 written; 64, 65 skipped.  sequence 1: rows at -3..-1 skipped, 0 written
     got0 = vo.unpack_stream_fast(buf[0, 0], mode, 0, 64)
     ref0, d0 = vo.encode_rows(x[0, 0], 0, s[0], kcb[0])
-    assert H.check_codes(got0[62:64], ref0[:2], d0[:2])[1] == 0
+    H.check_and_record_codes(f"out-of-range positions, mode {mode}", got0[62:64], ref0[:2], d0[:2])
     changed = np.flatnonzero(buf[1, 0] != 0xA5)
     off = vo.offset_table(mode, 0, 1)
     if mode == vo.MODE_VQ125:   # bit addresses -> bytes
@@ -158,11 +161,19 @@ def test_full_size_prefill_and_append_sampled(mode):
                      w.cap_len, near_tie_count=ties)
     torch.cuda.synchronize()
     buf = kcodes.cpu().numpy()
-    fails = 0
+    got_all, ref_all, d_all = [], [], []
     for b, h, t in samples:
         for row, tt in ((x[b, h, t:t + 1], t), (app[b, h, t % w.append:t % w.append + 1], w.prefill + t % w.append)):
             ref, d32 = vo.encode_rows(row, 0, s[h], kcb[h])
-            got = vo.unpack_stream_fast(buf[b, h], mode, 0, tt + 1)[tt:tt + 1]
-            _, f = H.check_codes(got, ref, d32)
-            fails += f
-    assert fails == 0
+            got_all.append(vo.unpack_stream_fast(buf[b, h], mode, 0, tt + 1)[tt:tt + 1].reshape(-1))
+            ref_all.append(ref.reshape(-1))
+            d_all.append(d32.reshape(ref.size, -1))
+    # the GPU's own counter covers every row encoded (16 x 8 x 16,640 rows x subvectors)
+    n_all = w.B * w.Hkv * (w.prefill + w.append) * (128 // vo.GEOMETRY[mode][1])
+    from tests import tie_log
+    ntie = int(ties.item())
+    H.check_and_record_codes(f"full-size Mistral-shaped key encode, mode {mode} (sampled rows; GPU counter over "
+                             f"all {n_all} codes)", np.concatenate(got_all), np.concatenate(ref_all),
+                             np.concatenate(d_all))
+    tie_log.record(f"full-size Mistral-shaped key encode, mode {mode}: GPU near-tie counter", n_all, 0, 0, ntie)
+    assert ntie <= tie_log.bound(n_all)

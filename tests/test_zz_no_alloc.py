@@ -35,6 +35,7 @@ def _case(mode, B, Hq, Hkv, lens, cap, seed):
     return t, qs, torch
 
 
+@pytest.mark.parametrize("num_splits", [0, 8])
 @pytest.mark.parametrize("mode,B,Hq,Hkv,lens,cap", [
     (0, 2, 8, 2, [900, 517], 1024),
     (1, 2, 10, 2, [300, 64], 320),
@@ -42,20 +43,44 @@ def _case(mode, B, Hq, Hkv, lens, cap, seed):
     (3, 2, 8, 2, [900, 517], 1024),
     (4, 2, 8, 2, [900, 517], 1024),
 ])
-def test_static_scratch_matches_workspace_entry_on_two_calls(mode, B, Hq, Hkv, lens, cap):
+def test_static_scratch_matches_workspace_entry_on_two_calls(mode, B, Hq, Hkv, lens, cap, num_splits):
+    """num_splits=8 forces several splits per (sequence, KV head), so the
+    tickets and split partials in the library's array are used: the last-CTA
+    merge (2, 4, 3, 1.25 bit) or the combine kernel (1.5 bit, whose CTAs
+    cover several sequences)."""
     t, qs, torch = _case(mode, B, Hq, Hkv, lens, cap, seed=21 + mode)
-    ws = _lib.decode_workspace(mode, B, Hq, Hkv, cap, max(lens))
+    ws = _lib.decode_workspace(mode, B, Hq, Hkv, cap, max(lens), num_splits)
+    if num_splits:
+        a = _lib.decode_args(mode, qs[0], t["kbuf"], t["vbuf"], t["lens"], t["kcb"], t["vcb"], t["s"], qs[0], ws,
+                             cap, max(lens), num_splits=num_splits)
+        assert _lib.vqkv_decode_num_splits(a) > 1
+        assert _lib.vqkv_decode_kernel_count(a) == (2 if mode == 1 else 1)
     for q in qs:   # two calls in a row; the second sees the first call's scratch contents
         ref = torch.empty((B, Hq, 128), dtype=torch.float16, device="cuda")
         got = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device="cuda")
         _lib.vqkv_decode_attn(mode, q, t["kbuf"], t["vbuf"], t["lens"], t["kcb"], t["vcb"], t["s"], ref, ws,
-                              cap, max(lens))
+                              cap, max(lens), num_splits=num_splits)
         _lib.vqkv_decode_attn_static(mode, q, t["kbuf"], t["vbuf"], t["lens"], t["kcb"], t["vcb"], t["s"], got,
-                                     cap, max(lens))
+                                     cap, max(lens), num_splits=num_splits)
         torch.cuda.synchronize()
         r, g = ref.cpu().numpy(), got.cpu().numpy()
         assert np.isfinite(g).all()
         assert vo.o_error(g, r.astype(np.float64)).max() <= H.O_TOL
+        assert _lib.vqkv_decode_static_error() == 0
+
+
+def test_static_error_word_reports_a_clamped_length_and_clears():
+    """An out-of-range sequence length is clamped and reported through the
+    error query; the next call starts from a clear error word."""
+    import torch
+    t, qs, _ = _case(0, 2, 8, 2, [50, 64], 64, seed=5)
+    bad = H.dev(np.array([50, 9999], dtype=np.int32))
+    out = torch.empty((2, 8, 128), dtype=torch.float16, device="cuda")
+    _lib.vqkv_decode_attn_static(0, qs[0], t["kbuf"], t["vbuf"], bad, t["kcb"], t["vcb"], t["s"], out, 64, 64)
+    assert _lib.vqkv_decode_static_error() & _lib.VQKV_DEVERR_SEQ_LEN
+    _lib.vqkv_decode_attn_static(0, qs[0], t["kbuf"], t["vbuf"], t["lens"], t["kcb"], t["vcb"], t["s"], out, 64,
+                                 64)
+    assert _lib.vqkv_decode_static_error() == 0
 
 
 def test_static_scratch_rejects_plans_beyond_its_size():

@@ -29,7 +29,7 @@ STATUS = {0: "VQKV_OK", 1: "VQKV_ERR_INVALID_ARG", 2: "VQKV_ERR_UNSUPPORTED", 3:
 
 EXPORTED = ["vqkv_code_bytes", "vqkv_decode_workspace_bytes", "vqkv_decode_num_splits", "vqkv_decode_kernel_count",
             "vqkv_encode", "vqkv_decode_attn", "vqkv_decode_attn_multi", "vqkv_decode_append",
-            "vqkv_decode_attn_static", "vqkv_encode_paged", "vqkv_decode_attn_paged", "vqkv_test_decode_ring_timeout",
+            "vqkv_decode_attn_static", "vqkv_decode_static_error", "vqkv_encode_paged", "vqkv_decode_attn_paged", "vqkv_test_decode_ring_timeout",
             "vqkv_fp16_decode_workspace_bytes", "vqkv_decode_attn_fp16", "vqkv_smoothing", "vqkv_calib_transform",
             "vqkv_kmeans_workspace_bytes", "vqkv_kmeans", "vqkv_kmeans_seed", "vqkv_kmeans_assign",
             "vqkv_kmeans_update_workspace_bytes", "vqkv_kmeans_update", "vqkv_status_string"]
@@ -131,6 +131,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.vqkv_decode_append.argtypes = [ctypes.POINTER(DecodeAppendArgs), ctypes.c_void_p]
         L.vqkv_decode_attn_static.restype = ctypes.c_int
         L.vqkv_decode_attn_static.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        L.vqkv_decode_static_error.restype = ctypes.c_int
+        L.vqkv_decode_static_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         L.vqkv_fp16_decode_workspace_bytes.restype = ctypes.c_size_t
         L.vqkv_fp16_decode_workspace_bytes.argtypes = [ctypes.POINTER(Fp16DecodeArgs)]
         L.vqkv_decode_attn_fp16.restype = ctypes.c_int
@@ -309,6 +311,16 @@ def vqkv_decode_attn_static(mode, q, k_codes, v_codes, seq_lens, k_codebook, v_c
     st = lib().vqkv_decode_attn_static(ctypes.byref(a), _stream(stream))
     if st != 0:
         raise VqkvError(st, "vqkv_decode_attn_static")
+
+
+def vqkv_decode_static_error(stream=None) -> int:
+    """Device error word (VQKV_DEVERR_* bits) of the last
+    vqkv_decode_attn_static call on the current device; waits for `stream`."""
+    flags = ctypes.c_uint32(0)
+    st = lib().vqkv_decode_static_error(ctypes.byref(flags), _stream(stream))
+    if st != 0:
+        raise VqkvError(st, "vqkv_decode_static_error")
+    return int(flags.value)
 
 
 def decode_workspace(mode, B, Hq, Hkv, cap_len, max_seq_len, num_splits=0, device="cuda", n_queries=1):

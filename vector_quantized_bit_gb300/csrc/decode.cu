@@ -503,7 +503,6 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   grid_dependency_wait();
   grid_dependents_launch();
   uint32_t uses = 0;        // super-tiles this warp has taken through its ring (all sequences)
-  bool timed_out = false;
 
   for (int b = b_begin; b < b_end; ++b) {
     // Every input load of the prologue is issued before the first one is
@@ -693,11 +692,12 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
         }
       }
 
+      int stalled = -1;   // ring index whose wait gave up
       for (int j = 0; j < n_mine; ++j) {
         const uint32_t st = (uses + j) % V2_STAGES;
         const uint32_t par = ((uses + j) / V2_STAGES) & 1u;
         if (!mbar_wait_bounded(mbar + 8 * st, par, p.max_polls)) {
-          timed_out = true;
+          stalled = j;
           break;
         }
         // the lane's code words: plane w (every lane's 16- or 8-byte piece
@@ -738,13 +738,16 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
           vq2_step<G::TPI, MODE>(s_cb, kbyte, vbyte, qa, kq, vq, t_begin + (warp + j * V2_WARPS) * G::TPI, cl,
                                  lane, m0, m1, l0, l1, acc);
       }
-      if (timed_out) {
-        // give the copies already issued a bounded chance to land before the
-        // ring is reused or the CTA exits, and report the failure
-        for (int j = 0; j < n_mine && j < V2_STAGES; ++j) {
-          const uint32_t st = (uses + n_mine - 1 - j) % V2_STAGES;
-          mbar_wait_bounded(mbar + 8 * st, ((uses + n_mine - 1 - j) / V2_STAGES) & 1u, p.max_polls);
-        }
+      if (stalled >= 0) {
+        // The copies in flight are exactly the ring indices issued but not
+        // consumed: index `stalled` and the refills issued ahead of it, i.e.
+        // stalled .. min(stalled + V2_STAGES - 2, n_mine - 1) (index j + S - 1
+        // is issued only after index j is consumed).  Give each of them a
+        // bounded chance to land, on its own stage and phase, before the
+        // ring is reused or the CTA exits, and report the failure.
+        const int last = min(stalled + V2_STAGES - 2, n_mine - 1);
+        for (int j = stalled; j <= last; ++j)
+          mbar_wait_bounded(mbar + 8 * ((uses + j) % V2_STAGES), ((uses + j) / V2_STAGES) & 1u, p.max_polls);
         if (lane == 0) atomicOr(p.err, VQKV_DEVERR_TIMEOUT);
       }
       uses += n_mine;

@@ -3,8 +3,6 @@
 // vqkv_decode_attn, but the split-KV scratch (error word, per-(sequence, KV
 // head) tickets, split partials) lives in a fixed array compiled into this
 // library instead of a caller-provided workspace.
-#include <mutex>
-
 #include "internal.h"
 #include "vqkv.h"
 
@@ -16,22 +14,16 @@ namespace {
 // clears the error word and the tickets before launching.
 static __device__ __align__(256) unsigned char g_decode_scratch[VQKV_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.
+// Device address of the scratch array in the current device's context.  It
+// is looked up on every call (with the device current): the lookup
+// allocates nothing, and a fresh lookup stays right after the context has
+// been torn down and rebuilt (cudaDeviceReset), where a cached address
+// would point into the old context.  The first lookup in a context may load
+// the library's device code into it.
 vqkv_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VQKV_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return VQKV_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return VQKV_ERR_CUDA;
+  *out = p;
   return VQKV_OK;
 }
 
@@ -57,4 +49,17 @@ extern "C" vqkv_status vqkv_decode_attn_static(const vqkv_decode_args* args, voi
   a.workspace = scratch;
   a.workspace_bytes = VQKV_STATIC_SCRATCH_BYTES;
   return vqkv_decode_attn(&a, stream);
+}
+
+extern "C" vqkv_status vqkv_decode_static_error(uint32_t* host_flags, void* stream) {
+  using namespace vqkv;
+  if (host_flags == nullptr) return VQKV_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  vqkv_status st = scratch_address(&scratch);
+  if (st != VQKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return VQKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return VQKV_ERR_CUDA;
+  return VQKV_OK;
 }
