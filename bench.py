@@ -74,6 +74,10 @@ def parse():
                     help="time the offline calibration stage (smoothing, key transform, K-Means training) instead")
     ap.add_argument("--ablation", action="store_true",
                     help="codebook utilisation and reconstruction error of the five key transforms instead")
+    ap.add_argument("--profile-encode", type=int, default=-1, choices=[-1, 0, 1],
+                    help="time the key prefill encode of 4 of the Mistral-shaped workload's sequences (4 x 8 x "
+                         "16,384 rows) in this code mode (0: 2-bit, 1: 1.5-bit), 3 calls, and exit: the command "
+                         "the encode ncu summaries are taken with")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
@@ -722,6 +726,41 @@ def encode_prefill_bench(w, dev, reps=3):
     return res
 
 
+def encode_profile_run(mode, B=4, calls=3):
+    """calls x vqkv_encode of the key prefill of B sequences of the
+    Mistral-shaped workload (B x 8 KV heads x 16,384 rows, 134 MB of fp16
+    rows at B = 4, more than L2), keys made on the GPU as in
+    encode_prefill_bench; prints the mean call time (CUDA events)."""
+    import torch
+    from vector_quantized_bit_gb300 import _build, _lib
+    _build.build()
+    dev = torch.device("cuda")
+    w = synth.WORKLOADS[4].with_mode(mode).scaled(B=B)
+    s_h, kcb_h, _ = host_calibration(w)
+    s, kcb = torch.from_numpy(s_h).to(dev), torch.from_numpy(kcb_h).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + w.config_id + 31)
+    x = torch.randn((w.B, w.Hkv, w.prefill, 128), generator=gen, device=dev)
+    for h in range(w.Hkv):
+        ch, sc = synth.outlier_channels(w, h)
+        x[:, h, :, torch.from_numpy(ch).to(dev)] *= torch.from_numpy(sc).to(dev)
+    x = x.half()
+    codes = torch.zeros((w.B, w.Hkv, _lib.vqkv_code_bytes(mode, w.cap_len)), dtype=torch.uint8, device=dev)
+    pos = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls):
+        _lib.vqkv_encode(mode, 0, x, pos, s, kcb, codes, w.cap_len, near_tie_count=cnt)
+    e1.record()
+    torch.cuda.synchronize()
+    rows = w.B * w.Hkv * w.prefill
+    ms = e0.elapsed_time(e1) / calls
+    print(json.dumps({"encode_profile": {"mode": mode, "rows": rows, "calls": calls, "ms_per_call": ms,
+                                         "rows_per_s": rows / (ms * 1e-3), "near_ties_all_calls": int(cnt.item())}}),
+          flush=True)
+
+
 def fp16_profile_run(w, lens, dev, n):
     """n eager vqkv_decode_attn_fp16 calls over seeded Gaussian fp16 K/V."""
     import torch
@@ -968,7 +1007,9 @@ def run_ablation(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_encode >= 0:
+        encode_profile_run(args.profile_encode)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.calib:
         run_calibration(args)

@@ -177,3 +177,62 @@ def test_full_size_prefill_and_append_sampled(mode):
                              np.concatenate(d_all))
     tie_log.record(f"full-size Mistral-shaped key encode, mode {mode}: GPU near-tie counter", n_all, 0, 0, ntie)
     assert ntie <= tie_log.bound(n_all)
+
+
+def _vq15_rows(seed, B, Hkv, n, scale=1.0):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((B, Hkv, n, 128)) * scale).astype(np.float16)
+
+
+@pytest.mark.parametrize("role", [0, 1])
+def test_vq15_many_rows_across_tiles_and_sequences(role):
+    """The many-rows 1.5-bit path (tensor-core screen in tiles of 8 rows):
+    300 rows per sequence, so tiles straddle sequences, ragged positions and
+    a partial last tile; every code against the oracle."""
+    w = synth.WORKLOADS[3].scaled(seq_len=2048, cap_len=2048, Hkv=2)
+    s, kcb, vcb = H.calibrate(w, sample_tokens=1024, iters=3)
+    cb = kcb if role == 0 else vcb
+    x = np.stack([np.stack([(synth.keys if role == 0 else synth.values)(w, b, h, 7, 300) for h in range(2)])
+                  for b in range(3)])
+    pos = [0, 19, 1700]
+    cap = 2048
+    buf, nties, err = H.gpu_encode(1, role, x, pos, s if role == 0 else None, cb, cap, with_ties=True)
+    assert err == 0
+    compare(f"1.5-bit many rows, role {role}", 1, role, x, s if role == 0 else None, cb, buf, pos, 300, nties)
+
+
+def test_vq15_many_rows_duplicate_centroids_and_exact_matches():
+    """Value rows made of centroids that appear two or three times in the
+    codebook (in different groups of 32 centroids): the nearest distance is
+    0 and tied, the lowest index must win, and the GPU counts the ties."""
+    s, kcb, vcb = H.random_codebooks(1, 1, 9)
+    vcb[0, 3000] = vcb[0, 100]
+    vcb[0, 2000] = vcb[0, 3] = vcb[0, 4001]
+    r = np.random.default_rng(4)
+    picks = np.array([100, 3, 3000, 2000, 4001, 17, 3, 100])
+    rows = []
+    for i in range(40):
+        c = picks[r.integers(len(picks), size=16)]
+        rows.append(vcb[0][c].reshape(128))
+    x = np.stack(rows)[None, None].astype(np.float16)
+    buf, nties, err = H.gpu_encode(1, 1, x, [0], None, vcb, 64, with_ties=True)
+    assert err == 0
+    got = vo.unpack_stream_fast(buf[0, 0], 1, 1, 40)
+    ref, d32 = vo.encode_rows(x[0, 0], 1, None, vcb[0])
+    assert np.array_equal(got, ref)   # exact matches: no rounding can move them
+    assert set(np.unique(got).tolist()) <= {3, 17, 100}
+    assert nties == int(np.isin(ref, [3, 100]).sum())
+    H.check_and_record_codes("1.5-bit many rows, duplicated centroids", got, ref, d32, nties, bounded=False)
+
+
+def test_vq15_many_rows_values_beyond_fp16_screening():
+    """Keys whose smoothed, rotated values exceed the fp16 range of the
+    tensor-core screen (tiny smoothing factors): those subvectors fall back
+    to the exhaustive exact search and still match the oracle."""
+    s, kcb, vcb = H.random_codebooks(1, 2, 12)
+    s[:, :16] = 1e-5
+    x = _vq15_rows(5, 2, 2, 30, scale=3.0)
+    kcb = (kcb.astype(np.float32) * 50).astype(np.float16)
+    buf, nties, err = H.gpu_encode(1, 0, x, [0, 30], s, kcb, 64, with_ties=True)
+    assert err == 0
+    compare("1.5-bit many rows, values beyond fp16", 1, 0, x, s, kcb, buf, [0, 30], 30, nties)

@@ -43,6 +43,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
 }
 
+// Plain arrival (count one) on the barrier's current phase.
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
 // One poll of phase `parity`; true when that phase has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
   uint32_t ok;

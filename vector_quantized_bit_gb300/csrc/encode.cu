@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "encode_common.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace vqkv {
 namespace {
@@ -330,7 +331,6 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq125_kernel(const EncodeP
 constexpr int TC_WARPS = 16;
 constexpr int TC_THREADS = TC_WARPS * 32;
 constexpr int TC_TABLE_BYTES = 4096 * 4 * 8;                 // [centroid][tig]{b0b1, b2b3}
-constexpr size_t kTcSmem = TC_TABLE_BYTES + TC_WARPS * (128 + 16) * 4 + 16;
 
 // fp16 hi and lo parts of two fp32 values: a ~= hi.x + lo.x to about 2^-22
 // relative (lo may be subnormal: then to about 6e-8 absolute).
@@ -418,124 +418,377 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
   return *s_cmax;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_kernel(const EncodeParams p) {
-  extern __shared__ __align__(16) unsigned char tsm[];
-  uint2* s_tbl = reinterpret_cast<uint2*>(tsm);
-  float* s_x = reinterpret_cast<float*>(tsm + TC_TABLE_BYTES);           // [warp][128] x'
-  float* s_xn = s_x + TC_WARPS * 128;                                      // [warp][16] |x'_j|^2
-  float* s_cmax = s_xn + TC_WARPS * 16;
+// Many rows of 1.5-bit encode on the fifth-generation tensor cores.  A tile
+// is 8 rows = 128 (row, subvector) pairs, the M of one tcgen05 MMA; the 4096
+// centroids are 32 chunks of N = 128.  Per chunk two MMAs accumulate into
+// tensor memory
+//   D[m][c] = [x_hi, 1, 1] . [-2c, |c|^2_hi, |c|^2_lo] + [x_lo] . [-2c]
+// = |c|^2 - 2 x'_j . c to about 2^-22 relative (the screened distance less
+// the subvector's own |x'_j|^2), with A (hi and lo parts of the transformed
+// rows) and B (the [-2c, |c|^2_hi, |c|^2_lo] table of all 4096 centroids) in
+// shared memory behind matrix descriptors.
+//
+// Roles (12 warps, one CTA per SM, persistent over the KV head's tiles; 12
+// warps leave each SM sub-partition 3 warps, so up to 168 registers a thread):
+//   warps 8-10   producers: transform rows pw, pw + 3, pw + 6 (< 8) of each
+//                tile (smoothing + Hadamard in double-float for keys), write
+//                A_hi / A_lo, x' and |x'_j|^2 into one of 4 stages;
+//   warp 11      allocates 512 tensor-memory columns and, from one thread,
+//                issues the MMAs: chunk by chunk, alternating between the two
+//                epilogue warpgroups' tiles, into two 128-column buffers per
+//                warpgroup;
+//   warps 0-3, 4-7  two epilogue warpgroups taking alternate tiles: thread m
+//                owns tensor-memory lane m, i.e. subvector m % 16 of row m / 16.
+// The epilogue does not rank candidates one by one: per group of 32
+// consecutive centroids it takes the group minimum (three-input min), and
+// keeps the three smallest group minima B1 <= B2 <= B3 with the groups of the
+// first two.  A centroid can be the exact nearest only if its screened
+// distance is within 2 eps of B1 (screen_eps bounds the screening error), so
+// with B3 above that margin every candidate lies in group G1 or, if B2 is
+// within it, G2: those 32 or 64 centroids are re-ranked with exact fp32
+// direct differences (as exact_d8), the lowest index winning ties.  With B3
+// inside the margin, or a row whose transformed values do not fit fp16, the
+// subvector is searched exhaustively.  Every decision therefore equals the
+// exhaustive fp32 search's.
+//
+// Every wait is bounded: a wait that runs out sets VQKV_DEVERR_TIMEOUT (when
+// the caller passed an error word) and an abort flag that ends every role's
+// loop; the MMA thread then waits (bounded) for its MMAs before the tensor
+// memory is freed.
+namespace um {
+constexpr int ROWS = 8;                       // rows per tile
+constexpr int M = ROWS * 16;                  // 128 MMA rows: (row, subvector)
+constexpr int N = 128;                        // centroids per MMA
+constexpr int CHUNKS = 4096 / N;              // 32
+constexpr int GROUP = 32;                     // centroids per group minimum
+constexpr int STAGES = 4;
+constexpr int PROD_WARPS = 3;
+constexpr int MMA_WARP = 8 + PROD_WARPS;      // 11
+constexpr int THREADS = (MMA_WARP + 1) * 32;  // 384
+constexpr int TABLE_BYTES = 4096 * 32;        // B: 4096 centroids x 16 fp16
+constexpr int A_BYTES = M * 32;               // one A tile: 128 x 16 fp16
+constexpr int ST_AHI = 0, ST_ALO = A_BYTES, ST_X = 2 * A_BYTES;
+constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + M * 4;
+constexpr int STAGE_BYTES = ST_FLAG + M * 4;
+constexpr int OFF_STAGES = TABLE_BYTES;
+constexpr int OFF_BAR = OFF_STAGES + STAGES * STAGE_BYTES;
+constexpr int NBAR = 2 * STAGES + 8 + 1;      // A full / empty, tensor-memory full / empty, MMAs done
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag, max centroid norm
+constexpr size_t SMEM = OFF_MISC + 16;
+constexpr uint32_t TMEM_COLS = 512;           // 2 warpgroups x 2 buffers x N
+constexpr uint32_t MAX_POLLS = 1u << 22;
+// row flags
+constexpr int F_OK = 0, F_EXHAUSTIVE = 1, F_SKIP = 2;
+}  // namespace um
+static_assert(um::SMEM <= 227 * 1024, "UMMA encode shared memory");
+static_assert(um::STAGE_BYTES % 16 == 0 && um::OFF_BAR % 8 == 0, "alignment");
+
+// Bounded wait on an mbarrier phase by every lane of a warp (or one thread:
+// pass a one-lane mask): false, with the abort flag set, when it runs out
+// or another role aborted.
+__device__ __forceinline__ bool um_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                        unsigned mask) {
+  bool ok = false;
+  for (uint32_t i = 0; i < um::MAX_POLLS; ++i) {
+    if (mbar_try_wait(mbar, parity)) {
+      ok = true;
+      break;
+    }
+    if ((i & 31) == 31 && *abort_flag) break;
+  }
+  ok = __all_sync(mask, ok);
+  if (!ok && !*abort_flag) {
+    *abort_flag = 1;
+    if (err) atomicOr(err, VQKV_DEVERR_TIMEOUT);
+  }
+  return ok;
+}
+
+// Exact fp32 distance of subvector x to centroid c read from the B table
+// (-2c as fp16, halved exactly): direct differences in channel order, one
+// rounding per operation, the same arithmetic as exact_d8.
+__device__ __forceinline__ float exact_d8_umma(const float (&x)[8], const unsigned char* table, int c) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(table + umma_kmajor_offset((uint32_t)c, 0));
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float y[8];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w[t]);
+    y[2 * t] = -0.5f * __low2float(h);
+    y[2 * t + 1] = -0.5f * __high2float(h);
+  }
+  float e = __fsub_rn(x[0], y[0]);
+  float d = __fmul_rn(e, e);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    e = __fsub_rn(x[i], y[i]);
+    d = __fmaf_rn(e, e, d);
+  }
+  return d;
+}
+
+// Exact search state: best distance and index, second-best distance.
+// Candidates may come in any index order: lower distance, then lower index.
+__device__ __forceinline__ void exact_push(float d, int c, float& dex, int& cex, float& dsec) {
+  if (d < dex || (d == dex && c < cex)) {
+    dsec = dex;
+    dex = d;
+    cex = c;
+  } else {
+    dsec = fminf(dsec, d);
+  }
+}
+
+__global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const EncodeParams p) {
+  using namespace um;
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar = sbase + OFF_BAR;
+  auto a_full = [&](int s) { return bar + 8u * s; };
+  auto a_empty = [&](int s) { return bar + 8u * (STAGES + s); };
+  auto t_full = [&](int wg, int b) { return bar + 8u * (2 * STAGES + 2 * wg + b); };
+  auto t_empty = [&](int wg, int b) { return bar + 8u * (2 * STAGES + 4 + 2 * wg + b); };
+  const uint32_t done_bar = bar + 8u * (2 * STAGES + 8);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  float* s_cmax = reinterpret_cast<float*>(smem + OFF_MISC + 8);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(a_full(s), PROD_WARPS);
+      mbar_init(a_empty(s), 4);
+    }
+    for (int wg = 0; wg < 2; ++wg)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(t_full(wg, b), 1);
+        mbar_init(t_empty(wg, b), 4);
+      }
+    mbar_init(done_bar, 1);
+    *s_abort = 0;
+    *s_cmax = 0.f;
+    mbar_init_fence();
+  }
+  if (warp == MMA_WARP) tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
   grid_dependency_wait();
   grid_dependents_launch();
+  __syncthreads();
 
-  const float Cmax = build_tc_table(p, kvh, s_tbl, s_cmax);
-  float* wx = s_x + warp * 128;
-  float* wxn = s_xn + warp * 16;
-  const uint32_t tbl_lane = smem_u32(s_tbl) + (gid * 4 + tig) * 8;   // + 32 per centroid
+  // B table: row c = [-2c (8 fp16), |c|^2 hi, |c|^2 lo, 0 x 6]
+  {
+    float cmax = 0.f;
+    for (int c = threadIdx.x; c < 4096; c += THREADS) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t m2[4];
+      float nn = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[t]);
+        const float a = __low2float(h), b = __high2float(h);
+        nn = __fmaf_rn(a, a, nn);
+        nn = __fmaf_rn(b, b, nn);
+        const __half2 mm = __floats2half2_rn(-2.f * a, -2.f * b);   // exact
+        m2[t] = *reinterpret_cast<const uint32_t*>(&mm);
+      }
+      const __half nh = __float2half_rn(nn);
+      const __half2 tail = __halves2half2(nh, __float2half_rn(nn - __half2float(nh)));
+      unsigned char* row = smem + umma_kmajor_offset((uint32_t)c, 0);
+      *reinterpret_cast<uint4*>(row) = make_uint4(m2[0], m2[1], m2[2], m2[3]);
+      *reinterpret_cast<uint4*>(row + 128) = make_uint4(*reinterpret_cast<const uint32_t*>(&tail), 0u, 0u, 0u);
+      cmax = fmaxf(cmax, sqrtf(nn));
+    }
+    for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(s_cmax), __float_as_int(cmax));   // non-negative floats
+    fence_proxy_async_smem();
+  }
+  tcgen05_before_sync();
+  __syncthreads();
+  tcgen05_after_sync();
+  const uint32_t tmem = *s_tmem;
+  const float Cmax = *s_cmax;
 
   const int rows = p.B * p.n_rows;
-  for (int r = blockIdx.x * TC_WARPS + warp; r < rows; r += gridDim.x * TC_WARPS) {
-    const int b = r / p.n_rows, n = r - b * p.n_rows;
-    const int t = p.pos[b] + n;
-    if (t < 0 || t >= p.cap_len) {
-      if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
-      continue;
-    }
-    float x[4];
-    transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
-    float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-    nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2, j = lane / 2
-    __syncwarp();
-    *reinterpret_cast<float4*>(wx + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
-    if ((lane & 1) == 0) wxn[lane >> 1] = nx;
-    __syncwarp();
-    // A fragments: subvectors gid (a0a1, a4a5) and gid+8 (a2a3, a6a7)
-    const float2 xa = *reinterpret_cast<const float2*>(wx + 8 * gid + 2 * tig);
-    const float2 xb = *reinterpret_cast<const float2*>(wx + 8 * (gid + 8) + 2 * tig);
-    uint32_t a0, a0l, a1, a1l;
-    split_half2(xa.x, xa.y, a0, a0l);
-    split_half2(xb.x, xb.y, a1, a1l);
-    const uint32_t a2 = tig == 0 ? pack_half2(1.f, 1.f) : 0u;   // picks |c|^2 hi + lo
-    const uint32_t a3 = a2;
+  const int tiles = (rows + ROWS - 1) / ROWS;
+  const int n_my = (int)blockIdx.x < tiles ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 
-    float b1a = __int_as_float(0x7f800000), b2a = b1a, b1b = b1a, b2b = b1a;
-    int i1a = 0, i1b = 0;
-#pragma unroll 4
-    for (int n0 = 0; n0 < 4096; n0 += 8) {
-      const uint2 bf = lds64(tbl_lane + n0 * 32);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(d, a0, a1, a2, a3, bf.x, bf.y);
-      mma_16816(d, a0l, a1l, 0u, 0u, bf.x, bf.y);
-      const int c0 = n0 + 2 * tig;
-      top2_push(d[0], c0, b1a, b2a, i1a);
-      top2_push(d[1], c0 + 1, b1a, b2a, i1a);
-      top2_push(d[2], c0, b1b, b2b, i1b);
-      top2_push(d[3], c0 + 1, b1b, b2b, i1b);
-    }
-    // per subvector (gid: "a", gid+8: "b"): margin, candidates, exact re-rank
-    int code[2];
-    bool tie[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = gid + 8 * h;
-      float b1 = h ? b1b : b1a, b2 = h ? b2b : b2a;
-      const int i1 = h ? i1b : i1a;
-      float best = b1;
-      best = fminf(best, __shfl_xor_sync(0xffffffffu, best, 1));
-      best = fminf(best, __shfl_xor_sync(0xffffffffu, best, 2));
-      const float xnorm = sqrtf(wxn[j]);
-      const float eps = screen_eps(xnorm, Cmax);
-      const float thr = best + 2.f * eps;
-      const bool hidden = b2 <= thr;   // a third candidate of this lane may be within the margin
-      const bool any_hidden = ((__ballot_sync(0xffffffffu, hidden) >> (4 * gid)) & 0xfu) != 0;
-      const float* xj = wx + 8 * j;
-      float dex = __int_as_float(0x7f800000), dsec = dex;
-      int cex = 0x7fffffff;
-      if (!any_hidden) {
-        if (b1 <= thr) {
-          dex = exact_d8(xj, s_tbl, i1);
-          cex = i1;
-        }
-      } else {
-        // exhaustive exact search, the 4 lanes of the group take 1024 centroids each
-        for (int c = tig; c < 4096; c += 4) {
-          const float dc = exact_d8(xj, s_tbl, c);
-          if (dc < dex) {
-            dsec = dex;
-            dex = dc;
-            cex = c;
+  if (warp >= 8 && warp < MMA_WARP) {
+    // ---------------- producers: rows pw, pw + 3, pw + 6 (< 8) of every tile
+    const int pw = warp - 8;
+    const int j = lane >> 1, half = lane & 1;
+    for (int k = 0; k < n_my; ++k) {
+      const int s = k % STAGES;
+      if (!um_wait(a_empty(s), ((k / STAGES) & 1) ^ 1, s_abort, p.err, 0xffffffffu)) break;
+      unsigned char* st = smem + OFF_STAGES + s * STAGE_BYTES;
+      const int gt = (int)blockIdx.x + k * (int)gridDim.x;
+#pragma unroll 1
+      for (int r = pw; r < ROWS; r += PROD_WARPS) {
+        const int row = gt * ROWS + r, m = 16 * r + j;
+        int flag = F_SKIP;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < rows) {
+          const int b = row / p.n_rows, n = row - b * p.n_rows;
+          const int t = p.pos[b] + n;
+          if (t < 0 || t >= p.cap_len) {
+            if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
           } else {
-            dsec = fminf(dsec, dc);
+            transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
+            flag = F_OK;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (!(fabsf(x[i]) < 32768.f)) flag = F_EXHAUSTIVE;   // beyond fp16 screening (or not finite)
+          }
+        }
+        if (flag == F_SKIP) x[0] = x[1] = x[2] = x[3] = 0.f;
+        uint32_t hi01, lo01, hi23, lo23;
+        split_half2(x[0], x[1], hi01, lo01);
+        split_half2(x[2], x[3], hi23, lo23);
+        const uint32_t off = umma_kmajor_offset((uint32_t)m, 4u * half);
+        *reinterpret_cast<uint2*>(st + ST_AHI + off) = make_uint2(hi01, hi23);
+        *reinterpret_cast<uint2*>(st + ST_ALO + off) = make_uint2(lo01, lo23);
+        *reinterpret_cast<uint2*>(st + ST_AHI + off + 128) =
+            make_uint2(half == 0 ? pack_half2(1.f, 1.f) : 0u, 0u);   // picks |c|^2 hi + lo
+        *reinterpret_cast<uint2*>(st + ST_ALO + off + 128) = make_uint2(0u, 0u);
+        *reinterpret_cast<float4*>(st + ST_X + (r * kHeadDim + 4 * lane) * 4) = make_float4(x[0], x[1], x[2], x[3]);
+        float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+        nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2
+        flag = max(flag, __shfl_xor_sync(0xffffffffu, flag, 1));
+        if (half == 0) {
+          reinterpret_cast<float*>(st + ST_NORM)[m] = nx;
+          reinterpret_cast<int*>(st + ST_FLAG)[m] = flag;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full(s));
+    }
+  } else if (warp == MMA_WARP) {
+    // ---------------- one thread issues every MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16_f32(M, N);
+      bool ok = true;
+      for (int i = 0; ok && 2 * i < n_my; ++i) {
+        const int nwg = 2 * i + 1 < n_my ? 2 : 1;
+        uint64_t dhi[2], dlo[2];
+        for (int wg = 0; wg < nwg && ok; ++wg) {
+          const int k = 2 * i + wg, s = k % STAGES;
+          ok = um_wait(a_full(s), (k / STAGES) & 1, s_abort, p.err, 1u);
+          const uint32_t st = sbase + OFF_STAGES + s * STAGE_BYTES;
+          dhi[wg] = umma_desc_kmajor(st + ST_AHI);
+          dlo[wg] = umma_desc_kmajor(st + ST_ALO);
+        }
+        tcgen05_after_sync();
+        for (int q = 0; ok && q < CHUNKS; ++q) {
+          const uint64_t dB = umma_desc_kmajor(sbase + (uint32_t)q * (N * 32));
+          const int bsel = q & 1;
+          const uint32_t use = (uint32_t)(i * (CHUNKS / 2) + (q >> 1));
+          for (int wg = 0; wg < nwg; ++wg) {
+            ok = um_wait(t_empty(wg, bsel), (use & 1) ^ 1, s_abort, p.err, 1u);
+            if (!ok) break;
+            tcgen05_after_sync();
+            const uint32_t d = tmem + (uint32_t)((2 * wg + bsel) * N);
+            umma_f16(d, dhi[wg], dB, idesc, 0u);
+            umma_f16(d, dlo[wg], dB, idesc, 1u);
+            umma_commit(t_full(wg, bsel));
           }
         }
       }
-      // merge the group's 4 lanes: lower distance, then lower index
+      // every MMA issued has completed before the tensor memory is freed
+      umma_commit(done_bar);
+      um_wait(done_bar, 0, s_abort, p.err, 1u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warpgroup wg: tiles wg, wg + 2, ...
+    const int wg = warp >> 2, ml = 32 * (warp & 3) + lane;   // tensor-memory lane = MMA row
+    const int r = ml >> 4, j = ml & 15;
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const unsigned char* table = smem;
+    int it = 0;
+    for (int k = wg; k < n_my; k += 2, ++it) {
+      const float inf = __int_as_float(0x7f800000);
+      float B1 = inf, B2 = inf, B3 = inf;
+      int G1 = 0, G2 = 0;
+      auto group = [&](const float (&v)[32], int gid) {
+        float g = fmin3(v[0], v[1], v[2]);
 #pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        const float od = __shfl_xor_sync(0xffffffffu, dex, o);
-        const float os = __shfl_xor_sync(0xffffffffu, dsec, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, cex, o);
-        if (od < dex || (od == dex && oc < cex)) {
-          dsec = fminf(dex, os);
-          dex = od;
-          cex = oc;
-        } else {
-          dsec = fminf(dsec, od);
+        for (int i = 3; i < 31; i += 2) g = fmin3(g, v[i], v[i + 1]);
+        g = fminf(g, v[31]);
+        const bool p1 = g < B1, p2 = g < B2;
+        B3 = fminf(B3, fmaxf(B2, g));
+        B2 = fminf(B2, fmaxf(B1, g));
+        B1 = fminf(B1, g);
+        G2 = p1 ? G1 : (p2 ? gid : G2);
+        G1 = p1 ? gid : G1;
+      };
+      bool ok = true;
+      for (int q = 0; q < CHUNKS; ++q) {
+        const int bsel = q & 1;
+        const uint32_t use = (uint32_t)(it * (CHUNKS / 2) + (q >> 1));
+        ok = um_wait(t_full(wg, bsel), use & 1, s_abort, p.err, 0xffffffffu);
+        if (!ok) break;
+        tcgen05_after_sync();
+        const uint32_t col = t_lane + (uint32_t)((2 * wg + bsel) * N);
+        float v[32], u[32];
+        tmem_ld32(col, v);
+        tmem_ld32(col + 32, u);
+        tmem_wait_ld();
+        group(v, 4 * q);
+        group(u, 4 * q + 1);
+        tmem_ld32(col + 64, v);
+        tmem_ld32(col + 96, u);
+        tmem_wait_ld();
+        tcgen05_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(t_empty(wg, bsel));
+        group(v, 4 * q + 2);
+        group(u, 4 * q + 3);
+      }
+      if (!ok) break;
+      const int s = k % STAGES;
+      if (!um_wait(a_full(s), (k / STAGES) & 1, s_abort, p.err, 0xffffffffu)) break;   // (complete already)
+      const unsigned char* st = smem + OFF_STAGES + s * STAGE_BYTES;
+      const int flag = reinterpret_cast<const int*>(st + ST_FLAG)[ml];
+      float xv[8];
+      {
+        const float4 a = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j) * 4);
+        const float4 b = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j + 4) * 4);
+        xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = b.x, xv[5] = b.y, xv[6] = b.z, xv[7] = b.w;
+      }
+      const float eps = screen_eps(sqrtf(reinterpret_cast<const float*>(st + ST_NORM)[ml]), Cmax);
+      const float thr = B1 + 2.f * eps;
+      float dex = __int_as_float(0x7f800000), dsec = dex;
+      int cex = 0x7fffffff;
+      if (flag == F_EXHAUSTIVE || (flag == F_OK && B3 <= thr)) {
+        for (int c = 0; c < 4096; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
+      } else if (flag == F_OK) {
+#pragma unroll 4
+        for (int c = GROUP * G1; c < GROUP * G1 + GROUP; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
+        if (B2 <= thr) {
+#pragma unroll 4
+          for (int c = GROUP * G2; c < GROUP * G2 + GROUP; ++c)
+            exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
         }
       }
-      code[h] = cex;
-      tie[h] = is_near_tie(dex, dsec);
-    }
-    count_near_ties(p.near_tie, tie[0], lane, 0x11111111u);
-    count_near_ties(p.near_tie, tie[1], lane, 0x11111111u);
-    // lane (gid, tig 0) holds the pair (gid, gid+8) of this token
-    if (tig == 0) {
-      uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
-      if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, gid), code[0], code[1]);
+      count_near_ties(p.near_tie, flag != F_SKIP && is_near_tie(dex, dsec), lane, 0xffffffffu);
+      // lane (row r, subvector j < 8) stores the pair (j, j + 8) of its row
+      const int hi = __shfl_down_sync(0xffffffffu, cex, 8);
+      if (j < 8 && flag != F_SKIP) {
+        const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
+        const int b = row / p.n_rows, n = row - b * p.n_rows;
+        const int t = p.pos[b] + n;
+        uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
+        if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, j), cex, hi);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_empty(s));
     }
   }
+  tcgen05_before_sync();
+  __syncthreads();
+  tcgen05_after_sync();
+  if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 
@@ -694,8 +947,8 @@ cudaError_t encode_prepare(int mode) {
   }
   if (mode != VQKV_MODE_VQ15) return cudaSuccess;
   {
-    const cudaError_t e0 = cudaFuncSetAttribute(encode_vq15_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kTcSmem);
+    const cudaError_t e0 = cudaFuncSetAttribute(encode_vq15_umma_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)um::SMEM);
     if (e0 != cudaSuccess) return e0;
     const cudaError_t e1 = cudaFuncSetAttribute(encode_vq15_tc_split_kernel,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSplitSmem);
@@ -714,7 +967,8 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
                                                          kEnc3Smem);
   if (mode == VQKV_MODE_VQ125)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq125_kernel<1>, ENC_THREADS, 0);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_tc_kernel, TC_THREADS, kTcSmem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_umma_kernel, um::THREADS,
+                                                       um::SMEM);
 }
 
 // split_rows: one row per CTA, candidates split over the CTA's warps.
@@ -738,7 +992,7 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
     return launch_pdl(encode_vq3_kernel<1>, grid, dim3(ENC_THREADS), kEnc3Smem, stream, p);
   }
   if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
-  return launch_pdl(encode_vq15_tc_kernel, grid, dim3(TC_THREADS), kTcSmem, stream, p);
+  return launch_pdl(encode_vq15_umma_kernel, grid, dim3(um::THREADS), um::SMEM, stream, p);
 }
 
 }  // namespace vqkv
