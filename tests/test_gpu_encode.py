@@ -23,7 +23,7 @@ def unpack_all(mode, role, buf, L):
     return [[vo.unpack_stream_fast(buf[b, h], mode, role, L) for h in range(Hkv)] for b in range(B)]
 
 
-def compare(name, mode, role, x, s, cb, gpu_buf, pos, n_rows, device_count=None):
+def compare(name, mode, role, x, s, cb, gpu_buf, pos, n_rows, device_count=None, bounded=True):
     """Oracle-encode every row and compare with the GPU stream bytes: no
     failing mismatch, near-ties recorded and bounded.  Returns the number of
     near-tie mismatches."""
@@ -37,7 +37,7 @@ def compare(name, mode, role, x, s, cb, gpu_buf, pos, n_rows, device_count=None)
             ref_all.append(ref.reshape(-1))
             d_all.append(d32.reshape(ref.size, -1))
     return H.check_and_record_codes(name, np.concatenate(got_all), np.concatenate(ref_all), np.concatenate(d_all),
-                                    device_count)
+                                    device_count, bounded)
 
 
 def test_tiny_config_keys_and_values():
@@ -235,4 +235,6 @@ def test_vq15_many_rows_values_beyond_fp16_screening():
     kcb = (kcb.astype(np.float32) * 50).astype(np.float16)
     buf, nties, err = H.gpu_encode(1, 0, x, [0, 30], s, kcb, 64, with_ties=True)
     assert err == 0
-    compare("1.5-bit many rows, values beyond fp16", 1, 0, x, s, kcb, buf, [0, 30], 30, nties)
+    # distances near 1e11: fp32 rounding alone puts some candidates within
+    # 1e-6 relative of each other, so the GPU's near-tie count is not bounded
+    compare("1.5-bit many rows, values beyond fp16", 1, 0, x, s, kcb, buf, [0, 30], 30, nties, bounded=False)

@@ -468,8 +468,8 @@ constexpr int THREADS = (MMA_WARP + 1) * 32;  // 384
 constexpr int TABLE_BYTES = 4096 * 32;        // B: 4096 centroids x 16 fp16
 constexpr int A_BYTES = M * 32;               // one A tile: 128 x 16 fp16
 constexpr int ST_AHI = 0, ST_ALO = A_BYTES, ST_X = 2 * A_BYTES;
-constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + M * 4;
-constexpr int STAGE_BYTES = ST_FLAG + M * 4;
+constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + M * 4, ST_POS = ST_FLAG + M * 4;
+constexpr int STAGE_BYTES = ST_POS + 16 * 4;  // + cache position of each row
 constexpr int OFF_STAGES = TABLE_BYTES;
 constexpr int OFF_BAR = OFF_STAGES + STAGES * STAGE_BYTES;
 constexpr int NBAR = 2 * STAGES + 8 + 1;      // A full / empty, tensor-memory full / empty, MMAs done
@@ -614,33 +614,60 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
   const int n_my = (int)blockIdx.x < tiles ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 
   if (warp >= 8 && warp < MMA_WARP) {
-    // ---------------- producers: rows pw, pw + 3, pw + 6 (< 8) of every tile
+    // ---------------- producers: rows pw, pw + 3, pw + 6 (< 8) of every tile.
+    // The raw rows of tile k + 1 are loaded while tile k is transformed.
     const int pw = warp - 8;
     const int j = lane >> 1, half = lane & 1;
-    for (int k = 0; k < n_my; ++k) {
-      const int s = k % STAGES;
-      if (!um_wait(a_empty(s), ((k / STAGES) & 1) ^ 1, s_abort, p.err, 0xffffffffu)) break;
-      unsigned char* st = smem + OFF_STAGES + s * STAGE_BYTES;
+    constexpr int PR = (ROWS + PROD_WARPS - 1) / PROD_WARPS;   // rows per producer warp (3)
+    const bool key = p.role == VQKV_ROLE_K;
+    const float4 s4 = key ? *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane)
+                          : make_float4(1.f, 1.f, 1.f, 1.f);
+    uint2 raw[PR];
+    int pos_t[PR];   // cache position of the row, or -1 (no row / out of range)
+    auto fetch = [&](int k) {
       const int gt = (int)blockIdx.x + k * (int)gridDim.x;
-#pragma unroll 1
-      for (int r = pw; r < ROWS; r += PROD_WARPS) {
-        const int row = gt * ROWS + r, m = 16 * r + j;
-        int flag = F_SKIP;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < rows) {
+#pragma unroll
+      for (int i = 0; i < PR; ++i) {
+        const int r = pw + PROD_WARPS * i, row = gt * ROWS + r;
+        pos_t[i] = -1;
+        raw[i] = make_uint2(0u, 0u);
+        if (r < ROWS && row < rows) {
           const int b = row / p.n_rows, n = row - b * p.n_rows;
           const int t = p.pos[b] + n;
           if (t < 0 || t >= p.cap_len) {
             if (lane == 0 && p.err) atomicOr(p.err, VQKV_DEVERR_POSITION);
           } else {
-            transform_row(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim, key_s(p, kvh), lane, x);
-            flag = F_OK;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (!(fabsf(x[i]) < 32768.f)) flag = F_EXHAUSTIVE;   // beyond fp16 screening (or not finite)
+            pos_t[i] = t;
+            raw[i] = *reinterpret_cast<const uint2*>(p.x + (((size_t)b * p.Hkv + kvh) * p.n_rows + n) * kHeadDim +
+                                                     4 * lane);
           }
         }
-        if (flag == F_SKIP) x[0] = x[1] = x[2] = x[3] = 0.f;
+      }
+    };
+    if (n_my > 0) fetch(0);
+    for (int k = 0; k < n_my; ++k) {
+      uint2 cur[PR];
+      int cur_t[PR];
+#pragma unroll
+      for (int i = 0; i < PR; ++i) cur[i] = raw[i], cur_t[i] = pos_t[i];
+      if (k + 1 < n_my) fetch(k + 1);
+      const int s = k % STAGES;
+      if (!um_wait(a_empty(s), ((k / STAGES) & 1) ^ 1, s_abort, p.err, 0xffffffffu)) break;
+      unsigned char* st = smem + OFF_STAGES + s * STAGE_BYTES;
+#pragma unroll
+      for (int i = 0; i < PR; ++i) {
+        const int r = pw + PROD_WARPS * i;
+        if (r >= ROWS) break;
+        const int m = 16 * r + j;
+        int flag = F_SKIP;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (cur_t[i] >= 0) {
+          transform_loaded(cur[i], key, s4, lane, x);
+          flag = F_OK;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (!(fabsf(x[e]) < 32768.f)) flag = F_EXHAUSTIVE;   // beyond fp16 screening (or not finite)
+        }
         uint32_t hi01, lo01, hi23, lo23;
         split_half2(x[0], x[1], hi01, lo01);
         split_half2(x[2], x[3], hi23, lo23);
@@ -658,6 +685,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
           reinterpret_cast<float*>(st + ST_NORM)[m] = nx;
           reinterpret_cast<int*>(st + ST_FLAG)[m] = flag;
         }
+        if (lane == 0) reinterpret_cast<int*>(st + ST_POS)[r] = cur_t[i];
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -709,18 +737,19 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
     for (int k = wg; k < n_my; k += 2, ++it) {
       const float inf = __int_as_float(0x7f800000);
       float B1 = inf, B2 = inf, B3 = inf;
-      int G1 = 0, G2 = 0;
-      auto group = [&](const float (&v)[32], int gid) {
-        float g = fmin3(v[0], v[1], v[2]);
+      // group minimum (a min3 tree, depth 4) with the group id in its 7 low
+      // mantissa bits, then the three smallest so far: the packing moves a
+      // value by less than 2^-16 of itself, which the margin below covers
+      auto group = [&](const float (&v)[32], uint32_t gid) {
+        float t[10];
 #pragma unroll
-        for (int i = 3; i < 31; i += 2) g = fmin3(g, v[i], v[i + 1]);
-        g = fminf(g, v[31]);
-        const bool p1 = g < B1, p2 = g < B2;
-        B3 = fminf(B3, fmaxf(B2, g));
-        B2 = fminf(B2, fmaxf(B1, g));
-        B1 = fminf(B1, g);
-        G2 = p1 ? G1 : (p2 ? gid : G2);
-        G1 = p1 ? gid : G1;
+        for (int i = 0; i < 10; ++i) t[i] = fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+        const float g = fminf(fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], t[5]), fmin3(t[6], t[7], t[8])),
+                              fmin3(t[9], v[30], v[31]));
+        const float gp = __uint_as_float((__float_as_uint(g) & ~0x7Fu) | gid);
+        B3 = fminf(B3, fmaxf(B2, gp));
+        B2 = fminf(B2, fmaxf(B1, gp));
+        B1 = fminf(B1, gp);
       };
       bool ok = true;
       for (int q = 0; q < CHUNKS; ++q) {
@@ -734,16 +763,16 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         tmem_ld32(col, v);
         tmem_ld32(col + 32, u);
         tmem_wait_ld();
-        group(v, 4 * q);
-        group(u, 4 * q + 1);
+        group(v, 4u * q);
+        group(u, 4u * q + 1u);
         tmem_ld32(col + 64, v);
         tmem_ld32(col + 96, u);
         tmem_wait_ld();
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(t_empty(wg, bsel));
-        group(v, 4 * q + 2);
-        group(u, 4 * q + 3);
+        group(v, 4u * q + 2u);
+        group(u, 4u * q + 3u);
       }
       if (!ok) break;
       const int s = k % STAGES;
@@ -757,15 +786,19 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = b.x, xv[5] = b.y, xv[6] = b.z, xv[7] = b.w;
       }
       const float eps = screen_eps(sqrtf(reinterpret_cast<const float*>(st + ST_NORM)[ml]), Cmax);
-      const float thr = B1 + 2.f * eps;
+      // a group can hold a candidate within 2 eps of the best when its packed
+      // minimum is within 2 eps plus both packing errors (< 2^-16 of each
+      // value) of the packed best
+      auto near = [&](float X) { return X <= B1 + 2.f * eps + 3.0517578125e-5f * (fabsf(B1) + fabsf(X)); };
+      const int G1 = (int)(__float_as_uint(B1) & 0x7Fu), G2 = (int)(__float_as_uint(B2) & 0x7Fu);
       float dex = __int_as_float(0x7f800000), dsec = dex;
       int cex = 0x7fffffff;
-      if (flag == F_EXHAUSTIVE || (flag == F_OK && B3 <= thr)) {
+      if (flag == F_EXHAUSTIVE || (flag == F_OK && near(B3))) {
         for (int c = 0; c < 4096; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
       } else if (flag == F_OK) {
 #pragma unroll 4
         for (int c = GROUP * G1; c < GROUP * G1 + GROUP; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
-        if (B2 <= thr) {
+        if (near(B2)) {
 #pragma unroll 4
           for (int c = GROUP * G2; c < GROUP * G2 + GROUP; ++c)
             exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
@@ -776,8 +809,8 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       const int hi = __shfl_down_sync(0xffffffffu, cex, 8);
       if (j < 8 && flag != F_SKIP) {
         const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
-        const int b = row / p.n_rows, n = row - b * p.n_rows;
-        const int t = p.pos[b] + n;
+        const int b = row / p.n_rows;
+        const int t = reinterpret_cast<const int*>(st + ST_POS)[r];
         uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
         if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, j), cex, hi);
       }
