@@ -420,36 +420,40 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 
 // Many rows of 1.5-bit encode on the fifth-generation tensor cores.  A tile
 // is 8 rows = 128 (row, subvector) pairs, the M of one tcgen05 MMA; the 4096
-// centroids are 32 chunks of N = 128.  Per chunk two MMAs accumulate into
-// tensor memory
-//   D[m][c] = [x_hi, 1, 1] . [-2c, |c|^2_hi, |c|^2_lo] + [x_lo] . [-2c]
-// = |c|^2 - 2 x'_j . c to about 2^-22 relative (the screened distance less
-// the subvector's own |x'_j|^2), with A (hi and lo parts of the transformed
-// rows) and B (the [-2c, |c|^2_hi, |c|^2_lo] table of all 4096 centroids) in
-// shared memory behind matrix descriptors.
+// centroids are 32 chunks of N = 128.  One MMA per chunk writes to tensor
+// memory
+//   D[m][c] = [x_hi, 1, 1] . [-2c, |c|^2_hi, |c|^2_lo] = |c|^2 - 2 x_hi . c,
+// the screened distance less the subvector's own |x'_j|^2, with x_hi the fp16
+// rounding of the transformed subvector (A) and the [-2c, |c|^2_hi, |c|^2_lo]
+// table of all 4096 centroids (B) in shared memory behind matrix
+// descriptors.  Its error is bounded by screen_eps_hi.  (A second MMA with
+// the fp16 remainder of x' would tighten the bound but doubles the shared
+// memory and tensor memory traffic, which bound this kernel.)
 //
-// Roles (12 warps, one CTA per SM, persistent over the KV head's tiles; 12
-// warps leave each SM sub-partition 3 warps, so up to 168 registers a thread):
+// Roles (13 warps, one CTA per SM, persistent over the KV head's tiles; up
+// to 128 registers a thread):
 //   warps 8-10   producers: transform rows pw, pw + 3, pw + 6 (< 8) of each
 //                tile (smoothing + Hadamard in double-float for keys), write
-//                A_hi / A_lo, x' and |x'_j|^2 into one of 4 stages;
-//   warp 11      allocates 512 tensor-memory columns and, from one thread,
-//                issues the MMAs: chunk by chunk, alternating between the two
-//                epilogue warpgroups' tiles, into two 128-column buffers per
-//                warpgroup;
+//                A, x' and |x'_j|^2 into one of 4 stages;
+//   warps 11, 12 one thread each issues the MMAs of one epilogue warpgroup,
+//                chunk by chunk into that warpgroup's two 128-column
+//                tensor-memory buffers (warp 11 also allocates the 512
+//                columns); separate issuers keep one warpgroup's wait for a
+//                free buffer from holding up the other's MMAs;
 //   warps 0-3, 4-7  two epilogue warpgroups taking alternate tiles: thread m
 //                owns tensor-memory lane m, i.e. subvector m % 16 of row m / 16.
 // The epilogue does not rank candidates one by one: per group of 32
 // consecutive centroids it takes the group minimum (three-input min), and
-// keeps the three smallest group minima B1 <= B2 <= B3 with the groups of the
-// first two.  A centroid can be the exact nearest only if its screened
-// distance is within 2 eps of B1 (screen_eps bounds the screening error), so
-// with B3 above that margin every candidate lies in group G1 or, if B2 is
-// within it, G2: those 32 or 64 centroids are re-ranked with exact fp32
-// direct differences (as exact_d8), the lowest index winning ties.  With B3
-// inside the margin, or a row whose transformed values do not fit fp16, the
-// subvector is searched exhaustively.  Every decision therefore equals the
-// exhaustive fp32 search's.
+// keeps the four smallest group minima B1 <= B2 <= B3 <= B4, each carrying
+// its group id.  A centroid can be the exact nearest only if its screened
+// distance is within 2 eps of B1, so with B4 above that margin every
+// candidate lies in G1, G2 or G3 (the latter two only when B2, B3 are within
+// the margin): those groups are re-ranked with exact fp32 direct differences
+// (as exact_d8), the lowest index winning ties; G1 by each lane, the rarer
+// G2 / G3 by the whole warp, one lane's group at a time.  With B4 inside the
+// margin, or a row whose transformed values do not fit fp16, the warp
+// searches that subvector exhaustively.  Every decision therefore equals
+// the exhaustive fp32 search's.
 //
 // Every wait is bounded: a wait that runs out sets VQKV_DEVERR_TIMEOUT (when
 // the caller passed an error word) and an abort flag that ends every role's
@@ -460,28 +464,42 @@ constexpr int ROWS = 8;                       // rows per tile
 constexpr int M = ROWS * 16;                  // 128 MMA rows: (row, subvector)
 constexpr int N = 128;                        // centroids per MMA
 constexpr int CHUNKS = 4096 / N;              // 32
+constexpr int NBUF = 2;                       // tensor-memory buffers per epilogue warpgroup
 constexpr int GROUP = 32;                     // centroids per group minimum
 constexpr int STAGES = 4;
 constexpr int PROD_WARPS = 3;
-constexpr int MMA_WARP = 8 + PROD_WARPS;      // 11
-constexpr int THREADS = (MMA_WARP + 1) * 32;  // 384
+constexpr int MMA_WARP = 8 + PROD_WARPS;      // 11 (warpgroup 0's issuer; 12: warpgroup 1's)
+constexpr int THREADS = (MMA_WARP + 2) * 32;  // 416
 constexpr int TABLE_BYTES = 4096 * 32;        // B: 4096 centroids x 16 fp16
 constexpr int A_BYTES = M * 32;               // one A tile: 128 x 16 fp16
-constexpr int ST_AHI = 0, ST_ALO = A_BYTES, ST_X = 2 * A_BYTES;
+constexpr int ST_A = 0, ST_X = A_BYTES;
 constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + M * 4, ST_POS = ST_FLAG + M * 4;
 constexpr int STAGE_BYTES = ST_POS + 16 * 4;  // + cache position of each row
 constexpr int OFF_STAGES = TABLE_BYTES;
 constexpr int OFF_BAR = OFF_STAGES + STAGES * STAGE_BYTES;
-constexpr int NBAR = 2 * STAGES + 8 + 1;      // A full / empty, tensor-memory full / empty, MMAs done
+constexpr int NBAR = 2 * STAGES + 4 * NBUF + 2;   // A full / empty, tensor-memory full / empty, MMAs done x 2
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag, max centroid norm
 constexpr size_t SMEM = OFF_MISC + 16;
-constexpr uint32_t TMEM_COLS = 512;           // 2 warpgroups x 2 buffers x N
+constexpr uint32_t TMEM_COLS = 512;           // 2 warpgroups x NBUF buffers x N
+static_assert(2 * NBUF * N <= (int)TMEM_COLS && CHUNKS % NBUF == 0 && N % GROUP == 0, "tensor-memory plan");
 constexpr uint32_t MAX_POLLS = 1u << 22;
 // row flags
 constexpr int F_OK = 0, F_EXHAUSTIVE = 1, F_SKIP = 2;
 }  // namespace um
 static_assert(um::SMEM <= 227 * 1024, "UMMA encode shared memory");
 static_assert(um::STAGE_BYTES % 16 == 0 && um::OFF_BAR % 8 == 0, "alignment");
+
+// Bound on |screened - exact| for one candidate of the single-MMA screen:
+// the fp16 rounding of x' leaves |x' - x_hi| <= 2^-11 |x'| per channel
+// (normal range; subnormal steps are covered by the absolute term), so
+// |2 (x' - x_hi) . c| <= 2^-10 |x'| |c|; the |c|^2 split, the tensor-core
+// fp32 accumulation and the exact search's own roundings are covered as in
+// screen_eps.
+__device__ __forceinline__ float screen_eps_hi(float xnorm, float cmax) {
+  const float sc = xnorm + cmax;
+  return 9.765625e-4f * xnorm * cmax + 4.76837158203125e-7f * cmax * cmax + 1e-6f * (cmax + 1.f) +
+         1.5e-5f * sc * sc;
+}
 
 // Bounded wait on an mbarrier phase by every lane of a warp (or one thread:
 // pass a one-lane mask): false, with the abort flag set, when it runs out
@@ -507,21 +525,23 @@ __device__ __forceinline__ bool um_wait(uint32_t mbar, uint32_t parity, volatile
 // Exact fp32 distance of subvector x to centroid c read from the B table
 // (-2c as fp16, halved exactly): direct differences in channel order, one
 // rounding per operation, the same arithmetic as exact_d8.
+// x_i - c_i is formed as fma(0.5, h_i, x_i) with h_i = -2 c_i: 0.5 h_i = -c_i
+// exactly, so it is the same correctly rounded difference.
 __device__ __forceinline__ float exact_d8_umma(const float (&x)[8], const unsigned char* table, int c) {
   const uint4 raw = *reinterpret_cast<const uint4*>(table + umma_kmajor_offset((uint32_t)c, 0));
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  float y[8];
+  float h[8];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const __half2 h = *reinterpret_cast<const __half2*>(&w[t]);
-    y[2 * t] = -0.5f * __low2float(h);
-    y[2 * t + 1] = -0.5f * __high2float(h);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+    h[2 * t] = f.x;
+    h[2 * t + 1] = f.y;
   }
-  float e = __fsub_rn(x[0], y[0]);
+  float e = __fmaf_rn(0.5f, h[0], x[0]);
   float d = __fmul_rn(e, e);
 #pragma unroll
   for (int i = 1; i < 8; ++i) {
-    e = __fsub_rn(x[i], y[i]);
+    e = __fmaf_rn(0.5f, h[i], x[i]);
     d = __fmaf_rn(e, e, d);
   }
   return d;
@@ -539,6 +559,27 @@ __device__ __forceinline__ void exact_push(float d, int c, float& dex, int& cex,
   }
 }
 
+// Merges another disjoint candidate set's (best, index, second) into a state.
+__device__ __forceinline__ void exact_merge(float od, int oc, float os, float& dex, int& cex, float& dsec) {
+  if (od < dex || (od == dex && oc < cex)) {
+    dsec = fminf(dex, os);
+    dex = od;
+    cex = oc;
+  } else {
+    dsec = fminf(dsec, od);
+  }
+}
+
+// The warp's combined (best, index, second) over the lanes' states, in every lane.
+__device__ __forceinline__ void exact_warp_reduce(float& d, int& c, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float od = __shfl_xor_sync(0xffffffffu, d, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+    const int oc = __shfl_xor_sync(0xffffffffu, c, o);
+    exact_merge(od, oc, os, d, c, s);
+  }
+}
+
 __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const EncodeParams p) {
   using namespace um;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -548,9 +589,9 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
   const uint32_t bar = sbase + OFF_BAR;
   auto a_full = [&](int s) { return bar + 8u * s; };
   auto a_empty = [&](int s) { return bar + 8u * (STAGES + s); };
-  auto t_full = [&](int wg, int b) { return bar + 8u * (2 * STAGES + 2 * wg + b); };
-  auto t_empty = [&](int wg, int b) { return bar + 8u * (2 * STAGES + 4 + 2 * wg + b); };
-  const uint32_t done_bar = bar + 8u * (2 * STAGES + 8);
+  auto t_full = [&](int wg, int b) { return bar + 8u * (2 * STAGES + NBUF * wg + b); };
+  auto t_empty = [&](int wg, int b) { return bar + 8u * (2 * STAGES + 2 * NBUF + NBUF * wg + b); };
+  auto done_bar = [&](int wg) { return bar + 8u * (2 * STAGES + 4 * NBUF + wg); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   float* s_cmax = reinterpret_cast<float*>(smem + OFF_MISC + 8);
@@ -561,11 +602,12 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       mbar_init(a_empty(s), 4);
     }
     for (int wg = 0; wg < 2; ++wg)
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < NBUF; ++b) {
         mbar_init(t_full(wg, b), 1);
         mbar_init(t_empty(wg, b), 4);
       }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar(0), 1);
+    mbar_init(done_bar(1), 1);
     *s_abort = 0;
     *s_cmax = 0.f;
     mbar_init_fence();
@@ -668,15 +710,10 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
           for (int e = 0; e < 4; ++e)
             if (!(fabsf(x[e]) < 32768.f)) flag = F_EXHAUSTIVE;   // beyond fp16 screening (or not finite)
         }
-        uint32_t hi01, lo01, hi23, lo23;
-        split_half2(x[0], x[1], hi01, lo01);
-        split_half2(x[2], x[3], hi23, lo23);
         const uint32_t off = umma_kmajor_offset((uint32_t)m, 4u * half);
-        *reinterpret_cast<uint2*>(st + ST_AHI + off) = make_uint2(hi01, hi23);
-        *reinterpret_cast<uint2*>(st + ST_ALO + off) = make_uint2(lo01, lo23);
-        *reinterpret_cast<uint2*>(st + ST_AHI + off + 128) =
+        *reinterpret_cast<uint2*>(st + ST_A + off) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+        *reinterpret_cast<uint2*>(st + ST_A + off + 128) =
             make_uint2(half == 0 ? pack_half2(1.f, 1.f) : 0u, 0u);   // picks |c|^2 hi + lo
-        *reinterpret_cast<uint2*>(st + ST_ALO + off + 128) = make_uint2(0u, 0u);
         *reinterpret_cast<float4*>(st + ST_X + (r * kHeadDim + 4 * lane) * 4) = make_float4(x[0], x[1], x[2], x[3]);
         float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
         nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2
@@ -691,40 +728,32 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       __syncwarp();
       if (lane == 0) mbar_arrive(a_full(s));
     }
-  } else if (warp == MMA_WARP) {
-    // ---------------- one thread issues every MMA
+  } else if (warp >= MMA_WARP) {
+    // ---------------- one thread per epilogue warpgroup issues its MMAs
+    const int wg = warp - MMA_WARP;
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16_f32(M, N);
       bool ok = true;
-      for (int i = 0; ok && 2 * i < n_my; ++i) {
-        const int nwg = 2 * i + 1 < n_my ? 2 : 1;
-        uint64_t dhi[2], dlo[2];
-        for (int wg = 0; wg < nwg && ok; ++wg) {
-          const int k = 2 * i + wg, s = k % STAGES;
-          ok = um_wait(a_full(s), (k / STAGES) & 1, s_abort, p.err, 1u);
-          const uint32_t st = sbase + OFF_STAGES + s * STAGE_BYTES;
-          dhi[wg] = umma_desc_kmajor(st + ST_AHI);
-          dlo[wg] = umma_desc_kmajor(st + ST_ALO);
-        }
+      int it = 0;
+      for (int k = wg; ok && k < n_my; k += 2, ++it) {
+        const int s = k % STAGES;
+        ok = um_wait(a_full(s), (k / STAGES) & 1, s_abort, p.err, 1u);
+        const uint64_t dA = umma_desc_kmajor(sbase + OFF_STAGES + s * STAGE_BYTES + ST_A);
         tcgen05_after_sync();
         for (int q = 0; ok && q < CHUNKS; ++q) {
-          const uint64_t dB = umma_desc_kmajor(sbase + (uint32_t)q * (N * 32));
-          const int bsel = q & 1;
-          const uint32_t use = (uint32_t)(i * (CHUNKS / 2) + (q >> 1));
-          for (int wg = 0; wg < nwg; ++wg) {
-            ok = um_wait(t_empty(wg, bsel), (use & 1) ^ 1, s_abort, p.err, 1u);
-            if (!ok) break;
-            tcgen05_after_sync();
-            const uint32_t d = tmem + (uint32_t)((2 * wg + bsel) * N);
-            umma_f16(d, dhi[wg], dB, idesc, 0u);
-            umma_f16(d, dlo[wg], dB, idesc, 1u);
-            umma_commit(t_full(wg, bsel));
-          }
+          const int bsel = q % NBUF;
+          const uint32_t use = (uint32_t)(it * (CHUNKS / NBUF) + q / NBUF);
+          ok = um_wait(t_empty(wg, bsel), (use & 1) ^ 1, s_abort, p.err, 1u);
+          if (!ok) break;
+          tcgen05_after_sync();
+          umma_f16(tmem + (uint32_t)((NBUF * wg + bsel) * N), dA, umma_desc_kmajor(sbase + (uint32_t)q * (N * 32)),
+                   idesc, 0u);
+          umma_commit(t_full(wg, bsel));
         }
       }
       // every MMA issued has completed before the tensor memory is freed
-      umma_commit(done_bar);
-      um_wait(done_bar, 0, s_abort, p.err, 1u);
+      umma_commit(done_bar(wg));
+      um_wait(done_bar(wg), 0, s_abort, p.err, 1u);
     }
     __syncwarp();
   } else {
@@ -736,9 +765,9 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
     int it = 0;
     for (int k = wg; k < n_my; k += 2, ++it) {
       const float inf = __int_as_float(0x7f800000);
-      float B1 = inf, B2 = inf, B3 = inf;
+      float B1 = inf, B2 = inf, B3 = inf, B4 = inf;
       // group minimum (a min3 tree, depth 4) with the group id in its 7 low
-      // mantissa bits, then the three smallest so far: the packing moves a
+      // mantissa bits, then the four smallest so far: the packing moves a
       // value by less than 2^-16 of itself, which the margin below covers
       auto group = [&](const float (&v)[32], uint32_t gid) {
         float t[10];
@@ -747,32 +776,37 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         const float g = fminf(fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], t[5]), fmin3(t[6], t[7], t[8])),
                               fmin3(t[9], v[30], v[31]));
         const float gp = __uint_as_float((__float_as_uint(g) & ~0x7Fu) | gid);
+        B4 = fminf(B4, fmaxf(B3, gp));
         B3 = fminf(B3, fmaxf(B2, gp));
         B2 = fminf(B2, fmaxf(B1, gp));
         B1 = fminf(B1, gp);
       };
       bool ok = true;
       for (int q = 0; q < CHUNKS; ++q) {
-        const int bsel = q & 1;
-        const uint32_t use = (uint32_t)(it * (CHUNKS / 2) + (q >> 1));
+        const int bsel = q % NBUF;
+        const uint32_t use = (uint32_t)(it * (CHUNKS / NBUF) + q / NBUF);
         ok = um_wait(t_full(wg, bsel), use & 1, s_abort, p.err, 0xffffffffu);
         if (!ok) break;
         tcgen05_after_sync();
-        const uint32_t col = t_lane + (uint32_t)((2 * wg + bsel) * N);
-        float v[32], u[32];
-        tmem_ld32(col, v);
-        tmem_ld32(col + 32, u);
+        const uint32_t col = t_lane + (uint32_t)((NBUF * wg + bsel) * N);
+        // four loads of 32 columns, each in flight while the previous group
+        // is reduced; the buffer is handed back once the last is in registers
+        float va[32], vb[32];
+        tmem_ld32(col, va);
         tmem_wait_ld();
-        group(v, 4u * q);
-        group(u, 4u * q + 1u);
-        tmem_ld32(col + 64, v);
-        tmem_ld32(col + 96, u);
+        tmem_ld32(col + 32, vb);
+        group(va, 4u * q);
+        tmem_wait_ld();
+        tmem_ld32(col + 64, va);
+        group(vb, 4u * q + 1u);
+        tmem_wait_ld();
+        tmem_ld32(col + 96, vb);
+        group(va, 4u * q + 2u);
         tmem_wait_ld();
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(t_empty(wg, bsel));
-        group(v, 4u * q + 2u);
-        group(u, 4u * q + 3u);
+        group(vb, 4u * q + 3u);
       }
       if (!ok) break;
       const int s = k % STAGES;
@@ -785,24 +819,58 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         const float4 b = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j + 4) * 4);
         xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = b.x, xv[5] = b.y, xv[6] = b.z, xv[7] = b.w;
       }
-      const float eps = screen_eps(sqrtf(reinterpret_cast<const float*>(st + ST_NORM)[ml]), Cmax);
+      const float eps = screen_eps_hi(sqrtf(reinterpret_cast<const float*>(st + ST_NORM)[ml]), Cmax);
       // a group can hold a candidate within 2 eps of the best when its packed
       // minimum is within 2 eps plus both packing errors (< 2^-16 of each
       // value) of the packed best
       auto near = [&](float X) { return X <= B1 + 2.f * eps + 3.0517578125e-5f * (fabsf(B1) + fabsf(X)); };
-      const int G1 = (int)(__float_as_uint(B1) & 0x7Fu), G2 = (int)(__float_as_uint(B2) & 0x7Fu);
+      const bool exh = flag == F_EXHAUSTIVE || (flag == F_OK && near(B4));
+      const bool need2 = flag == F_OK && !exh && near(B2), need3 = flag == F_OK && !exh && near(B3);
+      const int G1 = (int)(__float_as_uint(B1) & 0x7Fu);
       float dex = __int_as_float(0x7f800000), dsec = dex;
       int cex = 0x7fffffff;
-      if (flag == F_EXHAUSTIVE || (flag == F_OK && near(B3))) {
-        for (int c = 0; c < 4096; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
-      } else if (flag == F_OK) {
-#pragma unroll 4
-        for (int c = GROUP * G1; c < GROUP * G1 + GROUP; ++c) exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
-        if (near(B2)) {
-#pragma unroll 4
-          for (int c = GROUP * G2; c < GROUP * G2 + GROUP; ++c)
-            exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
+      // group G1 by each lane; lane l visits its group's centroids from the
+      // (l % 8)-th on: a centroid's 16 bytes sit in bank group c % 8, so the
+      // 32 lanes spread over all 8 bank groups at every step
+      {
+        const int rot = lane & 7;
+#pragma unroll 8
+        for (int i = 0; i < GROUP; ++i) {
+          const int c = GROUP * G1 + ((i + rot) & (GROUP - 1));
+          exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
         }
+      }
+      // groups G2 / G3 (few lanes) by the whole warp, one (lane, group) at a
+      // time, one centroid per lane; exhaustive searches likewise
+      const unsigned m2 = __ballot_sync(0xffffffffu, need2), m3 = __ballot_sync(0xffffffffu, need3);
+      unsigned mx = __ballot_sync(0xffffffffu, exh);
+      for (int pass = 0; pass < 2; ++pass) {
+        unsigned mset = pass == 0 ? m2 : m3;
+        const float Bp = pass == 0 ? B2 : B3;
+        while (mset) {
+          const int src = __ffs(mset) - 1;
+          mset &= mset - 1;
+          const int g = __shfl_sync(0xffffffffu, (int)(__float_as_uint(Bp) & 0x7Fu), src);
+          float xs[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
+          float d = exact_d8_umma(xs, table, GROUP * g + lane), sd = __int_as_float(0x7f800000);
+          int c = GROUP * g + lane;
+          exact_warp_reduce(d, c, sd);
+          if (lane == src) exact_merge(d, c, sd, dex, cex, dsec);
+        }
+      }
+      while (mx) {
+        const int src = __ffs(mx) - 1;
+        mx &= mx - 1;
+        float xs[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
+        float d = __int_as_float(0x7f800000), sd = d;
+        int c = 0x7fffffff;
+        for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_umma(xs, table, cc), cc, d, c, sd);
+        exact_warp_reduce(d, c, sd);
+        if (lane == src) dex = d, cex = c, dsec = sd;   // every candidate: replaces the group search
       }
       count_near_ties(p.near_tie, flag != F_SKIP && is_near_tie(dex, dsec), lane, 0xffffffffu);
       // lane (row r, subvector j < 8) stores the pair (j, j + 8) of its row
