@@ -722,6 +722,25 @@ def encode_prefill_bench(w, dev, reps=3):
                                               "near_ties": int(cnt.item()),
                                               "codes": w.B * w.Hkv * w.prefill * (128 // wm.d_sub)}
             del x
+        if mode == synth.MODE_VQ15:
+            # ALU floor: one fp32 compare per (subvector, candidate) on every lane;
+            # tensor floor: the screening MMAs (K = 16 per candidate) at the measured bf16/fp16 rate
+            props = torch.cuda.get_device_properties(dev)
+            try:
+                peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+            except (OSError, ValueError):
+                peaks = {}
+            mhz = peaks.get("sm_max_mhz") or 2070.0
+            cand = w.B * w.Hkv * w.prefill * (128 // wm.d_sub) * wm.entries
+            alu_peak = props.multi_processor_count * 128 * mhz * 1e6
+            tflops = peaks.get("bf16_tflops") or 1900.0
+            best_ms = min(out["K"]["ms"], out["V"]["ms"])
+            out["roofline"] = {"bound": "alu", "unit": "candidates/s", "achieved": cand / (best_ms * 1e-3),
+                               "peak": alu_peak, "frac": cand / (best_ms * 1e-3) / alu_peak,
+                               "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 lanes x {mhz:.0f} MHz, "
+                                              "one compare per candidate",
+                               "tensor_floor_ms": 2 * cand * 16 / (tflops * 1e12) * 1e3,
+                               "alu_floor_ms": cand / alu_peak * 1e3}
         res["2-bit" if mode == 0 else "1.5-bit"] = out
     return res
 
