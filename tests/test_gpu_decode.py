@@ -254,3 +254,65 @@ def test_full_size_sampled_heads(cfg):
     for b, h in heads:
         e = vo.o_error(o[b, h], ref[b, h])
         assert e <= H.O_TOL, (b, h, e)
+
+
+# ------------------------------------------------------------ flat plan (batches)
+
+@pytest.mark.parametrize("mode", [0, 2, 3, 4])
+def test_flat_plan_ragged_batch(mode):
+    """Batches use the flat plan: every CTA of a KV head takes an equal share
+    of all sequences' tiles, so a share can start and end inside sequences
+    and cover several short ones.  Lengths include 0, 1, a tile edge and the
+    capacity."""
+    r = np.random.default_rng(40 + mode)
+    B, Hq, Hkv, cap = 37, 8, 2, 320
+    lens = r.integers(0, cap + 1, size=B)
+    lens[:5] = [0, 1, 16, cap, 0]
+    q, kc, vc, kcb, vcb, s = random_case(mode, B, Hq, Hkv, lens, cap, seed=400 + mode)
+    kbuf, vbuf = H.pack_cache_role(mode, 0, kc, cap), H.pack_cache_role(mode, 1, vc, cap)
+    o = H.gpu_decode(mode, q, kbuf, vbuf, lens, kcb, vcb, s, cap, cap)
+    ref = oracle_o(q, kc, vc, kcb, vcb, s, lens)
+    assert np.isfinite(o).all()
+    assert np.all(o[lens == 0] == 0)
+    assert vo.o_error(o, ref).max() <= H.O_TOL
+    # the split plan (explicit split count) gives the same O up to fp32 regrouping
+    o2 = H.gpu_decode(mode, q, kbuf, vbuf, lens, kcb, vcb, s, cap, cap, num_splits=3)
+    assert vo.o_error(o2, ref).max() <= H.O_TOL
+
+
+def test_flat_plan_fewer_tiles_than_ctas():
+    """Three one-token sequences: fewer super-tiles than CTAs per KV head."""
+    q, kc, vc, kcb, vcb, s = random_case(0, 3, 4, 1, [1, 2, 1], 16, seed=41)
+    kbuf, vbuf = H.pack_cache_role(0, 0, kc, 16), H.pack_cache_role(0, 1, vc, 16)
+    o = H.gpu_decode(0, q, kbuf, vbuf, [1, 2, 1], kcb, vcb, s, 16, 16)
+    ref = oracle_o(q, kc, vc, kcb, vcb, s, [1, 2, 1])
+    assert vo.o_error(o, ref).max() <= H.O_TOL
+
+
+def test_flat_plan_workspace_is_reusable():
+    """Tickets of every sequence are back to zero after a flat-plan call."""
+    import torch
+    lens = [500, 0, 33, 1000, 7]
+    q, kc, vc, kcb, vcb, s = random_case(0, 5, 8, 2, lens, 1024, seed=42)
+    kbuf, vbuf = H.pack_cache_role(0, 0, kc, 1024), H.pack_cache_role(0, 1, vc, 1024)
+    ws = _lib.decode_workspace(0, 5, 8, 2, 1024, 1024)
+    a = H.gpu_decode(0, q, kbuf, vbuf, lens, kcb, vcb, s, 1024, 1024, workspace=ws)
+    b = H.gpu_decode(0, q, kbuf, vbuf, lens, kcb, vcb, s, 1024, 1024, workspace=ws)
+    assert np.array_equal(a, b)
+    t = ws[256:256 + 4 * 5 * 2].view(torch.int32).cpu().numpy()
+    assert np.all(t == 0)
+    assert vo.o_error(a, oracle_o(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
+
+
+def test_batch_beyond_flat_limit_uses_the_split_plan():
+    """More sequences than the flat plan takes (1024): the split plan."""
+    B = 1100
+    r = np.random.default_rng(43)
+    lens = r.integers(0, 33, size=B)
+    q, kc, vc, kcb, vcb, s = random_case(0, B, 4, 1, lens, 32, seed=43)
+    kbuf, vbuf = H.pack_cache_role(0, 0, kc, 32), H.pack_cache_role(0, 1, vc, 32)
+    o = H.gpu_decode(0, q, kbuf, vbuf, lens, kcb, vcb, s, 32, 32)
+    heads = [(int(b), h) for b in r.integers(B, size=20) for h in range(4)]
+    ref = vo.decode_attention(q, kc, vc, kcb, vcb, s, lens, heads=heads)
+    for b, h in heads:
+        assert vo.o_error(o[b, h], ref[b, h]) <= H.O_TOL

@@ -116,7 +116,7 @@ size_t decode_ticket_region_bytes(int B, int Hkv);
 namespace {
 
 struct DecodePlan {
-  int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1, cgroups = 1;
+  int n_splits = 1, tps = 1, bpg = 1, n_bgroups = 1, cgroups = 1, flat = 0;
   size_t tickets_off = 0, partials_off = 0, ws_bytes = 0;
 };
 
@@ -151,6 +151,27 @@ vqkv_status plan_decode(const PlanInput* a, DecodePlan* pl) {
   int bpg = 1;
   if (a->mode == VQKV_MODE_VQ15 && (long long)B * a->Hkv < slots) bpg = B;
   const int cgroups = (g * a->M + 7) / 8;   // CTAs per (sequence group, KV head, split)
+  // Flat plan for batches on the tile-ring decode: one wave of CTAs per (KV
+  // head, column group), each taking an equal share of all sequences' tiles,
+  // balanced by the actual lengths on the device (ragged batches leave no CTA
+  // idle).  Explicit split counts keep the split plan.
+  const bool ring = a->mode == VQKV_MODE_VQ2 || a->mode == VQKV_MODE_VQ4 || a->mode == VQKV_MODE_VQ3 ||
+                    a->mode == VQKV_MODE_VQ125;
+  const long long super_max = (tiles_max + unit_tiles - 1) / unit_tiles;
+  if (ring && a->num_splits == 0 && a->B > 1 && a->B <= kFlatMaxB && (long long)a->B * super_max < (1LL << 30)) {
+    const long long S = std::max<long long>(1, slots / ((long long)a->Hkv * cgroups));
+    pl->flat = 1;
+    pl->n_splits = (int)S;
+    pl->tps = 0;
+    pl->bpg = 1;
+    pl->n_bgroups = 1;
+    pl->cgroups = cgroups;
+    pl->tickets_off = kWsHeader;
+    pl->partials_off = decode_ticket_region_bytes(B, a->Hkv * cgroups);
+    pl->ws_bytes = pl->partials_off +
+                   sizeof(float) * (size_t)a->Hkv * (S + a->B - 1) * g * a->M * kPartialStride;
+    return VQKV_OK;
+  }
   const long long pairs = (long long)a->Hkv * ((B + bpg - 1) / bpg) * cgroups;
   // per-CTA prologue + merge in tile units
   const double setup_tiles = (a->mode == VQKV_MODE_VQ15) ? 24.0 : (a->mode == kModeFp16) ? 4.0 : 12.0;
@@ -353,6 +374,7 @@ vqkv_status decode_launch(const vqkv_decode_args* a, const vqkv_decode_append_ar
   p.tps = pl.tps;
   p.bpg = pl.bpg;
   p.defer_merge = pl.bpg > 1 ? 1 : 0;
+  p.flat = pl.flat;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(128.0f);
   p.qscale = scale * 1.4426950408889634f / std::sqrt(128.0f);
   if (ap != nullptr) {

@@ -117,11 +117,13 @@ constexpr int V15_Q_PITCH = 128;   // read once per sequence; a padded pitch mea
 constexpr int V2_APP_BYTES = V2_WARPS * 32 * (int)sizeof(Best);
 // Paged cache: the block ids of the CTA's token range, read once per sequence.
 constexpr int V2_BLK_CACHE = 512;
+// Flat plan (batches): per-sequence super-tile prefix sums, B <= kFlatMaxB.
 template <int MODE>
 struct V2Smem {
   static constexpr int APP_OFF = (V2Geo<MODE>::MBAR_OFF + V2_WARPS * V2_STAGES * 8 + 15) / 16 * 16;
   static constexpr int BLK_OFF = APP_OFF + V2_APP_BYTES;
-  static constexpr size_t BYTES = BLK_OFF + V2_BLK_CACHE * 4;
+  static constexpr int FLAT_OFF = BLK_OFF + V2_BLK_CACHE * 4;
+  static constexpr size_t BYTES = FLAT_OFF + (kFlatMaxB + 1 + 4) * 4;   // + T, S_eff, share bounds
 };
 constexpr size_t kV2Smem = V2Smem<VQKV_MODE_VQ2>::BYTES;
 constexpr size_t kV4Smem = V2Smem<VQKV_MODE_VQ4>::BYTES;
@@ -454,12 +456,46 @@ __device__ __noinline__ void append_rows(float4 xv, uint8_t* k_stream, uint8_t* 
   __syncthreads();
 }
 
+// Flat plan: s_pref[b] = super-tiles (TPI tiles of 16 tokens) of sequences
+// 0 .. b-1 at their clamped lengths, for b = 0 .. B.  All threads.
+template <int TPI>
+__device__ __forceinline__ void flat_prefix(const DecodeParams& p, int* s_pref) {
+  const int lane = threadIdx.x & 31;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const int L = min(max(p.seq_lens[b], 0), p.max_seq_len);   // (out-of-range lengths reported by load_len)
+    s_pref[b + 1] = ((L + V2_TILE - 1) / V2_TILE + TPI - 1) / TPI;
+  }
+  if (threadIdx.x == 0) s_pref[0] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {   // inclusive scan of s_pref[1..B], 32 entries per step
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int i = base + lane;
+      int v = i < p.B ? s_pref[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (i < p.B) s_pref[i + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// Flat plan: the CTA (of S_eff) whose share [T s / S_eff, T (s+1) / S_eff)
+// of the T super-tiles holds super-tile x.
+__device__ __forceinline__ int flat_cta_of(long long x, long long T, int S_eff) {
+  return (int)(((x + 1) * S_eff - 1) / T);
+}
+
 // Q: one query per sequence (kOneQuery: one limit, L, for every column),
 // several (kQueries: per-column causal limits, all columns in the CTA) or
 // several in column groups of up to 8, one CTA each (kQueryGroups).  PAGED:
 // tiles are found through the block table (at most two bulk copies per
 // step).
-template <int Q, bool PAGED, int MODE>
+template <int Q, bool PAGED, int MODE, bool FLAT>
 __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeParams p) {
   constexpr bool MULTI = Q != kOneQuery, GROUPS = Q == kQueryGroups;
   using G = V2Geo<MODE>;
@@ -504,7 +540,43 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
   grid_dependents_launch();
   uint32_t uses = 0;        // super-tiles this warp has taken through its ring (all sequences)
 
-  for (int b = b_begin; b < b_end; ++b) {
+  // Flat plan (batches of ragged sequences): the KV head's T super-tiles,
+  // all sequences in order, are cut into S_eff = min(n_splits, T) equal
+  // shares, CTA `split` taking [T split / S_eff, T (split+1) / S_eff); each
+  // overlap with a sequence is a piece, merged like a split.  Split 0 also
+  // writes the zero rows of empty sequences.
+  int* s_pref = reinterpret_cast<int*>(smem + Sm::FLAT_OFF);
+  int* s_flat = s_pref + kFlatMaxB + 1;   // T, S_eff, r0, r1 (read at piece boundaries only)
+  int b = b_begin, b_stop = b_end;
+  if (FLAT) {
+    flat_prefix<G::TPI>(p, s_pref);
+    const int T = s_pref[p.B], S_eff = min(p.n_splits, T);
+    b = p.B;
+    if (split < S_eff) {
+      const int r0 = (int)((long long)T * split / S_eff), r1 = (int)((long long)T * (split + 1) / S_eff);
+      if (threadIdx.x == 0) s_flat[0] = T, s_flat[1] = S_eff, s_flat[2] = r0, s_flat[3] = r1;
+      b = 0;
+      while (s_pref[b + 1] <= r0) ++b;   // the first sequence reaching into the share
+    }
+    b_stop = p.B;
+    if (split == 0) {
+      for (int i = threadIdx.x; i < p.B * nloc * kHeadDim; i += V2_THREADS) {
+        const int bb = i / (nloc * kHeadDim), c = col0 + (i / kHeadDim) % nloc;
+        if (s_pref[bb + 1] == s_pref[bb]) p.out[out_row(p, bb, kvh, c) + (i & (kHeadDim - 1))] = __float2half_rn(0.f);
+      }
+    }
+    __syncthreads();
+  }
+
+  for (; b < b_stop; ++b) {
+    int piece_t0 = 0, piece_t1 = 0;   // flat plan: this CTA's tiles of sequence b
+    if (FLAT) {
+      const int lo = s_pref[b], hi = s_pref[b + 1], r0 = s_flat[2], r1 = s_flat[3];
+      if (lo >= r1) break;
+      if (hi == lo) continue;   // empty sequence
+      piece_t0 = (max(r0, lo) - lo) * G::TPI;
+      piece_t1 = (min(r1, hi) - lo) * G::TPI;
+    }
     // Every input load of the prologue is issued before the first one is
     // used (the sequence length decides the rest): this warp's codebook
     // entry, its query column, and the new K / V row of a fused append.
@@ -539,8 +611,8 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     }
     const int L = load_len(p, b);
     const int ntiles = (L + V2_TILE - 1) / V2_TILE;
-    const int t_begin = split * p.tps;
-    const int t_end = min(t_begin + p.tps, ntiles);
+    const int t_begin = FLAT ? piece_t0 : split * p.tps;
+    const int t_end = min(FLAT ? piece_t1 : t_begin + p.tps, ntiles);
     const ColumnLimits cl = MULTI ? column_limits(p, L, tig, col0) : ColumnLimits{L, L, L};
     float acc[8][4];
 #pragma unroll
@@ -755,7 +827,14 @@ __global__ void __launch_bounds__(V2_THREADS, 1) decode_vq2_kernel(const DecodeP
     __syncthreads();   // every warp is done with the codebooks: reuse them for the combine
     stash_warp<V2_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Dim());
     __syncthreads();
-    finish_sequence<V2_WARPS, GROUPS, Dim>(p, b, kvh, split, s_comb, &s_last);
+    MergeSpan span = split_span(p, b, kvh, split, col0);
+    if (FLAT) {   // CTAs s_first .. s_last share sequence b; piece ids s + b
+      const int T = s_flat[0], S_eff = s_flat[1];
+      const int s_first = flat_cta_of(s_pref[b], T, S_eff), s_last = flat_cta_of(s_pref[b + 1] - 1, T, S_eff);
+      span = {split - s_first, s_last - s_first + 1,
+              (((size_t)kvh * (p.n_splits + p.B - 1) + s_first + b) * p.ncols + col0) * kPartialStride};
+    }
+    finish_sequence<V2_WARPS, GROUPS, Dim>(p, b, kvh, span, s_comb, &s_last);
     __syncthreads();   // (a warp that timed out still takes part in every barrier)
   }
 }
@@ -919,7 +998,7 @@ __global__ void __launch_bounds__(V15_THREADS, 1) decode_vq15_kernel(const Decod
     __syncthreads();   // every warp is done with its code slot: the combine area overlaps them
     stash_warp<V15_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, Vq15Dim());
     __syncthreads();
-    finish_sequence<V15_WARPS, GROUPS, Vq15Dim>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<V15_WARPS, GROUPS, Vq15Dim>(p, b, kvh, split_span(p, b, kvh, split, col0), s_comb, &s_last);
     __syncthreads();
   }
 }
@@ -957,24 +1036,29 @@ int decode_threads(int mode) { return mode == VQKV_MODE_VQ15 ? V15_THREADS : V2_
 namespace {
 using DecodeKernel = void (*)(DecodeParams);
 
-// [paged][query layout] instantiations of one mode's decode kernel.
+// [flat][paged][query layout] instantiations of one mode's decode kernel.
 template <int MODE>
 struct ByteCodeKernels {
-  static constexpr DecodeKernel k[2][3] = {
-      {decode_vq2_kernel<kOneQuery, false, MODE>, decode_vq2_kernel<kQueries, false, MODE>,
-       decode_vq2_kernel<kQueryGroups, false, MODE>},
-      {decode_vq2_kernel<kOneQuery, true, MODE>, decode_vq2_kernel<kQueries, true, MODE>,
-       decode_vq2_kernel<kQueryGroups, true, MODE>}};
+  static constexpr DecodeKernel k[2][2][3] = {
+      {{decode_vq2_kernel<kOneQuery, false, MODE, false>, decode_vq2_kernel<kQueries, false, MODE, false>,
+        decode_vq2_kernel<kQueryGroups, false, MODE, false>},
+       {decode_vq2_kernel<kOneQuery, true, MODE, false>, decode_vq2_kernel<kQueries, true, MODE, false>,
+        decode_vq2_kernel<kQueryGroups, true, MODE, false>}},
+      {{decode_vq2_kernel<kOneQuery, false, MODE, true>, decode_vq2_kernel<kQueries, false, MODE, true>,
+        decode_vq2_kernel<kQueryGroups, false, MODE, true>},
+       {decode_vq2_kernel<kOneQuery, true, MODE, true>, decode_vq2_kernel<kQueries, true, MODE, true>,
+        decode_vq2_kernel<kQueryGroups, true, MODE, true>}}};
 };
 struct Vq15Kernels {
-  static constexpr DecodeKernel k[2][3] = {
-      {decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
-       decode_vq15_kernel<kQueryGroups, false>},
-      {decode_vq15_kernel<kOneQuery, true>, decode_vq15_kernel<kQueries, true>,
-       decode_vq15_kernel<kQueryGroups, true>}};
+  static constexpr DecodeKernel k[2][2][3] = {
+      {{decode_vq15_kernel<kOneQuery, false>, decode_vq15_kernel<kQueries, false>,
+        decode_vq15_kernel<kQueryGroups, false>},
+       {decode_vq15_kernel<kOneQuery, true>, decode_vq15_kernel<kQueries, true>,
+        decode_vq15_kernel<kQueryGroups, true>}},
+      {{nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr}}};   // no flat plan at 1.5 bit
 };
 
-const DecodeKernel (*kernels_of(int mode))[3] {
+const DecodeKernel (*kernels_of(int mode))[2][3] {
   return mode == VQKV_MODE_VQ2   ? ByteCodeKernels<VQKV_MODE_VQ2>::k
          : mode == VQKV_MODE_VQ4 ? ByteCodeKernels<VQKV_MODE_VQ4>::k
          : mode == VQKV_MODE_VQ3 ? ByteCodeKernels<VQKV_MODE_VQ3>::k
@@ -987,21 +1071,25 @@ cudaError_t decode_prepare(int mode) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
   const auto ks = kernels_of(mode);
   cudaError_t e = cudaSuccess;
-  for (int pg = 0; pg < 2; ++pg)
-    for (int q = 0; q < 3; ++q)
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(ks[pg][q], a, (int)decode_smem_bytes(mode));
+  for (int fl = 0; fl < 2; ++fl)
+    for (int pg = 0; pg < 2; ++pg)
+      for (int q = 0; q < 3; ++q)
+        if (e == cudaSuccess && ks[fl][pg][q] != nullptr)
+          e = cudaFuncSetAttribute(ks[fl][pg][q], a, (int)decode_smem_bytes(mode));
   return e;
 }
 
 cudaError_t decode_occupancy(int mode, int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernels_of(mode)[0][kOneQuery],
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernels_of(mode)[0][0][kOneQuery],
                                                        decode_threads(mode), decode_smem_bytes(mode));
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   const int q = p.M == 1 ? kOneQuery : p.cgroups == 1 ? kQueries : kQueryGroups;
   const bool paged = p.block_table != nullptr;
-  return launch_pdl(kernels_of(mode)[paged][q], grid, dim3(decode_threads(mode)), decode_smem_bytes(mode), stream, p);
+  const DecodeKernel k = kernels_of(mode)[p.flat ? 1 : 0][paged][q];
+  if (k == nullptr) return cudaErrorInvalidValue;
+  return launch_pdl(k, grid, dim3(decode_threads(mode)), decode_smem_bytes(mode), stream, p);
 }
 
 }  // namespace vqkv

@@ -169,11 +169,25 @@ enum QueryLayout : int { kOneQuery = 0, kQueries = 1, kQueryGroups = 2 };
 __device__ __forceinline__ int cta_col0(const DecodeParams& p) { return 8 * (int)(blockIdx.z % p.cgroups); }
 __device__ __forceinline__ int cta_bgroup(const DecodeParams& p) { return (int)(blockIdx.z / p.cgroups); }
 
+// The CTAs that contribute to one (sequence, KV head, column group): this
+// CTA is number `part` of `n_parts`; the partials of all of them are rows
+// ncols * kPartialStride floats apart starting `first` floats into
+// p.partials (at the CTA's first column).
+struct MergeSpan {
+  int part, n_parts;
+  size_t first;
+};
+
+// Split plan: CTA `split` of p.n_splits, partials [B][Hkv][n_splits][ncols].
+__device__ __forceinline__ MergeSpan split_span(const DecodeParams& p, int b, int kvh, int split, int col0) {
+  return {split, p.n_splits, ((size_t)(b * p.Hkv + kvh) * p.n_splits * p.ncols + col0) * kPartialStride};
+}
+
 // COLGROUPS: the launch may split the columns into groups (multi-query
 // decode); otherwise the CTA holds all ncols columns.  DimOf: the stash
 // layout (row skew).
 template <int WARPS, bool COLGROUPS, typename DimOf>
-__device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, int split,
+__device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, int kvh, const MergeSpan& ms,
                                                 float* s_comb, int* s_last) {
   using C = CombineSmem<WARPS>;
   const float* wO = s_comb;
@@ -183,7 +197,9 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
   float* wM = s_comb + C::kMax;
   const int col0 = COLGROUPS ? cta_col0(p) : 0;
   const int G = COLGROUPS ? min(8, p.ncols - col0) : p.ncols;   // this CTA's columns
-  float* part = p.partials + (((size_t)(b * p.Hkv + kvh) * p.n_splits + split) * p.ncols + col0) * kPartialStride;
+  const size_t split_stride = (size_t)p.ncols * kPartialStride;
+  float* part = p.partials + ms.first + (size_t)ms.part * split_stride;
+  const int n_parts = ms.n_parts;
   const unsigned ticket = COLGROUPS ? (unsigned)((b * p.Hkv + kvh) * p.cgroups + blockIdx.z % p.cgroups)
                                     : (unsigned)(b * p.Hkv + kvh);
   // each warp's scale against the CTA's max of the column, once per (warp,
@@ -203,11 +219,11 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     float o = 0.f;
 #pragma unroll 4
     for (int w = 0; w < WARPS; ++w) o += col[w * 8 * C::kPitch] * wf[w * 8 + h];
-    if (p.n_splits == 1 || d == 0) {
+    if (n_parts == 1 || d == 0) {
       float l = 0.f;
 #pragma unroll 4
       for (int w = 0; w < WARPS; ++w) l += wl[w * 8 + h] * wf[w * 8 + h];
-      if (p.n_splits == 1) {
+      if (n_parts == 1) {
         p.out[out_row(p, b, kvh, col0 + h) + d] = __float2half_rn(l > 0.f ? o / l : 0.f);
         continue;
       }
@@ -216,7 +232,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     }
     part[h * kPartialStride + d] = o;
   }
-  if (p.n_splits == 1 || p.defer_merge) return;
+  if (n_parts == 1 || p.defer_merge) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned prev;
@@ -224,7 +240,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
                  : "=r"(prev)
                  : "l"(p.tickets + ticket)
                  : "memory");
-    *s_last = (prev == (unsigned)(p.n_splits - 1));
+    *s_last = (prev == (unsigned)(n_parts - 1));
   }
   __syncthreads();
   if (*s_last) {
@@ -233,8 +249,7 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     // has all its loads in flight at once and one rescale; the R threads of
     // an item then meet in shared memory.
     constexpr int THREADS = WARPS * 32, BATCH = 6;
-    const float* base = p.partials + ((size_t)(b * p.Hkv + kvh) * p.n_splits * p.ncols + col0) * kPartialStride;
-    const size_t split_stride = (size_t)p.ncols * kPartialStride;
+    const float* base = p.partials + ms.first;
     const int items = G * (kHeadDim / 8), R = THREADS / items;
     const int item = threadIdx.x % items, r = threadIdx.x / items;
     const int h = item / (kHeadDim / 8), d8 = (item % (kHeadDim / 8)) * 8;
@@ -243,13 +258,13 @@ __device__ __forceinline__ void finish_sequence(const DecodeParams& p, int b, in
     for (int i = 0; i < 8; ++i) O[i] = 0.f;
     if (r < R) {
       const float* col = base + h * kPartialStride;
-      for (int s0 = r; s0 < p.n_splits; s0 += BATCH * R) {
+      for (int s0 = r; s0 < n_parts; s0 += BATCH * R) {
         float2 ml[BATCH];
         float4 oa[BATCH], ob[BATCH];
 #pragma unroll
         for (int j = 0; j < BATCH; ++j) {
           const int sp = s0 + j * R;
-          if (sp < p.n_splits) {
+          if (sp < n_parts) {
             const float* ph = col + (size_t)sp * split_stride;
             ml[j] = __ldcg(reinterpret_cast<const float2*>(ph + 128));
             oa[j] = __ldcg(reinterpret_cast<const float4*>(ph + d8));

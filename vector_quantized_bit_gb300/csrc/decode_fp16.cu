@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(F_THREADS, 1) decode_fp16_kernel(const DecodeP
     __syncthreads();   // every warp is done with its ring: reuse it for the combine
     stash_warp<F_WARPS, 8>(s_comb, warp, lane, acc, m0, m1, l0, l1, NaturalDim());
     __syncthreads();
-    finish_sequence<F_WARPS, false, NaturalDim>(p, b, kvh, split, s_comb, &s_last);
+    finish_sequence<F_WARPS, false, NaturalDim>(p, b, kvh, split_span(p, b, kvh, split, 0), s_comb, &s_last);
     __syncthreads();
   }
 }

@@ -33,6 +33,8 @@ struct DecodeParams {
   int tps;                  // tiles per split
   int bpg;                  // sequences per CTA (grid.z = ceil(B / bpg))
   int defer_merge;          // 1: split partials are merged by the combine kernel
+  int flat = 0;             // 1: flat plan (tile-ring decode, batches): n_splits CTAs per KV head share
+                            // all sequences' tiles equally; partials [Hkv][n_splits + B - 1][ncols]
   float qscale;             // softmax_scale * log2(e) / sqrt(128)
   // Fused append (vqkv_decode_append): new rows [B][Hkv][128], or nullptr.
   const __half* k_new = nullptr;
@@ -51,6 +53,7 @@ struct DecodeParams {
 };
 
 constexpr int kPartialStride = 132;  // O[128], m, l, pad (rows 16-byte aligned)
+constexpr int kFlatMaxB = 1024;      // largest batch the flat plan takes
 
 struct EncodeParams {
   const __half* x;          // [B][Hkv][n_rows][128]
