@@ -462,7 +462,8 @@ template <int TPI>
 __device__ __forceinline__ void flat_prefix(const DecodeParams& p, int* s_pref) {
   const int lane = threadIdx.x & 31;
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const int L = min(max(p.seq_lens[b], 0), p.max_seq_len);   // (out-of-range lengths reported by load_len)
+    const int raw = p.seq_lens[b], L = min(max(raw, 0), p.max_seq_len);
+    if (raw != L && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(p.err, VQKV_DEVERR_SEQ_LEN);
     s_pref[b + 1] = ((L + V2_TILE - 1) / V2_TILE + TPI - 1) / TPI;
   }
   if (threadIdx.x == 0) s_pref[0] = 0;
