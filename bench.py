@@ -767,6 +767,8 @@ def encode_profile_run(mode, B=4, calls=3):
     codes = torch.zeros((w.B, w.Hkv, _lib.vqkv_code_bytes(mode, w.cap_len)), dtype=torch.uint8, device=dev)
     pos = torch.zeros(w.B, dtype=torch.int32, device=dev)
     cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    _lib.vqkv_encode(mode, 0, x, pos, s, kcb, codes, w.cap_len)   # warm-up (module load, attributes)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(calls):

@@ -430,14 +430,15 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 // the fp16 remainder of x' would tighten the bound but doubles the shared
 // memory and tensor memory traffic, which bound this kernel.)
 //
-// Roles (13 warps, one CTA per SM, persistent over the KV head's tiles; up
-// to 128 registers a thread):
-//   warps 8-10   producers: transform rows pw, pw + 3, pw + 6 (< 8) of each
+// Roles (12 warps, one CTA per SM, persistent over the KV head's tiles; 12
+// warps leave each SM sub-partition 3 warps, so up to 168 registers a thread,
+// enough for a whole 128-column chunk in flight per epilogue thread):
+//   warps 8, 9   producers: transform rows pw, pw + 2, pw + 4, pw + 6 of each
 //                tile (smoothing + Hadamard in double-float for keys), write
 //                A, x' and |x'_j|^2 into one of 4 stages;
-//   warps 11, 12 one thread each issues the MMAs of one epilogue warpgroup,
+//   warps 10, 11 one thread each issues the MMAs of one epilogue warpgroup,
 //                chunk by chunk into that warpgroup's two 128-column
-//                tensor-memory buffers (warp 11 also allocates the 512
+//                tensor-memory buffers (warp 10 also allocates the 512
 //                columns); separate issuers keep one warpgroup's wait for a
 //                free buffer from holding up the other's MMAs;
 //   warps 0-3, 4-7  two epilogue warpgroups taking alternate tiles: thread m
@@ -467,9 +468,9 @@ constexpr int CHUNKS = 4096 / N;              // 32
 constexpr int NBUF = 2;                       // tensor-memory buffers per epilogue warpgroup
 constexpr int GROUP = 32;                     // centroids per group minimum
 constexpr int STAGES = 4;
-constexpr int PROD_WARPS = 3;
-constexpr int MMA_WARP = 8 + PROD_WARPS;      // 11 (warpgroup 0's issuer; 12: warpgroup 1's)
-constexpr int THREADS = (MMA_WARP + 2) * 32;  // 416
+constexpr int PROD_WARPS = 2;
+constexpr int MMA_WARP = 8 + PROD_WARPS;      // 10 (warpgroup 0's issuer; 11: warpgroup 1's)
+constexpr int THREADS = (MMA_WARP + 2) * 32;  // 384
 constexpr int TABLE_BYTES = 4096 * 32;        // B: 4096 centroids x 16 fp16
 constexpr int A_BYTES = M * 32;               // one A tile: 128 x 16 fp16
 constexpr int ST_A = 0, ST_X = A_BYTES;
@@ -660,7 +661,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
     // The raw rows of tile k + 1 are loaded while tile k is transformed.
     const int pw = warp - 8;
     const int j = lane >> 1, half = lane & 1;
-    constexpr int PR = (ROWS + PROD_WARPS - 1) / PROD_WARPS;   // rows per producer warp (3)
+    constexpr int PR = (ROWS + PROD_WARPS - 1) / PROD_WARPS;   // rows per producer warp (4)
     const bool key = p.role == VQKV_ROLE_K;
     const float4 s4 = key ? *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane)
                           : make_float4(1.f, 1.f, 1.f, 1.f);
@@ -789,24 +790,21 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         if (!ok) break;
         tcgen05_after_sync();
         const uint32_t col = t_lane + (uint32_t)((NBUF * wg + bsel) * N);
-        // four loads of 32 columns, each in flight while the previous group
-        // is reduced; the buffer is handed back once the last is in registers
-        float va[32], vb[32];
-        tmem_ld32(col, va);
-        tmem_wait_ld();
-        tmem_ld32(col + 32, vb);
-        group(va, 4u * q);
-        tmem_wait_ld();
-        tmem_ld32(col + 64, va);
-        group(vb, 4u * q + 1u);
-        tmem_wait_ld();
-        tmem_ld32(col + 96, vb);
-        group(va, 4u * q + 2u);
+        // the whole chunk in flight at once (one wait); the buffer is handed
+        // back before the values are reduced
+        float v0[32], v1[32], v2[32], v3[32];
+        tmem_ld32(col, v0);
+        tmem_ld32(col + 32, v1);
+        tmem_ld32(col + 64, v2);
+        tmem_ld32(col + 96, v3);
         tmem_wait_ld();
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(t_empty(wg, bsel));
-        group(vb, 4u * q + 3u);
+        group(v0, 4u * q);
+        group(v1, 4u * q + 1u);
+        group(v2, 4u * q + 2u);
+        group(v3, 4u * q + 3u);
       }
       if (!ok) break;
       const int s = k % STAGES;
