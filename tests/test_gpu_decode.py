@@ -280,6 +280,50 @@ def test_flat_plan_ragged_batch(mode):
     assert vo.o_error(o2, ref).max() <= H.O_TOL
 
 
+@pytest.mark.parametrize("mode", [0, 4])
+def test_flat_plan_shares_with_merges(mode):
+    """More sequences than CTAs per KV head (37 > 152 / 8): the flat plan
+    cuts the tiles into equal shares, pieces of a sequence are merged."""
+    r = np.random.default_rng(50 + mode)
+    B, Hq, Hkv, cap = 37, 8, 8, 320
+    lens = r.integers(0, cap + 1, size=B)
+    lens[:4] = [0, 1, cap, 17]
+    q, kc, vc, kcb, vcb, s = random_case(mode, B, Hq, Hkv, lens, cap, seed=500 + mode)
+    kbuf, vbuf = H.pack_cache_role(mode, 0, kc, cap), H.pack_cache_role(mode, 1, vc, cap)
+    o = H.gpu_decode(mode, q, kbuf, vbuf, lens, kcb, vcb, s, cap, cap)
+    ref = oracle_o(q, kc, vc, kcb, vcb, s, lens)
+    assert np.all(o[lens == 0] == 0)
+    assert vo.o_error(o, ref).max() <= H.O_TOL
+
+
+def test_flat_plan_one_long_sequence_among_short_ones():
+    """One long sequence and three short ones: the long sequence is cut into
+    pieces over many CTAs and merged, the short ones share a CTA."""
+    lens = [3000, 10, 10, 10]
+    q, kc, vc, kcb, vcb, s = random_case(0, 4, 4, 2, lens, 3008, seed=51)
+    kbuf, vbuf = H.pack_cache_role(0, 0, kc, 3008), H.pack_cache_role(0, 1, vc, 3008)
+    o = H.gpu_decode(0, q, kbuf, vbuf, lens, kcb, vcb, s, 3008, 3008)
+    assert vo.o_error(o, oracle_o(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_flat_plan_even_lengths_with_an_empty_sequence(mode):
+    """Sixteen sequences of (nearly) one length on 19 CTAs per KV head: the
+    shares cross sequence boundaries at different tiles in every CTA; an
+    empty sequence gives a zero row."""
+    lens = [1600] * 16
+    lens[5] = 0
+    lens[9] = 1599
+    q, kc, vc, kcb, vcb, s = random_case(mode, 16, 8, 8, lens, 1600, seed=52 + mode)
+    kbuf, vbuf = H.pack_cache_role(mode, 0, kc, 1600), H.pack_cache_role(mode, 1, vc, 1600)
+    o = H.gpu_decode(mode, q, kbuf, vbuf, lens, kcb, vcb, s, 1600, 1600)
+    assert np.all(o[5] == 0)
+    assert vo.o_error(o, oracle_o(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
+    # one CTA per sequence (an explicit split count of 1) agrees
+    o1 = H.gpu_decode(mode, q, kbuf, vbuf, lens, kcb, vcb, s, 1600, 1600, num_splits=1)
+    assert vo.o_error(o1, oracle_o(q, kc, vc, kcb, vcb, s, lens)).max() <= H.O_TOL
+
+
 def test_flat_plan_fewer_tiles_than_ctas():
     """Three one-token sequences: fewer super-tiles than CTAs per KV head."""
     q, kc, vc, kcb, vcb, s = random_case(0, 3, 4, 1, [1, 2, 1], 16, seed=41)
