@@ -581,69 +581,6 @@ __device__ __forceinline__ void exact_warp_reduce(float& d, int& c, float& s) {
   }
 }
 
-// s + t as a hi + lo pair with lo = the rounding error of s + the low parts
-// (TwoSum, no renormalisation); 8 operations.
-__device__ __forceinline__ void lean_add(float ah, float al, float bh, float bl, float& sh, float& sl) {
-  const float t = __fadd_rn(ah, bh);
-  const float bb = __fsub_rn(t, ah);
-  const float e = __fadd_rn(__fsub_rn(ah, __fsub_rn(t, bb)), __fsub_rn(bh, bb));
-  sh = t;
-  sl = __fadd_rn(__fadd_rn(al, bl), e);
-}
-
-// The key transform of transform_loaded in fewer operations, for the
-// producers of the tcgen05 encode, which share their schedulers with the
-// epilogue warps: x / s as the product with the reciprocal rs = RN(1 / s)
-// plus the FMA remainder times rs, and each butterfly's rounding error
-// carried in an fp32 low part without renormalisation; the sum is rounded
-// once at the end.  Every term keeps a relative error near 2^-44, so the
-// result is the correctly rounded fp32 of the fp64 transform except where
-// that lies within about 2^-20 of an fp32 ulp of a rounding boundary.
-__device__ __forceinline__ void transform_key_lean(uint2 raw, float4 s, float4 rs, int lane, float (&x)[4]) {
-  const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x);
-  const __half2 x23 = *reinterpret_cast<const __half2*>(&raw.y);
-  const float xv[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-  const float sv[4] = {s.x, s.y, s.z, s.w}, rv[4] = {rs.x, rs.y, rs.z, rs.w};
-  float h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[i] = __fmul_rn(xv[i], rv[i]);
-    l[i] = __fmul_rn(__fmaf_rn(-h[i], sv[i], xv[i]), rv[i]);
-  }
-  {
-    float ah, al, bh, bl, ch, cl, dh, dl;
-    lean_add(h[0], l[0], h[1], l[1], ah, al);
-    lean_add(h[0], l[0], -h[1], -l[1], bh, bl);
-    lean_add(h[2], l[2], h[3], l[3], ch, cl);
-    lean_add(h[2], l[2], -h[3], -l[3], dh, dl);
-    lean_add(ah, al, ch, cl, h[0], l[0]);
-    lean_add(ah, al, -ch, -cl, h[2], l[2]);
-    lean_add(bh, bl, dh, dl, h[1], l[1]);
-    lean_add(bh, bl, -dh, -dl, h[3], l[3]);
-  }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float oh = __shfl_xor_sync(0xffffffffu, h[i], m);
-      const float ol = __shfl_xor_sync(0xffffffffu, l[i], m);
-      // lower lane: v + o; upper lane: o - v
-      lean_add(oh, ol, upper ? -h[i] : h[i], upper ? -l[i] : l[i], h[i], l[i]);
-    }
-  }
-  // x' = (h + l) * sqrt(2) / 16, rounded once
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const df v = two_sum(h[i], l[i]);
-    const float pr = __fmul_rn(v.h, sqrt2_hi());
-    float e = __fmaf_rn(v.h, sqrt2_hi(), -pr);
-    e = __fmaf_rn(v.h, sqrt2_lo(), e);
-    e = __fmaf_rn(v.l, sqrt2_hi(), e);
-    x[i] = __fmul_rn(__fadd_rn(pr, e), 0.0625f);
-  }
-}
-
 __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const EncodeParams p) {
   using namespace um;
   extern __shared__ __align__(1024) unsigned char smem[];
