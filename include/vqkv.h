@@ -142,7 +142,11 @@ typedef enum {
  *
  * For row n (0 <= n < n_rows) of sequence b and KV head h:
  *   role K: y = x / s[h] (per channel), x' = y . Hn with Hn = H/sqrt(128),
- *           H[i][k] = (-1)^popcount(i & k), x' rounded to fp32;
+ *           H[i][k] = (-1)^popcount(i & k), x' rounded to fp32 (computed in
+ *           pairs of fp32 to about 2^-44 of its terms first, so x' is the
+ *           correctly rounded value unless the exact one lies within about
+ *           2^-20 ulp of a rounding boundary; such a case can change a code
+ *           only between candidates whose distances are near-ties);
  *   role V: x' = x.
  *   For each subvector j of x' (d_sub = 2, 4 or 8 channels) the code is
  *   argmin_c sum_i (x'_{j,i} - C[h][c][i])^2 over the KV head's codebook C,

@@ -111,7 +111,7 @@ __device__ __forceinline__ void lean_add(float ah, float al, float bh, float bl,
 }
 
 // The key transform of transform_loaded in fewer operations, for the
-// many-row encode kernels: x / s as the product with the reciprocal rs = RN(1 / s)
+// encode kernels: x / s as the product with the reciprocal rs = RN(1 / s)
 // plus the FMA remainder times rs, and each butterfly's rounding error
 // carried in an fp32 low part without renormalisation; the sum is rounded
 // once at the end.  Every term keeps a relative error near 2^-44, so the
