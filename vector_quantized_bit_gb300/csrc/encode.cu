@@ -444,7 +444,8 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 //   warps 0-3, 4-7  two epilogue warpgroups taking alternate tiles: thread m
 //                owns tensor-memory lane m, i.e. subvector m % 16 of row m / 16.
 // The epilogue does not rank candidates one by one: per group of 32
-// consecutive centroids it takes the group minimum (three-input min), and
+// consecutive centroids it takes the group minimum, which the tensor-memory
+// load computes itself (tcgen05.ld.red ... .min, one load per group), and
 // keeps the four smallest group minima B1 <= B2 <= B3 <= B4, each carrying
 // its group id.  A centroid can be the exact nearest only if its screened
 // distance is within 2 eps of B1, so with B4 above that margin every
@@ -771,15 +772,11 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
     for (int k = wg; k < n_my; k += 2, ++it) {
       const float inf = __int_as_float(0x7f800000);
       float B1 = inf, B2 = inf, B3 = inf, B4 = inf;
-      // group minimum (a min3 tree, depth 4) with the group id in its 7 low
-      // mantissa bits, then the four smallest so far: the packing moves a
-      // value by less than 2^-16 of itself, which the margin below covers
-      auto group = [&](const float (&v)[32], uint32_t gid) {
-        float t[10];
-#pragma unroll
-        for (int i = 0; i < 10; ++i) t[i] = fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-        const float g = fminf(fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], t[5]), fmin3(t[6], t[7], t[8])),
-                              fmin3(t[9], v[30], v[31]));
+      // the group minimum (from the tensor-memory load's own reduction) with
+      // the group id in its 7 low mantissa bits, then the four smallest so
+      // far: the packing moves a value by less than 2^-16 of itself, which
+      // the margin below covers
+      auto group = [&](float g, uint32_t gid) {
         const float gp = __uint_as_float((__float_as_uint(g) & ~0x7Fu) | gid);
         B4 = fminf(B4, fmaxf(B3, gp));
         B3 = fminf(B3, fmaxf(B2, gp));
@@ -797,18 +794,19 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         // the whole chunk in flight at once (one wait); the buffer is handed
         // back before the values are reduced
         float v0[32], v1[32], v2[32], v3[32];
-        tmem_ld32(col, v0);
-        tmem_ld32(col + 32, v1);
-        tmem_ld32(col + 64, v2);
-        tmem_ld32(col + 96, v3);
+        float g0 = inf, g1 = inf, g2 = inf, g3 = inf;
+        tmem_ld32_min(col, v0, g0);
+        tmem_ld32_min(col + 32, v1, g1);
+        tmem_ld32_min(col + 64, v2, g2);
+        tmem_ld32_min(col + 96, v3, g3);
         tmem_wait_ld();
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(t_empty(wg, bsel));
-        group(v0, 4u * q);
-        group(v1, 4u * q + 1u);
-        group(v2, 4u * q + 2u);
-        group(v3, 4u * q + 3u);
+        group(g0, 4u * q);
+        group(g1, 4u * q + 1u);
+        group(g2, 4u * q + 2u);
+        group(g3, 4u * q + 3u);
       }
       if (!ok) break;
       const int s = k % STAGES;

@@ -92,6 +92,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tmem_ld32 that also returns min over the 32 columns (NaN ignored, as by
+// min.f32); m must be +inf on entry.  The minimum, like the values, is valid
+// after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_min(uint32_t taddr, float (&v)[32], float& m) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.min.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]),
+        "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]),
+        "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]),
+        "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31]), "+f"(m)
+      : "r"(taddr)
+      : "memory");
+}
+
 // min(a, b, c) in one instruction.
 __device__ __forceinline__ float fmin3(float a, float b, float c) {
   float d;
