@@ -238,3 +238,18 @@ def test_vq15_many_rows_values_beyond_fp16_screening():
     # distances near 1e11: fp32 rounding alone puts some candidates within
     # 1e-6 relative of each other, so the GPU's near-tie count is not bounded
     compare("1.5-bit many rows, values beyond fp16", 1, 0, x, s, kcb, buf, [0, 30], 30, nties, bounded=False)
+
+
+@pytest.mark.parametrize("n_rows", [2, 100])
+def test_vq15_codebook_beyond_the_screening_tables(n_rows):
+    """Centroids of norm up to about 1000: |c|^2 no longer fits the fp16
+    screening tables, so the KV head is searched exhaustively from the
+    codebook in global memory (few rows: the one-row kernel; many rows: the
+    tensor-memory kernel).  Codes still match the oracle."""
+    r = np.random.default_rng(13)
+    vcb = (r.standard_normal((1, 4096, 8)) * 300.0).astype(np.float16)
+    x = (r.standard_normal((2, 1, n_rows, 128)) * 300.0).astype(np.float16)
+    buf, nties, err = H.gpu_encode(1, 1, x, [0, 100], None, vcb, 256, with_ties=True)
+    assert err == 0
+    compare(f"1.5-bit codebook beyond the screen, {n_rows} rows", 1, 1, x, None, vcb, buf, [0, 100], n_rows, nties,
+            bounded=False)

@@ -379,6 +379,35 @@ __device__ __forceinline__ float exact_d8(const float* x, const uint2* tbl, int 
   return d;
 }
 
+// The same distance to centroid c read from the fp16 codebook in global
+// memory (cb8: its 8 channels).  x_i - c_i is the same correctly rounded
+// difference as above, so the two agree bit for bit.
+__device__ __forceinline__ float exact_d8_cb(const float* x, const __half* cb8) {
+  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(cb8));
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float y[8];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+    y[2 * t] = f.x;
+    y[2 * t + 1] = f.y;
+  }
+  float e = __fsub_rn(x[0], y[0]);
+  float d = __fmul_rn(e, e);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    e = __fsub_rn(x[i], y[i]);
+    d = __fmaf_rn(e, e, d);
+  }
+  return d;
+}
+
+// Largest centroid norm the fp16 screening tables hold exactly: -2c stays
+// exact and |c|^2 <= 16384 keeps its fp16 hi + lo split finite.  A KV head
+// with a larger centroid is searched exhaustively, from the codebook in
+// global memory (slow, but only such codebooks pay for it).
+constexpr float kScreenCmax = 128.f;
+
 // B table [centroid][tig]{-2c pair, (|c|^2, 1) or 0} of KV head kvh in
 // shared memory, and the largest centroid norm (returned; s_cmax is one
 // float of scratch).  Called by every thread of the CTA.
@@ -711,10 +740,11 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
             transform_key_lean(cur[i], s4, rs4, lane, x);
           else
             transform_loaded(cur[i], false, s4, lane, x);
-          flag = F_OK;
+          // beyond fp16 screening (or not finite), or a codebook beyond the table: exhaustive
+          flag = Cmax <= kScreenCmax ? F_OK : F_EXHAUSTIVE;
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            if (!(fabsf(x[e]) < 32768.f)) flag = F_EXHAUSTIVE;   // beyond fp16 screening (or not finite)
+            if (!(fabsf(x[e]) < 32768.f)) flag = F_EXHAUSTIVE;
         }
         const uint32_t off = umma_kmajor_offset((uint32_t)m, 4u * half);
         *reinterpret_cast<uint2*>(st + ST_A + off) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
@@ -868,7 +898,12 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         for (int i = 0; i < 8; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
         float d = __int_as_float(0x7f800000), sd = d;
         int c = 0x7fffffff;
-        for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_umma(xs, table, cc), cc, d, c, sd);
+        if (!(Cmax <= kScreenCmax)) {   // centroids beyond the table: from global memory
+          const __half* cb_head = p.cb + (size_t)kvh * 4096 * 8;
+          for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_cb(xs, cb_head + (size_t)cc * 8), cc, d, c, sd);
+        } else {
+          for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_umma(xs, table, cc), cc, d, c, sd);
+        }
         exact_warp_reduce(d, c, sd);
         if (lane == src) dex = d, cex = c, dsec = sd;   // every candidate: replaces the group search
       }
@@ -931,6 +966,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
     if (ks != nullptr) xs = *reinterpret_cast<const float4*>(ks + 4 * lane);
   }
   const float Cmax = build_tc_table(p, kvh, s_tbl, s_cmax);
+  const bool big = !(Cmax <= kScreenCmax);   // every subvector exhaustive, from global memory
+  const __half* cb_head = p.cb + (size_t)kvh * 4096 * 8;
   const uint32_t tbl_lane = smem_u32(s_tbl) + (gid * 4 + tig) * 8;
   const float inf = __int_as_float(0x7f800000);
 
@@ -949,7 +986,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
       nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2, j = lane / 2
       *reinterpret_cast<float4*>(s_x + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
       if ((lane & 1) == 0) s_xn[lane >> 1] = nx;
-      if (lane < 16) s_hidden[lane] = 0;
+      if (lane < 16) s_hidden[lane] = big ? 1 : 0;
     }
     __syncthreads();
     const float2 xa = *reinterpret_cast<const float2*>(s_x + 8 * gid + 2 * tig);
@@ -1007,7 +1044,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
     for (int j = 0; j < 16; ++j) {
       if (!s_hidden[j]) continue;   // uniform: read after the barrier
       Best e = best_init();
-      for (int c = threadIdx.x; c < 4096; c += TC_THREADS) best_push(e, exact_d8(s_x + 8 * j, s_tbl, c), c);
+      for (int c = threadIdx.x; c < 4096; c += TC_THREADS)
+        best_push(e, big ? exact_d8_cb(s_x + 8 * j, cb_head + (size_t)c * 8) : exact_d8(s_x + 8 * j, s_tbl, c), c);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) e = best_merge(e, best_shfl_xor(e, o));
       if (lane == 0) s_ex[warp] = e;
