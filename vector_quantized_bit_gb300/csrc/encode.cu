@@ -402,6 +402,21 @@ __device__ __forceinline__ float exact_d8_cb(const float* x, const __half* cb8) 
   return d;
 }
 
+// The same for 4 channels (2-bit codebooks).
+__device__ __forceinline__ float exact_d4_cb(const float* x, const __half* cb4) {
+  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(cb4));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+  float e = __fsub_rn(x[0], a.x);
+  float d = __fmul_rn(e, e);
+  e = __fsub_rn(x[1], a.y);
+  d = __fmaf_rn(e, e, d);
+  e = __fsub_rn(x[2], b.x);
+  d = __fmaf_rn(e, e, d);
+  e = __fsub_rn(x[3], b.y);
+  return __fmaf_rn(e, e, d);
+}
+
 // Largest centroid norm the fp16 screening tables hold exactly: -2c stays
 // exact and |c|^2 <= 16384 keeps its fp16 hi + lo split finite.  A KV head
 // with a larger centroid is searched exhaustively, from the codebook in
@@ -491,34 +506,44 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 // loop; the MMA thread then waits (bounded) for its MMAs before the tensor
 // memory is freed.
 namespace um {
-constexpr int ROWS = 8;                       // rows per tile
-constexpr int M = ROWS * 16;                  // 128 MMA rows: (row, subvector)
+constexpr int M = 128;                        // MMA rows: (row, subvector) pairs of a tile
 constexpr int N = 128;                        // centroids per MMA
-constexpr int CHUNKS = 4096 / N;              // 32
 constexpr int NBUF = 2;                       // tensor-memory buffers per epilogue warpgroup
 constexpr int GROUP = 32;                     // centroids per group minimum
 constexpr int STAGES = 4;
 constexpr int PROD_WARPS = 2;
 constexpr int MMA_WARP = 8 + PROD_WARPS;      // 10 (warpgroup 0's issuer; 11: warpgroup 1's)
 constexpr int THREADS = (MMA_WARP + 2) * 32;  // 384
-constexpr int TABLE_BYTES = 4096 * 32;        // B: 4096 centroids x 16 fp16
 constexpr int A_BYTES = M * 32;               // one A tile: 128 x 16 fp16
-constexpr int ST_A = 0, ST_X = A_BYTES;
-constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + M * 4, ST_POS = ST_FLAG + M * 4;
-constexpr int STAGE_BYTES = ST_POS + 16 * 4;  // + cache position of each row
-constexpr int OFF_STAGES = TABLE_BYTES;
-constexpr int OFF_BAR = OFF_STAGES + STAGES * STAGE_BYTES;
 constexpr int NBAR = 2 * STAGES + 4 * NBUF + 2;   // A full / empty, tensor-memory full / empty, MMAs done x 2
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag, max centroid norm
-constexpr size_t SMEM = OFF_MISC + 16;
 constexpr uint32_t TMEM_COLS = 512;           // 2 warpgroups x NBUF buffers x N
-static_assert(2 * NBUF * N <= (int)TMEM_COLS && CHUNKS % NBUF == 0 && N % GROUP == 0, "tensor-memory plan");
+static_assert(2 * NBUF * N <= (int)TMEM_COLS && N % GROUP == 0, "tensor-memory plan");
 constexpr uint32_t MAX_POLLS = 1u << 22;
 // row flags
 constexpr int F_OK = 0, F_EXHAUSTIVE = 1, F_SKIP = 2;
 }  // namespace um
-static_assert(um::SMEM <= 227 * 1024, "UMMA encode shared memory");
-static_assert(um::STAGE_BYTES % 16 == 0 && um::OFF_BAR % 8 == 0, "alignment");
+
+// Per code mode: 1.5 bit (4096 centroids of 8 channels, 16 subvectors a
+// row, 8 rows a tile) or 2 bit (256 of 4, 32 subvectors, 4 rows a tile).
+template <int MODE>
+struct UmGeo {
+  static constexpr int DSUB = MODE == VQKV_MODE_VQ15 ? 8 : 4;
+  static constexpr int E = MODE == VQKV_MODE_VQ15 ? 4096 : 256;
+  static constexpr int SUBV = kHeadDim / DSUB;           // subvectors per row
+  static constexpr int ROWS = um::M / SUBV;               // rows per tile
+  static constexpr int CHUNKS = E / um::N;               // MMAs per tile
+  static constexpr int TABLE_BYTES = E * 32;             // B: E centroids x 16 fp16
+  static constexpr int ST_A = 0, ST_X = um::A_BYTES;
+  static constexpr int ST_NORM = ST_X + ROWS * kHeadDim * 4, ST_FLAG = ST_NORM + um::M * 4;
+  static constexpr int ST_POS = ST_FLAG + um::M * 4;
+  static constexpr int STAGE_BYTES = ST_POS + 16 * 4;   // + cache position of each row
+  static constexpr int OFF_STAGES = TABLE_BYTES;
+  static constexpr int OFF_BAR = OFF_STAGES + um::STAGES * STAGE_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + um::NBAR * 8;   // tensor-memory base, abort flag, max centroid norm
+  static constexpr size_t SMEM = OFF_MISC + 16;
+  static_assert(SMEM <= 227 * 1024 && STAGE_BYTES % 16 == 0 && OFF_BAR % 8 == 0, "UMMA encode shared memory");
+  static_assert(CHUNKS % um::NBUF == 0 && E / um::GROUP <= 128 && ROWS <= 16, "tile plan (7-bit group ids)");
+};
 
 // Bound on |screened - exact| for one candidate of the single-MMA screen:
 // the fp16 rounding of x' leaves |x' - x_hi| <= 2^-11 |x'| per channel
@@ -553,17 +578,25 @@ __device__ __forceinline__ bool um_wait(uint32_t mbar, uint32_t parity, volatile
   return ok;
 }
 
-// Exact fp32 distance of subvector x to centroid c read from the B table
-// (-2c as fp16, halved exactly): direct differences in channel order, one
-// rounding per operation, the same arithmetic as exact_d8.
+// Exact fp32 distance of subvector x (D = 8 or 4 channels) to centroid c
+// read from the B table (-2c as fp16, halved exactly): direct differences in
+// channel order, one rounding per operation, the same arithmetic as
+// exact_d8 and vq2_search.
 // x_i - c_i is formed as fma(0.5, h_i, x_i) with h_i = -2 c_i: 0.5 h_i = -c_i
 // exactly, so it is the same correctly rounded difference.
-__device__ __forceinline__ float exact_d8_umma(const float (&x)[8], const unsigned char* table, int c) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(table + umma_kmajor_offset((uint32_t)c, 0));
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  float h[8];
+template <int D>
+__device__ __forceinline__ float exact_d_umma(const float (&x)[D], const unsigned char* table, int c) {
+  uint32_t w[D / 2];
+  if constexpr (D == 8) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(table + umma_kmajor_offset((uint32_t)c, 0));
+    w[0] = raw.x, w[1] = raw.y, w[2] = raw.z, w[3] = raw.w;
+  } else {
+    const uint2 raw = *reinterpret_cast<const uint2*>(table + umma_kmajor_offset((uint32_t)c, 0));
+    w[0] = raw.x, w[1] = raw.y;
+  }
+  float h[D];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
+  for (int t = 0; t < D / 2; ++t) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
     h[2 * t] = f.x;
     h[2 * t + 1] = f.y;
@@ -571,7 +604,7 @@ __device__ __forceinline__ float exact_d8_umma(const float (&x)[8], const unsign
   float e = __fmaf_rn(0.5f, h[0], x[0]);
   float d = __fmul_rn(e, e);
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
+  for (int i = 1; i < D; ++i) {
     e = __fmaf_rn(0.5f, h[i], x[i]);
     d = __fmaf_rn(e, e, d);
   }
@@ -611,8 +644,14 @@ __device__ __forceinline__ void exact_warp_reduce(float& d, int& c, float& s) {
   }
 }
 
-__global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const EncodeParams p) {
+template <int MODE>
+__global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const EncodeParams p) {
   using namespace um;
+  using Geo = UmGeo<MODE>;
+  constexpr int DSUB = Geo::DSUB, E = Geo::E, SUBV = Geo::SUBV, ROWS = Geo::ROWS, CHUNKS = Geo::CHUNKS;
+  constexpr int ST_A = Geo::ST_A, ST_X = Geo::ST_X, ST_NORM = Geo::ST_NORM, ST_FLAG = Geo::ST_FLAG;
+  constexpr int ST_POS = Geo::ST_POS, STAGE_BYTES = Geo::STAGE_BYTES, OFF_STAGES = Geo::OFF_STAGES;
+  constexpr int OFF_BAR = Geo::OFF_BAR, OFF_MISC = Geo::OFF_MISC;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -648,16 +687,23 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
   grid_dependents_launch();
   __syncthreads();
 
-  // B table: row c = [-2c (8 fp16), |c|^2 hi, |c|^2 lo, 0 x 6]
+  // B table: row c = [-2c (8 fp16), |c|^2 hi, |c|^2 lo, 0 x 6] (1.5 bit) or
+  // [-2c (4 fp16), |c|^2 hi, |c|^2 lo, 0 x 10] (2 bit)
   {
     float cmax = 0.f;
-    for (int c = threadIdx.x; c < 4096; c += THREADS) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * 4096 + c);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t m2[4];
+    for (int c = threadIdx.x; c < E; c += THREADS) {
+      uint32_t w[DSUB / 2];
+      if constexpr (DSUB == 8) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.cb) + (size_t)kvh * E + c);
+        w[0] = raw.x, w[1] = raw.y, w[2] = raw.z, w[3] = raw.w;
+      } else {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.cb) + (size_t)kvh * E + c);
+        w[0] = raw.x, w[1] = raw.y;
+      }
+      uint32_t m2[DSUB / 2];
       float nn = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < DSUB / 2; ++t) {
         const __half2 h = *reinterpret_cast<const __half2*>(&w[t]);
         const float a = __low2float(h), b = __high2float(h);
         nn = __fmaf_rn(a, a, nn);
@@ -667,9 +713,15 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       }
       const __half nh = __float2half_rn(nn);
       const __half2 tail = __halves2half2(nh, __float2half_rn(nn - __half2float(nh)));
+      const uint32_t tw = *reinterpret_cast<const uint32_t*>(&tail);
       unsigned char* row = smem + umma_kmajor_offset((uint32_t)c, 0);
-      *reinterpret_cast<uint4*>(row) = make_uint4(m2[0], m2[1], m2[2], m2[3]);
-      *reinterpret_cast<uint4*>(row + 128) = make_uint4(*reinterpret_cast<const uint32_t*>(&tail), 0u, 0u, 0u);
+      if constexpr (DSUB == 8) {
+        *reinterpret_cast<uint4*>(row) = make_uint4(m2[0], m2[1], m2[2], m2[3]);
+        *reinterpret_cast<uint4*>(row + 128) = make_uint4(tw, 0u, 0u, 0u);
+      } else {
+        *reinterpret_cast<uint4*>(row) = make_uint4(m2[0], m2[1], tw, 0u);
+        *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+      }
       cmax = fmaxf(cmax, sqrtf(nn));
     }
     for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
@@ -690,8 +742,9 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
     // ---------------- producers: rows pw, pw + 3, pw + 6 (< 8) of every tile.
     // The raw rows of tile k + 1 are loaded while tile k is transformed.
     const int pw = warp - 8;
-    const int j = lane >> 1, half = lane & 1;
-    constexpr int PR = (ROWS + PROD_WARPS - 1) / PROD_WARPS;   // rows per producer warp (4)
+    // 1.5 bit: lanes 2j, 2j + 1 hold subvector j; 2 bit: lane j holds subvector j
+    const int j = DSUB == 8 ? lane >> 1 : lane, half = DSUB == 8 ? lane & 1 : 0;
+    constexpr int PR = (ROWS + PROD_WARPS - 1) / PROD_WARPS;   // rows per producer warp (4 / 2)
     const bool key = p.role == VQKV_ROLE_K;
     const float4 s4 = key ? *reinterpret_cast<const float4*>(p.s + (size_t)kvh * kHeadDim + 4 * lane)
                           : make_float4(1.f, 1.f, 1.f, 1.f);
@@ -732,7 +785,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       for (int i = 0; i < PR; ++i) {
         const int r = pw + PROD_WARPS * i;
         if (r >= ROWS) break;
-        const int m = 16 * r + j;
+        const int m = SUBV * r + j;
         int flag = F_SKIP;
         float x[4] = {0.f, 0.f, 0.f, 0.f};
         if (cur_t[i] >= 0) {
@@ -746,14 +799,23 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
           for (int e = 0; e < 4; ++e)
             if (!(fabsf(x[e]) < 32768.f)) flag = F_EXHAUSTIVE;
         }
-        const uint32_t off = umma_kmajor_offset((uint32_t)m, 4u * half);
-        *reinterpret_cast<uint2*>(st + ST_A + off) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
-        *reinterpret_cast<uint2*>(st + ST_A + off + 128) =
-            make_uint2(half == 0 ? pack_half2(1.f, 1.f) : 0u, 0u);   // picks |c|^2 hi + lo
+        if constexpr (DSUB == 8) {
+          const uint32_t off = umma_kmajor_offset((uint32_t)m, 4u * half);
+          *reinterpret_cast<uint2*>(st + ST_A + off) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+          *reinterpret_cast<uint2*>(st + ST_A + off + 128) =
+              make_uint2(half == 0 ? pack_half2(1.f, 1.f) : 0u, 0u);   // picks |c|^2 hi + lo
+        } else {
+          const uint32_t off = umma_kmajor_offset((uint32_t)m, 0u);
+          *reinterpret_cast<uint4*>(st + ST_A + off) =
+              make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(1.f, 1.f), 0u);
+          *reinterpret_cast<uint4*>(st + ST_A + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+        }
         *reinterpret_cast<float4*>(st + ST_X + (r * kHeadDim + 4 * lane) * 4) = make_float4(x[0], x[1], x[2], x[3]);
         float nx = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-        nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2
-        flag = max(flag, __shfl_xor_sync(0xffffffffu, flag, 1));
+        if constexpr (DSUB == 8) {
+          nx += __shfl_xor_sync(0xffffffffu, nx, 1);   // |x'_j|^2
+          flag = max(flag, __shfl_xor_sync(0xffffffffu, flag, 1));
+        }
         if (half == 0) {
           reinterpret_cast<float*>(st + ST_NORM)[m] = nx;
           reinterpret_cast<int*>(st + ST_FLAG)[m] = flag;
@@ -795,7 +857,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
   } else {
     // ---------------- epilogue warpgroup wg: tiles wg, wg + 2, ...
     const int wg = warp >> 2, ml = 32 * (warp & 3) + lane;   // tensor-memory lane = MMA row
-    const int r = ml >> 4, j = ml & 15;
+    const int r = ml / SUBV, j = ml % SUBV;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const unsigned char* table = smem;
     int it = 0;
@@ -814,6 +876,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
         B1 = fminf(B1, gp);
       };
       bool ok = true;
+#pragma unroll 1
       for (int q = 0; q < CHUNKS; ++q) {
         const int bsel = q % NBUF;
         const uint32_t use = (uint32_t)(it * (CHUNKS / NBUF) + q / NBUF);
@@ -843,11 +906,14 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       if (!um_wait(a_full(s), (k / STAGES) & 1, s_abort, p.err, 0xffffffffu)) break;   // (complete already)
       const unsigned char* st = smem + OFF_STAGES + s * STAGE_BYTES;
       const int flag = reinterpret_cast<const int*>(st + ST_FLAG)[ml];
-      float xv[8];
+      float xv[DSUB];
       {
-        const float4 a = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j) * 4);
-        const float4 b = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j + 4) * 4);
-        xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = b.x, xv[5] = b.y, xv[6] = b.z, xv[7] = b.w;
+        const float4 a = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + DSUB * j) * 4);
+        xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w;
+        if constexpr (DSUB == 8) {
+          const float4 b = *reinterpret_cast<const float4*>(st + ST_X + (r * kHeadDim + 8 * j + 4) * 4);
+          xv[4] = b.x, xv[5] = b.y, xv[6] = b.z, xv[7] = b.w;
+        }
       }
       const float eps = screen_eps_hi(sqrtf(reinterpret_cast<const float*>(st + ST_NORM)[ml]), Cmax);
       // a group can hold a candidate within 2 eps of the best when its packed
@@ -867,7 +933,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
 #pragma unroll 8
         for (int i = 0; i < GROUP; ++i) {
           const int c = GROUP * G1 + ((i + rot) & (GROUP - 1));
-          exact_push(exact_d8_umma(xv, table, c), c, dex, cex, dsec);
+          exact_push(exact_d_umma<DSUB>(xv, table, c), c, dex, cex, dsec);
         }
       }
       // groups G2 / G3 (few lanes) by the whole warp, one (lane, group) at a
@@ -881,10 +947,10 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
           const int src = __ffs(mset) - 1;
           mset &= mset - 1;
           const int g = __shfl_sync(0xffffffffu, (int)(__float_as_uint(Bp) & 0x7Fu), src);
-          float xs[8];
+          float xs[DSUB];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
-          float d = exact_d8_umma(xs, table, GROUP * g + lane), sd = __int_as_float(0x7f800000);
+          for (int i = 0; i < DSUB; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
+          float d = exact_d_umma<DSUB>(xs, table, GROUP * g + lane), sd = __int_as_float(0x7f800000);
           int c = GROUP * g + lane;
           exact_warp_reduce(d, c, sd);
           if (lane == src) exact_merge(d, c, sd, dex, cex, dsec);
@@ -893,29 +959,40 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_vq15_umma_kernel(const 
       while (mx) {
         const int src = __ffs(mx) - 1;
         mx &= mx - 1;
-        float xs[8];
+        float xs[DSUB];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
+        for (int i = 0; i < DSUB; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
         float d = __int_as_float(0x7f800000), sd = d;
         int c = 0x7fffffff;
         if (!(Cmax <= kScreenCmax)) {   // centroids beyond the table: from global memory
-          const __half* cb_head = p.cb + (size_t)kvh * 4096 * 8;
-          for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_cb(xs, cb_head + (size_t)cc * 8), cc, d, c, sd);
+          const __half* cb_head = p.cb + (size_t)kvh * E * DSUB;
+          for (int cc = lane; cc < E; cc += 32) {
+            const float dd = DSUB == 8 ? exact_d8_cb(xs, cb_head + (size_t)cc * 8) : exact_d4_cb(xs, cb_head + (size_t)cc * 4);
+            exact_push(dd, cc, d, c, sd);
+          }
         } else {
-          for (int cc = lane; cc < 4096; cc += 32) exact_push(exact_d8_umma(xs, table, cc), cc, d, c, sd);
+          for (int cc = lane; cc < E; cc += 32) exact_push(exact_d_umma<DSUB>(xs, table, cc), cc, d, c, sd);
         }
         exact_warp_reduce(d, c, sd);
         if (lane == src) dex = d, cex = c, dsec = sd;   // every candidate: replaces the group search
       }
       count_near_ties(p.near_tie, flag != F_SKIP && is_near_tie(dex, dsec), lane, 0xffffffffu);
-      // lane (row r, subvector j < 8) stores the pair (j, j + 8) of its row
-      const int hi = __shfl_down_sync(0xffffffffu, cex, 8);
-      if (j < 8 && flag != F_SKIP) {
+      if constexpr (DSUB == 8) {
+        // lane (row r, subvector j < 8) stores the pair (j, j + 8) of its row
+        const int hi = __shfl_down_sync(0xffffffffu, cex, 8);
+        if (j < 8 && flag != F_SKIP) {
+          const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
+          const int b = row / p.n_rows;
+          const int t = reinterpret_cast<const int*>(st + ST_POS)[r];
+          uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
+          if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, j), cex, hi);
+        }
+      } else if (flag != F_SKIP) {   // one byte per subvector
         const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
         const int b = row / p.n_rows;
         const int t = reinterpret_cast<const int*>(st + ST_POS)[r];
-        uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
-        if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, j), cex, hi);
+        uint8_t* tb = tile_base(p, b, kvh, t, 16, 512);
+        if (tb) tb[vq2_code_offset(p.role, t & 15, j)] = (uint8_t)cex;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(a_empty(s));
@@ -1084,10 +1161,14 @@ cudaError_t encode_prepare(int mode) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(encode_vq3_kernel<ENC3_SPLIT>, a, (int)kEnc3Smem);
     return e;
   }
+  if (mode == VQKV_MODE_VQ2)
+    return cudaFuncSetAttribute(encode_umma_kernel<VQKV_MODE_VQ2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)UmGeo<VQKV_MODE_VQ2>::SMEM);
   if (mode != VQKV_MODE_VQ15) return cudaSuccess;
   {
-    const cudaError_t e0 = cudaFuncSetAttribute(encode_vq15_umma_kernel,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)um::SMEM);
+    const cudaError_t e0 = cudaFuncSetAttribute(encode_umma_kernel<VQKV_MODE_VQ15>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)UmGeo<VQKV_MODE_VQ15>::SMEM);
     if (e0 != cudaSuccess) return e0;
     const cudaError_t e1 = cudaFuncSetAttribute(encode_vq15_tc_split_kernel,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSplitSmem);
@@ -1098,7 +1179,8 @@ cudaError_t encode_prepare(int mode) {
 
 cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ2)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 4>, ENC_THREADS, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_umma_kernel<VQKV_MODE_VQ2>,
+                                                         um::THREADS, UmGeo<VQKV_MODE_VQ2>::SMEM);
   if (mode == VQKV_MODE_VQ4)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 2>, ENC_THREADS, 0);
   if (mode == VQKV_MODE_VQ3)
@@ -1106,8 +1188,8 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
                                                          kEnc3Smem);
   if (mode == VQKV_MODE_VQ125)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq125_kernel<1>, ENC_THREADS, 0);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq15_umma_kernel, um::THREADS,
-                                                       um::SMEM);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_umma_kernel<VQKV_MODE_VQ15>,
+                                                       um::THREADS, UmGeo<VQKV_MODE_VQ15>::SMEM);
 }
 
 // split_rows: one row per CTA, candidates split over the CTA's warps.
@@ -1115,7 +1197,8 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
   const dim3 grid(blocks_x, p.Hkv);
   if (mode == VQKV_MODE_VQ2) {
     if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 4>, grid, dim3(ENC_THREADS), 0, stream, p);
-    return launch_pdl(encode_vq2_kernel<1, 4>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_umma_kernel<VQKV_MODE_VQ2>, grid, dim3(um::THREADS), UmGeo<VQKV_MODE_VQ2>::SMEM,
+                      stream, p);
   }
   if (mode == VQKV_MODE_VQ4) {
     if (split_rows) return launch_pdl(encode_vq2_kernel<ENC_WARPS, 2>, grid, dim3(ENC_THREADS), 0, stream, p);
@@ -1131,7 +1214,8 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
     return launch_pdl(encode_vq3_kernel<1>, grid, dim3(ENC_THREADS), kEnc3Smem, stream, p);
   }
   if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
-  return launch_pdl(encode_vq15_umma_kernel, grid, dim3(um::THREADS), um::SMEM, stream, p);
+  return launch_pdl(encode_umma_kernel<VQKV_MODE_VQ15>, grid, dim3(um::THREADS), UmGeo<VQKV_MODE_VQ15>::SMEM,
+                    stream, p);
 }
 
 }  // namespace vqkv
