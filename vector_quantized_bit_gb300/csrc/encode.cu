@@ -462,14 +462,14 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
   return *s_cmax;
 }
 
-// Many rows of 1.5-bit encode on the fifth-generation tensor cores.  A tile
-// is 8 rows = 128 (row, subvector) pairs, the M of one tcgen05 MMA; the 4096
-// centroids are 32 chunks of N = 128.  One MMA per chunk writes to tensor
-// memory
+// Many rows of 1.5-bit or 2-bit encode on the fifth-generation tensor cores.
+// A tile is 128 (row, subvector) pairs, the M of one tcgen05 MMA: 8 rows of
+// 16 subvectors (1.5 bit) or 4 rows of 32 (2 bit); the 4096 (256) centroids
+// are 32 (2) chunks of N = 128.  One MMA per chunk writes to tensor memory
 //   D[m][c] = [x_hi, 1, 1] . [-2c, |c|^2_hi, |c|^2_lo] = |c|^2 - 2 x_hi . c,
 // the screened distance less the subvector's own |x'_j|^2, with x_hi the fp16
 // rounding of the transformed subvector (A) and the [-2c, |c|^2_hi, |c|^2_lo]
-// table of all 4096 centroids (B) in shared memory behind matrix
+// table of all the KV head's centroids (B) in shared memory behind matrix
 // descriptors.  Its error is bounded by screen_eps_hi.  (A second MMA with
 // the fp16 remainder of x' would tighten the bound but doubles the shared
 // memory and tensor memory traffic, which bound this kernel.)
@@ -477,8 +477,8 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 // Roles (12 warps, one CTA per SM, persistent over the KV head's tiles; 12
 // warps leave each SM sub-partition 3 warps, so up to 168 registers a thread,
 // enough for a whole 128-column chunk in flight per epilogue thread):
-//   warps 8, 9   producers: transform rows pw, pw + 2, pw + 4, pw + 6 of each
-//                tile (smoothing + Hadamard in double-float for keys), write
+//   warps 8, 9   producers: transform rows pw, pw + 2, ... of each tile
+//                (smoothing + Hadamard in double-float for keys), write
 //                A, x' and |x'_j|^2 into one of 4 stages;
 //   warps 10, 11 one thread each issues the MMAs of one epilogue warpgroup,
 //                chunk by chunk into that warpgroup's two 128-column
@@ -486,7 +486,8 @@ __device__ __forceinline__ float build_tc_table(const EncodeParams& p, int kvh, 
 //                columns); separate issuers keep one warpgroup's wait for a
 //                free buffer from holding up the other's MMAs;
 //   warps 0-3, 4-7  two epilogue warpgroups taking alternate tiles: thread m
-//                owns tensor-memory lane m, i.e. subvector m % 16 of row m / 16.
+//                owns tensor-memory lane m, i.e. subvector m % S of row m / S
+//                (S = 16 or 32 subvectors a row).
 // The epilogue does not rank candidates one by one: per group of 32
 // consecutive centroids it takes the group minimum, which the tensor-memory
 // load computes itself (tcgen05.ld.red ... .min, one load per group), and
