@@ -541,7 +541,11 @@ struct UmGeo {
   static constexpr int OFF_STAGES = TABLE_BYTES;
   static constexpr int OFF_BAR = OFF_STAGES + um::STAGES * STAGE_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + um::NBAR * 8;   // tensor-memory base, abort flag, max centroid norm
-  static constexpr size_t SMEM = OFF_MISC + 16;
+  // 2 bit: the codebook again as plain fp16 [E][4], 8 bytes a centroid, so
+  // that 16 lanes reading 16 consecutive centroids hit 16 distinct bank pairs
+  // in the exact re-rank (the B table's 32-byte rows give only 8)
+  static constexpr int OFF_CB4 = OFF_MISC + 16;
+  static constexpr size_t SMEM = OFF_CB4 + (DSUB == 4 ? E * 8 : 0);
   static_assert(SMEM <= 227 * 1024 && STAGE_BYTES % 16 == 0 && OFF_BAR % 8 == 0, "UMMA encode shared memory");
   static_assert(CHUNKS % um::NBUF == 0 && E / um::GROUP <= 128 && ROWS <= 16, "tile plan (7-bit group ids)");
 };
@@ -722,6 +726,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
       } else {
         *reinterpret_cast<uint4*>(row) = make_uint4(m2[0], m2[1], tw, 0u);
         *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint2*>(smem + Geo::OFF_CB4)[c] = make_uint2(w[0], w[1]);
       }
       cmax = fmaxf(cmax, sqrtf(nn));
     }
@@ -861,6 +866,24 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
     const int r = ml / SUBV, j = ml % SUBV;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const unsigned char* table = smem;
+    // exact fp32 distance of subvector xx to centroid c (as exact_d_umma)
+    auto exact = [&](const float (&xx)[DSUB], int c) -> float {
+      if constexpr (DSUB == 8) {
+        return exact_d_umma<8>(xx, table, c);
+      } else {
+        const uint2 raw = *reinterpret_cast<const uint2*>(smem + Geo::OFF_CB4 + 8 * c);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        float e = __fsub_rn(xx[0], a.x);
+        float d = __fmul_rn(e, e);
+        e = __fsub_rn(xx[1], a.y);
+        d = __fmaf_rn(e, e, d);
+        e = __fsub_rn(xx[2], b.x);
+        d = __fmaf_rn(e, e, d);
+        e = __fsub_rn(xx[3], b.y);
+        return __fmaf_rn(e, e, d);
+      }
+    };
     int it = 0;
     for (int k = wg; k < n_my; k += 2, ++it) {
       const float inf = __int_as_float(0x7f800000);
@@ -927,14 +950,15 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
       float dex = __int_as_float(0x7f800000), dsec = dex;
       int cex = 0x7fffffff;
       // group G1 by each lane; lane l visits its group's centroids from the
-      // (l % 8)-th on: a centroid's 16 bytes sit in bank group c % 8, so the
-      // 32 lanes spread over all 8 bank groups at every step
+      // (l % 8)-th on (1.5 bit: a centroid's 16 bytes sit in bank group c % 8,
+      // so the 32 lanes spread over all 8 bank groups at every step) or the
+      // (l % 16)-th on (2 bit: 8 bytes at bank pair c % 16)
       {
-        const int rot = lane & 7;
+        const int rot = lane & (DSUB == 8 ? 7 : 15);
 #pragma unroll 8
         for (int i = 0; i < GROUP; ++i) {
           const int c = GROUP * G1 + ((i + rot) & (GROUP - 1));
-          exact_push(exact_d_umma<DSUB>(xv, table, c), c, dex, cex, dsec);
+          exact_push(exact(xv, c), c, dex, cex, dsec);
         }
       }
       // groups G2 / G3 (few lanes) by the whole warp, one (lane, group) at a
@@ -951,7 +975,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
           float xs[DSUB];
 #pragma unroll
           for (int i = 0; i < DSUB; ++i) xs[i] = __shfl_sync(0xffffffffu, xv[i], src);
-          float d = exact_d_umma<DSUB>(xs, table, GROUP * g + lane), sd = __int_as_float(0x7f800000);
+          float d = exact(xs, GROUP * g + lane), sd = __int_as_float(0x7f800000);
           int c = GROUP * g + lane;
           exact_warp_reduce(d, c, sd);
           if (lane == src) exact_merge(d, c, sd, dex, cex, dsec);
@@ -972,7 +996,7 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
             exact_push(dd, cc, d, c, sd);
           }
         } else {
-          for (int cc = lane; cc < E; cc += 32) exact_push(exact_d_umma<DSUB>(xs, table, cc), cc, d, c, sd);
+          for (int cc = lane; cc < E; cc += 32) exact_push(exact(xs, cc), cc, d, c, sd);
         }
         exact_warp_reduce(d, c, sd);
         if (lane == src) dex = d, cex = c, dsec = sd;   // every candidate: replaces the group search
