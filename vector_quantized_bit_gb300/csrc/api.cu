@@ -460,9 +460,9 @@ vqkv_status encode_launch(const vqkv_encode_args* a, void* stream, const vqkv_pa
     blocks_x = (int)rows;
   } else {
     const long long want = (rows + encode_warps_per_cta() - 1) / encode_warps_per_cta();
-    // 1.5 and 2 bit: persistent tensor-memory CTAs over tiles of 8 / 4 rows,
-    // one wave; others: 4 waves
-    const int waves = (a->mode == VQKV_MODE_VQ15 || a->mode == VQKV_MODE_VQ2) ? 1 : 4;
+    // every mode but 4 bit: persistent tensor-memory CTAs over tiles of 8 or
+    // 4 rows, one wave; 4 bit: one warp per row, 4 waves
+    const int waves = a->mode == VQKV_MODE_VQ4 ? 4 : 1;
     long long cap = ((long long)di.sms * di.encode_bpsm[a->mode] * waves + a->Hkv - 1) / a->Hkv;
     if (cap < 1) cap = 1;
     blocks_x = (int)std::min(want, cap);

@@ -524,12 +524,13 @@ constexpr uint32_t MAX_POLLS = 1u << 22;
 constexpr int F_OK = 0, F_EXHAUSTIVE = 1, F_SKIP = 2;
 }  // namespace um
 
-// Per code mode: 1.5 bit (4096 centroids of 8 channels, 16 subvectors a
-// row, 8 rows a tile) or 2 bit (256 of 4, 32 subvectors, 4 rows a tile).
+// Per code mode: 8-channel subvectors (1.5 bit: 4096 centroids; 1.25 bit:
+// 1024), 16 a row, 8 rows a tile; or 4-channel ones (2 bit: 256 centroids;
+// 3 bit: 4096), 32 a row, 4 rows a tile.
 template <int MODE>
 struct UmGeo {
-  static constexpr int DSUB = MODE == VQKV_MODE_VQ15 ? 8 : 4;
-  static constexpr int E = MODE == VQKV_MODE_VQ15 ? 4096 : 256;
+  static constexpr int DSUB = (MODE == VQKV_MODE_VQ15 || MODE == VQKV_MODE_VQ125) ? 8 : 4;
+  static constexpr int E = MODE == VQKV_MODE_VQ2 ? 256 : MODE == VQKV_MODE_VQ125 ? 1024 : 4096;
   static constexpr int SUBV = kHeadDim / DSUB;           // subvectors per row
   static constexpr int ROWS = um::M / SUBV;               // rows per tile
   static constexpr int CHUNKS = E / um::N;               // MMAs per tile
@@ -541,9 +542,10 @@ struct UmGeo {
   static constexpr int OFF_STAGES = TABLE_BYTES;
   static constexpr int OFF_BAR = OFF_STAGES + um::STAGES * STAGE_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + um::NBAR * 8;   // tensor-memory base, abort flag, max centroid norm
-  // 2 bit: the codebook again as plain fp16 [E][4], 8 bytes a centroid, so
-  // that 16 lanes reading 16 consecutive centroids hit 16 distinct bank pairs
-  // in the exact re-rank (the B table's 32-byte rows give only 8)
+  // 4-channel modes: the codebook again as plain fp16 [E][4], 8 bytes a
+  // centroid, so that 16 lanes reading 16 consecutive centroids hit 16
+  // distinct bank pairs in the exact re-rank (the B table's 32-byte rows give
+  // only 8)
   static constexpr int OFF_CB4 = OFF_MISC + 16;
   static constexpr size_t SMEM = OFF_CB4 + (DSUB == 4 ? E * 8 : 0);
   static_assert(SMEM <= 227 * 1024 && STAGE_BYTES % 16 == 0 && OFF_BAR % 8 == 0, "UMMA encode shared memory");
@@ -1002,22 +1004,50 @@ __global__ void __launch_bounds__(um::THREADS, 1) encode_umma_kernel(const Encod
         if (lane == src) dex = d, cex = c, dsec = sd;   // every candidate: replaces the group search
       }
       count_near_ties(p.near_tie, flag != F_SKIP && is_near_tie(dex, dsec), lane, 0xffffffffu);
-      if constexpr (DSUB == 8) {
+      const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
+      const int b = row / p.n_rows;
+      const int t = flag != F_SKIP ? reinterpret_cast<const int*>(st + ST_POS)[r] : 0;
+      if constexpr (MODE == VQKV_MODE_VQ15) {
         // lane (row r, subvector j < 8) stores the pair (j, j + 8) of its row
         const int hi = __shfl_down_sync(0xffffffffu, cex, 8);
         if (j < 8 && flag != F_SKIP) {
-          const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
-          const int b = row / p.n_rows;
-          const int t = reinterpret_cast<const int*>(st + ST_POS)[r];
           uint8_t* tb = tile_base(p, b, kvh, t, 64, 1536);
           if (tb) store_pair(tb + vq15_pair_offset(p.role, t & 63, j), cex, hi);
         }
-      } else if (flag != F_SKIP) {   // one byte per subvector
-        const int row = ((int)blockIdx.x + k * (int)gridDim.x) * ROWS + r;
-        const int b = row / p.n_rows;
-        const int t = reinterpret_cast<const int*>(st + ST_POS)[r];
-        uint8_t* tb = tile_base(p, b, kvh, t, 16, 512);
-        if (tb) tb[vq2_code_offset(p.role, t & 15, j)] = (uint8_t)cex;
+      } else if constexpr (MODE == VQKV_MODE_VQ2) {   // one byte per subvector
+        if (flag != F_SKIP) {
+          uint8_t* tb = tile_base(p, b, kvh, t, 16, 512);
+          if (tb) tb[vq2_code_offset(p.role, t & 15, j)] = (uint8_t)cex;
+        }
+      } else if constexpr (MODE == VQKV_MODE_VQ3) {   // lane j < 16 stores the 12-bit pair (j, j + 16)
+        const int hi = __shfl_down_sync(0xffffffffu, cex, 16);
+        if (j < 16 && flag != F_SKIP) {
+          uint8_t* tb = tile_base(p, b, kvh, t, 16, 768);
+          if (tb) {
+            tb[vq3_byte_offset(p.role, t & 15, j, 0)] = (uint8_t)(cex & 0xff);
+            tb[vq3_byte_offset(p.role, t & 15, j, 1)] = (uint8_t)(((cex >> 8) & 0xf) | ((hi & 0xf) << 4));
+            tb[vq3_byte_offset(p.role, t & 15, j, 2)] = (uint8_t)(hi >> 4);
+          }
+        }
+      } else {   // 1.25 bit: lanes j < 4 of each row's half-warp pack a 40-bit group
+        const bool key = p.role == VQKV_ROLE_K;
+        const int base = lane & 16, g = lane & 3;
+        const uint32_t c0 = __shfl_sync(0xffffffffu, cex, base + (key ? g : 2 * g));
+        const uint32_t c1 = __shfl_sync(0xffffffffu, cex, base + (key ? g + 4 : 2 * g + 1));
+        const uint32_t c2 = __shfl_sync(0xffffffffu, cex, base + (key ? g + 8 : 2 * g + 8));
+        const uint32_t c3 = __shfl_sync(0xffffffffu, cex, base + (key ? g + 12 : 2 * g + 9));
+        if (j < 4 && flag != F_SKIP) {
+          const unsigned long long grp =
+              (unsigned long long)(c0 | (c1 << 10) | (c2 << 20)) | ((unsigned long long)c3 << 30);
+          uint8_t* tb = tile_base(p, b, kvh, t, 16, 320);
+          if (tb) {
+            const int rr = t & 15;
+            const int run = key ? 4 * (rr & 7) + g : 4 * g + ((rr & 7) >> 1);
+            const int n0 = key ? 5 * (rr >> 3) : 5 * (2 * (rr >> 3) + (rr & 1));
+#pragma unroll
+            for (int q = 0; q < 5; ++q) tb[vq125_run_byte(p.role, run, n0 + q)] = (uint8_t)(grp >> (8 * q));
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(a_empty(s));
@@ -1180,12 +1210,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) encode_vq15_tc_split_kernel(con
 int encode_warps_per_cta() { return ENC_WARPS; }
 
 cudaError_t encode_prepare(int mode) {
+  const cudaFuncAttribute smem_attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
   if (mode == VQKV_MODE_VQ3) {
-    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    cudaError_t e = cudaFuncSetAttribute(encode_vq3_kernel<1>, a, (int)kEnc3Smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(encode_vq3_kernel<ENC3_SPLIT>, a, (int)kEnc3Smem);
+    cudaError_t e = cudaFuncSetAttribute(encode_vq3_kernel<ENC3_SPLIT>, smem_attr, (int)kEnc3Smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(encode_umma_kernel<VQKV_MODE_VQ3>, smem_attr, (int)UmGeo<VQKV_MODE_VQ3>::SMEM);
     return e;
   }
+  if (mode == VQKV_MODE_VQ125)
+    return cudaFuncSetAttribute(encode_umma_kernel<VQKV_MODE_VQ125>, smem_attr, (int)UmGeo<VQKV_MODE_VQ125>::SMEM);
   if (mode == VQKV_MODE_VQ2)
     return cudaFuncSetAttribute(encode_umma_kernel<VQKV_MODE_VQ2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)UmGeo<VQKV_MODE_VQ2>::SMEM);
@@ -1209,10 +1242,11 @@ cudaError_t encode_occupancy(int mode, int* blocks_per_sm) {
   if (mode == VQKV_MODE_VQ4)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq2_kernel<1, 2>, ENC_THREADS, 0);
   if (mode == VQKV_MODE_VQ3)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq3_kernel<1>, ENC_THREADS,
-                                                         kEnc3Smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_umma_kernel<VQKV_MODE_VQ3>,
+                                                         um::THREADS, UmGeo<VQKV_MODE_VQ3>::SMEM);
   if (mode == VQKV_MODE_VQ125)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_vq125_kernel<1>, ENC_THREADS, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_umma_kernel<VQKV_MODE_VQ125>,
+                                                         um::THREADS, UmGeo<VQKV_MODE_VQ125>::SMEM);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, encode_umma_kernel<VQKV_MODE_VQ15>,
                                                        um::THREADS, UmGeo<VQKV_MODE_VQ15>::SMEM);
 }
@@ -1231,12 +1265,14 @@ cudaError_t launch_encode(int mode, const EncodeParams& p, int blocks_x, bool sp
   }
   if (mode == VQKV_MODE_VQ125) {
     if (split_rows) return launch_pdl(encode_vq125_kernel<ENC_WARPS>, grid, dim3(ENC_THREADS), 0, stream, p);
-    return launch_pdl(encode_vq125_kernel<1>, grid, dim3(ENC_THREADS), 0, stream, p);
+    return launch_pdl(encode_umma_kernel<VQKV_MODE_VQ125>, grid, dim3(um::THREADS), UmGeo<VQKV_MODE_VQ125>::SMEM,
+                      stream, p);
   }
   if (mode == VQKV_MODE_VQ3) {
     if (split_rows)
       return launch_pdl(encode_vq3_kernel<ENC3_SPLIT>, grid, dim3(ENC3_SPLIT * 32), kEnc3Smem, stream, p);
-    return launch_pdl(encode_vq3_kernel<1>, grid, dim3(ENC_THREADS), kEnc3Smem, stream, p);
+    return launch_pdl(encode_umma_kernel<VQKV_MODE_VQ3>, grid, dim3(um::THREADS), UmGeo<VQKV_MODE_VQ3>::SMEM,
+                      stream, p);
   }
   if (split_rows) return launch_pdl(encode_vq15_tc_split_kernel, grid, dim3(TC_THREADS), kTcSplitSmem, stream, p);
   return launch_pdl(encode_umma_kernel<VQKV_MODE_VQ15>, grid, dim3(um::THREADS), UmGeo<VQKV_MODE_VQ15>::SMEM,
