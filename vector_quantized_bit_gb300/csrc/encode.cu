@@ -48,7 +48,8 @@ __device__ __forceinline__ const float* key_s(const EncodeParams& p, int kvh) {
 // 256-entry codebooks, one byte per code.  DSUB = 4 (2 bit): lane l holds
 // subvector l (channels 4l..4l+3); DSUB = 2 (4 bit): lane l holds
 // subvectors 2l and 2l+1 (channels 4l, 4l+1 and 4l+2, 4l+3).
-// SPLIT = 1: one warp per row, 256 candidates per lane.
+// SPLIT = 1: one warp per row, 256 candidates per lane (many 4-bit rows;
+// many 2-bit rows go to the tensor-memory kernel below).
 // SPLIT = 8: the CTA's 8 warps share one row, 32 candidates each (few rows,
 // e.g. a decode-step append: latency instead of throughput).
 template <int SPLIT, int DSUB>
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_vq2_kernel(const EncodePar
 // 4096 / SPLIT candidates (SPLIT = 16 warps sharing one row per CTA), with
 // the fp32 codebook (or each warp's slice of it) in shared memory (64 KB,
 // read by broadcast).  Lanes 0..15 then write pair l from their own code
-// and lane l + 16's.
+// and lane l + 16's.  The library launches SPLIT = 16 for few rows (a
+// decode step's append); many rows go to the tensor-memory kernel below.
 constexpr size_t kEnc3Smem = 4096 * sizeof(float4);
 constexpr int ENC3_SPLIT = 16;
 
@@ -213,7 +215,8 @@ __global__ void __launch_bounds__(SPLIT == 1 ? ENC_THREADS : SPLIT * 32) encode_
 // SPLIT = 1, 1024 / SPLIT per warp otherwise); the halves merge across
 // lanes l and l + 16.  Lanes 0..3 then pack the row's four 40-bit groups
 // (K: subvectors g, g+4, g+8, g+12; V: 2g, 2g+1, 2g+8, 2g+9) and write 5
-// bytes each.
+// bytes each.  The library launches SPLIT = 8 for few rows (a decode step's
+// append); many rows go to the tensor-memory kernel below.
 
 // Search of one 8-channel subvector over candidates [c_lo, c_hi) (a multiple
 // of 4): fp32 direct differences in channel order, four chains over the
