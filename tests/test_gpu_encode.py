@@ -133,13 +133,14 @@ def test_near_tie_counter_counts_exact_ties():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 3, 4])
 def test_full_size_prefill_and_append_sampled(mode):
     """Mistral-7B-shaped encode at full size (16 sequences x 8 KV heads x
     16,384 prefill rows, then 256 appended rows at positions 16,384..16,639),
-    launched as one call each; the oracle re-encodes sampled rows."""
+    launched as one call each (the prefill on the tensor-memory kernel, at
+    1.5, 2, 3 and 1.25 bit); the oracle re-encodes sampled rows."""
     w = synth.WORKLOADS[4].with_mode(mode)
-    kw = dict(sample_tokens=2048, iters=2) if mode else dict(sample_tokens=2048, iters=10)
+    kw = dict(sample_tokens=2048, iters=2) if w.entries >= 1024 else dict(sample_tokens=2048, iters=10)
     s, kcb, vcb = H.calibrate(w, **kw)
     import torch
     sb = vo.code_bytes(mode, w.cap_len)
