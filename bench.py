@@ -74,10 +74,10 @@ def parse():
                     help="time the offline calibration stage (smoothing, key transform, K-Means training) instead")
     ap.add_argument("--ablation", action="store_true",
                     help="codebook utilisation and reconstruction error of the five key transforms instead")
-    ap.add_argument("--profile-encode", type=int, default=-1, choices=[-1, 0, 1],
+    ap.add_argument("--profile-encode", type=int, default=-1, choices=[-1, 0, 1, 3, 4],
                     help="time the key prefill encode of 4 of the Mistral-shaped workload's sequences (4 x 8 x "
-                         "16,384 rows) in this code mode (0: 2-bit, 1: 1.5-bit), 3 calls, and exit: the command "
-                         "the encode ncu summaries are taken with")
+                         "16,384 rows) in this code mode (0: 2-bit, 1: 1.5-bit, 3: 3-bit, 4: 1.25-bit), 3 calls, "
+                         "and exit: the command the encode ncu summaries are taken with")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="set up the workload, run this many plain (eager) steps and exit: "
                          "the command the ncu summaries under profiles/ are taken with")
